@@ -1,0 +1,417 @@
+#!/usr/bin/env python3
+"""Benchmark: KIVI quantized-KV decode step on one GB300.
+
+A step is one decode step of the whole cache: kivi_append (the lazy key-block
+flush / value-queue pop of the KIVI residual window, then the new token) and
+kivi_decode_attn (split-K attention over quantized + fp16 segments, merge).
+Prefill packing runs once before timing and is reported separately.
+
+Prints ONE JSON line.  Default workload: Llama-3-8B GQA layer shape at 32k
+context (batch 8, 32 query / 8 kv heads, d 128, 2-bit K/V, G 32, R 128).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-cpu-baseline]
+
+--impl reference times the CPU oracle (plain C, fp32) on the host cores on
+a bounded sample of the same workload.  Under torchrun (N > 1) every rank
+runs an independent replica of the workload on its own GPU (the path has no
+exchange step); rank 0 prints the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_quantized_kv_quantize_gb300 import workloads as W  # noqa: E402
+
+METRIC = "quantized-KV decode attention µs/step and cache GB/s vs HBM peak (1×GB300)"
+DEFAULT_WORKLOAD = "llama3_8b_gqa_32k"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes (read + write) of one decode-attention launch, from an ncu
+# capture of the kernel whose source hash is recorded beside it; reported
+# only while the kernel source is unchanged.
+NCU_TRAFFIC = {}
+
+
+def algorithmic_bytes(w: W.Workload, T, Tqk, Tqv) -> int:
+    """Cache bytes one decode-attention call must read, plus q and out:
+    packed codes and fp16 scale/zero of the quantized tokens and the fp16
+    residual tokens, per (sequence, kv head)."""
+    d, G = w.d, w.G
+    per_qk = d * w.kbits // 8 + 4 * d // G
+    per_qv = d * w.vbits // 8 + 4 * d // G
+    T, Tqk, Tqv = (np.asarray(x, np.int64) for x in (T, Tqk, Tqv))
+    cache = w.h_kv * int(np.sum(Tqk * per_qk + Tqv * per_qv + ((T - Tqk) + (T - Tqv)) * 2 * d))
+    return cache + 2 * w.b * w.h_q * d * 2
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        if j.get("hbm_gbs"):
+            return float(j["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("kivi_decode.cu", "kivi_internal.cuh"):
+        with open(os.path.join(ROOT, "bit_quantized_kv_quantize_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx = float(p[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, None
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    backend = "nccl" if os.environ.get("KIVI_BENCH_BACKEND", "") != "gloo" else "gloo"
+    dist.init_process_group(backend)
+    return rank, ws, dist
+
+
+def reduce_max(x: float, dist, device=None) -> float:
+    """Max over ranks (replicas run independently; the slowest sets the time)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        import torch
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline object)
+# ---------------------------------------------------------------------------
+
+def oracle_time(w: W.Workload, budget_s: float = 15.0, max_pairs: int = 8):
+    """Time the oracle's decode step (append + attention) on a sample of the
+    workload: the first b' sequences x h' kv heads (b' h' <= max_pairs) with
+    all their query heads, in one oracle cache whose attention rows spread
+    over the host cores.  Returns (us per full step, cores, sample text),
+    scaled to all b x h_kv (sequence, kv head) pairs by token count."""
+    import oracle
+    cores = os.cpu_count() or 1
+    oracle.set_threads(cores)
+    lens = w.lengths()
+    bs = min(w.b, max_pairs)
+    hs = min(w.h_kv, max(1, max_pairs // bs))
+    cap = w.capacity()
+    c = oracle.Cache(bs, hs, w.d, w.kbits, w.vbits, w.G, w.R, cap)
+    ts = int(lens[:bs].max())
+    Kh = np.zeros((bs, hs, ts, w.d), np.float16)
+    Vh = np.zeros_like(Kh)
+    for i in range(bs):
+        for j in range(hs):
+            n = int(lens[i])
+            Kh[i, j, :n] = W.prefill_slice(w, "K", i, j, n)
+            Vh[i, j, :n] = W.prefill_slice(w, "V", i, j, n)
+    c.prefill(Kh, Vh, lens[:bs])
+    del Kh, Vh
+    hg = w.group
+    steps, elapsed = 0, 0.0
+    while steps < max(1, w.steps) and elapsed < budget_s:
+        k, v = W.step_kv(w, steps)
+        q = W.step_q(w, steps)
+        k = np.ascontiguousarray(k[:bs, :hs])
+        v = np.ascontiguousarray(v[:bs, :hs])
+        q = np.ascontiguousarray(q[:bs, :hs * hg])
+        t0 = time.perf_counter()
+        c.append(k, v)
+        c.decode(q)
+        elapsed += time.perf_counter() - t0
+        steps += 1
+    scale = float(lens.sum() * w.h_kv) / float(lens[:bs].sum() * hs)
+    us = elapsed / steps * scale * 1e6
+    sample = (f"{bs} sequence(s) x {hs} kv head(s) of {w.b} x {w.h_kv}, {steps} step(s) of "
+              f"append + attention over {hg} query heads per kv head, scaled by token count "
+              f"to the whole batch; {elapsed:.1f} s of oracle time on {cores} threads")
+    return us, cores, sample
+
+
+def run_reference(args, w):
+    rank, ws, dist = 0, int(os.environ.get("WORLD_SIZE", "1")), None
+    if ws > 1 and int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    t0 = time.time()
+    us, cores, sample = oracle_time(w, budget_s=float(os.environ.get("KIVI_ORACLE_BUDGET_S", "20")))
+    line = {
+        "metric": METRIC, "value": round(us, 3), "unit": "us/step", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 6),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "impl": "reference",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": round(us, 3), "unit": "us/step", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(us, 3), "unit": "us/step", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "wall_s": round(time.time() - t0, 1),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    T = int(w.lengths().max()) + 1
+    return {"workload": w.name, "b": w.b, "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d,
+            "k_bits": w.kbits, "v_bits": w.vbits, "G": w.G, "R": w.R,
+            "context": T if not w.ragged else f"ragged {w.ragged[0]}-{w.ragged[1]}",
+            "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+            "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, w):
+    import torch
+    rank, ws, dist = dist_setup()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from bit_quantized_kv_quantize_gb300 import kivi as K
+
+    t_start = time.time()
+    cap = int(w.lengths().max()) + args.warmup + 2 * args.steps + 8
+    cache = K.KiviCache(w.b, w.h_kv, w.d, w.kbits, w.vbits, w.G, w.R, cap)
+    Kh, Vh, lens = W.prefill_kv(w)
+    Kd = torch.from_numpy(Kh).to(dev)
+    Vd = torch.from_numpy(Vh).to(dev)
+    del Kh, Vh
+    stream = torch.cuda.current_stream(dev)
+    # prefill pack, timed once (after one untimed run)
+    cache.prefill(Kd, Vd, lens)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    cache.prefill(Kd, Vd, lens)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    prefill_ms = e0.elapsed_time(e1)
+    del Kd, Vd
+    torch.cuda.empty_cache()
+
+    nsteps = args.warmup + args.steps + 1
+    host_k, host_v, host_q = [], [], []
+    for s in range(nsteps):
+        k, v = W.step_kv(w, s)
+        host_k.append(k)
+        host_v.append(v)
+        host_q.append(W.step_q(w, s))
+    kd = [torch.from_numpy(x).to(dev) for x in host_k]
+    vd = [torch.from_numpy(x).to(dev) for x in host_v]
+    qd = [torch.from_numpy(x).to(dev) for x in host_q]
+    out = torch.empty((w.b, w.h_q, w.d), dtype=torch.float16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def step(s):
+        cache.append(kd[s], vd[s])
+        cache.decode(qd[s], out)
+
+    for s in range(args.warmup):
+        flush.fill_(s)
+        step(s)
+    torch.cuda.synchronize(dev)
+
+    # ---- device-timed region: inputs resident in HBM --------------------
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    bytes_steps = []
+    cache.profile(True)
+    cache.profile_read()
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        for n in range(args.steps):
+            s = args.warmup + n
+            flush.fill_(n)
+            starts[n].record(stream)
+            step(s)
+            ends[n].record(stream)
+            T, Tqk, Tqv = cache.lengths()
+            bytes_steps.append(algorithmic_bytes(w, T, Tqk, Tqv))
+        torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    attn_ms_total, attn_launches = cache.profile_read()
+    cache.profile(False)
+    splits, launches = cache.plan()
+    ms_per_step = reduce_max(sum(step_ms) / args.steps, dist, dev)
+    attn_ms = reduce_max(attn_ms_total / max(1, attn_launches), dist, dev)
+    assert cache.check() == 0, "device status word set during the benchmark"
+
+    # ---- end to end through the C ABI with host buffers ------------------
+    pin_k = [torch.from_numpy(x).pin_memory() for x in host_k]
+    pin_v = [torch.from_numpy(x).pin_memory() for x in host_v]
+    pin_q = [torch.from_numpy(x).pin_memory() for x in host_q]
+    out_h = torch.empty((w.b, w.h_q, w.d), dtype=torch.float16).pin_memory()
+    kbuf = torch.empty_like(kd[0])
+    vbuf = torch.empty_like(vd[0])
+    qbuf = torch.empty_like(qd[0])
+    # the same cache continues (the sequences keep growing); inputs cycle
+    e2e_ms = []
+    for n in range(args.steps):
+        s = n % nsteps
+        flush.fill_(n)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        kbuf.copy_(pin_k[s], non_blocking=True)
+        vbuf.copy_(pin_v[s], non_blocking=True)
+        qbuf.copy_(pin_q[s], non_blocking=True)
+        cache.append(kbuf, vbuf)
+        cache.decode(qbuf, out)
+        out_h.copy_(out, non_blocking=True)
+        b.record(stream)
+        e2e_ms.append((a, b))
+    torch.cuda.synchronize(dev)
+    e2e_per = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_ms) / len(e2e_ms), dist, dev)
+    h2d = int(kbuf.numel() * 2 + vbuf.numel() * 2 + qbuf.numel() * 2)
+    d2h = int(out.numel() * 2)
+
+    peak, peak_kind = load_peaks()
+    bytes_per = float(np.mean(bytes_steps))
+    achieved = bytes_per / (attn_ms * 1e-3) / 1e9
+    us_step = ms_per_step * 1e3
+    line = {
+        "metric": METRIC,
+        "value": round(us_step, 3),
+        "unit": "us/step",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u2/u4 codes, f16 in, f32 accumulate",
+        "data": "synthetic",
+        "config": workload_config(w),
+        "attn_us": round(attn_ms * 1e3, 3),
+        "cache_gbs": round(bytes_per / (attn_ms * 1e-3) / 1e9, 1),
+        "bytes_per_step": int(bytes_per),
+        "prefill_us": round(prefill_ms * 1e3, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": "decode attention (split-K + merge)",
+                     "traffic": NCU_TRAFFIC.get(source_hash())},
+        "e2e": {"value": round(e2e_per * 1e3, 3), "unit": "us/step",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (1 + launches),
+        "splits": splits,
+        "clocks": clk.summary(),
+        "source_hash": source_hash(),
+    }
+    if rank == 0 and not args.no_cpu_baseline and ws == 1:
+        us, cores, sample = oracle_time(w, budget_s=float(os.environ.get("KIVI_ORACLE_BUDGET_S", "15")))
+        line["cpu_baseline"] = {"value": round(us, 3), "unit": "us/step", "cores": cores,
+                                "kind": "oracle", "sample": sample}
+    line["wall_s"] = round(time.time() - t_start, 1)
+    cache.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

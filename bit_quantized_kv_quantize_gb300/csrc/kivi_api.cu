@@ -1,0 +1,468 @@
+// kivi_api.cu -- host side of libkivi: the C ABI declared in include/kivi.h.
+//
+// Owns the cache's device memory, keeps a host mirror of the per-sequence
+// counters (T, Tqk, Tqv) that evolves by the same rule as the device copy
+// (KIVI core algorithm item 4), validates every argument before touching
+// anything, and launches the kernels of kivi_pack.cu / kivi_decode.cu on the
+// caller's stream.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <set>
+#include <vector>
+
+#include "../../include/kivi.h"
+#include "kivi_internal.cuh"
+
+namespace {
+
+constexpr uint32_t kMagic = 0x4b495649u;   // "KIVI"
+constexpr int kMaxProfile = 4096;
+
+thread_local char g_err[512] = "";
+
+void set_err(const char *fmt, const char *a = "", long v = 0) {
+    snprintf(g_err, sizeof g_err, fmt, a, v);
+}
+
+std::mutex g_live_mu;
+std::set<void *> g_live;
+
+}  // namespace
+
+struct kivi_cache {
+    uint32_t magic;
+    bool poisoned;
+    int max_tokens;
+    int device;
+    int num_sms;
+    KiviGeom g;
+    KiviDev dv;
+    std::vector<int> T, Tqk, Tqv;   // host mirror
+    DecodePlan last_plan;
+    bool profiling;
+    std::vector<cudaEvent_t> ev;   // pairs
+    int nprof;
+};
+
+namespace {
+
+kivi_status fail_cuda(kivi_cache *c, cudaError_t e, const char *where) {
+    if (c) c->poisoned = true;
+    snprintf(g_err, sizeof g_err, "%s: %s", where, cudaGetErrorString(e));
+    return KIVI_ERR_CUDA;
+}
+
+kivi_status check_handle(kivi_cache_t c) {
+    if (!c) {
+        set_err("null cache handle");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_live_mu);
+        if (!g_live.count((void *)c)) {
+            set_err("unknown or destroyed cache handle");
+            return KIVI_ERR_INVALID_ARG;
+        }
+    }
+    if (c->magic != kMagic) {
+        set_err("corrupt cache handle");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (c->poisoned) {
+        set_err("cache poisoned by an earlier CUDA error");
+        return KIVI_ERR_STATE;
+    }
+    return KIVI_OK;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+void free_dev(KiviDev &d) {
+    void *ps[] = {d.Kc, d.Ksz, d.Vc, d.Vsz, d.Kf, d.Vf, d.T, d.Tqk, d.Tqv, d.ticket, d.status,
+                  d.part, d.merge_ticket};
+    for (void *p : ps)
+        if (p) cudaFree(p);
+    memset(&d, 0, sizeof d);
+}
+
+}  // namespace
+
+extern "C" {
+
+int kivi_abi_version(void) { return KIVI_ABI_VERSION; }
+
+const char *kivi_last_error(void) { return g_err; }
+
+const char *kivi_status_str(kivi_status s) {
+    switch (s) {
+    case KIVI_OK: return "ok";
+    case KIVI_ERR_INVALID_ARG: return "invalid argument";
+    case KIVI_ERR_UNSUPPORTED: return "unsupported shape or bit width";
+    case KIVI_ERR_CAPACITY: return "capacity exceeded";
+    case KIVI_ERR_STATE: return "cache poisoned by an earlier CUDA error";
+    case KIVI_ERR_CUDA: return "CUDA error";
+    case KIVI_ERR_OOM: return "out of memory";
+    }
+    return "unknown status";
+}
+
+kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, int G, int R,
+                              int max_tokens, kivi_cache_t *out) {
+    g_err[0] = 0;
+    if (!out) {
+        set_err("out is null");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    *out = nullptr;
+    if (b < 1 || h_kv < 1 || d < 1 || G < 1 || R < 1 || max_tokens < 1) {
+        set_err("sizes must be positive");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (b > KIVI_MAX_BATCH) {
+        set_err("b above %s%ld", "", KIVI_MAX_BATCH);
+        return KIVI_ERR_UNSUPPORTED;
+    }
+    if ((k_bits != 2 && k_bits != 4) || (v_bits != 2 && v_bits != 4)) {
+        set_err("bits must be 2 or 4");
+        return KIVI_ERR_UNSUPPORTED;
+    }
+    if (G != 16 && G != 32 && G != 64 && G != 128) {
+        set_err("G must be 16, 32, 64 or 128");
+        return KIVI_ERR_UNSUPPORTED;
+    }
+    if (d != 64 && d != 128 && d != 256) {
+        set_err("d must be 64, 128 or 256");
+        return KIVI_ERR_UNSUPPORTED;
+    }
+    if (d % G != 0 || R % G != 0 || R > 4096) {
+        set_err("need d %% G == 0, R %% G == 0 and R <= 4096");
+        return KIVI_ERR_UNSUPPORTED;
+    }
+    const int q = G > KIVI_KBLK ? G : KIVI_KBLK;
+    if ((long)max_tokens + q > (1L << 30)) {
+        set_err("max_tokens too large");
+        return KIVI_ERR_UNSUPPORTED;
+    }
+    kivi_cache *c = new (std::nothrow) kivi_cache();
+    if (!c) {
+        set_err("host allocation failed");
+        return KIVI_ERR_OOM;
+    }
+    c->magic = kMagic;
+    c->poisoned = false;
+    c->max_tokens = max_tokens;
+    c->profiling = false;
+    c->nprof = 0;
+    memset(&c->last_plan, 0, sizeof c->last_plan);
+    KiviGeom &g = c->g;
+    g.b = b; g.h = h_kv; g.d = d; g.kbits = k_bits; g.vbits = v_bits; g.G = G; g.R = R;
+    g.fcap = (max_tokens + q - 1) / q * q;
+    g.nkb = g.fcap / KIVI_KBLK;
+    g.nkg = g.fcap / G;
+    g.nvb = g.fcap / KIVI_VBLK;
+    g.kc_blk = 2 * d * k_bits;
+    g.vc_blk = d * v_bits / 2;
+    g.vsz_blk = 2 * (d / G) * KIVI_VBLK;
+    g.smax = (g.fcap + 255) / 256 + 2;
+    if (g.smax > 1024) g.smax = 1024;
+    c->T.assign(b, 0);
+    c->Tqk.assign(b, 0);
+    c->Tqv.assign(b, 0);
+
+    cudaError_t e = cudaGetDevice(&c->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+    if (e != cudaSuccess) {
+        delete c;
+        snprintf(g_err, sizeof g_err, "no CUDA device: %s", cudaGetErrorString(e));
+        return KIVI_ERR_CUDA;
+    }
+    KiviDev &dv = c->dv;
+    memset(&dv, 0, sizeof dv);
+    const size_t bh = (size_t)b * h_kv;
+    struct Req { void **p; size_t bytes; } reqs[] = {
+        {(void **)&dv.Kc, bh * g.nkb * g.kc_blk * 4},
+        {(void **)&dv.Ksz, bh * g.nkg * 2 * d * 2},
+        {(void **)&dv.Vc, bh * g.nvb * g.vc_blk * 4},
+        {(void **)&dv.Vsz, bh * g.nvb * g.vsz_blk * 2},
+        {(void **)&dv.Kf, bh * R * d * 2},
+        {(void **)&dv.Vf, bh * (R + 1) * d * 2},
+        {(void **)&dv.T, (size_t)b * 4},
+        {(void **)&dv.Tqk, (size_t)b * 4},
+        {(void **)&dv.Tqv, (size_t)b * 4},
+        {(void **)&dv.ticket, (size_t)b * 4},
+        {(void **)&dv.status, 4},
+        {(void **)&dv.part, bh * KIVI_MAX_QPERKV * g.smax * (d + 2) * 4},
+        {(void **)&dv.merge_ticket, bh * 4 * 4},
+    };
+    for (auto &r : reqs) {
+        e = cudaMalloc(r.p, r.bytes);
+        if (e == cudaSuccess) e = cudaMemset(*r.p, 0, r.bytes);
+        if (e != cudaSuccess) {
+            free_dev(dv);
+            delete c;
+            cudaGetLastError();
+            snprintf(g_err, sizeof g_err, "device allocation failed: %s", cudaGetErrorString(e));
+            return e == cudaErrorMemoryAllocation ? KIVI_ERR_OOM : KIVI_ERR_CUDA;
+        }
+    }
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        free_dev(dv);
+        delete c;
+        snprintf(g_err, sizeof g_err, "create: %s", cudaGetErrorString(e));
+        return KIVI_ERR_CUDA;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_live_mu);
+        g_live.insert(c);
+    }
+    *out = c;
+    return KIVI_OK;
+}
+
+kivi_status kivi_cache_destroy(kivi_cache_t c) {
+    g_err[0] = 0;
+    if (!c) {
+        set_err("null cache handle");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_live_mu);
+        if (!g_live.erase((void *)c)) {
+            set_err("unknown or destroyed cache handle");
+            return KIVI_ERR_INVALID_ARG;
+        }
+    }
+    cudaDeviceSynchronize();
+    cudaGetLastError();
+    free_dev(c->dv);
+    for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
+    c->magic = 0;
+    delete c;
+    return KIVI_OK;
+}
+
+kivi_status kivi_prefill(kivi_cache_t c, const void *K, const void *V, const int32_t *t,
+                         int t_stride, kivi_stream_t stream) {
+    g_err[0] = 0;
+    kivi_status s = check_handle(c);
+    if (s != KIVI_OK) return s;
+    if (!t || t_stride < 0) {
+        set_err("t is null or t_stride negative");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    SeqLens lens;
+    int maxt = 0;
+    for (int i = 0; i < c->g.b; ++i) {
+        if (t[i] < 0 || t[i] > t_stride) {
+            set_err("t[i] outside [0, t_stride] for i = %s%ld", "", i);
+            return KIVI_ERR_INVALID_ARG;
+        }
+        if (t[i] > c->max_tokens) {
+            set_err("t[i] above max_tokens for i = %s%ld", "", i);
+            return KIVI_ERR_CAPACITY;
+        }
+        lens.t[i] = t[i];
+        maxt = t[i] > maxt ? t[i] : maxt;
+    }
+    if (maxt > 0 && (!K || !V)) {
+        set_err("K or V is null");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (maxt > 0 && (!aligned16(K) || !aligned16(V))) {
+        set_err("K and V must be 16-byte aligned");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    cudaError_t e = kivi_launch_prefill(c->g, c->dv, (const __half *)K, (const __half *)V, lens,
+                                        t_stride, (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail_cuda(c, e, "prefill");
+    for (int i = 0; i < c->g.b; ++i) {
+        c->T[i] = t[i];
+        c->Tqk[i] = t[i] - t[i] % c->g.R;
+        c->Tqv[i] = t[i] > c->g.R ? t[i] - c->g.R : 0;
+    }
+    return KIVI_OK;
+}
+
+kivi_status kivi_append(kivi_cache_t c, const void *k, const void *v, kivi_stream_t stream) {
+    g_err[0] = 0;
+    kivi_status s = check_handle(c);
+    if (s != KIVI_OK) return s;
+    if (!k || !v) {
+        set_err("k or v is null");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (!aligned16(k) || !aligned16(v)) {
+        set_err("k and v must be 16-byte aligned");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    for (int i = 0; i < c->g.b; ++i)
+        if (c->T[i] + 1 > c->max_tokens) {
+            set_err("sequence %s%ld is full", "", i);
+            return KIVI_ERR_CAPACITY;
+        }
+    cudaError_t e = kivi_launch_append(c->g, c->dv, (const __half *)k, (const __half *)v,
+                                       (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail_cuda(c, e, "append");
+    const int R = c->g.R;
+    for (int i = 0; i < c->g.b; ++i) {
+        if (c->T[i] - c->Tqk[i] == R) c->Tqk[i] += R;
+        if (c->T[i] - c->Tqv[i] == R + 1) c->Tqv[i] += 1;
+        c->T[i] += 1;
+    }
+    return KIVI_OK;
+}
+
+kivi_status kivi_decode_attn(kivi_cache_t c, const void *q, int h_q, void *out,
+                             kivi_stream_t stream) {
+    g_err[0] = 0;
+    kivi_status s = check_handle(c);
+    if (s != KIVI_OK) return s;
+    if (!q || !out) {
+        set_err("q or out is null");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (h_q < 1 || h_q % c->g.h != 0) {
+        set_err("h_q must be a positive multiple of h_kv");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (h_q / c->g.h > KIVI_MAX_QPERKV) {
+        set_err("h_q / h_kv above 8");
+        return KIVI_ERR_UNSUPPORTED;
+    }
+    if (!aligned16(q) || !aligned16(out)) {
+        set_err("q and out must be 16-byte aligned");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    int maxT = 0;
+    for (int i = 0; i < c->g.b; ++i) maxT = c->T[i] > maxT ? c->T[i] : maxT;
+    DecodePlan plan = kivi_plan_decode(c->g, h_q, maxT, c->num_sms);
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (c->profiling && c->nprof < kMaxProfile) {
+        if ((int)c->ev.size() < 2 * (c->nprof + 1)) {
+            cudaEvent_t a, b;
+            if (cudaEventCreate(&a) == cudaSuccess && cudaEventCreate(&b) == cudaSuccess) {
+                c->ev.push_back(a);
+                c->ev.push_back(b);
+            }
+        }
+        if ((int)c->ev.size() >= 2 * (c->nprof + 1)) {
+            e0 = c->ev[2 * c->nprof];
+            e1 = c->ev[2 * c->nprof + 1];
+            c->nprof++;
+        }
+    }
+    cudaError_t e = kivi_launch_decode(c->g, c->dv, (const __half *)q, h_q, (__half *)out, plan,
+                                       (cudaStream_t)stream, e0, e1);
+    if (e != cudaSuccess) return fail_cuda(c, e, "decode_attn");
+    c->last_plan = plan;
+    return KIVI_OK;
+}
+
+kivi_status kivi_cache_lengths(kivi_cache_t c, int32_t *T, int32_t *Tqk, int32_t *Tqv) {
+    g_err[0] = 0;
+    kivi_status s = check_handle(c);
+    if (s != KIVI_OK && s != KIVI_ERR_STATE) return s;
+    for (int i = 0; i < c->g.b; ++i) {
+        if (T) T[i] = c->T[i];
+        if (Tqk) Tqk[i] = c->Tqk[i];
+        if (Tqv) Tqv[i] = c->Tqv[i];
+    }
+    return KIVI_OK;
+}
+
+kivi_status kivi_cache_export_sizes(kivi_cache_t c, size_t sizes[6]) {
+    g_err[0] = 0;
+    kivi_status s = check_handle(c);
+    if (s != KIVI_OK && s != KIVI_ERR_STATE) return s;
+    if (!sizes) {
+        set_err("sizes is null");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    const KiviGeom &g = c->g;
+    const size_t bh = (size_t)g.b * g.h;
+    sizes[0] = bh * g.nkb * g.kc_blk * 4;
+    sizes[1] = bh * g.nkg * 2 * g.d * 2;
+    sizes[2] = bh * g.nvb * g.vc_blk * 4;
+    sizes[3] = bh * g.nvb * g.vsz_blk * 2;
+    sizes[4] = bh * g.R * g.d * 2;
+    sizes[5] = bh * (g.R + 1) * g.d * 2;
+    return KIVI_OK;
+}
+
+kivi_status kivi_cache_export(kivi_cache_t c, void *Kc, void *Ksz, void *Vc, void *Vsz, void *Kf,
+                              void *Vf, kivi_stream_t stream) {
+    g_err[0] = 0;
+    kivi_status s = check_handle(c);
+    if (s != KIVI_OK) return s;
+    size_t sz[6];
+    kivi_cache_export_sizes(c, sz);
+    const void *src[6] = {c->dv.Kc, c->dv.Ksz, c->dv.Vc, c->dv.Vsz, c->dv.Kf, c->dv.Vf};
+    void *dst[6] = {Kc, Ksz, Vc, Vsz, Kf, Vf};
+    cudaStream_t st = (cudaStream_t)stream;
+    for (int k = 0; k < 6; ++k) {
+        if (!dst[k]) continue;
+        cudaError_t e = cudaMemcpyAsync(dst[k], src[k], sz[k], cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess) return fail_cuda(c, e, "export");
+    }
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return fail_cuda(c, e, "export");
+    return KIVI_OK;
+}
+
+kivi_status kivi_cache_check(kivi_cache_t c, uint32_t *flags, kivi_stream_t stream) {
+    g_err[0] = 0;
+    kivi_status s = check_handle(c);
+    if (s != KIVI_OK) return s;
+    if (!flags) {
+        set_err("flags is null");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(flags, c->dv.status, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->dv.status, 0, 4, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return fail_cuda(c, e, "check");
+    return KIVI_OK;
+}
+
+kivi_status kivi_profile_enable(kivi_cache_t c, int on) {
+    g_err[0] = 0;
+    kivi_status s = check_handle(c);
+    if (s != KIVI_OK) return s;
+    c->profiling = on != 0;
+    return KIVI_OK;
+}
+
+kivi_status kivi_profile_read(kivi_cache_t c, double *total_ms, int *launches) {
+    g_err[0] = 0;
+    kivi_status s = check_handle(c);
+    if (s != KIVI_OK) return s;
+    double tot = 0.0;
+    for (int k = 0; k < c->nprof; ++k) {
+        cudaError_t e = cudaEventSynchronize(c->ev[2 * k + 1]);
+        float ms = 0.f;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, c->ev[2 * k], c->ev[2 * k + 1]);
+        if (e != cudaSuccess) return fail_cuda(c, e, "profile_read");
+        tot += ms;
+    }
+    if (total_ms) *total_ms = tot;
+    if (launches) *launches = c->nprof;
+    c->nprof = 0;
+    return KIVI_OK;
+}
+
+kivi_status kivi_decode_plan(kivi_cache_t c, int *splits, int *launches) {
+    g_err[0] = 0;
+    kivi_status s = check_handle(c);
+    if (s != KIVI_OK && s != KIVI_ERR_STATE) return s;
+    if (splits) *splits = c->last_plan.splits;
+    if (launches) *launches = c->last_plan.launches;
+    return KIVI_OK;
+}
+
+}  // extern "C"

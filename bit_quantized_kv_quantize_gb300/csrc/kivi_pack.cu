@@ -1,0 +1,361 @@
+// kivi_pack.cu -- quantize-and-pack kernels: prefill (keys, values, fp16
+// residual fill) and the per-token append with its lazy maintenance.
+//
+// Method: "Literature audit -- Group 2", section 1 KIVI, core algorithm
+// items 1-4 (quantizer, per-channel key groups along tokens, per-token value
+// groups along channels, fp16 residual window with the key-block flush at R
+// and the value-queue pop at R + 1).
+//
+// All kernels stream HBM once: a CTA stages its token tile in shared memory,
+// computes per-group min/max, then writes whole packed words (coalesced:
+// consecutive threads write consecutive words).
+#include "kivi_internal.cuh"
+
+namespace {
+
+__device__ __forceinline__ void flag(unsigned *status, unsigned f) { atomicOr(status, f); }
+
+// ---------------------------------------------------------------------------
+// Prefill keys: one CTA per (super block of TB = max(64, G) tokens, kv head,
+// sequence).  Quantizes tokens [0, nqk), nqk = t - t mod R.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) prefill_keys_kernel(KiviGeom g, KiviDev dv,
+                                                           const __half *__restrict__ K,
+                                                           SeqLens lens, int t_stride) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int TB = g.G > KIVI_KBLK ? g.G : KIVI_KBLK;
+    const int sb = blockIdx.x, j = blockIdx.y, i = blockIdx.z;
+    const int t = lens.t[i];
+    const int nqk = t - t % g.R;
+    const int tok0 = sb * TB;
+    if (tok0 >= nqk) return;
+    const int d = g.d;
+    const int ntok = min(TB, nqk - tok0);   // a multiple of G
+    const int ngr = ntok / g.G;
+
+    __half *xs = reinterpret_cast<__half *>(smem);                     // [TB][d]
+    float *sfz = reinterpret_cast<float *>(smem + (size_t)TB * d * 2); // [TB/G][2][d]
+
+    // stage the tile (16-byte vectors)
+    const __half *src = K + (((size_t)i * g.h + j) * t_stride + tok0) * d;
+    const int nvec = ntok * d / 8;
+    for (int e = threadIdx.x; e < nvec; e += blockDim.x)
+        reinterpret_cast<uint4 *>(xs)[e] = reinterpret_cast<const uint4 *>(src)[e];
+    __syncthreads();
+
+    // scale and zero per (group, channel)
+    __half *ksz = dv.Ksz + ksz_slice(g, i, j);
+    for (int e = threadIdx.x; e < ngr * d; e += blockDim.x) {
+        int gr = e / d, c = e - gr * d;
+        float mn = __half2float(xs[(size_t)gr * g.G * d + c]), mx = mn;
+        for (int k = 1; k < g.G; ++k) {
+            float x = __half2float(xs[((size_t)gr * g.G + k) * d + c]);
+            mn = fminf(mn, x);
+            mx = fmaxf(mx, x);
+        }
+        QParams p = qparams(mn, mx, g.kbits);
+        int grp = tok0 / g.G + gr;
+        ksz[ksz_locate(g, grp, c, 0)] = p.s16;
+        ksz[ksz_locate(g, grp, c, 1)] = p.z16;
+        sfz[(gr * 2 + 0) * d + c] = p.sf;
+        sfz[(gr * 2 + 1) * d + c] = p.zf;
+    }
+    __syncthreads();
+
+    // packed words of every 64-token block that starts inside [tok0, nqk)
+    const int nblk = (ntok + KIVI_KBLK - 1) / KIVI_KBLK;
+    const int cph = 16 / g.kbits;
+    uint32_t *kc = dv.Kc + kc_slice(g, i, j);
+    for (int e = threadIdx.x; e < nblk * g.kc_blk; e += blockDim.x) {
+        int kbl = e / g.kc_blk, wb = e - kbl * g.kc_blk;
+        KWord kw = kword_decode(wb, g.kbits);
+        uint32_t word = 0;
+#pragma unroll 2
+        for (int half = 0; half < 2; ++half) {
+            int c = kw.c0 + half;
+            for (int r = 0; r < cph; ++r) {
+                int tl = kbl * KIVI_KBLK + 8 * (kw.pos0 + r) + kw.g;   // token within the tile
+                if (tl < ntok) {
+                    int gr = tl / g.G;
+                    float x = __half2float(xs[(size_t)tl * d + c]);
+                    uint32_t q = qcode(x, sfz[(gr * 2) * d + c], sfz[(gr * 2 + 1) * d + c], g.kbits);
+                    word |= q << (16 * half + r * g.kbits);
+                }
+            }
+        }
+        kc[(size_t)(tok0 / KIVI_KBLK + kbl) * g.kc_blk + wb] = word;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Prefill values: one CTA per (64 tokens = 4 value blocks, kv head,
+// sequence).  Quantizes tokens [0, nqv), nqv = max(t - R, 0).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) prefill_values_kernel(KiviGeom g, KiviDev dv,
+                                                             const __half *__restrict__ V,
+                                                             SeqLens lens, int t_stride) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int sb = blockIdx.x, j = blockIdx.y, i = blockIdx.z;
+    const int t = lens.t[i];
+    const int nqv = t > g.R ? t - g.R : 0;
+    const int tok0 = sb * 64;
+    if (tok0 >= nqv) return;
+    const int d = g.d, ngi = d / g.G;
+    const int ntok = min(64, nqv - tok0);
+    __half *xs = reinterpret_cast<__half *>(smem);                          // [64][d]
+    float *sfz = reinterpret_cast<float *>(smem + (size_t)64 * d * 2);     // [64][2][ngi]
+
+    const __half *src = V + (((size_t)i * g.h + j) * t_stride + tok0) * d;
+    for (int e = threadIdx.x; e < ntok * d / 8; e += blockDim.x)
+        reinterpret_cast<uint4 *>(xs)[e] = reinterpret_cast<const uint4 *>(src)[e];
+    __syncthreads();
+
+    const int nvblk = (ntok + KIVI_VBLK - 1) / KIVI_VBLK;   // value blocks touched
+    __half *vsz = dv.Vsz + vsz_slice(g, i, j);
+    for (int e = threadIdx.x; e < nvblk * KIVI_VBLK * ngi; e += blockDim.x) {
+        int tl = e / ngi, gi = e - tl * ngi;
+        int tau = tok0 + tl;
+        __half s16 = __float2half_rn(0.f), z16 = s16;
+        if (tl < ntok) {
+            const __half *x = xs + (size_t)tl * d + gi * g.G;
+            float mn = __half2float(x[0]), mx = mn;
+            for (int k = 1; k < g.G; ++k) {
+                float v = __half2float(x[k]);
+                mn = fminf(mn, v);
+                mx = fmaxf(mx, v);
+            }
+            QParams p = qparams(mn, mx, g.vbits);
+            s16 = p.s16;
+            z16 = p.z16;
+            sfz[(tl * 2 + 0) * ngi + gi] = p.sf;
+            sfz[(tl * 2 + 1) * ngi + gi] = p.zf;
+        }
+        vsz[vsz_locate(g, tau, gi, 0)] = s16;   // tokens past nqv: zero
+        vsz[vsz_locate(g, tau, gi, 1)] = z16;
+    }
+    __syncthreads();
+
+    const int cs = v_cs(g), cph = 16 / g.vbits;
+    uint32_t *vc = dv.Vc + vc_slice(g, i, j);
+    for (int e = threadIdx.x; e < nvblk * g.vc_blk; e += blockDim.x) {
+        int vbl = e / g.vc_blk, wb = e - vbl * g.vc_blk;
+        VWord vw = vword_decode(wb, d, g.vbits, cs);
+        uint32_t word = 0;
+        for (int half = 0; half < 2; ++half) {
+            int tl = vbl * KIVI_VBLK + vw.tt0 + half;
+            if (tl >= ntok) continue;
+            for (int r = 0; r < cph; ++r) {
+                int c = 8 * (vw.ci0 + r) + vw.g;
+                int gi = c / g.G;
+                float x = __half2float(xs[(size_t)tl * d + c]);
+                uint32_t q = qcode(x, sfz[(tl * 2) * ngi + gi], sfz[(tl * 2 + 1) * ngi + gi], g.vbits);
+                word |= q << (16 * half + r * g.vbits);
+            }
+        }
+        vc[(size_t)(tok0 / KIVI_VBLK + vbl) * g.vc_blk + wb] = word;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Prefill fp16 windows and counters: one CTA per (kv head, sequence).
+// Key token tau in [nqk, t) goes to slot tau % R; value token tau in
+// [nqv, t) to slot tau % (R + 1).
+// ---------------------------------------------------------------------------
+__global__ void prefill_residual_kernel(KiviGeom g, KiviDev dv, const __half *__restrict__ K,
+                                        const __half *__restrict__ V, SeqLens lens, int t_stride) {
+    const int j = blockIdx.x, i = blockIdx.y;
+    const int t = lens.t[i];
+    const int nqk = t - t % g.R, nqv = t > g.R ? t - g.R : 0;
+    const int vpt = g.d / 8;   // uint4 per token
+    const uint4 *ks = reinterpret_cast<const uint4 *>(K + ((size_t)i * g.h + j) * t_stride * g.d);
+    const uint4 *vs = reinterpret_cast<const uint4 *>(V + ((size_t)i * g.h + j) * t_stride * g.d);
+    uint4 *kf = reinterpret_cast<uint4 *>(dv.Kf + kf_slice(g, i, j));
+    uint4 *vf = reinterpret_cast<uint4 *>(dv.Vf + vf_slice(g, i, j));
+    for (int e = threadIdx.x; e < (t - nqk) * vpt; e += blockDim.x) {
+        int tau = nqk + e / vpt, c = e % vpt;
+        kf[(size_t)(tau % g.R) * vpt + c] = ks[(size_t)tau * vpt + c];
+    }
+    for (int e = threadIdx.x; e < (t - nqv) * vpt; e += blockDim.x) {
+        int tau = nqv + e / vpt, c = e % vpt;
+        vf[(size_t)(tau % (g.R + 1)) * vpt + c] = vs[(size_t)tau * vpt + c];
+    }
+    if (j == 0 && threadIdx.x == 0) {
+        dv.T[i] = t;
+        dv.Tqk[i] = nqk;
+        dv.Tqv[i] = nqv;
+        dv.ticket[i] = 0u;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Append: one CTA per (kv head, sequence).  Lazy maintenance of item 4, then
+// the new token joins the fp16 windows.  The last CTA of a sequence to finish
+// advances that sequence's counters (all CTAs read them first).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) append_kernel(KiviGeom g, KiviDev dv,
+                                                     const __half *__restrict__ knew,
+                                                     const __half *__restrict__ vnew) {
+    const int j = blockIdx.x, i = blockIdx.y;
+    const int d = g.d, R = g.R;
+    const int T = dv.T[i], Tqk = dv.Tqk[i], Tqv = dv.Tqv[i];
+    __shared__ int s_ok;
+    if (threadIdx.x == 0) {
+        int ok = T >= 0 && T < g.fcap && Tqk >= 0 && Tqk % R == 0 && T - Tqk >= 0 &&
+                 T - Tqk <= R && Tqv >= 0 && T - Tqv >= 0 && T - Tqv <= R + 1;
+        if (!ok) flag(dv.status, KIVI_FLAG_COUNTER);
+        s_ok = ok;
+    }
+    __syncthreads();
+    if (!s_ok) return;
+    const bool flush = (T - Tqk) == R;
+    const bool pop = (T - Tqv) == R + 1;
+    const __half *kf = dv.Kf + kf_slice(g, i, j);
+    __half *kfw = dv.Kf + kf_slice(g, i, j);
+    __half *vfw = dv.Vf + vf_slice(g, i, j);
+
+    if (flush) {
+        // keys [Tqk, Tqk + R): token tau lives in slot tau - Tqk (Tqk % R == 0)
+        __half *ksz = dv.Ksz + ksz_slice(g, i, j);
+        const int ngr = R / g.G;
+        for (int e = threadIdx.x; e < ngr * d; e += blockDim.x) {
+            int gr = e / d, c = e - gr * d;
+            float mn = __half2float(kf[(size_t)gr * g.G * d + c]), mx = mn;
+            for (int k = 1; k < g.G; ++k) {
+                float x = __half2float(kf[((size_t)gr * g.G + k) * d + c]);
+                mn = fminf(mn, x);
+                mx = fmaxf(mx, x);
+            }
+            QParams p = qparams(mn, mx, g.kbits);
+            int grp = Tqk / g.G + gr;
+            ksz[ksz_locate(g, grp, c, 0)] = p.s16;
+            ksz[ksz_locate(g, grp, c, 1)] = p.z16;
+        }
+        __syncthreads();
+        const int kb0 = Tqk / KIVI_KBLK, kb1 = (Tqk + R - 1) / KIVI_KBLK;
+        const int cph = 16 / g.kbits;
+        uint32_t *kc = dv.Kc + kc_slice(g, i, j);
+        for (int e = threadIdx.x; e < (kb1 - kb0 + 1) * g.kc_blk; e += blockDim.x) {
+            int kb = kb0 + e / g.kc_blk, wb = e % g.kc_blk;
+            KWord kw = kword_decode(wb, g.kbits);
+            uint32_t old = kc[(size_t)kb * g.kc_blk + wb];
+            uint32_t word = 0;
+            for (int half = 0; half < 2; ++half) {
+                int c = kw.c0 + half;
+                for (int r = 0; r < cph; ++r) {
+                    int tau = kb * KIVI_KBLK + 8 * (kw.pos0 + r) + kw.g;
+                    int sh = 16 * half + r * g.kbits;
+                    uint32_t mask = ((1u << g.kbits) - 1u) << sh;
+                    if (tau < Tqk) {
+                        word |= old & mask;                     // earlier tokens stay
+                    } else if (tau < Tqk + R) {
+                        int grp = tau / g.G;
+                        float sf = __half2float(ksz[ksz_locate(g, grp, c, 0)]);
+                        float zf = __half2float(ksz[ksz_locate(g, grp, c, 1)]);
+                        float x = __half2float(kf[(size_t)(tau - Tqk) * d + c]);
+                        word |= qcode(x, sf, zf, g.kbits) << sh;
+                    }                                           // later tokens: zero
+                }
+            }
+            kc[(size_t)kb * g.kc_blk + wb] = word;
+        }
+    }
+
+    if (pop) {
+        // value token Tqv, slot Tqv % (R + 1)
+        const __half *x = dv.Vf + vf_slice(g, i, j) + (size_t)(Tqv % (R + 1)) * d;
+        const int ngi = d / g.G;
+        __half *vsz = dv.Vsz + vsz_slice(g, i, j);
+        uint32_t *vc = dv.Vc + vc_slice(g, i, j);
+        const int vb = Tqv / KIVI_VBLK, tt = Tqv % KIVI_VBLK;
+        if (tt == 0) {   // a fresh value block: clear it so untouched fields read zero
+            for (int e = threadIdx.x; e < g.vc_blk; e += blockDim.x) vc[(size_t)vb * g.vc_blk + e] = 0u;
+            for (int e = threadIdx.x; e < g.vsz_blk; e += blockDim.x)
+                vsz[(size_t)vb * g.vsz_blk + e] = __float2half_rn(0.f);
+        }
+        __shared__ float s_sf[16], s_zf[16];   // d / G <= 16
+        __syncthreads();
+        for (int gi = threadIdx.x; gi < ngi; gi += blockDim.x) {
+            float mn = __half2float(x[gi * g.G]), mx = mn;
+            for (int k = 1; k < g.G; ++k) {
+                float v = __half2float(x[gi * g.G + k]);
+                mn = fminf(mn, v);
+                mx = fmaxf(mx, v);
+            }
+            QParams p = qparams(mn, mx, g.vbits);
+            vsz[vsz_locate(g, Tqv, gi, 0)] = p.s16;
+            vsz[vsz_locate(g, Tqv, gi, 1)] = p.z16;
+            s_sf[gi] = p.sf;
+            s_zf[gi] = p.zf;
+        }
+        __syncthreads();
+        // the token's halves: lane class g (8) x channel words w (d vbits / 128)
+        const int nwv = d * g.vbits / 128, cph = 16 / g.vbits, cs = v_cs(g);
+        const int p = tt >> 3, tq = (tt & 7) >> 1, half = tt & 1;
+        for (int e = threadIdx.x; e < 8 * nwv; e += blockDim.x) {
+            int gg = e / nwv, w = e - gg * nwv;
+            uint32_t bits = 0;
+            for (int r = 0; r < cph; ++r) {
+                int c = 8 * (w * cph + r) + gg;
+                int gi = c / g.G;
+                bits |= qcode(__half2float(x[c]), s_sf[gi], s_zf[gi], g.vbits) << (r * g.vbits);
+            }
+            int L = 4 * gg + tq, u = p * nwv + w;
+            size_t wd = (size_t)vb * g.vc_blk + (size_t)(u / cs) * 32 * cs + (size_t)L * cs + (u % cs);
+            reinterpret_cast<uint16_t *>(vc + wd)[half] = (uint16_t)bits;
+        }
+    }
+    __syncthreads();   // maintenance has read the slots the new token overwrites
+
+    const __half *kn = knew + ((size_t)i * g.h + j) * d;
+    const __half *vn = vnew + ((size_t)i * g.h + j) * d;
+    for (int c = threadIdx.x; c < d / 8; c += blockDim.x) {
+        reinterpret_cast<uint4 *>(kfw + (size_t)(T % R) * d)[c] = reinterpret_cast<const uint4 *>(kn)[c];
+        reinterpret_cast<uint4 *>(vfw + (size_t)(T % (R + 1)) * d)[c] = reinterpret_cast<const uint4 *>(vn)[c];
+    }
+
+    // last CTA of this sequence advances the counters
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        unsigned prev = atomicAdd(&dv.ticket[i], 1u);
+        if (prev == (unsigned)g.h - 1u) {
+            dv.T[i] = T + 1;
+            dv.Tqk[i] = Tqk + (flush ? R : 0);
+            dv.Tqv[i] = Tqv + (pop ? 1 : 0);
+            dv.ticket[i] = 0u;
+            __threadfence();
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t kivi_launch_prefill(const KiviGeom &g, const KiviDev &dv, const __half *K,
+                                const __half *V, const SeqLens &lens, int t_stride,
+                                cudaStream_t st) {
+    int maxt = 0;
+    for (int i = 0; i < g.b; ++i) maxt = lens.t[i] > maxt ? lens.t[i] : maxt;
+    if (maxt > 0) {
+        const int TB = g.G > KIVI_KBLK ? g.G : KIVI_KBLK;
+        size_t smk = (size_t)TB * g.d * 2 + (size_t)(TB / g.G) * 2 * g.d * 4;
+        cudaError_t e = cudaFuncSetAttribute(prefill_keys_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smk);
+        if (e != cudaSuccess) return e;
+        dim3 gk((maxt + TB - 1) / TB, g.h, g.b);
+        prefill_keys_kernel<<<gk, 256, smk, st>>>(g, dv, K, lens, t_stride);
+        size_t smv = (size_t)64 * g.d * 2 + (size_t)64 * 2 * (g.d / g.G) * 4;
+        e = cudaFuncSetAttribute(prefill_values_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smv);
+        if (e != cudaSuccess) return e;
+        dim3 gv((maxt + 63) / 64, g.h, g.b);
+        prefill_values_kernel<<<gv, 256, smv, st>>>(g, dv, V, lens, t_stride);
+    }
+    prefill_residual_kernel<<<dim3(g.h, g.b), 256, 0, st>>>(g, dv, K, V, lens, t_stride);
+    return cudaGetLastError();
+}
+
+cudaError_t kivi_launch_append(const KiviGeom &g, const KiviDev &dv, const __half *k,
+                               const __half *v, cudaStream_t st) {
+    append_kernel<<<dim3(g.h, g.b), 256, 0, st>>>(g, dv, k, v);
+    return cudaGetLastError();
+}
