@@ -166,8 +166,10 @@ kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, in
     g.kc_blk = 2 * d * k_bits;
     g.vc_blk = d * v_bits / 2;
     g.vsz_blk = 2 * (d / G) * KIVI_VBLK;
-    g.smax = (g.fcap + 255) / 256 + 2;
-    if (g.smax > 1024) g.smax = 1024;
+    // decode partials per (sequence, query head): tensor-core splits of at
+    // least kivi_min_blocks_per_split() blocks, plus the tail CTAs
+    g.smax = (g.nkb + kivi_min_blocks_per_split() - 1) / kivi_min_blocks_per_split() +
+             (R + 2 * KIVI_KBLK - 1) / KIVI_KBLK + 2;
     c->T.assign(b, 0);
     c->Tqk.assign(b, 0);
     c->Tqv.assign(b, 0);
@@ -337,9 +339,7 @@ kivi_status kivi_decode_attn(kivi_cache_t c, const void *q, int h_q, void *out,
         set_err("q and out must be 16-byte aligned");
         return KIVI_ERR_INVALID_ARG;
     }
-    int maxT = 0;
-    for (int i = 0; i < c->g.b; ++i) maxT = c->T[i] > maxT ? c->T[i] : maxT;
-    DecodePlan plan = kivi_plan_decode(c->g, h_q, maxT, c->num_sms);
+    DecodePlan plan = kivi_plan_decode(c->g, h_q, c->Tqk.data(), c->Tqv.data(), c->num_sms);
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (c->profiling && c->nprof < kMaxProfile) {
         if ((int)c->ev.size() < 2 * (c->nprof + 1)) {

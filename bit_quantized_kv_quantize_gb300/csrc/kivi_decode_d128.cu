@@ -1,0 +1,8 @@
+// kivi_decode_d128.cu -- decode-attention kernels for head dimension 128
+// (one translation unit per head dimension so the variants build in parallel).
+#include "kivi_decode_impl.cuh"
+
+cudaError_t kivi_launch_decode_d128(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq,
+                                   __half *out, const DecodePlan &plan, cudaStream_t st) {
+    return launch_d<128>(g, dv, q, hq, out, plan, st);
+}

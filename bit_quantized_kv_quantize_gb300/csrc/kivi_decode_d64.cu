@@ -1,0 +1,8 @@
+// kivi_decode_d64.cu -- decode-attention kernels for head dimension 64
+// (one translation unit per head dimension so the variants build in parallel).
+#include "kivi_decode_impl.cuh"
+
+cudaError_t kivi_launch_decode_d64(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq,
+                                   __half *out, const DecodePlan &plan, cudaStream_t st) {
+    return launch_d<64>(g, dv, q, hq, out, plan, st);
+}

@@ -176,10 +176,13 @@ __device__ __forceinline__ uint32_t qcode(float x, float sf, float zf, int bits)
 
 // ---- host-side launchers (kivi_pack.cu, kivi_decode.cu) ----------------------------
 struct DecodePlan {
-    int splits;      // CTAs along the token axis per (sequence, kv head, head group)
-    int blocks_per;  // 64-token blocks per split
+    int splits;      // tensor-core CTAs along the token axis per (sequence, kv head, head group)
+    int blocks_per;  // 64-token blocks per such CTA
+    int tails;       // CUDA-core CTAs covering the blocks that hold fp16 keys or values
     int qgroups;     // head groups of <= 4 query heads per kv head
-    int launches;
+    int warps;       // warps per CTA
+    int stages;      // shared-memory stages per warp
+    int launches;    // kernel launches per decode call
 };
 
 cudaError_t kivi_launch_prefill(const KiviGeom &g, const KiviDev &dv, const __half *K,
@@ -187,7 +190,8 @@ cudaError_t kivi_launch_prefill(const KiviGeom &g, const KiviDev &dv, const __ha
                                 cudaStream_t st);
 cudaError_t kivi_launch_append(const KiviGeom &g, const KiviDev &dv, const __half *k,
                                const __half *v, cudaStream_t st);
-DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, int maxT, int num_sms);
+DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *Tqk, const int *Tqv, int num_sms);
+int kivi_min_blocks_per_split();
 cudaError_t kivi_launch_decode(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq,
                                __half *out, const DecodePlan &plan, cudaStream_t st,
                                cudaEvent_t ev0, cudaEvent_t ev1);
