@@ -410,6 +410,8 @@ def run_ncu_case(args, w):
     del Kh, Vh
     cache.prefill(Kd, Vd, lens)
     del Kd, Vd
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
     k, v = W.step_kv(w, 0)
     cache.append(torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev))
     q = torch.from_numpy(W.step_q(w, 0)).to(dev)

@@ -38,32 +38,35 @@ DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *Tqk, const int
     const int hg = hq / g.h;
     p.qgroups = (hg + 3) / 4;
     p.tails = (g.R + 2 * KIVI_KBLK - 1) / KIVI_KBLK;
+    // Two CTAs per SM (the kernel is compiled for <= 128 registers a thread):
+    // each CTA gets ~110 KB of shared memory for its warps' rings of stages.
+    const int sb = stage_bytes(g);
+    const int budget = env_int("KIVI_DECODE_SMEM_KB", 110) * 1024;
     p.warps = env_int("KIVI_DECODE_WARPS", 8);
     if (p.warps > 8) p.warps = 8;
-    const int sb = stage_bytes(g);
-    const int budget = 200 * 1024;
+    while (p.warps > 1 && budget / (p.warps * sb) < 2) p.warps /= 2;
     int stages = budget / (p.warps * sb);
-    stages = stages > 4 ? 4 : (stages < 2 ? 2 : stages);
+    stages = stages > 4 ? 4 : (stages < 1 ? 1 : stages);
     p.stages = env_int("KIVI_DECODE_STAGES", stages);
     while (p.stages > 1 && (size_t)p.warps * p.stages * sb > 220 * 1024) --p.stages;
-    while (p.warps > 1 && (size_t)p.warps * p.stages * sb > 220 * 1024) p.warps /= 2;
     const size_t cta_smem = (size_t)p.warps * p.stages * sb + 1024;
-    int per_sm = (int)((228 * 1024) / cta_smem);
-    if (per_sm < 1) per_sm = 1;
-    if (per_sm * p.warps > 16) per_sm = 16 / p.warps > 0 ? 16 / p.warps : 1;
+    int per_sm = (int)((227 * 1024) / cta_smem);
+    per_sm = per_sm > 2 ? 2 : (per_sm < 1 ? 1 : per_sm);
     int nfull = 0;
     for (int i = 0; i < g.b; ++i) {
         int n = (Tqk[i] < Tqv[i] ? Tqk[i] : Tqv[i]) / KIVI_KBLK;
         nfull = n > nfull ? n : nfull;
     }
     const long pairs = (long)g.b * g.h * p.qgroups;
-    const int waves = env_int("KIVI_DECODE_WAVES", 4);
+    const int waves = env_int("KIVI_DECODE_WAVES", 2);
     const long slots = (long)num_sms * per_sm * waves;
     int splits = (int)((slots + pairs - 1) / pairs);
     if (splits < 1) splits = 1;
+    // blocks per split: a multiple of the warp count (warps get equal shares)
     const int min_bp = env_int("KIVI_DECODE_MIN_BLOCKS", kivi_min_blocks_per_split());
     int bp = nfull > 0 ? (nfull + splits - 1) / splits : 1;
     if (bp < min_bp) bp = min_bp;
+    bp = (bp + p.warps - 1) / p.warps * p.warps;
     splits = nfull > 0 ? (nfull + bp - 1) / bp : 0;
     if (splits + p.tails > g.smax) {
         bp = (nfull + (g.smax - p.tails) - 1) / (g.smax - p.tails);

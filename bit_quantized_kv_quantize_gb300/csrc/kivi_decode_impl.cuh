@@ -116,55 +116,73 @@ __device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
     return h2u(__hfma2(u2h(a), u2h(b), u2h(c)));
 }
 
-// Unpack field r of both 16-bit halves of w as fp16 (off + code): the field
-// is moved to the top mantissa bits and or-ed into the offset's pattern.
-template <int BITS>
-__device__ __forceinline__ uint32_t unpack(uint32_t w, int r) {
-    if (BITS == 2) {   // off = 4: fp16 0x4400, mantissa bits 8..9 weigh 1
-        uint32_t x = r <= 4 ? (w << (8 - 2 * r)) : (w >> (2 * r - 8));
-        return (x & 0x03000300u) | 0x44004400u;
-    } else {           // off = 16: fp16 0x4C00, mantissa bits 6..9 weigh 1
-        uint32_t x = r <= 1 ? (w << (6 - 4 * r)) : (w >> (4 * r - 6));
-        return (x & 0x03C003C0u) | 0x4C004C00u;
+// Unpack field r of both 16-bit halves of w as fp16 (off + code).  The field
+// is moved (by at most a few shifts shared between fields) to a mantissa
+// position p of an fp16 constant whose exponent makes bit p weigh 1, and
+// or-ed into it: the value is 2^(10 - p) + code.  Keys use p in {4, 6, 8}
+// (offsets 64, 16, 4), values p in {6, 8} (offsets 16, 4) so that the
+// offset, which the accumulator carries and the zero-point MMA removes
+// exactly, stays small against the value sums.  4-bit fields sit at p = 6.
+struct View {
+    int shl, shr;          // shift left / right applied to the word
+    uint32_t mask, magic;  // field mask at its target position, fp16 pattern of the offset
+    float off;
+};
+template <int BITS, bool KEY>
+__host__ __device__ constexpr View view_of(int r) {
+    if (BITS == 4) {       // field bits [4r, 4r + 4) -> bits 6..9, offset 16
+        return r <= 1 ? View{6 - 4 * r, 0, 0x03C003C0u, 0x4C004C00u, 16.f}
+                      : View{0, 4 * r - 6, 0x03C003C0u, 0x4C004C00u, 16.f};
+    }
+    // 2-bit field bits [2r, 2r + 2)
+    const View p4{0, 0, 0x00300030u, 0x54005400u, 64.f};   // target bits 4..5
+    const View p6{0, 0, 0x00C000C0u, 0x4C004C00u, 16.f};   // target bits 6..7
+    const View p8{0, 0, 0x03000300u, 0x44004400u, 4.f};    // target bits 8..9
+    if (KEY) {
+        switch (r) {
+        case 0: return View{4, 0, p4.mask, p4.magic, p4.off};
+        case 1: return View{4, 0, p6.mask, p6.magic, p6.off};
+        case 2: return p4;
+        case 3: return p6;
+        case 4: return p8;
+        case 5: return View{0, 6, p4.mask, p4.magic, p4.off};
+        case 6: return View{0, 6, p6.mask, p6.magic, p6.off};
+        default: return View{0, 6, p8.mask, p8.magic, p8.off};
+        }
+    }
+    switch (r) {
+    case 0: return View{8, 0, p8.mask, p8.magic, p8.off};
+    case 1: return View{4, 0, p6.mask, p6.magic, p6.off};
+    case 2: return View{4, 0, p8.mask, p8.magic, p8.off};
+    case 3: return p6;
+    case 4: return p8;
+    case 5: return View{0, 4, p6.mask, p6.magic, p6.off};
+    case 6: return View{0, 4, p8.mask, p8.magic, p8.off};
+    default: return View{0, 8, p6.mask, p6.magic, p6.off};
     }
 }
-template <int BITS>
-constexpr float code_offset() { return BITS == 2 ? 4.f : 16.f; }
+template <int BITS, bool KEY>
+__device__ __forceinline__ uint32_t unpack(uint32_t w, int r) {   // r folds to a constant once unrolled
+    const View v = view_of<BITS, KEY>(r);
+    const uint32_t x = v.shl ? (w << v.shl) : (v.shr ? (w >> v.shr) : w);
+    return (x & v.mask) | v.magic;
+}
+template <int BITS, bool KEY>
+__host__ __device__ constexpr float slot_offset(int r) { return view_of<BITS, KEY>(r).off; }
 
 // ---------------------------------------------------------------------------
-// CUDA-core path for the tail (tokens with fp16 keys or values, or partial
-// blocks): one warp per token, lane owns channels lane + 32 k.
+// CUDA-core path for the tail (the last blocks, holding fp16 keys or values):
+// one warp per token, lane owns channels lane + 32 k.  Geometry is
+// compile-time except R (one modulo per token).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float key_at(const KiviGeom &g, const uint32_t *kc, const __half *ksz,
-                                        const __half *kf, int Tqk, int c, int tau) {
-    if (tau < Tqk) {
-        int sh;
-        size_t w = kc_locate(g, c, tau, &sh);
-        uint32_t code = (kc[w] >> sh) & ((1u << g.kbits) - 1u);
-        int grp = tau / g.G;
-        return (float)code * __half2float(ksz[ksz_locate(g, grp, c, 0)]) +
-               __half2float(ksz[ksz_locate(g, grp, c, 1)]);
-    }
-    return __half2float(kf[(size_t)(tau % g.R) * g.d + c]);
-}
-
-__device__ __forceinline__ float value_at(const KiviGeom &g, const uint32_t *vc, const __half *vsz,
-                                          const __half *vf, int Tqv, int c, int tau) {
-    if (tau < Tqv) {
-        int sh;
-        size_t w = vc_locate(g, c, tau, &sh);
-        uint32_t code = (vc[w] >> sh) & ((1u << g.vbits) - 1u);
-        int gi = c / g.G;
-        return (float)code * __half2float(vsz[vsz_locate(g, tau, gi, 0)]) +
-               __half2float(vsz[vsz_locate(g, tau, gi, 1)]);
-    }
-    return __half2float(vf[(size_t)(tau % (g.R + 1)) * g.d + c]);
-}
-
-template <int D>
+template <int D, int KB, int VB, int SH>
 __device__ void tail_tokens(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, int i,
                             int j, int e0, int nh, int t0, int t1, float *wm, float *wl, float *wo) {
     constexpr int CPL = D / 32;
+    constexpr int G = 16 << SH;
+    constexpr int CPHK = 16 / KB, NWK = KB / 2, CPHV = 16 / VB, NWV = D * VB / 128;
+    constexpr int WLV = D * VB / 64, CSV = WLV < 4 ? WLV : 4;
+    constexpr int KC_BLK = 2 * D * KB, VC_BLK = D * VB / 2, VSZ_BLK = 2 * (D / G) * 16;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int hg = hq / g.h;
     const int Tqk = dv.Tqk[i], Tqv = dv.Tqv[i];
@@ -189,21 +207,59 @@ __device__ void tail_tokens(const KiviGeom &g, const KiviDev &dv, const __half *
     const __half *vf = dv.Vf + vf_slice(g, i, j);
     for (int tau = t0 + warp; tau < t1; tau += nw) {
         float kv[CPL], vv[CPL];
+        if (tau < Tqk) {
+            const int kb = tau >> 6, pos = (tau & 63) >> 3, gg = tau & 7;
+            const int wi = pos / CPHK, r = pos % CPHK;
+            const __half *sz = ksz + (size_t)(tau / G) * 2 * D;
 #pragma unroll
-        for (int k = 0; k < CPL; ++k) {
-            kv[k] = key_at(g, kc, ksz, kf, Tqk, lane + 32 * k, tau);
-            vv[k] = value_at(g, vc, vsz, vf, Tqv, lane + 32 * k, tau);
+            for (int k = 0; k < CPL; ++k) {
+                const int c = lane + 32 * k;
+                const int u = (2 * (c >> 4) + ((c >> 3) & 1)) * NWK + wi;
+                const int L = 4 * gg + ((c & 7) >> 1);
+                const uint32_t w = kc[(size_t)kb * KC_BLK + (u >> 2) * 128 + 4 * L + (u & 3)];
+                const uint32_t code = (w >> (16 * (c & 1) + r * KB)) & ((1u << KB) - 1u);
+                kv[k] = (float)code * __half2float(sz[c]) + __half2float(sz[D + c]);
+            }
+        } else {
+            const __half *src = kf + (size_t)(tau % g.R) * D;
+#pragma unroll
+            for (int k = 0; k < CPL; ++k) kv[k] = __half2float(src[lane + 32 * k]);
         }
+        if (tau < Tqv) {
+            const int vb = tau >> 4, tt = tau & 15;
+            const int p = tt >> 3, t = (tt & 7) >> 1, hi = tt & 1;
+            const __half *sz = vsz + (size_t)vb * VSZ_BLK;
+#pragma unroll
+            for (int k = 0; k < CPL; ++k) {
+                const int c = lane + 32 * k;
+                const int ci = c >> 3, w = ci / CPHV, r = ci % CPHV;
+                const int L = 4 * (c & 7) + t, u = p * NWV + w;
+                const uint32_t word = vc[(size_t)vb * VC_BLK + (u / CSV) * 32 * CSV + L * CSV + (u % CSV)];
+                const uint32_t code = (word >> (16 * hi + r * VB)) & ((1u << VB) - 1u);
+                const int gi = c / G;
+                vv[k] = (float)code * __half2float(sz[gi * 16 + tt]) + __half2float(sz[(D / G + gi) * 16 + tt]);
+            }
+        } else {
+            const __half *src = vf + (size_t)(tau % (g.R + 1)) * D;
+#pragma unroll
+            for (int k = 0; k < CPL; ++k) vv[k] = __half2float(src[lane + 32 * k]);
+        }
+        float dot[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            float dot = 0.f;
+            dot[e] = 0.f;
 #pragma unroll
-            for (int k = 0; k < CPL; ++k) dot = fmaf(qr[e][k], kv[k], dot);
+            for (int k = 0; k < CPL; ++k) dot[e] = fmaf(qr[e][k], kv[k], dot[e]);
+        }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-            float mn = fmaxf(m[e], dot);
-            float corr = ex2(m[e] - mn);
-            float p = ex2(dot - mn);
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dot[e] += __shfl_xor_sync(0xffffffffu, dot[e], o);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float mn = fmaxf(m[e], dot[e]);
+            const float corr = ex2(m[e] - mn);
+            const float p = ex2(dot[e] - mn);
             l[e] = l[e] * corr + p;
 #pragma unroll
             for (int k = 0; k < CPL; ++k) acc[e][k] = fmaf(p, vv[k], acc[e][k] * corr);
@@ -283,7 +339,6 @@ __device__ void mma_blocks(const KiviGeom &g, const KiviDev &dv, const __half *q
     constexpr int nkrows = 2 * (SH >= 2 ? 1 : (4 >> SH));   // key scale/zero rows per block
     constexpr int nzr = 2 * ngi;            // value scale/zero rows per 16-token block
     const float alpha = kLog2e * rsqrtf((float)D);
-    constexpr float offK = code_offset<KB>(), offV = code_offset<VB>();
 
     // ---- query fragments (B operand of the score MMA) ----
     uint32_t qB[NJ][2];
@@ -345,16 +400,16 @@ __device__ void mma_blocks(const KiviGeom &g, const KiviDev &dv, const __half *q
                 a0 = *reinterpret_cast<const uint32_t *>(sKsz + gq * D + 16 * jj + 2 * tq);
                 a2 = *reinterpret_cast<const uint32_t *>(sKsz + gq * D + 16 * jj + 8 + 2 * tq);
             }
-            mma16816(dc, a0, 0u, a2, 0u, odd ? 0u : qB[jj][0], odd ? 0u : qB[jj][1]);
+            mma16816(dc, a0, 0u, a2, 0u, qB[jj][0], qB[jj][1]);
         }
-        // corr[rp] for head tq = row(2rp+1) - off * row(2rp)   (rows held by lanes 4 row + tq)
-        float kcor[4];
+        // sum_c q_c z_c (row 2rp + 1) and sum_c q_c s_c (row 2rp) of group rp for
+        // head tq; rows are held by lanes 4 row + tq (column 2 tq)
+        float kz[4], ks[4];
 #pragma unroll
         for (int rp = 0; rp < 4; ++rp) {
-            if (rp > (3 >> sh)) { kcor[rp] = 0.f; continue; }
-            float zr = __shfl_sync(0xffffffffu, dc[0], ((2 * rp + 1) & 7) * 4 + tq);
-            float sr = __shfl_sync(0xffffffffu, dc[0], ((2 * rp) & 7) * 4 + tq);
-            kcor[rp] = zr - offK * sr;
+            if (rp > (3 >> sh)) { kz[rp] = ks[rp] = 0.f; continue; }
+            kz[rp] = __shfl_sync(0xffffffffu, dc[0], ((2 * rp + 1) & 7) * 4 + tq);
+            ks[rp] = __shfl_sync(0xffffffffu, dc[0], ((2 * rp) & 7) * 4 + tq);
         }
 
         // ---- scores ----
@@ -390,8 +445,8 @@ __device__ void mma_blocks(const KiviGeom &g, const KiviDev &dv, const __half *q
             for (int mm = 0; mm < 4; ++mm) {
                 const int rp = mm >> sh;
                 const int wi = (2 * mm) / CPHK, r0 = (2 * mm) % CPHK;
-                const uint32_t a0 = unpack<KB>(W[0][wi], r0), a1 = unpack<KB>(W[0][wi], r0 + 1);
-                const uint32_t a2 = unpack<KB>(W[1][wi], r0), a3 = unpack<KB>(W[1][wi], r0 + 1);
+                const uint32_t a0 = unpack<KB, true>(W[0][wi], r0), a1 = unpack<KB, true>(W[0][wi], r0 + 1);
+                const uint32_t a2 = unpack<KB, true>(W[1][wi], r0), a3 = unpack<KB, true>(W[1][wi], r0 + 1);
                 mma16816(sc[mm], a0, a1, a2, a3, b0[rp], b1[rp]);
             }
         }
@@ -401,9 +456,11 @@ __device__ void mma_blocks(const KiviGeom &g, const KiviDev &dv, const __half *q
         float mx = -INFINITY;
 #pragma unroll
         for (int mm = 0; mm < 4; ++mm) {
-            const float cr = kcor[mm >> sh];
-            p[mm][0] = (sc[mm][0] + sc[mm][1] + cr) * alpha;
-            p[mm][1] = (sc[mm][2] + sc[mm][3] + cr) * alpha;
+            // row g of tile mm reads field slot r0, row g + 8 slot r0 + 1
+            const int rp = mm >> sh, r0 = (2 * mm) % CPHK;
+            const float o0 = slot_offset<KB, true>(r0), o1 = slot_offset<KB, true>(r0 + 1);
+            p[mm][0] = (sc[mm][0] + sc[mm][1] + fmaf(-o0, ks[rp], kz[rp])) * alpha;
+            p[mm][1] = (sc[mm][2] + sc[mm][3] + fmaf(-o1, ks[rp], kz[rp])) * alpha;
             mx = fmaxf(mx, fmaxf(p[mm][0], p[mm][1]));
         }
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
@@ -420,19 +477,21 @@ __device__ void mma_blocks(const KiviGeom &g, const KiviDev &dv, const __half *q
             ps += p[mm][0] + p[mm][1];
         }
         lrun = lrun * scl + ps;
+        if (__any_sync(0xffffffffu, scl != 1.f)) {   // the running max moved for some head
 #pragma unroll
-        for (int mm = 0; mm < NJ; ++mm) {
-            oacc[mm][0] *= scl;
-            oacc[mm][1] *= scl;
-            oacc[mm][2] *= scl;
-            oacc[mm][3] *= scl;
-        }
+            for (int mm = 0; mm < NJ; ++mm) {
+                oacc[mm][0] *= scl;
+                oacc[mm][1] *= scl;
+                oacc[mm][2] *= scl;
+                oacc[mm][3] *= scl;
+            }
 #pragma unroll
-        for (int zt = 0; zt < 2; ++zt) {
-            zacc[zt][0] *= scl;
-            zacc[zt][1] *= scl;
-            zacc[zt][2] *= scl;
-            zacc[zt][3] *= scl;
+            for (int zt = 0; zt < 2; ++zt) {
+                zacc[zt][0] *= scl;
+                zacc[zt][1] *= scl;
+                zacc[zt][2] *= scl;
+                zacc[zt][3] *= scl;
+            }
         }
 
         // ---- weights times values, 16 tokens at a time ----
@@ -482,8 +541,8 @@ __device__ void mma_blocks(const KiviGeom &g, const KiviDev &dv, const __half *q
                 const int ci0 = 2 * mm;
                 const int w = ci0 / CPHV, r0 = ci0 % CPHV;
                 const uint32_t Wp0 = Wv[0 * NWV + w], Wp1 = Wv[1 * NWV + w];
-                const uint32_t a0 = unpack<VB>(Wp0, r0), a1 = unpack<VB>(Wp0, r0 + 1);
-                const uint32_t a2 = unpack<VB>(Wp1, r0), a3 = unpack<VB>(Wp1, r0 + 1);
+                const uint32_t a0 = unpack<VB, false>(Wp0, r0), a1 = unpack<VB, false>(Wp0, r0 + 1);
+                const uint32_t a2 = unpack<VB, false>(Wp1, r0), a3 = unpack<VB, false>(Wp1, r0 + 1);
                 const int gi = mm >> sh;
                 mma16816(oacc[mm], a0, a1, a2, a3, b0[gi], b1[gi]);
             }
@@ -542,11 +601,11 @@ __device__ void mma_blocks(const KiviGeom &g, const KiviDev &dv, const __half *q
         zr[zt][0] = zacc[zt][0] + zacc[zt][1];   // row zt*16 + gq
         zr[zt][1] = zacc[zt][2] + zacc[zt][3];   // row zt*16 + gq + 8
     }
-    float vcor[16];
+    float vz[16], vs[16];
 #pragma unroll
     for (int gi = 0; gi < 16; ++gi) {
         if (gi >= ngi) {
-            vcor[gi] = 0.f;
+            vz[gi] = vs[gi] = 0.f;
             continue;
         }
         const int rs = gi, rz = ngi + gi;   // rows of the scale / zero sums
@@ -556,7 +615,8 @@ __device__ void mma_blocks(const KiviGeom &g, const KiviDev &dv, const __half *q
         const float z_t1 = __shfl_sync(0xffffffffu, (rz & 8) ? zr[1][1] : zr[1][0], (rz & 7) * 4 + tq);
         const float ssum = rs < 16 ? s_t0 : s_t1;
         const float zsum = rz < 16 ? z_t0 : z_t1;
-        vcor[gi] = zsum - offV * ssum;
+        vz[gi] = zsum;
+        vs[gi] = ssum;
     }
     if (gq == 0) {
         wm[tq] = mrun;
@@ -564,9 +624,11 @@ __device__ void mma_blocks(const KiviGeom &g, const KiviDev &dv, const __half *q
     }
 #pragma unroll
     for (int mm = 0; mm < NJ; ++mm) {
-        const float cr = vcor[mm >> sh];
-        wo[tq * D + 16 * mm + gq] = oacc[mm][0] + oacc[mm][1] + cr;
-        wo[tq * D + 16 * mm + gq + 8] = oacc[mm][2] + oacc[mm][3] + cr;
+        // channel rows 16 mm + gq and + 8 read value field slots r0 and r0 + 1
+        const int gi = mm >> sh, r0 = (2 * mm) % CPHV;
+        const float o0 = slot_offset<VB, false>(r0), o1 = slot_offset<VB, false>(r0 + 1);
+        wo[tq * D + 16 * mm + gq] = oacc[mm][0] + oacc[mm][1] + fmaf(-o0, vs[gi], vz[gi]);
+        wo[tq * D + 16 * mm + gq + 8] = oacc[mm][2] + oacc[mm][3] + fmaf(-o1, vs[gi], vz[gi]);
     }
 }
 
@@ -579,7 +641,7 @@ __device__ void mma_blocks(const KiviGeom &g, const KiviDev &dv, const __half *q
 // CTA-level merge of warps and the last-CTA merge of splits.
 // ---------------------------------------------------------------------------
 template <int D, int KB, int VB, int SH>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(256, 2)
     decode_kernel(KiviGeom g, KiviDev dv, const __half *__restrict__ q, int hq,
                   __half *__restrict__ out, DecodePlan plan) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -609,7 +671,7 @@ __global__ void __launch_bounds__(256, 1)
     } else {
         const int t0 = nfull * KIVI_KBLK + (s - plan.splits) * KIVI_KBLK;
         const int t1 = min(T, t0 + KIVI_KBLK);
-        tail_tokens<D>(g, dv, q, hq, i, j, e0, nh, t0, t1, wm, wl, wo);
+        tail_tokens<D, KB, VB, SH>(g, dv, q, hq, i, j, e0, nh, t0, t1, wm, wl, wo);
     }
     __syncthreads();
 
