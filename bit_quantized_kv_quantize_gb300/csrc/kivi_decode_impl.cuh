@@ -117,55 +117,60 @@ __device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
 }
 
 // Unpack field r of both 16-bit halves of w as fp16 (off + code).  The field
-// is moved (by at most a few shifts shared between fields) to a mantissa
+// is moved (by a shift shared between fields, or none) to a mantissa
 // position p of an fp16 constant whose exponent makes bit p weigh 1, and
-// or-ed into it: the value is 2^(10 - p) + code.  Keys use p in {4, 6, 8}
-// (offsets 64, 16, 4), values p in {6, 8} (offsets 16, 4) so that the
-// offset, which the accumulator carries and the zero-point MMA removes
-// exactly, stays small against the value sums.  4-bit fields sit at p = 6.
+// or-ed into it: the value is 2^(10 - p) + code.
+//   keys:   p in {4, 6, 8} (offsets 64, 16, 4); the accumulator carries
+//           off * sum(q s), removed with the zero-point MMA's sum(q s) row;
+//           against score-sized sums this costs < 1e-4 relative.
+//   values: any p <= 8; the offset is subtracted in fp16 before the MMA
+//           (exact), because the weighted value sums can be far smaller
+//           than off * sum(p s).
 struct View {
     int shl, shr;          // shift left / right applied to the word
     uint32_t mask, magic;  // field mask at its target position, fp16 pattern of the offset
     float off;
 };
+__host__ __device__ constexpr View at_pos(int p, int width, int shl, int shr) {
+    // field of `width` bits at mantissa bit p; fp16 2^(10 - p) = exponent field 25 - p
+    return View{shl, shr, (((1u << width) - 1u) << p) * 0x10001u, (uint32_t)(25 - p) * 0x04000400u,
+                (float)(1 << (10 - p))};
+}
 template <int BITS, bool KEY>
 __host__ __device__ constexpr View view_of(int r) {
-    if (BITS == 4) {       // field bits [4r, 4r + 4) -> bits 6..9, offset 16
-        return r <= 1 ? View{6 - 4 * r, 0, 0x03C003C0u, 0x4C004C00u, 16.f}
-                      : View{0, 4 * r - 6, 0x03C003C0u, 0x4C004C00u, 16.f};
+    if (BITS == 4) {
+        if (KEY)   // field bits [4r, 4r + 4) -> bits 6..9, offset 16
+            return r <= 1 ? at_pos(6, 4, 6 - 4 * r, 0) : at_pos(6, 4, 0, 4 * r - 6);
+        // values: slots 0, 1 in place (p = 0, 4); slots 2, 3 shifted to p = 4
+        return r == 0 ? at_pos(0, 4, 0, 0) : (r == 1 ? at_pos(4, 4, 0, 0) : at_pos(4, 4, 0, 4 * r - 4));
     }
     // 2-bit field bits [2r, 2r + 2)
-    const View p4{0, 0, 0x00300030u, 0x54005400u, 64.f};   // target bits 4..5
-    const View p6{0, 0, 0x00C000C0u, 0x4C004C00u, 16.f};   // target bits 6..7
-    const View p8{0, 0, 0x03000300u, 0x44004400u, 4.f};    // target bits 8..9
     if (KEY) {
         switch (r) {
-        case 0: return View{4, 0, p4.mask, p4.magic, p4.off};
-        case 1: return View{4, 0, p6.mask, p6.magic, p6.off};
-        case 2: return p4;
-        case 3: return p6;
-        case 4: return p8;
-        case 5: return View{0, 6, p4.mask, p4.magic, p4.off};
-        case 6: return View{0, 6, p6.mask, p6.magic, p6.off};
-        default: return View{0, 6, p8.mask, p8.magic, p8.off};
+        case 0: return at_pos(4, 2, 4, 0);
+        case 1: return at_pos(6, 2, 4, 0);
+        case 2: return at_pos(4, 2, 0, 0);
+        case 3: return at_pos(6, 2, 0, 0);
+        case 4: return at_pos(8, 2, 0, 0);
+        case 5: return at_pos(4, 2, 0, 6);
+        case 6: return at_pos(6, 2, 0, 6);
+        default: return at_pos(8, 2, 0, 6);
         }
     }
-    switch (r) {
-    case 0: return View{8, 0, p8.mask, p8.magic, p8.off};
-    case 1: return View{4, 0, p6.mask, p6.magic, p6.off};
-    case 2: return View{4, 0, p8.mask, p8.magic, p8.off};
-    case 3: return p6;
-    case 4: return p8;
-    case 5: return View{0, 4, p6.mask, p6.magic, p6.off};
-    case 6: return View{0, 4, p8.mask, p8.magic, p8.off};
-    default: return View{0, 8, p6.mask, p6.magic, p6.off};
-    }
+    // values: slots 0..4 in place (p = 0, 2, 4, 6, 8); slots 5..7 via one shift
+    return r <= 4 ? at_pos(2 * r, 2, 0, 0) : at_pos(2 * r - 6, 2, 0, 6);
 }
 template <int BITS, bool KEY>
 __device__ __forceinline__ uint32_t unpack(uint32_t w, int r) {   // r folds to a constant once unrolled
     const View v = view_of<BITS, KEY>(r);
     const uint32_t x = v.shl ? (w << v.shl) : (v.shr ? (w >> v.shr) : w);
     return (x & v.mask) | v.magic;
+}
+// value fields: the exact code as fp16 (offset subtracted, exact)
+template <int BITS>
+__device__ __forceinline__ uint32_t unpack_exact(uint32_t w, int r) {
+    const View v = view_of<BITS, false>(r);
+    return h2u(__hsub2(u2h(unpack<BITS, false>(w, r)), u2h(v.magic)));
 }
 template <int BITS, bool KEY>
 __host__ __device__ constexpr float slot_offset(int r) { return view_of<BITS, KEY>(r).off; }
@@ -337,7 +342,6 @@ __device__ void mma_blocks(const KiviGeom &g, const KiviDev &dv, const __half *q
     constexpr int sh = SH;                  // log2(G / 16): M-tile m -> group m >> sh
     constexpr int ngi = (D / 16) >> SH;     // value channel groups (d / G)
     constexpr int nkrows = 2 * (SH >= 2 ? 1 : (4 >> SH));   // key scale/zero rows per block
-    constexpr int nzr = 2 * ngi;            // value scale/zero rows per 16-token block
     const float alpha = kLog2e * rsqrtf((float)D);
 
     // ---- query fragments (B operand of the score MMA) ----
@@ -358,7 +362,7 @@ __device__ void mma_blocks(const KiviGeom &g, const KiviDev &dv, const __half *q
     float oacc[NJ][4];
 #pragma unroll
     for (int mm = 0; mm < NJ; ++mm) oacc[mm][0] = oacc[mm][1] = oacc[mm][2] = oacc[mm][3] = 0.f;
-    float zacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float zacc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
     float mrun = -INFINITY, lrun = 0.f;
 
     const uint32_t *kc = dv.Kc + kc_slice(g, i, j);
@@ -485,13 +489,10 @@ __device__ void mma_blocks(const KiviGeom &g, const KiviDev &dv, const __half *q
                 oacc[mm][2] *= scl;
                 oacc[mm][3] *= scl;
             }
-#pragma unroll
-            for (int zt = 0; zt < 2; ++zt) {
-                zacc[zt][0] *= scl;
-                zacc[zt][1] *= scl;
-                zacc[zt][2] *= scl;
-                zacc[zt][3] *= scl;
-            }
+            zacc[0][0] *= scl;
+            zacc[0][1] *= scl;
+            zacc[0][2] *= scl;
+            zacc[0][3] *= scl;
         }
 
         // ---- weights times values, 16 tokens at a time ----
@@ -541,27 +542,25 @@ __device__ void mma_blocks(const KiviGeom &g, const KiviDev &dv, const __half *q
                 const int ci0 = 2 * mm;
                 const int w = ci0 / CPHV, r0 = ci0 % CPHV;
                 const uint32_t Wp0 = Wv[0 * NWV + w], Wp1 = Wv[1 * NWV + w];
-                const uint32_t a0 = unpack<VB, false>(Wp0, r0), a1 = unpack<VB, false>(Wp0, r0 + 1);
-                const uint32_t a2 = unpack<VB, false>(Wp1, r0), a3 = unpack<VB, false>(Wp1, r0 + 1);
+                const uint32_t a0 = unpack_exact<VB>(Wp0, r0), a1 = unpack_exact<VB>(Wp0, r0 + 1);
+                const uint32_t a2 = unpack_exact<VB>(Wp1, r0), a3 = unpack_exact<VB>(Wp1, r0 + 1);
                 const int gi = mm >> sh;
                 mma16816(oacc[mm], a0, a1, a2, a3, b0[gi], b1[gi]);
             }
-            // value zero-point rows: [s | z][gi][16 tokens]
+            // value zero points: rows [z][gi][16 tokens] (the codes entered exactly)
             const uint32_t bz0 = odd ? PL0 : PH0, bz1 = odd ? PL1 : PH1;
-#pragma unroll
-            for (int zt = 0; zt < 2; ++zt) {
-                if (zt * 16 >= nzr) continue;
-                const int r0 = zt * 16 + gq, r1 = r0 + 8;
+            {
+                const __half *zrow = vszk + ngi * 16;
                 uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-                if (r0 < nzr) {
-                    a0 = *reinterpret_cast<const uint32_t *>(vszk + r0 * 16 + 2 * tq);
-                    a2 = *reinterpret_cast<const uint32_t *>(vszk + r0 * 16 + 2 * tq + 8);
+                if (gq < ngi) {
+                    a0 = *reinterpret_cast<const uint32_t *>(zrow + gq * 16 + 2 * tq);
+                    a2 = *reinterpret_cast<const uint32_t *>(zrow + gq * 16 + 2 * tq + 8);
                 }
-                if (r1 < nzr) {
-                    a1 = *reinterpret_cast<const uint32_t *>(vszk + r1 * 16 + 2 * tq);
-                    a3 = *reinterpret_cast<const uint32_t *>(vszk + r1 * 16 + 2 * tq + 8);
+                if (gq + 8 < ngi) {
+                    a1 = *reinterpret_cast<const uint32_t *>(zrow + (gq + 8) * 16 + 2 * tq);
+                    a3 = *reinterpret_cast<const uint32_t *>(zrow + (gq + 8) * 16 + 2 * tq + 8);
                 }
-                mma16816(zacc[zt], a0, a1, a2, a3, bz0, bz1);
+                mma16816(zacc[0], a0, a1, a2, a3, bz0, bz1);
             }
         }
 
@@ -594,41 +593,21 @@ __device__ void mma_blocks(const KiviGeom &g, const KiviDev &dv, const __half *q
     lrun += __shfl_xor_sync(0xffffffffu, lrun, 4);
     lrun += __shfl_xor_sync(0xffffffffu, lrun, 8);
     lrun += __shfl_xor_sync(0xffffffffu, lrun, 16);
-    // value zero-point correction per channel group: z-row sum - off * s-row sum
-    float zr[2][2];
+    // value zero-point sums per channel group gi: row gi of zacc (column pair 2 tq)
+    const float zr0 = zacc[0][0] + zacc[0][1], zr1 = zacc[0][2] + zacc[0][3];
+    float vz[16];
 #pragma unroll
-    for (int zt = 0; zt < 2; ++zt) {
-        zr[zt][0] = zacc[zt][0] + zacc[zt][1];   // row zt*16 + gq
-        zr[zt][1] = zacc[zt][2] + zacc[zt][3];   // row zt*16 + gq + 8
-    }
-    float vz[16], vs[16];
-#pragma unroll
-    for (int gi = 0; gi < 16; ++gi) {
-        if (gi >= ngi) {
-            vz[gi] = vs[gi] = 0.f;
-            continue;
-        }
-        const int rs = gi, rz = ngi + gi;   // rows of the scale / zero sums
-        const float s_t0 = __shfl_sync(0xffffffffu, (rs & 8) ? zr[0][1] : zr[0][0], (rs & 7) * 4 + tq);
-        const float s_t1 = __shfl_sync(0xffffffffu, (rs & 8) ? zr[1][1] : zr[1][0], (rs & 7) * 4 + tq);
-        const float z_t0 = __shfl_sync(0xffffffffu, (rz & 8) ? zr[0][1] : zr[0][0], (rz & 7) * 4 + tq);
-        const float z_t1 = __shfl_sync(0xffffffffu, (rz & 8) ? zr[1][1] : zr[1][0], (rz & 7) * 4 + tq);
-        const float ssum = rs < 16 ? s_t0 : s_t1;
-        const float zsum = rz < 16 ? z_t0 : z_t1;
-        vz[gi] = zsum;
-        vs[gi] = ssum;
-    }
+    for (int gi = 0; gi < 16; ++gi)
+        vz[gi] = gi < ngi ? __shfl_sync(0xffffffffu, gi < 8 ? zr0 : zr1, (gi & 7) * 4 + tq) : 0.f;
     if (gq == 0) {
         wm[tq] = mrun;
         wl[tq] = lrun;
     }
 #pragma unroll
     for (int mm = 0; mm < NJ; ++mm) {
-        // channel rows 16 mm + gq and + 8 read value field slots r0 and r0 + 1
-        const int gi = mm >> sh, r0 = (2 * mm) % CPHV;
-        const float o0 = slot_offset<VB, false>(r0), o1 = slot_offset<VB, false>(r0 + 1);
-        wo[tq * D + 16 * mm + gq] = oacc[mm][0] + oacc[mm][1] + fmaf(-o0, vs[gi], vz[gi]);
-        wo[tq * D + 16 * mm + gq + 8] = oacc[mm][2] + oacc[mm][3] + fmaf(-o1, vs[gi], vz[gi]);
+        const int gi = mm >> sh;
+        wo[tq * D + 16 * mm + gq] = oacc[mm][0] + oacc[mm][1] + vz[gi];
+        wo[tq * D + 16 * mm + gq + 8] = oacc[mm][2] + oacc[mm][3] + vz[gi];
     }
 }
 
