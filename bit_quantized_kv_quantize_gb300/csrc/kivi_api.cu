@@ -32,6 +32,8 @@ std::set<void *> g_live;
 
 }  // namespace
 
+void kivi_set_last_error(const char *msg) { snprintf(g_err, sizeof g_err, "%s", msg ? msg : ""); }
+
 struct kivi_cache {
     uint32_t magic;
     bool poisoned;

@@ -185,6 +185,9 @@ struct DecodePlan {
     int launches;    // kernel launches per decode call
 };
 
+// Sets the calling thread's text for kivi_last_error() (kivi_api.cu).
+void kivi_set_last_error(const char *msg);
+
 cudaError_t kivi_launch_prefill(const KiviGeom &g, const KiviDev &dv, const __half *K,
                                 const __half *V, const SeqLens &lens, int t_stride,
                                 cudaStream_t st);

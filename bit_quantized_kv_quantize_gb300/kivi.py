@@ -21,7 +21,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "capacity exceede
 EXPORTS = ["kivi_cache_create", "kivi_cache_destroy", "kivi_prefill", "kivi_append",
            "kivi_decode_attn", "kivi_cache_lengths", "kivi_cache_export_sizes",
            "kivi_cache_export", "kivi_cache_check", "kivi_profile_enable", "kivi_profile_read",
-           "kivi_decode_plan", "kivi_status_str", "kivi_last_error", "kivi_abi_version"]
+           "kivi_decode_plan", "kivi_status_str", "kivi_last_error", "kivi_abi_version",
+           "kivi_decode_attn_noalloc"]
 
 
 class KiviError(RuntimeError):

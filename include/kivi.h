@@ -151,6 +151,35 @@ kivi_status kivi_profile_read(kivi_cache_t c, double *total_ms, int *launches);
  * NULL): splits per (sequence, kv head) and kernel launches per call. */
 kivi_status kivi_decode_plan(kivi_cache_t c, int *splits, int *launches);
 
+/* A packed cache held in caller-owned device memory, in the format that
+ * kivi_cache_export documents (arrays and fcap as there), with the
+ * per-sequence counters as DEVICE int32 arrays of b entries. */
+typedef struct {
+    int b, h_kv, d, k_bits, v_bits, G, R, max_tokens;
+    const void *Kc, *Ksz, *Vc, *Vsz, *Kf, *Vf;   /* device, 16-byte aligned */
+    const int32_t *T, *Tqk, *Tqv;                 /* device counters */
+} kivi_packed_cache;
+
+/* Decode attention that allocates nothing.  (The pages have no counterpart:
+ * this is a library service for callers that cannot call cudaMalloc, e.g.
+ * code running while a framework's memory pool owns the device memory, in
+ * an allocator callback, or under a real-time budget that forbids device
+ * allocation after start-up.)  Computes exactly what kivi_decode_attn
+ * computes, over the cache described by *cache; q and out as there.
+ * Its scratch (split partials, merge tickets, status word) lives in one
+ * fixed 16 MiB __device__ array inside the library, which every GPU that
+ * loads the library holds until the process exits; shapes whose scratch
+ * b * h_q * (splits + tails) * (d + 2) * 4 bytes plus tickets exceed it are
+ * rejected with KIVI_ERR_UNSUPPORTED and a kivi_last_error() message.  The
+ * call launches on `stream` and clears the tickets itself; all calls share
+ * the array, so calls whose kernels overlap on the GPU race and must not be
+ * issued.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  No cudaMalloc, cudaFree or other allocating
+ * routine is called. */
+kivi_status kivi_decode_attn_noalloc(const kivi_packed_cache *cache, const void *q, int h_q,
+                                     void *out, kivi_stream_t stream);
+
 const char *kivi_status_str(kivi_status s);
 /* Text of the last error on the calling thread ("" if none). */
 const char *kivi_last_error(void);
