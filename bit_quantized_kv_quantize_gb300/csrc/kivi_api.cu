@@ -171,7 +171,7 @@ kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, in
     // decode partials per (sequence, query head): tensor-core splits of at
     // least kivi_min_blocks_per_split() blocks, plus the tail CTAs
     g.smax = (g.nkb + kivi_min_blocks_per_split() - 1) / kivi_min_blocks_per_split() +
-             (R + 2 * KIVI_KBLK - 1) / KIVI_KBLK + 2;
+             (R + KIVI_KBLK + KIVI_TAILBLK - 1) / KIVI_TAILBLK + 2;
     c->T.assign(b, 0);
     c->Tqk.assign(b, 0);
     c->Tqv.assign(b, 0);

@@ -37,7 +37,8 @@ DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *Tqk, const int
     DecodePlan p;
     const int hg = hq / g.h;
     p.qgroups = (hg + 3) / 4;
-    p.tails = (g.R + 2 * KIVI_KBLK - 1) / KIVI_KBLK;
+    // the tail spans at most R + 1 fp16 tokens plus 63 of a partly fp16 block
+    p.tails = (g.R + KIVI_KBLK + KIVI_TAILBLK - 1) / KIVI_TAILBLK;
     // Two CTAs per SM (the kernel is compiled for <= 128 registers a thread):
     // each CTA gets ~110 KB of shared memory for its warps' rings of stages.
     const int sb = stage_bytes(g);

@@ -160,11 +160,33 @@ __host__ __device__ constexpr View view_of(int r) {
     // values: slots 0..4 in place (p = 0, 2, 4, 6, 8); slots 5..7 via one shift
     return r <= 4 ? at_pos(2 * r, 2, 0, 0) : at_pos(2 * r - 6, 2, 0, 6);
 }
-template <int BITS, bool KEY>
-__device__ __forceinline__ uint32_t unpack(uint32_t w, int r) {   // r folds to a constant once unrolled
-    const View v = view_of<BITS, KEY>(r);
+// (x & mask) | magic as one lop3 with both constants as immediates; the
+// plain C++ form compiles to two ALU instructions on this target.
+template <uint32_t MASK, uint32_t MAGIC>
+__device__ __forceinline__ uint32_t and_or(uint32_t x) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "n"(MASK), "n"(MAGIC));
+    return r;
+}
+template <int BITS, bool KEY, int R>
+__device__ __forceinline__ uint32_t unpack_t(uint32_t w) {
+    constexpr View v = view_of<BITS, KEY>(R);
     const uint32_t x = v.shl ? (w << v.shl) : (v.shr ? (w >> v.shr) : w);
-    return (x & v.mask) | v.magic;
+    return and_or<v.mask, v.magic>(x);
+}
+// runtime-looking slot index r (a constant once the caller's loops unroll)
+template <int BITS, bool KEY>
+__device__ __forceinline__ uint32_t unpack(uint32_t w, int r) {
+    switch (r) {
+    case 0: return unpack_t<BITS, KEY, 0>(w);
+    case 1: return unpack_t<BITS, KEY, 1>(w);
+    case 2: return unpack_t<BITS, KEY, 2>(w);
+    case 3: return unpack_t<BITS, KEY, 3>(w);
+    case 4: return unpack_t<BITS, KEY, (BITS == 2 ? 4 : 3)>(w);
+    case 5: return unpack_t<BITS, KEY, (BITS == 2 ? 5 : 3)>(w);
+    case 6: return unpack_t<BITS, KEY, (BITS == 2 ? 6 : 3)>(w);
+    default: return unpack_t<BITS, KEY, (BITS == 2 ? 7 : 3)>(w);
+    }
 }
 // value fields: the exact code as fp16 (offset subtracted, exact)
 template <int BITS>
@@ -181,13 +203,62 @@ __host__ __device__ constexpr float slot_offset(int r) { return view_of<BITS, KE
 // compile-time except R (one modulo per token).
 // ---------------------------------------------------------------------------
 template <int D, int KB, int VB, int SH>
-__device__ void tail_tokens(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, int i,
-                            int j, int e0, int nh, int t0, int t1, float *wm, float *wl, float *wo) {
+__device__ __forceinline__ void tail_load(const KiviGeom &g, const uint32_t *kc, const __half *ksz,
+                                          const __half *kf, const uint32_t *vc, const __half *vsz,
+                                          const __half *vf, int Tqk, int Tqv, int tau, int lane,
+                                          float (&kv)[D / 32], float (&vv)[D / 32]) {
     constexpr int CPL = D / 32;
     constexpr int G = 16 << SH;
     constexpr int CPHK = 16 / KB, NWK = KB / 2, CPHV = 16 / VB, NWV = D * VB / 128;
     constexpr int WLV = D * VB / 64, CSV = WLV < 4 ? WLV : 4;
     constexpr int KC_BLK = 2 * D * KB, VC_BLK = D * VB / 2, VSZ_BLK = 2 * (D / G) * 16;
+    if (tau < Tqk) {
+        const int kb = tau >> 6, pos = (tau & 63) >> 3, gg = tau & 7;
+        const int wi = pos / CPHK, r = pos % CPHK;
+        const __half *sz = ksz + (size_t)(tau / G) * 2 * D;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) {
+            const int c = lane + 32 * k;
+            const int u = (2 * (c >> 4) + ((c >> 3) & 1)) * NWK + wi;
+            const int L = 4 * gg + ((c & 7) >> 1);
+            const uint32_t w = __ldg(kc + (size_t)kb * KC_BLK + (u >> 2) * 128 + 4 * L + (u & 3));
+            const uint32_t code = (w >> (16 * (c & 1) + r * KB)) & ((1u << KB) - 1u);
+            kv[k] = (float)code * __half2float(sz[c]) + __half2float(sz[D + c]);
+        }
+    } else {
+        const __half *src = kf + (size_t)(tau % g.R) * D;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) kv[k] = __half2float(src[lane + 32 * k]);
+    }
+    if (tau < Tqv) {
+        const int vb = tau >> 4, tt = tau & 15;
+        const int p = tt >> 3, t = (tt & 7) >> 1, hi = tt & 1;
+        const __half *sz = vsz + (size_t)vb * VSZ_BLK;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) {
+            const int c = lane + 32 * k;
+            const int ci = c >> 3, w = ci / CPHV, r = ci % CPHV;
+            const int L = 4 * (c & 7) + t, u = p * NWV + w;
+            const uint32_t word = __ldg(vc + (size_t)vb * VC_BLK + (u / CSV) * 32 * CSV + L * CSV + (u % CSV));
+            const uint32_t code = (word >> (16 * hi + r * VB)) & ((1u << VB) - 1u);
+            const int gi = c / G;
+            vv[k] = (float)code * __half2float(sz[gi * 16 + tt]) + __half2float(sz[(D / G + gi) * 16 + tt]);
+        }
+    } else {
+        const __half *src = vf + (size_t)(tau % (g.R + 1)) * D;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) vv[k] = __half2float(src[lane + 32 * k]);
+    }
+}
+
+// Tail CTA: tokens [t0, t1) (at most KIVI_TAILBLK), one warp per token, lane
+// owns channels lane + 32 k; each warp loads all of its tokens before
+// computing so that their memory latencies overlap.
+template <int D, int KB, int VB, int SH>
+__device__ void tail_tokens(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, int i,
+                            int j, int e0, int nh, int t0, int t1, float *wm, float *wl, float *wo) {
+    constexpr int CPL = D / 32;
+    constexpr int TPW = 4;   // tokens per warp: KIVI_TAILBLK / 8 warps
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int hg = hq / g.h;
     const int Tqk = dv.Tqk[i], Tqv = dv.Tqv[i];
@@ -210,65 +281,38 @@ __device__ void tail_tokens(const KiviGeom &g, const KiviDev &dv, const __half *
     const uint32_t *vc = dv.Vc + vc_slice(g, i, j);
     const __half *vsz = dv.Vsz + vsz_slice(g, i, j);
     const __half *vf = dv.Vf + vf_slice(g, i, j);
-    for (int tau = t0 + warp; tau < t1; tau += nw) {
-        float kv[CPL], vv[CPL];
-        if (tau < Tqk) {
-            const int kb = tau >> 6, pos = (tau & 63) >> 3, gg = tau & 7;
-            const int wi = pos / CPHK, r = pos % CPHK;
-            const __half *sz = ksz + (size_t)(tau / G) * 2 * D;
+    for (int base = t0 + warp; base < t1; base += nw * TPW) {
+        float kv[TPW][CPL], vv[TPW][CPL];
 #pragma unroll
-            for (int k = 0; k < CPL; ++k) {
-                const int c = lane + 32 * k;
-                const int u = (2 * (c >> 4) + ((c >> 3) & 1)) * NWK + wi;
-                const int L = 4 * gg + ((c & 7) >> 1);
-                const uint32_t w = kc[(size_t)kb * KC_BLK + (u >> 2) * 128 + 4 * L + (u & 3)];
-                const uint32_t code = (w >> (16 * (c & 1) + r * KB)) & ((1u << KB) - 1u);
-                kv[k] = (float)code * __half2float(sz[c]) + __half2float(sz[D + c]);
+        for (int x = 0; x < TPW; ++x) {
+            const int tau = base + x * nw;
+            if (tau < t1)
+                tail_load<D, KB, VB, SH>(g, kc, ksz, kf, vc, vsz, vf, Tqk, Tqv, tau, lane, kv[x], vv[x]);
+        }
+#pragma unroll
+        for (int x = 0; x < TPW; ++x) {
+            if (base + x * nw >= t1) break;
+            float dot[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                dot[e] = 0.f;
+#pragma unroll
+                for (int k = 0; k < CPL; ++k) dot[e] = fmaf(qr[e][k], kv[x][k], dot[e]);
             }
-        } else {
-            const __half *src = kf + (size_t)(tau % g.R) * D;
 #pragma unroll
-            for (int k = 0; k < CPL; ++k) kv[k] = __half2float(src[lane + 32 * k]);
-        }
-        if (tau < Tqv) {
-            const int vb = tau >> 4, tt = tau & 15;
-            const int p = tt >> 3, t = (tt & 7) >> 1, hi = tt & 1;
-            const __half *sz = vsz + (size_t)vb * VSZ_BLK;
+            for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-            for (int k = 0; k < CPL; ++k) {
-                const int c = lane + 32 * k;
-                const int ci = c >> 3, w = ci / CPHV, r = ci % CPHV;
-                const int L = 4 * (c & 7) + t, u = p * NWV + w;
-                const uint32_t word = vc[(size_t)vb * VC_BLK + (u / CSV) * 32 * CSV + L * CSV + (u % CSV)];
-                const uint32_t code = (word >> (16 * hi + r * VB)) & ((1u << VB) - 1u);
-                const int gi = c / G;
-                vv[k] = (float)code * __half2float(sz[gi * 16 + tt]) + __half2float(sz[(D / G + gi) * 16 + tt]);
+                for (int e = 0; e < 4; ++e) dot[e] += __shfl_xor_sync(0xffffffffu, dot[e], o);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float mn = fmaxf(m[e], dot[e]);
+                const float corr = ex2(m[e] - mn);
+                const float p = ex2(dot[e] - mn);
+                l[e] = l[e] * corr + p;
+#pragma unroll
+                for (int k = 0; k < CPL; ++k) acc[e][k] = fmaf(p, vv[x][k], acc[e][k] * corr);
+                m[e] = mn;
             }
-        } else {
-            const __half *src = vf + (size_t)(tau % (g.R + 1)) * D;
-#pragma unroll
-            for (int k = 0; k < CPL; ++k) vv[k] = __half2float(src[lane + 32 * k]);
-        }
-        float dot[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            dot[e] = 0.f;
-#pragma unroll
-            for (int k = 0; k < CPL; ++k) dot[e] = fmaf(qr[e][k], kv[k], dot[e]);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) dot[e] += __shfl_xor_sync(0xffffffffu, dot[e], o);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float mn = fmaxf(m[e], dot[e]);
-            const float corr = ex2(m[e] - mn);
-            const float p = ex2(dot[e] - mn);
-            l[e] = l[e] * corr + p;
-#pragma unroll
-            for (int k = 0; k < CPL; ++k) acc[e][k] = fmaf(p, vv[k], acc[e][k] * corr);
-            m[e] = mn;
         }
     }
 #pragma unroll
@@ -639,17 +683,19 @@ __global__ void __launch_bounds__(256, 2)
     float *wres = reinterpret_cast<float *>(ring + warp * wstride);
     float *wm = wres, *wl = wres + 4, *wo = wres + 8;
 
+    // CTAs x < tails take the tail (dispatched first: short, latency-bound,
+    // they overlap the streaming CTAs); the rest stream whole blocks.
     const int s = blockIdx.x;
-    if (s < plan.splits) {
+    if (s >= plan.tails) {
         if (threadIdx.x < nw * plan.stages) mbar_init(bars + threadIdx.x, 1);
         fence_mbar_init();
         __syncthreads();
-        const int kb0 = s * plan.blocks_per, kb1 = min(nfull, kb0 + plan.blocks_per);
+        const int kb0 = (s - plan.tails) * plan.blocks_per, kb1 = min(nfull, kb0 + plan.blocks_per);
         mma_blocks<D, KB, VB, SH>(g, dv, q, hq, i, j, e0, nh, kb0, kb1, plan.stages, wstride, ring,
                                   bars, wm, wl, wo);
     } else {
-        const int t0 = nfull * KIVI_KBLK + (s - plan.splits) * KIVI_KBLK;
-        const int t1 = min(T, t0 + KIVI_KBLK);
+        const int t0 = nfull * KIVI_KBLK + s * KIVI_TAILBLK;
+        const int t1 = min(T, t0 + KIVI_TAILBLK);
         tail_tokens<D, KB, VB, SH>(g, dv, q, hq, i, j, e0, nh, t0, t1, wm, wl, wo);
     }
     __syncthreads();

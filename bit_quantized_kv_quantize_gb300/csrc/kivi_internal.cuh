@@ -17,6 +17,7 @@
 #define KIVI_MAX_QPERKV 8
 #define KIVI_KBLK 64   // tokens per key block
 #define KIVI_VBLK 16   // tokens per value block
+#define KIVI_TAILBLK 32  // tokens per decode tail CTA
 
 // status-word bits (also documented in kivi.h)
 #define KIVI_FLAG_COUNTER 1u

@@ -83,7 +83,7 @@ extern "C" kivi_status kivi_decode_attn_noalloc(const kivi_packed_cache *pc, con
     g.vc_blk = d * g.vbits / 2;
     g.vsz_blk = 2 * (d / G) * KIVI_VBLK;
     g.smax = (g.nkb + kivi_min_blocks_per_split() - 1) / kivi_min_blocks_per_split() +
-             (R + 2 * KIVI_KBLK - 1) / KIVI_KBLK + 2;
+             (R + KIVI_KBLK + KIVI_TAILBLK - 1) / KIVI_TAILBLK + 2;
 
     // Plan for the capacity (the counters stay on the device): every
     // sequence is taken as full, CTAs past a sequence's data end at once.
