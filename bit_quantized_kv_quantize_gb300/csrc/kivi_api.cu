@@ -168,10 +168,6 @@ kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, in
     g.kc_blk = 2 * d * k_bits;
     g.vc_blk = d * v_bits / 2;
     g.vsz_blk = 2 * (d / G) * KIVI_VBLK;
-    // decode partials per (sequence, query head): tensor-core splits of at
-    // least kivi_min_blocks_per_split() blocks, plus the tail CTAs
-    g.smax = (g.nkb + kivi_min_blocks_per_split() - 1) / kivi_min_blocks_per_split() +
-             (R + KIVI_KBLK + KIVI_TAILBLK - 1) / KIVI_TAILBLK + 2;
     c->T.assign(b, 0);
     c->Tqk.assign(b, 0);
     c->Tqv.assign(b, 0);
@@ -183,6 +179,9 @@ kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, in
         snprintf(g_err, sizeof g_err, "no CUDA device: %s", cudaGetErrorString(e));
         return KIVI_ERR_CUDA;
     }
+    // decode partials per (sequence, query head): one per persistent CTA that
+    // touches the pair (the plan keeps the count within this bound)
+    g.smax = kivi_partial_slots(b, h_kv, c->num_sms);
     KiviDev &dv = c->dv;
     memset(&dv, 0, sizeof dv);
     const size_t bh = (size_t)b * h_kv;
@@ -341,7 +340,9 @@ kivi_status kivi_decode_attn(kivi_cache_t c, const void *q, int h_q, void *out,
         set_err("q and out must be 16-byte aligned");
         return KIVI_ERR_INVALID_ARG;
     }
-    DecodePlan plan = kivi_plan_decode(c->g, h_q, c->Tqk.data(), c->Tqv.data(), c->num_sms);
+    DecodeUnits units;
+    DecodePlan plan = kivi_plan_decode(c->g, h_q, c->T.data(), c->Tqk.data(), c->Tqv.data(),
+                                       c->num_sms, &units);
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (c->profiling && c->nprof < kMaxProfile) {
         if ((int)c->ev.size() < 2 * (c->nprof + 1)) {
@@ -358,7 +359,7 @@ kivi_status kivi_decode_attn(kivi_cache_t c, const void *q, int h_q, void *out,
         }
     }
     cudaError_t e = kivi_launch_decode(c->g, c->dv, (const __half *)q, h_q, (__half *)out, plan,
-                                       (cudaStream_t)stream, e0, e1);
+                                       units, (cudaStream_t)stream, e0, e1);
     if (e != cudaSuccess) return fail_cuda(c, e, "decode_attn");
     c->last_plan = plan;
     return KIVI_OK;
@@ -462,7 +463,7 @@ kivi_status kivi_decode_plan(kivi_cache_t c, int *splits, int *launches) {
     g_err[0] = 0;
     kivi_status s = check_handle(c);
     if (s != KIVI_OK && s != KIVI_ERR_STATE) return s;
-    if (splits) *splits = c->last_plan.splits;
+    if (splits) *splits = c->last_plan.ctas;
     if (launches) *launches = c->last_plan.launches;
     return KIVI_OK;
 }

@@ -1,21 +1,23 @@
 // kivi_decode.cu -- launch planning and dispatch of the decode-attention
-// kernels (kivi_decode_impl.cuh, instantiated per head dimension in
+// kernel (kivi_decode_impl.cuh, instantiated per head dimension in
 // kivi_decode_d{64,128,256}.cu).
 //
-// The plan splits each (sequence, kv head) token axis into chunks of whole
-// 64-token blocks (split-K, one CTA each) so that the grid covers the GPU's
-// SMs several times over, and adds the tail CTAs that cover the last blocks
-// holding fp16 keys or values (at most R + 64 tokens).
+// The kernel is persistent: a fixed grid of CTAs (two per SM) splits the
+// work units of all (sequence, kv head, head group) pairs evenly, so every
+// CTA streams about the same number of bytes whatever the batch and context
+// lengths (no partial last wave).  A unit is one 64-token block; blocks that
+// hold fp16 window tokens (the last few of each sequence) read their window
+// rows through a chain of dependent loads and count MW units each.
 #include <cstdlib>
 
 #include "kivi_internal.cuh"
 
 cudaError_t kivi_launch_decode_d64(const KiviGeom &, const KiviDev &, const __half *, int, __half *,
-                                   const DecodePlan &, cudaStream_t);
+                                   const DecodePlan &, const DecodeUnits &, cudaStream_t);
 cudaError_t kivi_launch_decode_d128(const KiviGeom &, const KiviDev &, const __half *, int, __half *,
-                                    const DecodePlan &, cudaStream_t);
+                                    const DecodePlan &, const DecodeUnits &, cudaStream_t);
 cudaError_t kivi_launch_decode_d256(const KiviGeom &, const KiviDev &, const __half *, int, __half *,
-                                    const DecodePlan &, cudaStream_t);
+                                    const DecodePlan &, const DecodeUnits &, cudaStream_t);
 
 namespace {
 int env_int(const char *name, int dflt) {
@@ -29,65 +31,83 @@ int stage_bytes(const KiviGeom &g) {
     int ksz = (g.G >= KIVI_KBLK ? 1 : KIVI_KBLK / g.G) * 2 * g.d * 2;
     return g.kc_blk * 4 + ksz + 4 * g.vc_blk * 4 + 4 * g.vsz_blk * 2;
 }
+
+long long cta_of(long long u, long long U, int C) { return ((u + 1) * C - 1) / U; }
+
+constexpr int kCtasPerSm = 2;   // the kernel is compiled for <= 128 registers a thread
 }  // namespace
 
-int kivi_min_blocks_per_split() { return 8; }
+int kivi_partial_slots(int b, int h, int num_sms) {
+    const int cmax = num_sms * kCtasPerSm;
+    return (2 * cmax + b * h - 1) / (b * h) + 4;
+}
 
-DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *Tqk, const int *Tqv, int num_sms) {
+DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *T, const int *Tqk, const int *Tqv,
+                            int num_sms, DecodeUnits *units) {
     DecodePlan p;
     const int hg = hq / g.h;
     p.qgroups = (hg + 3) / 4;
-    // the tail spans at most R + 1 fp16 tokens plus 63 of a partly fp16 block
-    p.tails = (g.R + KIVI_KBLK + KIVI_TAILBLK - 1) / KIVI_TAILBLK;
-    // Two CTAs per SM (the kernel is compiled for <= 128 registers a thread):
-    // each CTA gets ~110 KB of shared memory for its warps' rings of stages.
+    p.launches = 1;
+    // shared memory: two CTAs per SM, ~110 KB each for the warps' rings of at
+    // least two stages
     const int sb = stage_bytes(g);
     const int budget = env_int("KIVI_DECODE_SMEM_KB", 110) * 1024;
     p.warps = env_int("KIVI_DECODE_WARPS", 8);
     if (p.warps > 8) p.warps = 8;
-    while (p.warps > 1 && budget / (p.warps * sb) < 2) p.warps /= 2;
+    while (p.warps > 1 && budget / (p.warps * sb) < 2) --p.warps;
     int stages = budget / (p.warps * sb);
-    stages = stages > 4 ? 4 : (stages < 1 ? 1 : stages);
+    stages = stages > 4 ? 4 : (stages < 2 ? 2 : stages);
     p.stages = env_int("KIVI_DECODE_STAGES", stages);
-    while (p.stages > 1 && (size_t)p.warps * p.stages * sb > 220 * 1024) --p.stages;
-    const size_t cta_smem = (size_t)p.warps * p.stages * sb + 1024;
-    int per_sm = (int)((227 * 1024) / cta_smem);
-    per_sm = per_sm > 2 ? 2 : (per_sm < 1 ? 1 : per_sm);
-    int nfull = 0;
+    while (p.stages > 2 && (size_t)p.warps * p.stages * sb > 220 * 1024) --p.stages;
+
+    // units per pair of each sequence
+    const int MW = env_int("KIVI_DECODE_MIXED_WEIGHT", 8);
+    units->mixed_weight = MW;
+    units->start[0] = 0;
     for (int i = 0; i < g.b; ++i) {
-        int n = (Tqk[i] < Tqv[i] ? Tqk[i] : Tqv[i]) / KIVI_KBLK;
-        nfull = n > nfull ? n : nfull;
+        const int nf = (Tqk[i] < Tqv[i] ? Tqk[i] : Tqv[i]) / KIVI_KBLK;
+        const int nb = (T[i] + KIVI_KBLK - 1) / KIVI_KBLK;
+        int w = nf + MW * (nb - nf);
+        if (w < 1) w = 1;   // an empty sequence still gets its (zero) output written
+        units->full[i] = nf;
+        units->start[i + 1] = units->start[i] + w;
     }
-    const long pairs = (long)g.b * g.h * p.qgroups;
-    const int waves = env_int("KIVI_DECODE_WAVES", 2);
-    const long slots = (long)num_sms * per_sm * waves;
-    int splits = (int)((slots + pairs - 1) / pairs);
-    if (splits < 1) splits = 1;
-    // blocks per split: a multiple of the warp count (warps get equal shares)
-    const int min_bp = env_int("KIVI_DECODE_MIN_BLOCKS", kivi_min_blocks_per_split());
-    int bp = nfull > 0 ? (nfull + splits - 1) / splits : 1;
-    if (bp < min_bp) bp = min_bp;
-    bp = (bp + p.warps - 1) / p.warps * p.warps;
-    splits = nfull > 0 ? (nfull + bp - 1) / bp : 0;
-    if (splits + p.tails > g.smax) {
-        bp = (nfull + (g.smax - p.tails) - 1) / (g.smax - p.tails);
-        splits = (nfull + bp - 1) / bp;
+    const long long HQG = (long long)g.h * p.qgroups;
+    units->total = HQG * units->start[g.b];
+    const long long U = units->total;
+    int C = env_int("KIVI_DECODE_CTAS", num_sms * kCtasPerSm);
+    if ((long long)C > U) C = (int)U;
+    // every pair's partials must fit the cache's slots
+    for (;;) {
+        int worst = 1;
+        for (int i = 0; i < g.b; ++i) {
+            const int w = units->start[i + 1] - units->start[i];
+            for (long long jq = 0; jq < HQG; ++jq) {
+                const long long P = HQG * units->start[i] + jq * w;
+                const int np = (int)(cta_of(P + w - 1, U, C) - cta_of(P, U, C) + 1);
+                worst = np > worst ? np : worst;
+            }
+        }
+        if (worst <= g.smax || C == 1) {
+            p.max_parts = worst;
+            break;
+        }
+        C = (int)((long long)C * g.smax / (worst + 1));
+        if (C < 1) C = 1;
     }
-    p.splits = splits;
-    p.blocks_per = bp;
-    p.launches = 1;
+    p.ctas = C;
     return p;
 }
 
 cudaError_t kivi_launch_decode(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq,
-                               __half *out, const DecodePlan &plan, cudaStream_t st,
-                               cudaEvent_t ev0, cudaEvent_t ev1) {
+                               __half *out, const DecodePlan &plan, const DecodeUnits &units,
+                               cudaStream_t st, cudaEvent_t ev0, cudaEvent_t ev1) {
     if (ev0) cudaEventRecord(ev0, st);
     cudaError_t e;
     switch (g.d) {
-    case 64: e = kivi_launch_decode_d64(g, dv, q, hq, out, plan, st); break;
-    case 128: e = kivi_launch_decode_d128(g, dv, q, hq, out, plan, st); break;
-    default: e = kivi_launch_decode_d256(g, dv, q, hq, out, plan, st); break;
+    case 64: e = kivi_launch_decode_d64(g, dv, q, hq, out, plan, units, st); break;
+    case 128: e = kivi_launch_decode_d128(g, dv, q, hq, out, plan, units, st); break;
+    default: e = kivi_launch_decode_d256(g, dv, q, hq, out, plan, units, st); break;
     }
     if (ev1) cudaEventRecord(ev1, st);
     return e;

@@ -1,4 +1,5 @@
-// kivi_decode_impl.cuh -- split-K decode attention over the quantized cache.
+// kivi_decode_impl.cuh -- persistent split-K decode attention over the
+// quantized cache.
 //
 // Method: "Literature audit -- Group 2", section 1 KIVI, core algorithm
 // item 5: scores q.k / sqrt(d) over the quantized keys followed by the fp16
@@ -6,28 +7,27 @@
 // followed by the fp16 values.  Query head i reads kv head i / (h_q / h_kv)
 // (GQA, README note of 2025-01-18 in the same section).
 //
-// Work split.  A CTA owns one (sequence, kv head, group of <= 4 query heads)
-// and a token range, so each packed word is read from HBM once.  Full 64-token
-// blocks whose keys AND values are quantized go through the tensor-core path:
-// each warp streams its blocks through a private ring of shared-memory stages
-// filled by bulk TMA copies (cp.async.bulk + mbarrier) and runs
-//   scores   S[tok, col] = sum_c (4 + code) * B[c, col]      (m16n8k16, f16 in, f32 acc)
-//   values   O[ch, col]  = sum_t (4 + code) * P[t, col]
-// with the unpacked code in the A operand (one shift + one lop3 per half2:
-// the 2-bit field lands in the top mantissa bits of fp16 4.0, the 4-bit field
-// in those of 16.0) and the per-group scale folded into B.  Column pairs
-// (2e, 2e+1) carry an exact two-term fp16 split of B for query head e:
+// Work split.  The grid is persistent (two CTAs per SM).  The 64-token blocks
+// of every (sequence, kv head, group of <= 4 query heads) are laid end to end
+// as work units and each CTA takes an equal contiguous share, so all CTAs
+// stream about the same number of bytes.  Inside a CTA, each warp streams its
+// blocks through a private ring of shared-memory stages filled by bulk TMA
+// copies (cp.async.bulk + mbarrier) and runs
+//   scores   S[tok, col] = sum_c (off + code) * B[c, col]   (m16n8k16, f16 in, f32 acc)
+//   values   O[ch, col]  = sum_t code * P[t, col]
+// with the unpacked code in the A operand (one lop3, sometimes after a shift:
+// the field becomes mantissa bits of an fp16 constant) and the per-group
+// scale folded into B.  Column pairs (2e, 2e+1) carry an exact two-term fp16
+// split of B for query head e:
 //   keys:   q_c s = hi + lo with hi = RN(q s), lo = fma(q, s, -hi)  (exact)
 //   values: p s  = hi + lo from p = ph + pl (fp16 hi/lo of the fp32 weight)
-// so the tensor-core sums carry fp32-level precision.  The zero points and
-// the +4 / +16 offset enter through small MMAs over the scale/zero rows:
-//   keys:   corr[g, e] = sum_c q_c z_c - off sum_c q_c s_c
-//   values: corr[gi, e] = sum_t p_t z_t - off sum_t p_t s_t
-// Blocks holding fp16 keys or values (the residual window) form a short tail
-// handled on CUDA cores by extra CTAs.  Every CTA writes (m, l, acc[d]) in
-// base 2 (scores pre-multiplied by log2(e) / sqrt(d)); the last CTA of each
-// (sequence, kv head, head group) merges the partials with log-sum-exp
-// weights and writes the fp16 output.
+// so the tensor-core sums carry fp32-level precision.  The zero points (and
+// the key offset) enter through small MMAs over the scale/zero rows.  Blocks
+// that also hold tokens of the fp16 windows add, for those tokens, MMAs over
+// fp16 rows copied into shared memory.  Each CTA merges its warps per pair
+// and writes (m, l, acc[d]) in base 2 (scores pre-multiplied by
+// log2(e) / sqrt(d)); the last CTA to finish a pair merges its partials with
+// log-sum-exp weights and writes the fp16 output.
 #pragma once
 #include "kivi_internal.cuh"
 
@@ -197,137 +197,9 @@ __device__ __forceinline__ uint32_t unpack_exact(uint32_t w, int r) {
 template <int BITS, bool KEY>
 __host__ __device__ constexpr float slot_offset(int r) { return view_of<BITS, KEY>(r).off; }
 
-// ---------------------------------------------------------------------------
-// CUDA-core path for the tail (the last blocks, holding fp16 keys or values):
-// one warp per token, lane owns channels lane + 32 k.  Geometry is
-// compile-time except R (one modulo per token).
-// ---------------------------------------------------------------------------
-template <int D, int KB, int VB, int SH>
-__device__ __forceinline__ void tail_load(const KiviGeom &g, const uint32_t *kc, const __half *ksz,
-                                          const __half *kf, const uint32_t *vc, const __half *vsz,
-                                          const __half *vf, int Tqk, int Tqv, int tau, int lane,
-                                          float (&kv)[D / 32], float (&vv)[D / 32]) {
-    constexpr int CPL = D / 32;
-    constexpr int G = 16 << SH;
-    constexpr int CPHK = 16 / KB, NWK = KB / 2, CPHV = 16 / VB, NWV = D * VB / 128;
-    constexpr int WLV = D * VB / 64, CSV = WLV < 4 ? WLV : 4;
-    constexpr int KC_BLK = 2 * D * KB, VC_BLK = D * VB / 2, VSZ_BLK = 2 * (D / G) * 16;
-    if (tau < Tqk) {
-        const int kb = tau >> 6, pos = (tau & 63) >> 3, gg = tau & 7;
-        const int wi = pos / CPHK, r = pos % CPHK;
-        const __half *sz = ksz + (size_t)(tau / G) * 2 * D;
-#pragma unroll
-        for (int k = 0; k < CPL; ++k) {
-            const int c = lane + 32 * k;
-            const int u = (2 * (c >> 4) + ((c >> 3) & 1)) * NWK + wi;
-            const int L = 4 * gg + ((c & 7) >> 1);
-            const uint32_t w = __ldg(kc + (size_t)kb * KC_BLK + (u >> 2) * 128 + 4 * L + (u & 3));
-            const uint32_t code = (w >> (16 * (c & 1) + r * KB)) & ((1u << KB) - 1u);
-            kv[k] = (float)code * __half2float(sz[c]) + __half2float(sz[D + c]);
-        }
-    } else {
-        const __half *src = kf + (size_t)(tau % g.R) * D;
-#pragma unroll
-        for (int k = 0; k < CPL; ++k) kv[k] = __half2float(src[lane + 32 * k]);
-    }
-    if (tau < Tqv) {
-        const int vb = tau >> 4, tt = tau & 15;
-        const int p = tt >> 3, t = (tt & 7) >> 1, hi = tt & 1;
-        const __half *sz = vsz + (size_t)vb * VSZ_BLK;
-#pragma unroll
-        for (int k = 0; k < CPL; ++k) {
-            const int c = lane + 32 * k;
-            const int ci = c >> 3, w = ci / CPHV, r = ci % CPHV;
-            const int L = 4 * (c & 7) + t, u = p * NWV + w;
-            const uint32_t word = __ldg(vc + (size_t)vb * VC_BLK + (u / CSV) * 32 * CSV + L * CSV + (u % CSV));
-            const uint32_t code = (word >> (16 * hi + r * VB)) & ((1u << VB) - 1u);
-            const int gi = c / G;
-            vv[k] = (float)code * __half2float(sz[gi * 16 + tt]) + __half2float(sz[(D / G + gi) * 16 + tt]);
-        }
-    } else {
-        const __half *src = vf + (size_t)(tau % (g.R + 1)) * D;
-#pragma unroll
-        for (int k = 0; k < CPL; ++k) vv[k] = __half2float(src[lane + 32 * k]);
-    }
-}
-
-// Tail CTA: tokens [t0, t1) (at most KIVI_TAILBLK), one warp per token, lane
-// owns channels lane + 32 k; each warp loads all of its tokens before
-// computing so that their memory latencies overlap.
-template <int D, int KB, int VB, int SH>
-__device__ void tail_tokens(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, int i,
-                            int j, int e0, int nh, int t0, int t1, float *wm, float *wl, float *wo) {
-    constexpr int CPL = D / 32;
-    constexpr int TPW = 4;   // tokens per warp: KIVI_TAILBLK / 8 warps
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int hg = hq / g.h;
-    const int Tqk = dv.Tqk[i], Tqv = dv.Tqv[i];
-    const float qscale = kLog2e * rsqrtf((float)D);
-    float qr[4][CPL], m[4], l[4], acc[4][CPL];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        m[e] = -INFINITY;
-        l[e] = 0.f;
-#pragma unroll
-        for (int k = 0; k < CPL; ++k) {
-            acc[e][k] = 0.f;
-            qr[e][k] = e < nh ? __half2float(q[((size_t)i * hq + j * hg + e0 + e) * D + lane + 32 * k]) * qscale
-                              : 0.f;
-        }
-    }
-    const uint32_t *kc = dv.Kc + kc_slice(g, i, j);
-    const __half *ksz = dv.Ksz + ksz_slice(g, i, j);
-    const __half *kf = dv.Kf + kf_slice(g, i, j);
-    const uint32_t *vc = dv.Vc + vc_slice(g, i, j);
-    const __half *vsz = dv.Vsz + vsz_slice(g, i, j);
-    const __half *vf = dv.Vf + vf_slice(g, i, j);
-    for (int base = t0 + warp; base < t1; base += nw * TPW) {
-        float kv[TPW][CPL], vv[TPW][CPL];
-#pragma unroll
-        for (int x = 0; x < TPW; ++x) {
-            const int tau = base + x * nw;
-            if (tau < t1)
-                tail_load<D, KB, VB, SH>(g, kc, ksz, kf, vc, vsz, vf, Tqk, Tqv, tau, lane, kv[x], vv[x]);
-        }
-#pragma unroll
-        for (int x = 0; x < TPW; ++x) {
-            if (base + x * nw >= t1) break;
-            float dot[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                dot[e] = 0.f;
-#pragma unroll
-                for (int k = 0; k < CPL; ++k) dot[e] = fmaf(qr[e][k], kv[x][k], dot[e]);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) dot[e] += __shfl_xor_sync(0xffffffffu, dot[e], o);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float mn = fmaxf(m[e], dot[e]);
-                const float corr = ex2(m[e] - mn);
-                const float p = ex2(dot[e] - mn);
-                l[e] = l[e] * corr + p;
-#pragma unroll
-                for (int k = 0; k < CPL; ++k) acc[e][k] = fmaf(p, vv[x][k], acc[e][k] * corr);
-                m[e] = mn;
-            }
-        }
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        if (lane == 0) {
-            wm[e] = m[e];
-            wl[e] = l[e];
-        }
-#pragma unroll
-        for (int k = 0; k < CPL; ++k) wo[e * D + lane + 32 * k] = acc[e][k];
-    }
-}
 
 // ---------------------------------------------------------------------------
-// Tensor-core path over full blocks.
+// Shared-memory geometry
 // ---------------------------------------------------------------------------
 struct StageGeom {
     int kc_bytes, ksz_bytes, vc_bytes, vsz_bytes, bytes;
@@ -341,457 +213,746 @@ __host__ __device__ __forceinline__ StageGeom stage_geom(const KiviGeom &g) {
     s.bytes = s.kc_bytes + s.ksz_bytes + s.vc_bytes + s.vsz_bytes;
     return s;
 }
-
-// Bytes of one warp's region of the dynamic shared memory: its ring of
-// stages, which after the main loop also holds the warp's result
-// (m[4], l[4], o[4][d] in fp32).
+// One warp's region of dynamic shared memory: its ring of stages (a mixed
+// block's 16 x d fp16 tile goes into the next slot, which is kept free then);
+// at the end of a segment it also holds the warp's result (m[4], l[4],
+// o[4][d] in fp32).
 __host__ __device__ __forceinline__ size_t warp_region(const KiviGeom &g, int stages) {
-    size_t ring = (size_t)stages * stage_geom(g).bytes;
-    size_t res = ((size_t)(8 + 4 * g.d) * 4 + 127) / 128 * 128;
-    return ring > res ? ring : res;
+    const size_t sb = stage_geom(g).bytes;
+    size_t ring = (size_t)(stages >= 2 ? stages : 2) * sb;
+    size_t res = (size_t)(8 + 4 * g.d) * 4;
+    size_t m = ring > res ? ring : res;
+    return (m + 127) / 128 * 128;
 }
 __host__ __device__ __forceinline__ size_t bar_region(int warps, int stages) {
     return ((size_t)warps * stages * 8 + 127) / 128 * 128;
 }
 
+// Stage block kb: lanes 0-3 each issue one of its four bulk copies (packed
+// keys, key scale/zero rows, packed values, value scale/zero rows); lane 0
+// also arms the barrier (the order of arming and completion does not matter:
+// the phase needs lane 0's arrival).  Called by the whole warp.
 __device__ __forceinline__ void issue_block(const KiviGeom &g, const StageGeom &sg, unsigned char *st,
                                             uint64_t *bar, const uint32_t *kc, const __half *ksz,
                                             const uint32_t *vc, const __half *vsz, int kb) {
-    mbar_expect_tx(bar, (unsigned)sg.bytes);
+    const int lane = threadIdx.x & 31;
+    if (lane >= 4) return;
+    if (lane == 0) mbar_expect_tx(bar, (unsigned)sg.bytes);
     const int grp0 = g.G >= KIVI_KBLK ? (kb * KIVI_KBLK) / g.G : kb * (KIVI_KBLK / g.G);
-    bulk_g2s(st, kc + (size_t)kb * g.kc_blk, sg.kc_bytes, bar);
-    bulk_g2s(st + sg.kc_bytes, ksz + (size_t)grp0 * 2 * g.d, sg.ksz_bytes, bar);
-    bulk_g2s(st + sg.kc_bytes + sg.ksz_bytes, vc + (size_t)kb * 4 * g.vc_blk, sg.vc_bytes, bar);
-    bulk_g2s(st + sg.kc_bytes + sg.ksz_bytes + sg.vc_bytes, vsz + (size_t)kb * 4 * g.vsz_blk,
-             sg.vsz_bytes, bar);
+    const void *src;
+    unsigned off, bytes;
+    if (lane == 0) {
+        src = kc + (size_t)kb * g.kc_blk; off = 0; bytes = sg.kc_bytes;
+    } else if (lane == 1) {
+        src = ksz + (size_t)grp0 * 2 * g.d; off = sg.kc_bytes; bytes = sg.ksz_bytes;
+    } else if (lane == 2) {
+        src = vc + (size_t)kb * 4 * g.vc_blk; off = sg.kc_bytes + sg.ksz_bytes; bytes = sg.vc_bytes;
+    } else {
+        src = vsz + (size_t)kb * 4 * g.vsz_blk; off = sg.kc_bytes + sg.ksz_bytes + sg.vc_bytes;
+        bytes = sg.vsz_bytes;
+    }
+    bulk_g2s(st + off, src, bytes, bar);
 }
 
-template <int D, int KB, int VB, int SH>
-__device__ void mma_blocks(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, int i, int j,
-                           int e0, int nh, int kb_begin, int kb_end, int stages, size_t wstride,
-                           unsigned char *ring, uint64_t *bars, float *wm, float *wl, float *wo) {
-    constexpr int NJ = D / 16;              // k-steps over channels / M-tiles of channels
-    constexpr int NWK = KB / 2;             // key words per (j, hh) per lane
-    constexpr int CPHK = 16 / KB;           // key fields per 16-bit half
-    constexpr int CPHV = 16 / VB;           // value fields per 16-bit half
-    constexpr int NWV = D * VB / 128;       // value words per token pair per lane
-    constexpr int WLV = D * VB / 64;        // value words per lane per 16-token block
-    constexpr int CSV = WLV < 4 ? WLV : 4;  // value chunk size
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+// L2 prefetches for a block that will be read late: its packed data, and the
+// fp16 window rows [a, b) of a ring of `ring` rows (at most `ring` rows, so
+// at most one wrap).
+__device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void prefetch_block(const KiviGeom &g, const StageGeom &sg, const uint32_t *kc,
+                                               const __half *ksz, const uint32_t *vc, const __half *vsz,
+                                               int kb) {
+    const int grp0 = g.G >= KIVI_KBLK ? (kb * KIVI_KBLK) / g.G : kb * (KIVI_KBLK / g.G);
+    prefetch_l2(kc + (size_t)kb * g.kc_blk, sg.kc_bytes);
+    prefetch_l2(ksz + (size_t)grp0 * 2 * g.d, sg.ksz_bytes);
+    prefetch_l2(vc + (size_t)kb * 4 * g.vc_blk, sg.vc_bytes);
+    prefetch_l2(vsz + (size_t)kb * 4 * g.vsz_blk, sg.vsz_bytes);
+}
+template <int D>
+__device__ __forceinline__ void prefetch_rows(const __half *win, int ring, int a, int b) {
+    if (a >= b) return;
+    const int r0 = a % ring, n = b - a;
+    const int n1 = min(n, ring - r0);
+    prefetch_l2(win + (size_t)r0 * D, (unsigned)n1 * D * 2);
+    if (n > n1) prefetch_l2(win, (unsigned)(n - n1) * D * 2);
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+
+// ---------------------------------------------------------------------------
+// Per-warp running state of one (sequence, kv head, head group) segment.
+// Thread (gq, tq) owns query head tq's running max / sum and the output
+// accumulators of channel rows 16 mm + gq and + 8 (columns: tq hi, tq lo).
+// ---------------------------------------------------------------------------
+template <int D>
+struct WarpAcc {
+    float oacc[D / 16][4];
+    float zacc[4];
+    float mrun, lrun;
+};
+
+template <int D>
+__device__ __forceinline__ void acc_reset(WarpAcc<D> &A) {
+#pragma unroll
+    for (int mm = 0; mm < D / 16; ++mm) A.oacc[mm][0] = A.oacc[mm][1] = A.oacc[mm][2] = A.oacc[mm][3] = 0.f;
+    A.zacc[0] = A.zacc[1] = A.zacc[2] = A.zacc[3] = 0.f;
+    A.mrun = -INFINITY;
+    A.lrun = 0.f;
+}
+
+// Online softmax over the block: p[t][0..1] holds the scores (log2 units) of
+// rows gq and gq + 8 of tile t for head tq; on return it holds the weights
+// exp2(score - m).  At least one score of the block is finite.
+template <int D>
+__device__ __forceinline__ void softmax_update(WarpAcc<D> &A, float (&p)[4][2]) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) mx = fmaxf(mx, fmaxf(p[t][0], p[t][1]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float mnew = fmaxf(A.mrun, mx);
+    const float scl = ex2(A.mrun - mnew);
+    A.mrun = mnew;
+    float ps = 0.f;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        p[t][0] = ex2(p[t][0] - mnew);
+        p[t][1] = ex2(p[t][1] - mnew);
+        ps += p[t][0] + p[t][1];
+    }
+    A.lrun = A.lrun * scl + ps;
+    if (__any_sync(0xffffffffu, scl != 1.f)) {   // the running max moved for some head
+#pragma unroll
+        for (int mm = 0; mm < D / 16; ++mm) {
+            A.oacc[mm][0] *= scl;
+            A.oacc[mm][1] *= scl;
+            A.oacc[mm][2] *= scl;
+            A.oacc[mm][3] *= scl;
+        }
+        A.zacc[0] *= scl;
+        A.zacc[1] *= scl;
+        A.zacc[2] *= scl;
+        A.zacc[3] *= scl;
+    }
+}
+
+// Weights of tile rows (gq, gq + 8) for head tq -> B fragments of the P.V
+// MMA (k = tokens 2tq, 2tq+1 and 2tq+8, 2tq+9; column gq = head gq/2,
+// hi or lo), as fp16 hi and lo parts.
+struct PFrag {
+    uint32_t PH0, PH1, PL0, PL1;
+};
+__device__ __forceinline__ PFrag p_fragments(float p0, float p1, int tq, int eB) {
+    const __half2 ph = __floats2half2_rn(p0, p1);
+    const float2 phf = __half22float2(ph);
+    const __half2 pl = __floats2half2_rn(p0 - phf.x, p1 - phf.y);
+    const int src1 = 8 * tq + eB, src2 = 8 * tq + 4 + eB;
+    const uint32_t h1 = __shfl_sync(0xffffffffu, h2u(ph), src1);
+    const uint32_t h2 = __shfl_sync(0xffffffffu, h2u(ph), src2);
+    const uint32_t l1 = __shfl_sync(0xffffffffu, h2u(pl), src1);
+    const uint32_t l2 = __shfl_sync(0xffffffffu, h2u(pl), src2);
+    PFrag f;
+    f.PH0 = prmt(h1, h2, 0x5410u);
+    f.PH1 = prmt(h1, h2, 0x7632u);
+    f.PL0 = prmt(l1, l2, 0x5410u);
+    f.PL1 = prmt(l1, l2, 0x7632u);
+    return f;
+}
+
+// ---------------------------------------------------------------------------
+// One 64-token block, read from a shared-memory stage that a bulk TMA copy
+// filled with the block's packed codes and scale/zero rows.
+//
+// MIXED blocks also hold tokens of the fp16 windows (keys >= Tqk, values >=
+// Tqv) or run past the end T.  Their quantized tokens still go through the
+// packed path (value weights masked to the quantized tokens); each 16-token
+// tile with window tokens is copied as fp16 rows (swizzled 16-byte chunks,
+// other rows zero) into a free ring slot and multiplied from there with
+// ldmatrix fragments; scores past T are masked.
+// ---------------------------------------------------------------------------
+struct MixCtx {
+    int tb;                      // first token of the block
+    int T, Tqk, Tqv, R;
+    const __half *kwin, *vwin;   // fp16 windows of this (sequence, kv head)
+    __half *tile;                // 16 x d fp16 scratch in shared memory
+};
+
+// Copy rows [tau0, tau0 + 16) of an fp16 window into the swizzled tile: row r,
+// 16-byte chunk c lands at chunk c ^ (r & 7); rows outside [lo, T) are zero.
+// The copies are asynchronous (cp.async, zero-filled outside the rows), so
+// all of a lane's chunks are in flight together; the caller's __syncwarp
+// after the return publishes the tile to the other lanes.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+template <int D>
+__device__ __forceinline__ void stage_window(__half *tile, const __half *win, int ring, int tau0, int lo,
+                                             int T) {
+    constexpr int CPR = D / 8;
+    const int lane = threadIdx.x & 31;
+    const int r0 = tau0 >= 0 ? tau0 % ring : 0;
+#pragma unroll
+    for (int e = lane; e < 16 * CPR; e += 32) {
+        const int r = e / CPR, c = e % CPR;
+        const int tau = tau0 + r;
+        const bool ok = tau >= lo && tau < T;
+        int slot = r0 + r;
+        slot = slot >= ring ? slot - ring : slot;   // ring >= 16 rows: at most one wrap
+        cp_async16(tile + r * D + 8 * (c ^ (r & 7)), win + (size_t)(ok ? slot : 0) * D + 8 * c, ok);
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t keep_halves(uint32_t x, bool lo, bool hi) {
+    return x & ((lo ? 0x0000FFFFu : 0u) | (hi ? 0xFFFF0000u : 0u));
+}
+
+template <int D, int KB, int VB, int SH, bool MIXED>
+__device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D / 16][2],
+                                         const unsigned char *sb, const StageGeom &sg, const KiviGeom &g,
+                                         float alpha, const MixCtx &mx) {
+    constexpr int NJ = D / 16;
+    constexpr int CPHK = 16 / KB, NWK = KB / 2;
+    constexpr int CPHV = 16 / VB, NWV = D * VB / 128;
+    constexpr int WLV = D * VB / 64, CSV = WLV < 4 ? WLV : 4;
+    constexpr int sh = SH;
+    constexpr int ngi = (D / 16) >> SH;
+    constexpr int nkrows = 2 * (SH >= 2 ? 1 : (4 >> SH));
+    const int lane = threadIdx.x & 31;
     const int gq = lane >> 2, tq = lane & 3;
     const bool odd = gq & 1;
-    const int eB = gq >> 1;                 // query head of this thread's B column
-    const int hg = hq / g.h;
-    const StageGeom sg = stage_geom(g);
-    constexpr int sh = SH;                  // log2(G / 16): M-tile m -> group m >> sh
-    constexpr int ngi = (D / 16) >> SH;     // value channel groups (d / G)
-    constexpr int nkrows = 2 * (SH >= 2 ? 1 : (4 >> SH));   // key scale/zero rows per block
-    const float alpha = kLog2e * rsqrtf((float)D);
+    const int eB = gq >> 1;
+    const int mi = lane >> 3, rr = lane & 7;
+    const uint32_t nm = odd ? 0xBC00BC00u : 0u;   // -1 for lo columns, 0 for hi
+    const uint32_t m1 = odd ? 0x3C003C00u : 0u;   // 1 for lo columns, 0 for hi
+    const uint32_t *sK = reinterpret_cast<const uint32_t *>(sb);
+    const __half *sKsz = reinterpret_cast<const __half *>(sb + sg.kc_bytes);
+    const uint32_t *sV = reinterpret_cast<const uint32_t *>(sb + sg.kc_bytes + sg.ksz_bytes);
+    const __half *sVsz = reinterpret_cast<const __half *>(sb + sg.kc_bytes + sg.ksz_bytes + sg.vc_bytes);
 
-    // ---- query fragments (B operand of the score MMA) ----
-    uint32_t qB[NJ][2];
+    // ---- key zero points: sum_c q_c z_c and sum_c q_c s_c per group ----
+    float dc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int jj = 0; jj < NJ; ++jj)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            uint32_t v = 0;
-            if (eB < nh)
-                v = *reinterpret_cast<const uint32_t *>(
-                    q + ((size_t)i * hq + j * hg + e0 + eB) * D + 16 * jj + 8 * hh + 2 * tq);
-            qB[jj][hh] = v;
+    for (int jj = 0; jj < NJ; ++jj) {
+        uint32_t a0 = 0, a2 = 0;
+        if (gq < nkrows) {
+            a0 = *reinterpret_cast<const uint32_t *>(sKsz + gq * D + 16 * jj + 2 * tq);
+            a2 = *reinterpret_cast<const uint32_t *>(sKsz + gq * D + 16 * jj + 8 + 2 * tq);
         }
-    const uint32_t nm = odd ? 0xBC00BC00u : 0u;     // -1 for lo columns, 0 for hi
-    const uint32_t m1 = odd ? 0x3C003C00u : 0u;     // 1 for lo columns, 0 for hi
-
-    float oacc[NJ][4];
+        mma16816(dc, a0, 0u, a2, 0u, qB[jj][0], qB[jj][1]);
+    }
+    float kz[4], ks[4];
 #pragma unroll
-    for (int mm = 0; mm < NJ; ++mm) oacc[mm][0] = oacc[mm][1] = oacc[mm][2] = oacc[mm][3] = 0.f;
-    float zacc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-    float mrun = -INFINITY, lrun = 0.f;
+    for (int rp = 0; rp < 4; ++rp) {
+        if (rp > (3 >> sh)) { kz[rp] = ks[rp] = 0.f; continue; }
+        kz[rp] = __shfl_sync(0xffffffffu, dc[0], ((2 * rp + 1) & 7) * 4 + tq);
+        ks[rp] = __shfl_sync(0xffffffffu, dc[0], ((2 * rp) & 7) * 4 + tq);
+    }
 
-    const uint32_t *kc = dv.Kc + kc_slice(g, i, j);
-    const __half *ksz = dv.Ksz + ksz_slice(g, i, j);
-    const uint32_t *vc = dv.Vc + vc_slice(g, i, j);
-    const __half *vsz = dv.Vsz + vsz_slice(g, i, j);
-    unsigned char *myring = ring + (size_t)warp * wstride;
-    uint64_t *mybars = bars + warp * stages;
-
-    const int nb = kb_begin + warp < kb_end ? (kb_end - kb_begin - warp + nw - 1) / nw : 0;
-    int issued = nb < stages ? nb : stages;
-    if (lane == 0)
-        for (int it = 0; it < issued; ++it)
-            issue_block(g, sg, myring + (size_t)it * sg.bytes, mybars + it, kc, ksz, vc, vsz,
-                        kb_begin + warp + it * nw);
-    __syncwarp();
-
-    bool timed_out = false;
-    for (int it = 0; it < nb; ++it) {
-        const int st = it % stages;
-        const unsigned phase = (unsigned)(it / stages) & 1u;
-        if (!mbar_wait(mybars + st, phase)) {
-            timed_out = true;
-            break;
-        }
-        const unsigned char *sb = myring + (size_t)st * sg.bytes;
-        const uint32_t *sK = reinterpret_cast<const uint32_t *>(sb);
-        const __half *sKsz = reinterpret_cast<const __half *>(sb + sg.kc_bytes);
-        const uint32_t *sV = reinterpret_cast<const uint32_t *>(sb + sg.kc_bytes + sg.ksz_bytes);
-        const __half *sVsz =
-            reinterpret_cast<const __half *>(sb + sg.kc_bytes + sg.ksz_bytes + sg.vc_bytes);
-
-        // ---- key zero-point correction: rows = (group, s|z) of this block ----
-        float dc[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- scores from the packed keys ----
+    float sc[4][4];
 #pragma unroll
-        for (int jj = 0; jj < NJ; ++jj) {
-            uint32_t a0 = 0, a2 = 0;
-            if (gq < nkrows) {
-                a0 = *reinterpret_cast<const uint32_t *>(sKsz + gq * D + 16 * jj + 2 * tq);
-                a2 = *reinterpret_cast<const uint32_t *>(sKsz + gq * D + 16 * jj + 8 + 2 * tq);
-            }
-            mma16816(dc, a0, 0u, a2, 0u, qB[jj][0], qB[jj][1]);
+    for (int mm = 0; mm < 4; ++mm) sc[mm][0] = sc[mm][1] = sc[mm][2] = sc[mm][3] = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < NJ; ++jj) {
+        uint32_t W[2][NWK];
+        if (KB == 2) {
+            const uint4 w4 = *reinterpret_cast<const uint4 *>(sK + (jj >> 1) * 128 + lane * 4);
+            W[0][0] = (jj & 1) ? w4.z : w4.x;
+            W[1][0] = (jj & 1) ? w4.w : w4.y;
+        } else {
+            const uint4 w4 = *reinterpret_cast<const uint4 *>(sK + jj * 128 + lane * 4);
+            W[0][0] = w4.x;
+            W[0][NWK - 1] = w4.y;
+            W[1][0] = w4.z;
+            W[1][NWK - 1] = w4.w;
         }
-        // sum_c q_c z_c (row 2rp + 1) and sum_c q_c s_c (row 2rp) of group rp for
-        // head tq; rows are held by lanes 4 row + tq (column 2 tq)
-        float kz[4], ks[4];
+        uint32_t b0[4], b1[4];
 #pragma unroll
         for (int rp = 0; rp < 4; ++rp) {
-            if (rp > (3 >> sh)) { kz[rp] = ks[rp] = 0.f; continue; }
-            kz[rp] = __shfl_sync(0xffffffffu, dc[0], ((2 * rp + 1) & 7) * 4 + tq);
-            ks[rp] = __shfl_sync(0xffffffffu, dc[0], ((2 * rp) & 7) * 4 + tq);
+            b0[rp] = b1[rp] = 0u;
+            if (rp > (3 >> sh)) continue;   // groups present in this block
+            const uint32_t s0 = *reinterpret_cast<const uint32_t *>(sKsz + 2 * rp * D + 16 * jj + 2 * tq);
+            const uint32_t s1 = *reinterpret_cast<const uint32_t *>(sKsz + 2 * rp * D + 16 * jj + 8 + 2 * tq);
+            const uint32_t h0 = hmul2u(qB[jj][0], s0), h1 = hmul2u(qB[jj][1], s1);
+            b0[rp] = hfma2u(qB[jj][0], s0, hmul2u(h0, nm));
+            b1[rp] = hfma2u(qB[jj][1], s1, hmul2u(h1, nm));
         }
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm) {
+            const int rp = mm >> sh;
+            const int wi = (2 * mm) / CPHK, r0 = (2 * mm) % CPHK;
+            const uint32_t a0 = unpack<KB, true>(W[0][wi], r0), a1 = unpack<KB, true>(W[0][wi], r0 + 1);
+            const uint32_t a2 = unpack<KB, true>(W[1][wi], r0), a3 = unpack<KB, true>(W[1][wi], r0 + 1);
+            mma16816(sc[mm], a0, a1, a2, a3, b0[rp], b1[rp]);
+        }
+    }
+    float p[4][2];
+#pragma unroll
+    for (int mm = 0; mm < 4; ++mm) {
+        // row gq of tile mm reads field slot r0, row gq + 8 slot r0 + 1
+        const int rp = mm >> sh, r0 = (2 * mm) % CPHK;
+        const float o0 = slot_offset<KB, true>(r0), o1 = slot_offset<KB, true>(r0 + 1);
+        p[mm][0] = (sc[mm][0] + sc[mm][1] + fmaf(-o0, ks[rp], kz[rp])) * alpha;
+        p[mm][1] = (sc[mm][2] + sc[mm][3] + fmaf(-o1, ks[rp], kz[rp])) * alpha;
+    }
+    if (MIXED) {
+        // tiles of window keys (Tqk is a multiple of G >= 16: tiles are whole)
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm) {
+            const int tau0 = mx.tb + 16 * mm;
+            if (tau0 >= mx.Tqk && tau0 < mx.T) {
+                __syncwarp();
+                stage_window<D>(mx.tile, mx.kwin, mx.R, tau0, mx.Tqk, mx.T);
+                __syncwarp();
+                float f[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const int row = rr + 8 * (mi & 1), ch = 2 * jj + (mi >> 1);
+                    uint32_t a[4];
+                    ldsm_x4(a, mx.tile + row * D + 8 * (ch ^ (row & 7)));
+                    mma16816(f, a[0], a[1], a[2], a[3], odd ? 0u : qB[jj][0], odd ? 0u : qB[jj][1]);
+                }
+                p[mm][0] = f[0] * alpha;
+                p[mm][1] = f[2] * alpha;
+            }
+            if (tau0 + gq >= mx.T) p[mm][0] = -INFINITY;
+            if (tau0 + gq + 8 >= mx.T) p[mm][1] = -INFINITY;
+        }
+    }
+    softmax_update<D>(A, p);
 
-        // ---- scores ----
-        float sc[4][4];
+    // ---- weights times values, 16 tokens at a time ----
 #pragma unroll
-        for (int mm = 0; mm < 4; ++mm) sc[mm][0] = sc[mm][1] = sc[mm][2] = sc[mm][3] = 0.f;
+    for (int kk = 0; kk < 4; ++kk) {
+        const PFrag f = p_fragments(p[kk][0], p[kk][1], tq, eB);
+        // weights of quantized value tokens (tokens 2tq, 2tq+1 | 2tq+8, 2tq+9)
+        uint32_t PH0 = f.PH0, PH1 = f.PH1, PL0 = f.PL0, PL1 = f.PL1;
+        if (MIXED) {
+            const int tk = mx.tb + 16 * kk + 2 * tq;
+            const bool q0 = tk < mx.Tqv, q1 = tk + 1 < mx.Tqv, q8 = tk + 8 < mx.Tqv, q9 = tk + 9 < mx.Tqv;
+            PH0 = keep_halves(PH0, q0, q1);
+            PL0 = keep_halves(PL0, q0, q1);
+            PH1 = keep_halves(PH1, q8, q9);
+            PL1 = keep_halves(PL1, q8, q9);
+        }
+        const uint32_t PL0m = hmul2u(PL0, m1), PL1m = hmul2u(PL1, m1);
+        const __half *vszk = sVsz + kk * g.vsz_blk;
+        uint32_t b0[16], b1[16];
 #pragma unroll
-        for (int jj = 0; jj < NJ; ++jj) {
-            uint32_t W[2][NWK];   // [hh][wi]
-            if (KB == 2) {
-                const uint4 w4 = *reinterpret_cast<const uint4 *>(sK + (jj >> 1) * 128 + lane * 4);
-                W[0][0] = (jj & 1) ? w4.z : w4.x;
-                W[1][0] = (jj & 1) ? w4.w : w4.y;
+        for (int gi = 0; gi < 16; ++gi) {
+            b0[gi] = b1[gi] = 0u;
+            if (gi >= ngi) continue;
+            const uint32_t v0 = *reinterpret_cast<const uint32_t *>(vszk + gi * 16 + 2 * tq);
+            const uint32_t v1 = *reinterpret_cast<const uint32_t *>(vszk + gi * 16 + 2 * tq + 8);
+            const uint32_t h0 = hmul2u(PH0, v0), hh1 = hmul2u(PH1, v1);
+            b0[gi] = hfma2u(PL0m, v0, hfma2u(PH0, v0, hmul2u(h0, nm)));
+            b1[gi] = hfma2u(PL1m, v1, hfma2u(PH1, v1, hmul2u(hh1, nm)));
+        }
+        uint32_t Wv[WLV];
+        const uint32_t *sVk = sV + kk * g.vc_blk;
+#pragma unroll
+        for (int ch = 0; ch < WLV / CSV; ++ch) {
+            if (CSV == 4) {
+                const uint4 w4 = *reinterpret_cast<const uint4 *>(sVk + ch * 128 + lane * 4);
+                Wv[ch * 4 + 0] = w4.x;
+                Wv[ch * 4 + 1] = w4.y;
+                Wv[ch * 4 + 2] = w4.z;
+                Wv[ch * 4 + 3] = w4.w;
             } else {
-                const uint4 w4 = *reinterpret_cast<const uint4 *>(sK + jj * 128 + lane * 4);
-                W[0][0] = w4.x;
-                W[0][NWK - 1] = w4.y;
-                W[1][0] = w4.z;
-                W[1][NWK - 1] = w4.w;
-            }
-            uint32_t b0[4], b1[4];
-#pragma unroll
-            for (int rp = 0; rp < 4; ++rp) {
-                if (rp > (3 >> sh)) continue;   // groups present in this block
-                b0[rp] = b1[rp] = 0u;
-                const uint32_t s0 = *reinterpret_cast<const uint32_t *>(sKsz + 2 * rp * D + 16 * jj + 2 * tq);
-                const uint32_t s1 = *reinterpret_cast<const uint32_t *>(sKsz + 2 * rp * D + 16 * jj + 8 + 2 * tq);
-                const uint32_t h0 = hmul2u(qB[jj][0], s0), h1 = hmul2u(qB[jj][1], s1);
-                b0[rp] = hfma2u(qB[jj][0], s0, hmul2u(h0, nm));
-                b1[rp] = hfma2u(qB[jj][1], s1, hmul2u(h1, nm));
-            }
-#pragma unroll
-            for (int mm = 0; mm < 4; ++mm) {
-                const int rp = mm >> sh;
-                const int wi = (2 * mm) / CPHK, r0 = (2 * mm) % CPHK;
-                const uint32_t a0 = unpack<KB, true>(W[0][wi], r0), a1 = unpack<KB, true>(W[0][wi], r0 + 1);
-                const uint32_t a2 = unpack<KB, true>(W[1][wi], r0), a3 = unpack<KB, true>(W[1][wi], r0 + 1);
-                mma16816(sc[mm], a0, a1, a2, a3, b0[rp], b1[rp]);
+                const uint2 w2 = *reinterpret_cast<const uint2 *>(sVk + ch * 64 + lane * 2);
+                Wv[ch * 2 + 0] = w2.x;
+                Wv[ch * 2 + 1] = w2.y;
             }
         }
-
-        // ---- online softmax (head tq; rows 16 mm + gq and + 8) ----
-        float p[4][2];
-        float mx = -INFINITY;
 #pragma unroll
-        for (int mm = 0; mm < 4; ++mm) {
-            // row g of tile mm reads field slot r0, row g + 8 slot r0 + 1
-            const int rp = mm >> sh, r0 = (2 * mm) % CPHK;
-            const float o0 = slot_offset<KB, true>(r0), o1 = slot_offset<KB, true>(r0 + 1);
-            p[mm][0] = (sc[mm][0] + sc[mm][1] + fmaf(-o0, ks[rp], kz[rp])) * alpha;
-            p[mm][1] = (sc[mm][2] + sc[mm][3] + fmaf(-o1, ks[rp], kz[rp])) * alpha;
-            mx = fmaxf(mx, fmaxf(p[mm][0], p[mm][1]));
+        for (int mm = 0; mm < NJ; ++mm) {
+            const int ci0 = 2 * mm;
+            const int w = ci0 / CPHV, r0 = ci0 % CPHV;
+            const uint32_t Wp0 = Wv[0 * NWV + w], Wp1 = Wv[1 * NWV + w];
+            const uint32_t a0 = unpack_exact<VB>(Wp0, r0), a1 = unpack_exact<VB>(Wp0, r0 + 1);
+            const uint32_t a2 = unpack_exact<VB>(Wp1, r0), a3 = unpack_exact<VB>(Wp1, r0 + 1);
+            mma16816(A.oacc[mm], a0, a1, a2, a3, b0[mm >> sh], b1[mm >> sh]);
         }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float mnew = fmaxf(mrun, mx);
-        const float scl = ex2(mrun - mnew);
-        mrun = mnew;
-        float ps = 0.f;
-#pragma unroll
-        for (int mm = 0; mm < 4; ++mm) {
-            p[mm][0] = ex2(p[mm][0] - mnew);
-            p[mm][1] = ex2(p[mm][1] - mnew);
-            ps += p[mm][0] + p[mm][1];
+        // value zero points: rows [z][gi][16 tokens] (the codes entered exactly)
+        const uint32_t bz0 = odd ? PL0 : PH0, bz1 = odd ? PL1 : PH1;
+        const __half *zrow = vszk + ngi * 16;
+        uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+        if (gq < ngi) {
+            a0 = *reinterpret_cast<const uint32_t *>(zrow + gq * 16 + 2 * tq);
+            a2 = *reinterpret_cast<const uint32_t *>(zrow + gq * 16 + 2 * tq + 8);
         }
-        lrun = lrun * scl + ps;
-        if (__any_sync(0xffffffffu, scl != 1.f)) {   // the running max moved for some head
-#pragma unroll
-            for (int mm = 0; mm < NJ; ++mm) {
-                oacc[mm][0] *= scl;
-                oacc[mm][1] *= scl;
-                oacc[mm][2] *= scl;
-                oacc[mm][3] *= scl;
-            }
-            zacc[0][0] *= scl;
-            zacc[0][1] *= scl;
-            zacc[0][2] *= scl;
-            zacc[0][3] *= scl;
+        if (gq + 8 < ngi) {
+            a1 = *reinterpret_cast<const uint32_t *>(zrow + (gq + 8) * 16 + 2 * tq);
+            a3 = *reinterpret_cast<const uint32_t *>(zrow + (gq + 8) * 16 + 2 * tq + 8);
         }
-
-        // ---- weights times values, 16 tokens at a time ----
+        mma16816(A.zacc, a0, a1, a2, a3, bz0, bz1);
+        if (MIXED) {
+            // window value tokens of this tile: fp16 rows, A = rows transposed
+            const int tau0 = mx.tb + 16 * kk;
+            if (tau0 + 15 >= mx.Tqv && tau0 < mx.T) {
+                __syncwarp();
+                stage_window<D>(mx.tile, mx.vwin, mx.R + 1, tau0, mx.Tqv, mx.T);
+                __syncwarp();
+                const uint32_t c0 = odd ? f.PL0 : f.PH0, c1 = odd ? f.PL1 : f.PH1;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const __half2 ph = __floats2half2_rn(p[kk][0], p[kk][1]);
-            const float2 phf = __half22float2(ph);
-            const __half2 pl = __floats2half2_rn(p[kk][0] - phf.x, p[kk][1] - phf.y);
-            const int src1 = 8 * tq + eB, src2 = 8 * tq + 4 + eB;
-            const uint32_t h1 = __shfl_sync(0xffffffffu, h2u(ph), src1);
-            const uint32_t h2 = __shfl_sync(0xffffffffu, h2u(ph), src2);
-            const uint32_t l1 = __shfl_sync(0xffffffffu, h2u(pl), src1);
-            const uint32_t l2 = __shfl_sync(0xffffffffu, h2u(pl), src2);
-            const uint32_t PH0 = prmt(h1, h2, 0x5410u), PH1 = prmt(h1, h2, 0x7632u);
-            const uint32_t PL0 = prmt(l1, l2, 0x5410u), PL1 = prmt(l1, l2, 0x7632u);
-            const uint32_t PL0m = hmul2u(PL0, m1), PL1m = hmul2u(PL1, m1);
-            const __half *vszk = sVsz + kk * g.vsz_blk;
-            uint32_t b0[16], b1[16];
-#pragma unroll
-            for (int gi = 0; gi < 16; ++gi) {
-                if (gi >= ngi) continue;
-                const uint32_t v0 = *reinterpret_cast<const uint32_t *>(vszk + gi * 16 + 2 * tq);
-                const uint32_t v1 = *reinterpret_cast<const uint32_t *>(vszk + gi * 16 + 2 * tq + 8);
-                const uint32_t h0 = hmul2u(PH0, v0), hh1 = hmul2u(PH1, v1);
-                b0[gi] = hfma2u(PL0m, v0, hfma2u(PH0, v0, hmul2u(h0, nm)));
-                b1[gi] = hfma2u(PL1m, v1, hfma2u(PH1, v1, hmul2u(hh1, nm)));
-            }
-            // value codes of this 16-token block: WLV words per lane
-            uint32_t Wv[WLV];
-            const uint32_t *sVk = sV + kk * g.vc_blk;
-#pragma unroll
-            for (int ch = 0; ch < WLV / CSV; ++ch) {
-                if (CSV == 4) {
-                    const uint4 w4 = *reinterpret_cast<const uint4 *>(sVk + ch * 128 + lane * 4);
-                    Wv[ch * 4 + 0] = w4.x;
-                    Wv[ch * 4 + 1] = w4.y;
-                    Wv[ch * 4 + 2] = w4.z;
-                    Wv[ch * 4 + 3] = w4.w;
-                } else {
-                    const uint2 w2 = *reinterpret_cast<const uint2 *>(sVk + ch * 64 + lane * 2);
-                    Wv[ch * 2 + 0] = w2.x;
-                    Wv[ch * 2 + 1] = w2.y;
+                for (int mm = 0; mm < NJ; ++mm) {
+                    const int row = rr + 8 * (mi >> 1), ch = 2 * mm + (mi & 1);
+                    uint32_t a[4];
+                    ldsm_x4_t(a, mx.tile + row * D + 8 * (ch ^ (row & 7)));
+                    mma16816(A.oacc[mm], a[0], a[1], a[2], a[3], c0, c1);
                 }
             }
-#pragma unroll
-            for (int mm = 0; mm < NJ; ++mm) {
-                const int ci0 = 2 * mm;
-                const int w = ci0 / CPHV, r0 = ci0 % CPHV;
-                const uint32_t Wp0 = Wv[0 * NWV + w], Wp1 = Wv[1 * NWV + w];
-                const uint32_t a0 = unpack_exact<VB>(Wp0, r0), a1 = unpack_exact<VB>(Wp0, r0 + 1);
-                const uint32_t a2 = unpack_exact<VB>(Wp1, r0), a3 = unpack_exact<VB>(Wp1, r0 + 1);
-                const int gi = mm >> sh;
-                mma16816(oacc[mm], a0, a1, a2, a3, b0[gi], b1[gi]);
-            }
-            // value zero points: rows [z][gi][16 tokens] (the codes entered exactly)
-            const uint32_t bz0 = odd ? PL0 : PH0, bz1 = odd ? PL1 : PH1;
-            {
-                const __half *zrow = vszk + ngi * 16;
-                uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-                if (gq < ngi) {
-                    a0 = *reinterpret_cast<const uint32_t *>(zrow + gq * 16 + 2 * tq);
-                    a2 = *reinterpret_cast<const uint32_t *>(zrow + gq * 16 + 2 * tq + 8);
-                }
-                if (gq + 8 < ngi) {
-                    a1 = *reinterpret_cast<const uint32_t *>(zrow + (gq + 8) * 16 + 2 * tq);
-                    a3 = *reinterpret_cast<const uint32_t *>(zrow + (gq + 8) * 16 + 2 * tq + 8);
-                }
-                mma16816(zacc[0], a0, a1, a2, a3, bz0, bz1);
-            }
-        }
-
-        // ---- refill this stage ----
-        __syncwarp();
-        if (it + stages < nb) {
-            if (lane == 0) {
-                fence_proxy_async();
-                issue_block(g, sg, myring + (size_t)st * sg.bytes, mybars + st, kc, ksz, vc, vsz,
-                            kb_begin + warp + (it + stages) * nw);
-            }
-            ++issued;
         }
     }
-    if (timed_out) {
-        if (lane == 0) atomicOr(dv.status, KIVI_FLAG_WAIT);
-        // wait (bounded) for this warp's copies still in flight before leaving;
-        // the consumed count is where the loop stopped
-        for (int it = 0; it < issued; ++it) {
-            if (mbar_try_wait(mybars + (it % stages), (unsigned)(it / stages) & 1u)) continue;
-            mbar_wait(mybars + (it % stages), (unsigned)(it / stages) & 1u);
-        }
-        mrun = -INFINITY;
-        lrun = 0.f;
-#pragma unroll
-        for (int mm = 0; mm < NJ; ++mm) oacc[mm][0] = oacc[mm][1] = oacc[mm][2] = oacc[mm][3] = 0.f;
-    }
+}
 
-    // ---- per-warp result ----
+// Per-warp result: m, l per head and o[head][d] = sum p v (value zero points
+// included), written at the start of the warp's region.
+template <int D, int SH>
+__device__ __forceinline__ void warp_result(WarpAcc<D> &A, float *wres) {
+    constexpr int NJ = D / 16;
+    constexpr int ngi = (D / 16) >> SH;
+    const int lane = threadIdx.x & 31;
+    const int gq = lane >> 2, tq = lane & 3;
+    float lrun = A.lrun;
     lrun += __shfl_xor_sync(0xffffffffu, lrun, 4);
     lrun += __shfl_xor_sync(0xffffffffu, lrun, 8);
     lrun += __shfl_xor_sync(0xffffffffu, lrun, 16);
-    // value zero-point sums per channel group gi: row gi of zacc (column pair 2 tq)
-    const float zr0 = zacc[0][0] + zacc[0][1], zr1 = zacc[0][2] + zacc[0][3];
+    const float zr0 = A.zacc[0] + A.zacc[1], zr1 = A.zacc[2] + A.zacc[3];
     float vz[16];
 #pragma unroll
     for (int gi = 0; gi < 16; ++gi)
         vz[gi] = gi < ngi ? __shfl_sync(0xffffffffu, gi < 8 ? zr0 : zr1, (gi & 7) * 4 + tq) : 0.f;
+    __syncwarp();
     if (gq == 0) {
-        wm[tq] = mrun;
-        wl[tq] = lrun;
+        wres[tq] = A.mrun;
+        wres[4 + tq] = lrun;
     }
+    float *wo = wres + 8;
 #pragma unroll
     for (int mm = 0; mm < NJ; ++mm) {
-        const int gi = mm >> sh;
-        wo[tq * D + 16 * mm + gq] = oacc[mm][0] + oacc[mm][1] + vz[gi];
-        wo[tq * D + 16 * mm + gq + 8] = oacc[mm][2] + oacc[mm][3] + vz[gi];
+        const int gi = mm >> SH;
+        wo[tq * D + 16 * mm + gq] = A.oacc[mm][0] + A.oacc[mm][1] + vz[gi];
+        wo[tq * D + 16 * mm + gq + 8] = A.oacc[mm][2] + A.oacc[mm][3] + vz[gi];
     }
 }
 
 // ---------------------------------------------------------------------------
-// The kernel: MMA CTAs (x < splits) and tail CTAs (x >= splits), then the
-// CTA-level merge of warps and the last-CTA merge of splits.
+// The persistent kernel.  Work units: for each (sequence i, kv head j, head
+// group qg), its blocks whose keys and values are all quantized (one unit
+// each) and its remaining blocks (MW units each), laid end to end; CTA c
+// takes units [c U / C, (c+1) U / C).  Each stretch of one (i, j, qg) inside
+// a CTA is a segment: the CTA's warps share its blocks, merge in shared
+// memory and write one partial; the last CTA to finish a segment of that
+// (i, j, qg) merges all of its partials.
 // ---------------------------------------------------------------------------
-// ---------------------------------------------------------------------------
-// The kernel: MMA CTAs (x < splits) and tail CTAs (x >= splits), then the
-// CTA-level merge of warps and the last-CTA merge of splits.
-// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ long long cta_of_unit(long long u, long long U, int C) {
+    return ((u + 1) * C - 1) / U;
+}
+
 template <int D, int KB, int VB, int SH>
 __global__ void __launch_bounds__(256, 2)
     decode_kernel(KiviGeom g, KiviDev dv, const __half *__restrict__ q, int hq,
-                  __half *__restrict__ out, DecodePlan plan) {
+                  __half *__restrict__ out, DecodePlan plan, DecodeUnits units) {
     extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int NJ = D / 16;
     const int nw = blockDim.x >> 5;
-    const int warp = threadIdx.x >> 5;
-    const int i = blockIdx.z, j = blockIdx.y / plan.qgroups, qg = blockIdx.y % plan.qgroups;
-    const int hg = hq / g.h;
-    const int e0 = qg * 4, nh = min(4, hg - e0);
-    const int T = dv.T[i], Tqk = dv.Tqk[i], Tqv = dv.Tqv[i];
-    const int nfull = min(Tqk, Tqv) / KIVI_KBLK;
-    const int nsplit_total = plan.splits + plan.tails;
-
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, tq = lane & 3;
+    const int eB = gq >> 1;
+    const int hg = hq / g.h, QG = plan.qgroups, HQG = g.h * QG;
+    const StageGeom sg = stage_geom(g);
+    const size_t wstride = warp_region(g, plan.stages);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
     unsigned char *ring = smem + bar_region(nw, plan.stages);
-    const size_t wstride = warp_region(g, plan.stages);
-    float *wres = reinterpret_cast<float *>(ring + warp * wstride);
-    float *wm = wres, *wl = wres + 4, *wo = wres + 8;
-
-    // CTAs x < tails take the tail (dispatched first: short, latency-bound,
-    // they overlap the streaming CTAs); the rest stream whole blocks.
-    const int s = blockIdx.x;
-    if (s >= plan.tails) {
-        if (threadIdx.x < nw * plan.stages) mbar_init(bars + threadIdx.x, 1);
-        fence_mbar_init();
-        __syncthreads();
-        const int kb0 = (s - plan.tails) * plan.blocks_per, kb1 = min(nfull, kb0 + plan.blocks_per);
-        mma_blocks<D, KB, VB, SH>(g, dv, q, hq, i, j, e0, nh, kb0, kb1, plan.stages, wstride, ring,
-                                  bars, wm, wl, wo);
-    } else {
-        const int t0 = nfull * KIVI_KBLK + s * KIVI_TAILBLK;
-        const int t1 = min(T, t0 + KIVI_TAILBLK);
-        tail_tokens<D, KB, VB, SH>(g, dv, q, hq, i, j, e0, nh, t0, t1, wm, wl, wo);
-    }
-    __syncthreads();
-
-    // ---- merge the warps of this CTA into one partial per query head ----
-    float *part = dv.part;
-    for (int x = threadIdx.x; x < nh * (D + 2); x += blockDim.x) {
-        const int e = x / (D + 2), c = x % (D + 2);
-        float M = -INFINITY;
-        for (int w = 0; w < nw; ++w) M = fmaxf(M, reinterpret_cast<const float *>(ring + w * wstride)[e]);
-        float val = 0.f;
-        if (c == 0) {
-            val = M;
-        } else if (M != -INFINITY) {
-            for (int w = 0; w < nw; ++w) {
-                const float *r = reinterpret_cast<const float *>(ring + w * wstride);
-                const float f = ex2(r[e] - M);
-                val += f * (c == 1 ? r[4 + e] : r[8 + e * D + (c - 2)]);
-            }
-        }
-        part[(((size_t)i * hq + j * hg + e0 + e) * g.smax + s) * (D + 2) + c] = val;
-    }
-
-    // ---- the last CTA of this (sequence, kv head, head group) merges ----
+    unsigned char *myregion = ring + warp * wstride;
+    uint64_t *mybars = bars + warp * plan.stages;
+    const float alpha = kLog2e * rsqrtf((float)D);
+    const long long U = units.total;
+    const int C = gridDim.x, c = blockIdx.x;
+    long long u = (long long)c * U / C;
+    const long long u_end = (long long)(c + 1) * U / C;
+    __shared__ int s_seg[5];
     __shared__ int s_last;
     __shared__ float sML[8];
+    // The barriers live for the whole kernel: a warp numbers the blocks it
+    // streams across all its segments (seq), block n goes to slot n % stages
+    // and completes phase n / stages of that slot's barrier.
+    if (threadIdx.x < nw * plan.stages) mbar_init(bars + threadIdx.x, 1);
+    fence_mbar_init();
     __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        unsigned *tk = dv.merge_ticket + ((size_t)i * g.h + j) * 4 + qg;
-        const unsigned prev = atomicAdd(tk, 1u);
-        s_last = prev == (unsigned)nsplit_total - 1u;
-        if (s_last) *tk = 0u;
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    if (threadIdx.x < nh) {
-        const int e = threadIdx.x;
-        const float *pp = part + ((size_t)i * hq + j * hg + e0 + e) * g.smax * (D + 2);
-        float M = -INFINITY;
-        for (int x = 0; x < nsplit_total; ++x) M = fmaxf(M, __ldcg(pp + (size_t)x * (D + 2)));
-        float L = 0.f;
-        if (M != -INFINITY)
-            for (int x = 0; x < nsplit_total; ++x)
-                L += ex2(__ldcg(pp + (size_t)x * (D + 2)) - M) * __ldcg(pp + (size_t)x * (D + 2) + 1);
-        sML[e] = M;
-        sML[4 + e] = L;
-    }
-    __syncthreads();
-    for (int x = threadIdx.x; x < nh * D; x += blockDim.x) {
-        const int e = x / D, c = x % D;
-        const float M = sML[e], L = sML[4 + e];
-        const float *pp = part + ((size_t)i * hq + j * hg + e0 + e) * g.smax * (D + 2);
-        float a = 0.f;
-        if (M != -INFINITY) {
-            for (int y = 0; y < nsplit_total; ++y)
-                a += ex2(__ldcg(pp + (size_t)y * (D + 2)) - M) * __ldcg(pp + (size_t)y * (D + 2) + 2 + c);
-            a = a / L;
+    unsigned seq = 0;
+    bool dead = false;   // a wait of this warp timed out: it streams no more blocks
+
+    while (u < u_end) {
+        if (threadIdx.x == 0) {
+            int lo = 0, hi = g.b;   // largest i with HQG * start[i] <= u
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if ((long long)HQG * units.start[mid] <= u) lo = mid; else hi = mid;
+            }
+            const int Wi = units.start[lo + 1] - units.start[lo];
+            const long long rem = u - (long long)HQG * units.start[lo];
+            s_seg[0] = lo;
+            s_seg[1] = (int)(rem / Wi);
+            s_seg[2] = (int)(rem % Wi);
+            s_seg[3] = (int)min((long long)Wi, rem % Wi + (u_end - u));
+            s_seg[4] = Wi;
         }
-        out[((size_t)i * hq + j * hg + e0 + e) * D + c] = __float2half_rn(a);
+        // the rings were last written and read by generic stores and loads
+        // (the previous segment's merge): order them before the async copies
+        fence_proxy_async();
+        __syncthreads();
+        const int i = s_seg[0], jq = s_seg[1], o0 = s_seg[2], o1 = s_seg[3], Wi = s_seg[4];
+        const int j = jq / QG, qg = jq % QG;
+        const int e0 = qg * 4, nh = min(4, hg - e0);
+        const int T = dv.T[i], Tqk = dv.Tqk[i], Tqv = dv.Tqv[i];
+        const int nfull = min(Tqk, Tqv) / KIVI_KBLK;
+        const int nblk = (T + KIVI_KBLK - 1) / KIVI_KBLK;
+        const int nfh = units.full[i];
+        const int MW = units.mixed_weight;
+
+        // query fragments of this (sequence, kv head, head group)
+        uint32_t qB[NJ][2];
+#pragma unroll
+        for (int jj = 0; jj < NJ; ++jj)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+                qB[jj][hh] = eB < nh ? *reinterpret_cast<const uint32_t *>(
+                                           q + ((size_t)i * hq + j * hg + e0 + eB) * D + 16 * jj + 8 * hh + 2 * tq)
+                                     : 0u;
+        WarpAcc<D> A;
+        acc_reset<D>(A);
+
+        // Blocks of the segment: units [o0, min(o1, nfh)) are blocks of the
+        // same index, units nfh + MW m in [o0, o1) are block nfh + m; blocks
+        // past the data (>= nblk) are skipped.
+        const uint32_t *kc = dv.Kc + kc_slice(g, i, j);
+        const __half *ksz = dv.Ksz + ksz_slice(g, i, j);
+        const uint32_t *vc = dv.Vc + vc_slice(g, i, j);
+        const __half *vsz = dv.Vsz + vsz_slice(g, i, j);
+        const int nA = max(0, min(o1, nfh) - o0);
+        const int m0 = o0 > nfh ? (o0 - nfh + MW - 1) / MW : 0;
+        const int m1 = o1 > nfh ? (o1 - nfh + MW - 1) / MW : 0;
+        const int nL = nA + max(0, m1 - m0);
+        auto blk = [&](int x) { return x < nA ? o0 + x : nfh + m0 + (x - nA); };
+        auto first_at_least = [&](int kb) {   // first x with blk(x) >= kb (blk increases)
+            int lo = 0, hi = nL;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (blk(mid) >= kb) hi = mid; else lo = mid + 1;
+            }
+            return lo;
+        };
+        const int nD = first_at_least(nblk);            // blocks with data
+        const int xm = min(first_at_least(nfull), nD);  // mixed blocks: [xm, nD)
+        const int nP = xm, nM = nD - xm;
+        // Warps by cost: a mixed block costs MW packed blocks (its window
+        // loads are a chain of dependent reads).  Mixed block k goes to warp
+        // k % nw; the packed blocks fill the warps up to an equal cost, as
+        // contiguous runs.
+        auto packed_of = [&](int w) {
+            const int n1 = nM % nw, nl = nw - n1;   // warps w < n1 hold one more mixed block
+            if (n1 == 0) return nP / nw + (w < nP % nw ? 1 : 0);
+            if (nP <= nl * MW) return w < n1 ? 0 : nP / nl + (w - n1 < nP % nl ? 1 : 0);
+            const int tot = nP + n1 * MW;
+            return tot / nw + (w < tot % nw ? 1 : 0) - (w < n1 ? MW : 0);
+        };
+        int ps = 0;
+        for (int w = 0; w < warp; ++w) ps += packed_of(w);
+        const int pw = dead ? 0 : packed_of(warp);
+        const int cm = dead ? 0 : (nM > warp ? (nM - warp + nw - 1) / nw : 0);
+        const int nb = pw + cm;   // this warp's blocks: pw packed, then cm mixed
+        auto kb_of = [&](int it) { return it < pw ? blk(ps + it) : blk(xm + warp + (it - pw) * nw); };
+        auto mixed = [&](int it) { return it >= pw; };
+        MixCtx mc;
+        mc.tb = 0;
+        mc.T = T;
+        mc.Tqk = Tqk;
+        mc.Tqv = Tqv;
+        mc.R = g.R;
+        mc.kwin = dv.Kf + kf_slice(g, i, j);
+        mc.vwin = dv.Vf + vf_slice(g, i, j);
+        mc.tile = nullptr;
+        // A block is issued ahead only if the block before it is not mixed: a
+        // mixed block uses the next block's slot as its fp16 scratch.
+        int issued = 0;
+        auto ring_slot = [&](int it) { return (int)((seq + (unsigned)it) % (unsigned)plan.stages); };
+        auto parity = [&](int it) { return ((seq + (unsigned)it) / (unsigned)plan.stages) & 1u; };
+        while (issued < nb && issued < plan.stages && (issued == 0 || !mixed(issued - 1))) {
+            issue_block(g, sg, myregion + (size_t)ring_slot(issued) * sg.bytes, mybars + ring_slot(issued), kc,
+                        ksz, vc, vsz, kb_of(issued));
+            ++issued;
+        }
+        __syncwarp();
+        // Mixed blocks come last in a warp's list and are not read ahead: two
+        // blocks before the first of them, bring their packed data and window
+        // rows into L2 so that their loads do not wait on HBM.
+        int first_mixed = nb;
+        while (first_mixed > 0 && mixed(first_mixed - 1)) --first_mixed;
+        const int pf_at = first_mixed - 2 > 0 ? first_mixed - 2 : 0;
+        int timed_out_at = -1;
+        for (int it = 0; it < nb; ++it) {
+            if (it == pf_at && lane == 0) {
+                for (int x = first_mixed; x < nb; ++x) {
+                    const int kb = kb_of(x), tb = kb * KIVI_KBLK, te = min(tb + KIVI_KBLK, T);
+                    prefetch_block(g, sg, kc, ksz, vc, vsz, kb);
+                    prefetch_rows<D>(mc.kwin, g.R, max(tb, Tqk), te);
+                    prefetch_rows<D>(mc.vwin, g.R + 1, max(tb, Tqv), te);
+                }
+            }
+            const int st = ring_slot(it);
+            if (issued <= it) {   // deferred behind a mixed block
+                // the slot held the mixed block's fp16 tiles (generic and
+                // cp.async writes): order them before the bulk copies
+                fence_proxy_async();
+                __syncwarp();
+                issue_block(g, sg, myregion + (size_t)st * sg.bytes, mybars + st, kc, ksz, vc, vsz, kb_of(it));
+                issued = it + 1;
+                __syncwarp();
+            }
+            if (!__all_sync(0xffffffffu, mbar_wait(mybars + st, parity(it)))) {
+                timed_out_at = it;
+                break;
+            }
+            const unsigned char *sb = myregion + (size_t)st * sg.bytes;
+            if (!mixed(it)) {
+                do_block<D, KB, VB, SH, false>(A, qB, sb, sg, g, alpha, mc);
+            } else {
+                mc.tb = kb_of(it) * KIVI_KBLK;
+                mc.tile = reinterpret_cast<__half *>(myregion + (size_t)ring_slot(it + 1) * sg.bytes);
+                do_block<D, KB, VB, SH, true>(A, qB, sb, sg, g, alpha, mc);
+            }
+            __syncwarp();
+            // Refill the slot just read.  Its packed data was only read (by
+            // loads whose values the block has consumed): no proxy fence.
+            while (issued < nb && issued <= it + plan.stages && !mixed(issued - 1)) {
+                issue_block(g, sg, myregion + (size_t)ring_slot(issued) * sg.bytes, mybars + ring_slot(issued),
+                            kc, ksz, vc, vsz, kb_of(issued));
+                ++issued;
+            }
+        }
+        if (timed_out_at >= 0) {
+            if (lane == 0) atomicOr(dv.status, KIVI_FLAG_WAIT);
+            // wait (bounded) for this warp's copies still in flight before
+            // its region is reused; the warp then streams nothing more
+            for (int it = timed_out_at; it < issued; ++it) mbar_wait(mybars + ring_slot(it), parity(it));
+            acc_reset<D>(A);
+            dead = true;
+        }
+        seq += (unsigned)nb;
+
+        // ---- merge the warps into this CTA's partial of (i, j, qg) ----
+        __syncwarp();
+        warp_result<D, SH>(A, reinterpret_cast<float *>(myregion));
+        __syncthreads();
+        const long long Pp = (long long)HQG * units.start[i] + (long long)jq * Wi;
+        const int cfirst = (int)cta_of_unit(Pp, U, C);
+        const int np = (int)cta_of_unit(Pp + Wi - 1, U, C) - cfirst + 1;
+        const int slot = c - cfirst;
+        float *part = dv.part;
+        for (int x = threadIdx.x; x < nh * (D + 2); x += blockDim.x) {
+            const int e = x / (D + 2), cc = x % (D + 2);
+            float M = -INFINITY;
+            for (int w = 0; w < nw; ++w) M = fmaxf(M, reinterpret_cast<const float *>(ring + w * wstride)[e]);
+            float val = 0.f;
+            if (cc == 0) {
+                val = M;
+            } else if (M != -INFINITY) {
+                for (int w = 0; w < nw; ++w) {
+                    const float *r = reinterpret_cast<const float *>(ring + w * wstride);
+                    const float fw = ex2(r[e] - M);
+                    val += fw * (cc == 1 ? r[4 + e] : r[8 + e * D + (cc - 2)]);
+                }
+            }
+            part[(((size_t)i * hq + j * hg + e0 + e) * g.smax + slot) * (D + 2) + cc] = val;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            unsigned *tk = dv.merge_ticket + ((size_t)i * g.h + j) * 4 + qg;
+            const unsigned prev = atomicAdd(tk, 1u);
+            s_last = prev == (unsigned)np - 1u;
+            if (s_last) *tk = 0u;
+        }
+        __syncthreads();
+        if (s_last) {
+            __threadfence();
+            if (threadIdx.x < nh) {
+                const int e = threadIdx.x;
+                const float *pp = part + ((size_t)i * hq + j * hg + e0 + e) * g.smax * (D + 2);
+                float M = -INFINITY;
+                for (int x = 0; x < np; ++x) M = fmaxf(M, __ldcg(pp + (size_t)x * (D + 2)));
+                float L = 0.f;
+                if (M != -INFINITY)
+                    for (int x = 0; x < np; ++x)
+                        L += ex2(__ldcg(pp + (size_t)x * (D + 2)) - M) * __ldcg(pp + (size_t)x * (D + 2) + 1);
+                sML[e] = M;
+                sML[4 + e] = L;
+            }
+            __syncthreads();
+            for (int x = threadIdx.x; x < nh * D; x += blockDim.x) {
+                const int e = x / D, cc = x % D;
+                const float M = sML[e], L = sML[4 + e];
+                const float *pp = part + ((size_t)i * hq + j * hg + e0 + e) * g.smax * (D + 2);
+                float a = 0.f;
+                if (M != -INFINITY) {
+                    for (int y = 0; y < np; ++y)
+                        a += ex2(__ldcg(pp + (size_t)y * (D + 2)) - M) * __ldcg(pp + (size_t)y * (D + 2) + 2 + cc);
+                    a = a / L;
+                }
+                out[((size_t)i * hq + j * hg + e0 + e) * D + cc] = __float2half_rn(a);
+            }
+        }
+        __syncthreads();
+        u += o1 - o0;
     }
 }
 
 template <int D, int KB, int VB, int SH>
 cudaError_t launch_t(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, __half *out,
-                     const DecodePlan &plan, cudaStream_t st) {
+                     const DecodePlan &plan, const DecodeUnits &units, cudaStream_t st) {
     const size_t smem = bar_region(plan.warps, plan.stages) + (size_t)plan.warps * warp_region(g, plan.stages);
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, KB, VB, SH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(plan.splits + plan.tails, g.h * plan.qgroups, g.b);
-    decode_kernel<D, KB, VB, SH><<<grid, plan.warps * 32, smem, st>>>(g, dv, q, hq, out, plan);
+    decode_kernel<D, KB, VB, SH><<<plan.ctas, plan.warps * 32, smem, st>>>(g, dv, q, hq, out, plan, units);
     return cudaGetLastError();
 }
 
 template <int D, int KB, int VB>
 cudaError_t launch_g(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, __half *out,
-                     const DecodePlan &plan, cudaStream_t st) {
+                     const DecodePlan &plan, const DecodeUnits &units, cudaStream_t st) {
     switch (g.G) {
-    case 16: return launch_t<D, KB, VB, 0>(g, dv, q, hq, out, plan, st);
-    case 32: return launch_t<D, KB, VB, 1>(g, dv, q, hq, out, plan, st);
-    case 64: return launch_t<D, KB, VB, 2>(g, dv, q, hq, out, plan, st);
+    case 16: return launch_t<D, KB, VB, 0>(g, dv, q, hq, out, plan, units, st);
+    case 32: return launch_t<D, KB, VB, 1>(g, dv, q, hq, out, plan, units, st);
+    case 64: return launch_t<D, KB, VB, 2>(g, dv, q, hq, out, plan, units, st);
     default:
-        if constexpr (D >= 128) return launch_t<D, KB, VB, 3>(g, dv, q, hq, out, plan, st);
+        if constexpr (D >= 128) return launch_t<D, KB, VB, 3>(g, dv, q, hq, out, plan, units, st);
         return cudaErrorInvalidValue;
     }
 }
 
 template <int D>
 cudaError_t launch_d(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, __half *out,
-                     const DecodePlan &plan, cudaStream_t st) {
-    if (g.kbits == 2 && g.vbits == 2) return launch_g<D, 2, 2>(g, dv, q, hq, out, plan, st);
-    if (g.kbits == 2 && g.vbits == 4) return launch_g<D, 2, 4>(g, dv, q, hq, out, plan, st);
-    if (g.kbits == 4 && g.vbits == 2) return launch_g<D, 4, 2>(g, dv, q, hq, out, plan, st);
-    return launch_g<D, 4, 4>(g, dv, q, hq, out, plan, st);
+                     const DecodePlan &plan, const DecodeUnits &units, cudaStream_t st) {
+    if (g.kbits == 2 && g.vbits == 2) return launch_g<D, 2, 2>(g, dv, q, hq, out, plan, units, st);
+    if (g.kbits == 2 && g.vbits == 4) return launch_g<D, 2, 4>(g, dv, q, hq, out, plan, units, st);
+    if (g.kbits == 4 && g.vbits == 2) return launch_g<D, 4, 2>(g, dv, q, hq, out, plan, units, st);
+    return launch_g<D, 4, 4>(g, dv, q, hq, out, plan, units, st);
 }
 
 }  // namespace

@@ -17,7 +17,6 @@
 #define KIVI_MAX_QPERKV 8
 #define KIVI_KBLK 64   // tokens per key block
 #define KIVI_VBLK 16   // tokens per value block
-#define KIVI_TAILBLK 32  // tokens per decode tail CTA
 
 // status-word bits (also documented in kivi.h)
 #define KIVI_FLAG_COUNTER 1u
@@ -32,7 +31,7 @@ struct KiviGeom {
     int kc_blk;   // words per key block   = 2 d kbits
     int vc_blk;   // words per value block = d vbits / 2
     int vsz_blk;  // halves per value block of scale/zero = 2 (d/G) 16
-    int smax;     // decode splits the partial buffer holds per (sequence, query head)
+    int smax;     // decode partials the buffer holds per (sequence, query head)
 };
 
 struct KiviDev {
@@ -177,13 +176,23 @@ __device__ __forceinline__ uint32_t qcode(float x, float sf, float zf, int bits)
 
 // ---- host-side launchers (kivi_pack.cu, kivi_decode.cu) ----------------------------
 struct DecodePlan {
-    int splits;      // tensor-core CTAs along the token axis per (sequence, kv head, head group)
-    int blocks_per;  // 64-token blocks per such CTA
-    int tails;       // CUDA-core CTAs covering the blocks that hold fp16 keys or values
+    int ctas;        // persistent CTAs (grid size)
     int qgroups;     // head groups of <= 4 query heads per kv head
     int warps;       // warps per CTA
     int stages;      // shared-memory stages per warp
+    int max_parts;   // most partials any (sequence, kv head, head group) receives
     int launches;    // kernel launches per decode call
+};
+
+// Work units of one decode call: per sequence i, each of its (kv head, head
+// group) pairs counts full[i] fully quantized blocks (one unit each) and its
+// remaining blocks (mixed_weight units each); start[] is the prefix over
+// sequences of the units of one pair.
+struct DecodeUnits {
+    long long total;
+    int mixed_weight;
+    int start[KIVI_MAX_BATCH + 1];
+    int full[KIVI_MAX_BATCH];
 };
 
 // Sets the calling thread's text for kivi_last_error() (kivi_api.cu).
@@ -194,8 +203,10 @@ cudaError_t kivi_launch_prefill(const KiviGeom &g, const KiviDev &dv, const __ha
                                 cudaStream_t st);
 cudaError_t kivi_launch_append(const KiviGeom &g, const KiviDev &dv, const __half *k,
                                const __half *v, cudaStream_t st);
-DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *Tqk, const int *Tqv, int num_sms);
-int kivi_min_blocks_per_split();
+DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *T, const int *Tqk, const int *Tqv,
+                            int num_sms, DecodeUnits *units);
+// partial slots per (sequence, query head) a cache of this shape allocates
+int kivi_partial_slots(int b, int h, int num_sms);
 cudaError_t kivi_launch_decode(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq,
-                               __half *out, const DecodePlan &plan, cudaStream_t st,
-                               cudaEvent_t ev0, cudaEvent_t ev1);
+                               __half *out, const DecodePlan &plan, const DecodeUnits &units,
+                               cudaStream_t st, cudaEvent_t ev0, cudaEvent_t ev1);

@@ -82,19 +82,18 @@ extern "C" kivi_status kivi_decode_attn_noalloc(const kivi_packed_cache *pc, con
     g.kc_blk = 2 * d * g.kbits;
     g.vc_blk = d * g.vbits / 2;
     g.vsz_blk = 2 * (d / G) * KIVI_VBLK;
-    g.smax = (g.nkb + kivi_min_blocks_per_split() - 1) / kivi_min_blocks_per_split() +
-             (R + KIVI_KBLK + KIVI_TAILBLK - 1) / KIVI_TAILBLK + 2;
-
     // Plan for the capacity (the counters stay on the device): every
-    // sequence is taken as full, CTAs past a sequence's data end at once.
+    // sequence is taken as full; blocks past a sequence's data are skipped.
     int full[KIVI_MAX_BATCH];
     for (int i = 0; i < b; ++i) full[i] = g.fcap;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return fail(KIVI_ERR_CUDA, "no usable CUDA device");
-    const DecodePlan plan = kivi_plan_decode(g, h_q, full, full, sms);
-    g.smax = plan.splits + plan.tails;   // partial stride: exactly what this plan writes
+    g.smax = kivi_partial_slots(b, h, sms);
+    DecodeUnits units;   // on the stack: no allocation
+    const DecodePlan plan = kivi_plan_decode(g, h_q, full, full, full, sms, &units);
+    g.smax = plan.max_parts;   // partial stride: exactly what this plan writes
 
     const size_t part_bytes = (size_t)b * h_q * g.smax * (d + 2) * sizeof(float);
     const size_t ticket_off = (part_bytes + 255) / 256 * 256;
@@ -126,7 +125,8 @@ extern "C" kivi_status kivi_decode_attn_noalloc(const kivi_packed_cache *pc, con
     dv.part = reinterpret_cast<float *>(scratch);
     dv.merge_ticket = reinterpret_cast<unsigned *>(scratch + ticket_off);
     dv.status = reinterpret_cast<unsigned *>(scratch + status_off);
-    e = kivi_launch_decode(g, dv, (const __half *)q, h_q, (__half *)out, plan, st, nullptr, nullptr);
+    e = kivi_launch_decode(g, dv, (const __half *)q, h_q, (__half *)out, plan, units, st, nullptr,
+                           nullptr);
     if (e != cudaSuccess) return fail(KIVI_ERR_CUDA, cudaGetErrorString(e));
     return KIVI_OK;
 }

@@ -148,7 +148,7 @@ kivi_status kivi_profile_enable(kivi_cache_t c, int on);
 kivi_status kivi_profile_read(kivi_cache_t c, double *total_ms, int *launches);
 
 /* How the last kivi_decode_attn call was launched (HOST outputs, any may be
- * NULL): splits per (sequence, kv head) and kernel launches per call. */
+ * NULL): persistent CTAs of the decode kernel and kernel launches per call. */
 kivi_status kivi_decode_plan(kivi_cache_t c, int *splits, int *launches);
 
 /* A packed cache held in caller-owned device memory, in the format that
