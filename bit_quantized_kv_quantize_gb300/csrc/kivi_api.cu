@@ -83,8 +83,7 @@ kivi_status check_handle(kivi_cache_t c) {
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 void free_dev(KiviDev &d) {
-    void *ps[] = {d.Kc, d.Ksz, d.Vc, d.Vsz, d.Kf, d.Vf, d.T, d.Tqk, d.Tqv, d.ticket, d.status,
-                  d.part, d.merge_ticket};
+    void *ps[] = {d.blk, d.Kf, d.Vf, d.T, d.Tqk, d.Tqv, d.ticket, d.status, d.part, d.merge_ticket};
     for (void *p : ps)
         if (p) cudaFree(p);
     memset(&d, 0, sizeof d);
@@ -161,13 +160,7 @@ kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, in
     memset(&c->last_plan, 0, sizeof c->last_plan);
     KiviGeom &g = c->g;
     g.b = b; g.h = h_kv; g.d = d; g.kbits = k_bits; g.vbits = v_bits; g.G = G; g.R = R;
-    g.fcap = (max_tokens + q - 1) / q * q;
-    g.nkb = g.fcap / KIVI_KBLK;
-    g.nkg = g.fcap / G;
-    g.nvb = g.fcap / KIVI_VBLK;
-    g.kc_blk = 2 * d * k_bits;
-    g.vc_blk = d * v_bits / 2;
-    g.vsz_blk = 2 * (d / G) * KIVI_VBLK;
+    kivi_geom_init(g, max_tokens);
     c->T.assign(b, 0);
     c->Tqk.assign(b, 0);
     c->Tqv.assign(b, 0);
@@ -186,10 +179,7 @@ kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, in
     memset(&dv, 0, sizeof dv);
     const size_t bh = (size_t)b * h_kv;
     struct Req { void **p; size_t bytes; } reqs[] = {
-        {(void **)&dv.Kc, bh * g.nkb * g.kc_blk * 4},
-        {(void **)&dv.Ksz, bh * g.nkg * 2 * d * 2},
-        {(void **)&dv.Vc, bh * g.nvb * g.vc_blk * 4},
-        {(void **)&dv.Vsz, bh * g.nvb * g.vsz_blk * 2},
+        {(void **)&dv.blk, bh * g.nkb * g.rec_bytes},
         {(void **)&dv.Kf, bh * R * d * 2},
         {(void **)&dv.Vf, bh * (R + 1) * d * 2},
         {(void **)&dv.T, (size_t)b * 4},
@@ -401,18 +391,72 @@ kivi_status kivi_cache_export(kivi_cache_t c, void *Kc, void *Ksz, void *Vc, voi
     g_err[0] = 0;
     kivi_status s = check_handle(c);
     if (s != KIVI_OK) return s;
+    const KiviGeom &g = c->g;
     size_t sz[6];
     kivi_cache_export_sizes(c, sz);
-    const void *src[6] = {c->dv.Kc, c->dv.Ksz, c->dv.Vc, c->dv.Vsz, c->dv.Kf, c->dv.Vf};
-    void *dst[6] = {Kc, Ksz, Vc, Vsz, Kf, Vf};
     cudaStream_t st = (cudaStream_t)stream;
-    for (int k = 0; k < 6; ++k) {
+    const void *src[2] = {c->dv.Kf, c->dv.Vf};
+    void *dst[2] = {Kf, Vf};
+    for (int k = 0; k < 2; ++k) {
         if (!dst[k]) continue;
-        cudaError_t e = cudaMemcpyAsync(dst[k], src[k], sz[k], cudaMemcpyDeviceToHost, st);
+        cudaError_t e = cudaMemcpyAsync(dst[k], src[k], sz[4 + k], cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess) return fail_cuda(c, e, "export");
+    }
+    std::vector<unsigned char> rec;
+    if (Kc || Ksz || Vc || Vsz) {
+        rec.resize((size_t)g.b * g.h * g.nkb * g.rec_bytes);
+        cudaError_t e = cudaMemcpyAsync(rec.data(), c->dv.blk, rec.size(), cudaMemcpyDeviceToHost, st);
         if (e != cudaSuccess) return fail_cuda(c, e, "export");
     }
     cudaError_t e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return fail_cuda(c, e, "export");
+    if (rec.empty()) return KIVI_OK;
+    // split the block records into the four documented arrays
+    const size_t kcb = (size_t)g.kc_blk * 4, vcb = (size_t)4 * g.vc_blk * 4, vszb = (size_t)4 * g.vsz_blk * 2;
+    const size_t rowsb = (size_t)2 * g.d * 2;   // one key group's scale and zero rows
+    for (int i = 0; i < g.b; ++i)
+        for (int j = 0; j < g.h; ++j)
+            for (int kb = 0; kb < g.nkb; ++kb) {
+                const unsigned char *r = rec.data() + rec_off(g, i, j, kb);
+                const size_t slice = (size_t)i * g.h + j;
+                if (Kc) memcpy((unsigned char *)Kc + (slice * g.nkb + kb) * kcb, r, kcb);
+                if (Vc) memcpy((unsigned char *)Vc + (slice * g.nkb + kb) * vcb, r + g.off_vc, vcb);
+                if (Vsz) memcpy((unsigned char *)Vsz + (slice * g.nkb + kb) * vszb, r + g.off_vsz, vszb);
+                if (Ksz) {
+                    if (g.G <= KIVI_KBLK)
+                        memcpy((unsigned char *)Ksz + (slice * g.nkg + (size_t)kb * g.kgr) * rowsb, r + g.off_ksz,
+                               g.kgr * rowsb);
+                    else if (kb % (g.G / KIVI_KBLK) == 0)   // first of the group's records
+                        memcpy((unsigned char *)Ksz + (slice * g.nkg + kb / (g.G / KIVI_KBLK)) * rowsb,
+                               r + g.off_ksz, rowsb);
+                }
+            }
+    return KIVI_OK;
+}
+
+kivi_status kivi_cache_export_records(kivi_cache_t c, void *records, size_t *bytes, kivi_stream_t stream) {
+    g_err[0] = 0;
+    kivi_status s = check_handle(c);
+    if (s != KIVI_OK) return s;
+    if (!bytes) {
+        set_err("bytes is null");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    const KiviGeom &g = c->g;
+    const size_t need = (size_t)g.b * g.h * g.nkb * g.rec_bytes;
+    if (!records) {
+        *bytes = need;
+        return KIVI_OK;
+    }
+    if (*bytes < need) {
+        snprintf(g_err, sizeof g_err, "records buffer holds %zu bytes, %zu needed", *bytes, need);
+        return KIVI_ERR_INVALID_ARG;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(records, c->dv.blk, need, cudaMemcpyDefault, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return fail_cuda(c, e, "export_records");
+    *bytes = need;
     return KIVI_OK;
 }
 

@@ -27,10 +27,6 @@ int env_int(const char *name, int dflt) {
     return x > 0 ? x : dflt;
 }
 
-int stage_bytes(const KiviGeom &g) {
-    int ksz = (g.G >= KIVI_KBLK ? 1 : KIVI_KBLK / g.G) * 2 * g.d * 2;
-    return g.kc_blk * 4 + ksz + 4 * g.vc_blk * 4 + 4 * g.vsz_blk * 2;
-}
 
 long long cta_of(long long u, long long U, int C) { return ((u + 1) * C - 1) / U; }
 
@@ -50,7 +46,7 @@ DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *T, const int *
     p.launches = 1;
     // shared memory: two CTAs per SM, ~110 KB each for the warps' rings of at
     // least two stages
-    const int sb = stage_bytes(g);
+    const int sb = g.rec_bytes;   // a stage holds one block record
     const int budget = env_int("KIVI_DECODE_SMEM_KB", 110) * 1024;
     p.warps = env_int("KIVI_DECODE_WARPS", 8);
     if (p.warps > 8) p.warps = 8;

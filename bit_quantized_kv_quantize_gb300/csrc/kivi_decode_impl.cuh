@@ -205,12 +205,12 @@ struct StageGeom {
     int kc_bytes, ksz_bytes, vc_bytes, vsz_bytes, bytes;
 };
 __host__ __device__ __forceinline__ StageGeom stage_geom(const KiviGeom &g) {
-    StageGeom s;
-    s.kc_bytes = g.kc_blk * 4;
-    s.ksz_bytes = (g.G >= KIVI_KBLK ? 1 : KIVI_KBLK / g.G) * 2 * g.d * 2;
-    s.vc_bytes = 4 * g.vc_blk * 4;
-    s.vsz_bytes = 4 * g.vsz_blk * 2;
-    s.bytes = s.kc_bytes + s.ksz_bytes + s.vc_bytes + s.vsz_bytes;
+    StageGeom s;   // a stage holds one block record
+    s.kc_bytes = g.off_ksz;
+    s.ksz_bytes = g.off_vc - g.off_ksz;
+    s.vc_bytes = g.off_vsz - g.off_vc;
+    s.vsz_bytes = g.rec_bytes - g.off_vsz;
+    s.bytes = g.rec_bytes;
     return s;
 }
 // One warp's region of dynamic shared memory: its ring of stages (a mixed
@@ -228,30 +228,14 @@ __host__ __device__ __forceinline__ size_t bar_region(int warps, int stages) {
     return ((size_t)warps * stages * 8 + 127) / 128 * 128;
 }
 
-// Stage block kb: lanes 0-3 each issue one of its four bulk copies (packed
-// keys, key scale/zero rows, packed values, value scale/zero rows); lane 0
-// also arms the barrier (the order of arming and completion does not matter:
-// the phase needs lane 0's arrival).  Called by the whole warp.
-__device__ __forceinline__ void issue_block(const KiviGeom &g, const StageGeom &sg, unsigned char *st,
-                                            uint64_t *bar, const uint32_t *kc, const __half *ksz,
-                                            const uint32_t *vc, const __half *vsz, int kb) {
-    const int lane = threadIdx.x & 31;
-    if (lane >= 4) return;
-    if (lane == 0) mbar_expect_tx(bar, (unsigned)sg.bytes);
-    const int grp0 = g.G >= KIVI_KBLK ? (kb * KIVI_KBLK) / g.G : kb * (KIVI_KBLK / g.G);
-    const void *src;
-    unsigned off, bytes;
-    if (lane == 0) {
-        src = kc + (size_t)kb * g.kc_blk; off = 0; bytes = sg.kc_bytes;
-    } else if (lane == 1) {
-        src = ksz + (size_t)grp0 * 2 * g.d; off = sg.kc_bytes; bytes = sg.ksz_bytes;
-    } else if (lane == 2) {
-        src = vc + (size_t)kb * 4 * g.vc_blk; off = sg.kc_bytes + sg.ksz_bytes; bytes = sg.vc_bytes;
-    } else {
-        src = vsz + (size_t)kb * 4 * g.vsz_blk; off = sg.kc_bytes + sg.ksz_bytes + sg.vc_bytes;
-        bytes = sg.vsz_bytes;
+// Stage block kb: one bulk copy of its record (packed keys, key scale/zero
+// rows, packed values, value scale/zero rows, back to back).  Lane 0 issues.
+__device__ __forceinline__ void issue_block(const StageGeom &sg, unsigned char *st, uint64_t *bar,
+                                            const unsigned char *recs, int kb) {
+    if ((threadIdx.x & 31) == 0) {
+        mbar_expect_tx(bar, (unsigned)sg.bytes);
+        bulk_g2s(st, recs + (size_t)kb * sg.bytes, (unsigned)sg.bytes, bar);
     }
-    bulk_g2s(st + off, src, bytes, bar);
 }
 
 // L2 prefetches for a block that will be read late: its packed data, and the
@@ -260,15 +244,7 @@ __device__ __forceinline__ void issue_block(const KiviGeom &g, const StageGeom &
 __device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ void prefetch_block(const KiviGeom &g, const StageGeom &sg, const uint32_t *kc,
-                                               const __half *ksz, const uint32_t *vc, const __half *vsz,
-                                               int kb) {
-    const int grp0 = g.G >= KIVI_KBLK ? (kb * KIVI_KBLK) / g.G : kb * (KIVI_KBLK / g.G);
-    prefetch_l2(kc + (size_t)kb * g.kc_blk, sg.kc_bytes);
-    prefetch_l2(ksz + (size_t)grp0 * 2 * g.d, sg.ksz_bytes);
-    prefetch_l2(vc + (size_t)kb * 4 * g.vc_blk, sg.vc_bytes);
-    prefetch_l2(vsz + (size_t)kb * 4 * g.vsz_blk, sg.vsz_bytes);
-}
+
 template <int D>
 __device__ __forceinline__ void prefetch_rows(const __half *win, int ring, int a, int b) {
     if (a >= b) return;
@@ -740,10 +716,7 @@ __global__ void __launch_bounds__(256, 2)
         // Blocks of the segment: units [o0, min(o1, nfh)) are blocks of the
         // same index, units nfh + MW m in [o0, o1) are block nfh + m; blocks
         // past the data (>= nblk) are skipped.
-        const uint32_t *kc = dv.Kc + kc_slice(g, i, j);
-        const __half *ksz = dv.Ksz + ksz_slice(g, i, j);
-        const uint32_t *vc = dv.Vc + vc_slice(g, i, j);
-        const __half *vsz = dv.Vsz + vsz_slice(g, i, j);
+        const unsigned char *recs = dv.blk + rec_off(g, i, j, 0);
         const int nA = max(0, min(o1, nfh) - o0);
         const int m0 = o0 > nfh ? (o0 - nfh + MW - 1) / MW : 0;
         const int m1 = o1 > nfh ? (o1 - nfh + MW - 1) / MW : 0;
@@ -793,8 +766,8 @@ __global__ void __launch_bounds__(256, 2)
         auto ring_slot = [&](int it) { return (int)((seq + (unsigned)it) % (unsigned)plan.stages); };
         auto parity = [&](int it) { return ((seq + (unsigned)it) / (unsigned)plan.stages) & 1u; };
         while (issued < nb && issued < plan.stages && (issued == 0 || !mixed(issued - 1))) {
-            issue_block(g, sg, myregion + (size_t)ring_slot(issued) * sg.bytes, mybars + ring_slot(issued), kc,
-                        ksz, vc, vsz, kb_of(issued));
+            issue_block(sg, myregion + (size_t)ring_slot(issued) * sg.bytes, mybars + ring_slot(issued), recs,
+                        kb_of(issued));
             ++issued;
         }
         __syncwarp();
@@ -809,7 +782,7 @@ __global__ void __launch_bounds__(256, 2)
             if (it == pf_at && lane == 0) {
                 for (int x = first_mixed; x < nb; ++x) {
                     const int kb = kb_of(x), tb = kb * KIVI_KBLK, te = min(tb + KIVI_KBLK, T);
-                    prefetch_block(g, sg, kc, ksz, vc, vsz, kb);
+                    prefetch_l2(recs + (size_t)kb * sg.bytes, (unsigned)sg.bytes);
                     prefetch_rows<D>(mc.kwin, g.R, max(tb, Tqk), te);
                     prefetch_rows<D>(mc.vwin, g.R + 1, max(tb, Tqv), te);
                 }
@@ -820,7 +793,7 @@ __global__ void __launch_bounds__(256, 2)
                 // cp.async writes): order them before the bulk copies
                 fence_proxy_async();
                 __syncwarp();
-                issue_block(g, sg, myregion + (size_t)st * sg.bytes, mybars + st, kc, ksz, vc, vsz, kb_of(it));
+                issue_block(sg, myregion + (size_t)st * sg.bytes, mybars + st, recs, kb_of(it));
                 issued = it + 1;
                 __syncwarp();
             }
@@ -840,8 +813,8 @@ __global__ void __launch_bounds__(256, 2)
             // Refill the slot just read.  Its packed data was only read (by
             // loads whose values the block has consumed): no proxy fence.
             while (issued < nb && issued <= it + plan.stages && !mixed(issued - 1)) {
-                issue_block(g, sg, myregion + (size_t)ring_slot(issued) * sg.bytes, mybars + ring_slot(issued),
-                            kc, ksz, vc, vsz, kb_of(issued));
+                issue_block(sg, myregion + (size_t)ring_slot(issued) * sg.bytes, mybars + ring_slot(issued), recs,
+                            kb_of(issued));
                 ++issued;
             }
         }

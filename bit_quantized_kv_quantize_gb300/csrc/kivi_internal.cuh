@@ -7,6 +7,15 @@
 // one lane's word feeds the A operand of an m16n8k16 MMA directly); values
 // in 16-token blocks, each word carrying two tokens, each half packing one
 // token along channels (channels interleaved by 8).  Scale and zero are fp16.
+//
+// In device memory the four packed arrays are interleaved by 64-token block:
+// the record of block kb of (sequence i, kv head j) holds, back to back,
+//   key codes of block kb          kc_blk words
+//   key scale/zero rows            [groups of block kb][2][d] fp16
+//   value codes of blocks 4kb..+3  4 vc_blk words
+//   value scale/zero of the same   4 vsz_blk fp16
+// so the decode kernel fetches a block with one bulk copy.  With G = 128 a
+// key group spans two blocks and both records carry its rows.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -31,14 +40,32 @@ struct KiviGeom {
     int kc_blk;   // words per key block   = 2 d kbits
     int vc_blk;   // words per value block = d vbits / 2
     int vsz_blk;  // halves per value block of scale/zero = 2 (d/G) 16
+    int kgr;      // key groups whose rows a record holds = max(1, 64 / G)
+    int off_ksz, off_vc, off_vsz, rec_bytes;   // record layout (bytes)
     int smax;     // decode partials the buffer holds per (sequence, query head)
 };
 
+// Fills the derived fields of g from b, h, d, kbits, vbits, G, R and the
+// token capacity.
+inline void kivi_geom_init(KiviGeom &g, int max_tokens) {
+    const int q = g.G > 64 ? g.G : 64;
+    g.fcap = (max_tokens + q - 1) / q * q;
+    g.nkb = g.fcap / 64;
+    g.nkg = g.fcap / g.G;
+    g.nvb = g.fcap / 16;
+    g.kc_blk = 2 * g.d * g.kbits;
+    g.vc_blk = g.d * g.vbits / 2;
+    g.vsz_blk = 2 * (g.d / g.G) * 16;
+    g.kgr = g.G >= 64 ? 1 : 64 / g.G;
+    g.off_ksz = g.kc_blk * 4;
+    g.off_vc = g.off_ksz + g.kgr * 2 * g.d * 2;
+    g.off_vsz = g.off_vc + 4 * g.vc_blk * 4;
+    g.rec_bytes = g.off_vsz + 4 * g.vsz_blk * 2;
+    g.smax = 0;
+}
+
 struct KiviDev {
-    uint32_t *Kc;
-    __half *Ksz;
-    uint32_t *Vc;
-    __half *Vsz;
+    unsigned char *blk;     // block records [b][h][nkb][rec_bytes]
     __half *Kf;
     __half *Vf;
     int *T, *Tqk, *Tqv;     // device counters [b]
@@ -52,18 +79,50 @@ struct SeqLens {
     int t[KIVI_MAX_BATCH];
 };
 
-// ---- slice bases -----------------------------------------------------------
-__host__ __device__ __forceinline__ size_t kc_slice(const KiviGeom &g, int i, int j) {
-    return ((size_t)i * g.h + j) * (size_t)g.nkb * g.kc_blk;
+// ---- records and slice bases ----------------------------------------------------
+__host__ __device__ __forceinline__ size_t rec_off(const KiviGeom &g, int i, int j, int kb) {
+    return (((size_t)i * g.h + j) * g.nkb + kb) * (size_t)g.rec_bytes;
 }
-__host__ __device__ __forceinline__ size_t ksz_slice(const KiviGeom &g, int i, int j) {
-    return ((size_t)i * g.h + j) * (size_t)g.nkg * 2 * g.d;
+// key code words of block kb
+__host__ __device__ __forceinline__ uint32_t *kc_words(const KiviGeom &g, unsigned char *blk, int i, int j,
+                                                       int kb) {
+    return reinterpret_cast<uint32_t *>(blk + rec_off(g, i, j, kb));
 }
-__host__ __device__ __forceinline__ size_t vc_slice(const KiviGeom &g, int i, int j) {
-    return ((size_t)i * g.h + j) * (size_t)g.nvb * g.vc_blk;
+// key scale/zero rows held by record kb: [kgr][2][d]
+__host__ __device__ __forceinline__ __half *ksz_rows(const KiviGeom &g, unsigned char *blk, int i, int j,
+                                                     int kb) {
+    return reinterpret_cast<__half *>(blk + rec_off(g, i, j, kb) + g.off_ksz);
 }
-__host__ __device__ __forceinline__ size_t vsz_slice(const KiviGeom &g, int i, int j) {
-    return ((size_t)i * g.h + j) * (size_t)g.nvb * g.vsz_blk;
+// value code words of value block vb
+__host__ __device__ __forceinline__ uint32_t *vc_words(const KiviGeom &g, unsigned char *blk, int i, int j,
+                                                       int vb) {
+    return reinterpret_cast<uint32_t *>(blk + rec_off(g, i, j, vb >> 2) + g.off_vc) + (size_t)(vb & 3) * g.vc_blk;
+}
+// value scale/zero halves of value block vb: [2][d/G][16]
+__host__ __device__ __forceinline__ __half *vsz_halves(const KiviGeom &g, unsigned char *blk, int i, int j,
+                                                       int vb) {
+    return reinterpret_cast<__half *>(blk + rec_off(g, i, j, vb >> 2) + g.off_vsz) + (size_t)(vb & 3) * g.vsz_blk;
+}
+// scale (sz = 0) or zero (sz = 1) of key group grp, channel c: written to
+// every record that holds the group, read from the first
+__device__ __forceinline__ void ksz_store(const KiviGeom &g, unsigned char *blk, int i, int j, int grp, int c,
+                                          __half s16, __half z16) {
+    if (g.G <= 64) {
+        __half *r = ksz_rows(g, blk, i, j, grp / g.kgr) + (size_t)(grp % g.kgr) * 2 * g.d;
+        r[c] = s16;
+        r[g.d + c] = z16;
+    } else {
+        for (int k = 0; k < g.G / 64; ++k) {
+            __half *r = ksz_rows(g, blk, i, j, grp * (g.G / 64) + k);
+            r[c] = s16;
+            r[g.d + c] = z16;
+        }
+    }
+}
+__device__ __forceinline__ __half ksz_load(const KiviGeom &g, unsigned char *blk, int i, int j, int grp, int c,
+                                           int sz) {
+    if (g.G <= 64) return ksz_rows(g, blk, i, j, grp / g.kgr)[((size_t)(grp % g.kgr) * 2 + sz) * g.d + c];
+    return ksz_rows(g, blk, i, j, grp * (g.G / 64))[(size_t)sz * g.d + c];
 }
 __host__ __device__ __forceinline__ size_t kf_slice(const KiviGeom &g, int i, int j) {
     return ((size_t)i * g.h + j) * (size_t)g.R * g.d;
@@ -93,17 +152,6 @@ __device__ __forceinline__ KWord kword_decode(int wb, int kbits) {
     w.pos0 = wi * (16 / kbits);
     return w;
 }
-// word index inside the slice and bit shift of (channel c, token tau)
-__device__ __forceinline__ size_t kc_locate(const KiviGeom &g, int c, int tau, int *shift) {
-    int kb = tau >> 6, pos = (tau & 63) >> 3, gg = tau & 7;
-    int cph = 16 / g.kbits, nwk = g.kbits >> 1;
-    int wi = pos / cph, r = pos - wi * cph;
-    int j = c >> 4, hh = (c >> 3) & 1, t = (c & 7) >> 1, hi = c & 1;
-    int L = 4 * gg + t;
-    int u = (2 * j + hh) * nwk + wi;
-    *shift = 16 * hi + r * g.kbits;
-    return (size_t)kb * g.kc_blk + (size_t)(u >> 2) * 128 + 4 * L + (u & 3);
-}
 
 // ---- value word geometry -------------------------------------------------------
 __device__ __forceinline__ int v_cs(const KiviGeom &g) {
@@ -128,24 +176,10 @@ __device__ __forceinline__ VWord vword_decode(int wb, int d, int vbits, int cs) 
     v.ci0 = w * (16 / vbits);
     return v;
 }
-__device__ __forceinline__ size_t vc_locate(const KiviGeom &g, int c, int tau, int *shift) {
-    int vb = tau >> 4, tt = tau & 15;
-    int p = tt >> 3, t = (tt & 7) >> 1, hi = tt & 1;
-    int gg = c & 7, ci = c >> 3;
-    int cph = 16 / g.vbits;
-    int w = ci / cph, r = ci - w * cph;
-    int nwv = g.d * g.vbits / 128, cs = v_cs(g);
-    int L = 4 * gg + t;
-    int u = p * nwv + w;
-    *shift = 16 * hi + r * g.vbits;
-    return (size_t)vb * g.vc_blk + (size_t)(u / cs) * 32 * cs + (size_t)L * cs + (u % cs);
-}
-// fp16 scale (sz = 0) or zero (sz = 1) of value token tau, channel group gi
-__device__ __forceinline__ size_t vsz_locate(const KiviGeom &g, int tau, int gi, int sz) {
-    return (size_t)(tau >> 4) * g.vsz_blk + ((size_t)sz * (g.d / g.G) + gi) * 16 + (tau & 15);
-}
-__device__ __forceinline__ size_t ksz_locate(const KiviGeom &g, int grp, int c, int sz) {
-    return ((size_t)grp * 2 + sz) * g.d + c;
+// fp16 scale (sz = 0) or zero (sz = 1) of value token tau, channel group gi,
+// within its value block's scale/zero halves
+__device__ __forceinline__ int vsz_in_block(const KiviGeom &g, int tau, int gi, int sz) {
+    return (sz * (g.d / g.G) + gi) * 16 + (tau & 15);
 }
 
 // ---- the quantizer (item 1), bit-exact with IEEE fp32 ---------------------------

@@ -67,21 +67,14 @@ extern "C" kivi_status kivi_decode_attn_noalloc(const kivi_packed_cache *pc, con
         return fail(KIVI_ERR_UNSUPPORTED, "unsupported G, d or R");
     if (h_q < 1 || h_q % h != 0) return fail(KIVI_ERR_INVALID_ARG, "h_q must be a positive multiple of h_kv");
     if (h_q / h > KIVI_MAX_QPERKV) return fail(KIVI_ERR_UNSUPPORTED, "h_q / h_kv above 8");
-    const void *ptrs[] = {pc->Kc, pc->Ksz, pc->Vc, pc->Vsz, pc->Kf, pc->Vf, q, out};
+    const void *ptrs[] = {pc->blocks, pc->Kf, pc->Vf, q, out};
     for (const void *p : ptrs)
         if (!p || ((uintptr_t)p & 15u)) return fail(KIVI_ERR_INVALID_ARG, "array pointers must be non-null and 16-byte aligned");
     if (!pc->T || !pc->Tqk || !pc->Tqv) return fail(KIVI_ERR_INVALID_ARG, "counter pointers are null");
 
     KiviGeom g;
-    const int qq = G > KIVI_KBLK ? G : KIVI_KBLK;
     g.b = b; g.h = h; g.d = d; g.kbits = pc->k_bits; g.vbits = pc->v_bits; g.G = G; g.R = R;
-    g.fcap = (pc->max_tokens + qq - 1) / qq * qq;
-    g.nkb = g.fcap / KIVI_KBLK;
-    g.nkg = g.fcap / G;
-    g.nvb = g.fcap / KIVI_VBLK;
-    g.kc_blk = 2 * d * g.kbits;
-    g.vc_blk = d * g.vbits / 2;
-    g.vsz_blk = 2 * (d / G) * KIVI_VBLK;
+    kivi_geom_init(g, pc->max_tokens);
     // Plan for the capacity (the counters stay on the device): every
     // sequence is taken as full; blocks past a sequence's data are skipped.
     int full[KIVI_MAX_BATCH];
@@ -113,10 +106,7 @@ extern "C" kivi_status kivi_decode_attn_noalloc(const kivi_packed_cache *pc, con
 
     KiviDev dv;
     memset(&dv, 0, sizeof dv);
-    dv.Kc = (uint32_t *)pc->Kc;
-    dv.Ksz = (__half *)pc->Ksz;
-    dv.Vc = (uint32_t *)pc->Vc;
-    dv.Vsz = (__half *)pc->Vsz;
+    dv.blk = (unsigned char *)pc->blocks;
     dv.Kf = (__half *)pc->Kf;
     dv.Vf = (__half *)pc->Vf;
     dv.T = (int *)pc->T;

@@ -44,7 +44,6 @@ __global__ void __launch_bounds__(256) prefill_keys_kernel(KiviGeom g, KiviDev d
     __syncthreads();
 
     // scale and zero per (group, channel)
-    __half *ksz = dv.Ksz + ksz_slice(g, i, j);
     for (int e = threadIdx.x; e < ngr * d; e += blockDim.x) {
         int gr = e / d, c = e - gr * d;
         float mn = __half2float(xs[(size_t)gr * g.G * d + c]), mx = mn;
@@ -54,9 +53,7 @@ __global__ void __launch_bounds__(256) prefill_keys_kernel(KiviGeom g, KiviDev d
             mx = fmaxf(mx, x);
         }
         QParams p = qparams(mn, mx, g.kbits);
-        int grp = tok0 / g.G + gr;
-        ksz[ksz_locate(g, grp, c, 0)] = p.s16;
-        ksz[ksz_locate(g, grp, c, 1)] = p.z16;
+        ksz_store(g, dv.blk, i, j, tok0 / g.G + gr, c, p.s16, p.z16);
         sfz[(gr * 2 + 0) * d + c] = p.sf;
         sfz[(gr * 2 + 1) * d + c] = p.zf;
     }
@@ -65,7 +62,6 @@ __global__ void __launch_bounds__(256) prefill_keys_kernel(KiviGeom g, KiviDev d
     // packed words of every 64-token block that starts inside [tok0, nqk)
     const int nblk = (ntok + KIVI_KBLK - 1) / KIVI_KBLK;
     const int cph = 16 / g.kbits;
-    uint32_t *kc = dv.Kc + kc_slice(g, i, j);
     for (int e = threadIdx.x; e < nblk * g.kc_blk; e += blockDim.x) {
         int kbl = e / g.kc_blk, wb = e - kbl * g.kc_blk;
         KWord kw = kword_decode(wb, g.kbits);
@@ -83,7 +79,7 @@ __global__ void __launch_bounds__(256) prefill_keys_kernel(KiviGeom g, KiviDev d
                 }
             }
         }
-        kc[(size_t)(tok0 / KIVI_KBLK + kbl) * g.kc_blk + wb] = word;
+        kc_words(g, dv.blk, i, j, tok0 / KIVI_KBLK + kbl)[wb] = word;
     }
 }
 
@@ -111,7 +107,6 @@ __global__ void __launch_bounds__(256) prefill_values_kernel(KiviGeom g, KiviDev
     __syncthreads();
 
     const int nvblk = (ntok + KIVI_VBLK - 1) / KIVI_VBLK;   // value blocks touched
-    __half *vsz = dv.Vsz + vsz_slice(g, i, j);
     for (int e = threadIdx.x; e < nvblk * KIVI_VBLK * ngi; e += blockDim.x) {
         int tl = e / ngi, gi = e - tl * ngi;
         int tau = tok0 + tl;
@@ -130,13 +125,13 @@ __global__ void __launch_bounds__(256) prefill_values_kernel(KiviGeom g, KiviDev
             sfz[(tl * 2 + 0) * ngi + gi] = p.sf;
             sfz[(tl * 2 + 1) * ngi + gi] = p.zf;
         }
-        vsz[vsz_locate(g, tau, gi, 0)] = s16;   // tokens past nqv: zero
-        vsz[vsz_locate(g, tau, gi, 1)] = z16;
+        __half *vsz = vsz_halves(g, dv.blk, i, j, tau >> 4);
+        vsz[vsz_in_block(g, tau, gi, 0)] = s16;   // tokens past nqv: zero
+        vsz[vsz_in_block(g, tau, gi, 1)] = z16;
     }
     __syncthreads();
 
     const int cs = v_cs(g), cph = 16 / g.vbits;
-    uint32_t *vc = dv.Vc + vc_slice(g, i, j);
     for (int e = threadIdx.x; e < nvblk * g.vc_blk; e += blockDim.x) {
         int vbl = e / g.vc_blk, wb = e - vbl * g.vc_blk;
         VWord vw = vword_decode(wb, d, g.vbits, cs);
@@ -152,7 +147,7 @@ __global__ void __launch_bounds__(256) prefill_values_kernel(KiviGeom g, KiviDev
                 word |= q << (16 * half + r * g.vbits);
             }
         }
-        vc[(size_t)(tok0 / KIVI_VBLK + vbl) * g.vc_blk + wb] = word;
+        vc_words(g, dv.blk, i, j, tok0 / KIVI_VBLK + vbl)[wb] = word;
     }
 }
 
@@ -215,7 +210,6 @@ __global__ void __launch_bounds__(256) append_kernel(KiviGeom g, KiviDev dv,
 
     if (flush) {
         // keys [Tqk, Tqk + R): token tau lives in slot tau - Tqk (Tqk % R == 0)
-        __half *ksz = dv.Ksz + ksz_slice(g, i, j);
         const int ngr = R / g.G;
         for (int e = threadIdx.x; e < ngr * d; e += blockDim.x) {
             int gr = e / d, c = e - gr * d;
@@ -226,18 +220,16 @@ __global__ void __launch_bounds__(256) append_kernel(KiviGeom g, KiviDev dv,
                 mx = fmaxf(mx, x);
             }
             QParams p = qparams(mn, mx, g.kbits);
-            int grp = Tqk / g.G + gr;
-            ksz[ksz_locate(g, grp, c, 0)] = p.s16;
-            ksz[ksz_locate(g, grp, c, 1)] = p.z16;
+            ksz_store(g, dv.blk, i, j, Tqk / g.G + gr, c, p.s16, p.z16);
         }
         __syncthreads();
         const int kb0 = Tqk / KIVI_KBLK, kb1 = (Tqk + R - 1) / KIVI_KBLK;
         const int cph = 16 / g.kbits;
-        uint32_t *kc = dv.Kc + kc_slice(g, i, j);
         for (int e = threadIdx.x; e < (kb1 - kb0 + 1) * g.kc_blk; e += blockDim.x) {
             int kb = kb0 + e / g.kc_blk, wb = e % g.kc_blk;
             KWord kw = kword_decode(wb, g.kbits);
-            uint32_t old = kc[(size_t)kb * g.kc_blk + wb];
+            uint32_t *kc = kc_words(g, dv.blk, i, j, kb);
+            uint32_t old = kc[wb];
             uint32_t word = 0;
             for (int half = 0; half < 2; ++half) {
                 int c = kw.c0 + half;
@@ -249,14 +241,14 @@ __global__ void __launch_bounds__(256) append_kernel(KiviGeom g, KiviDev dv,
                         word |= old & mask;                     // earlier tokens stay
                     } else if (tau < Tqk + R) {
                         int grp = tau / g.G;
-                        float sf = __half2float(ksz[ksz_locate(g, grp, c, 0)]);
-                        float zf = __half2float(ksz[ksz_locate(g, grp, c, 1)]);
+                        float sf = __half2float(ksz_load(g, dv.blk, i, j, grp, c, 0));
+                        float zf = __half2float(ksz_load(g, dv.blk, i, j, grp, c, 1));
                         float x = __half2float(kf[(size_t)(tau - Tqk) * d + c]);
                         word |= qcode(x, sf, zf, g.kbits) << sh;
                     }                                           // later tokens: zero
                 }
             }
-            kc[(size_t)kb * g.kc_blk + wb] = word;
+            kc[wb] = word;
         }
     }
 
@@ -264,13 +256,12 @@ __global__ void __launch_bounds__(256) append_kernel(KiviGeom g, KiviDev dv,
         // value token Tqv, slot Tqv % (R + 1)
         const __half *x = dv.Vf + vf_slice(g, i, j) + (size_t)(Tqv % (R + 1)) * d;
         const int ngi = d / g.G;
-        __half *vsz = dv.Vsz + vsz_slice(g, i, j);
-        uint32_t *vc = dv.Vc + vc_slice(g, i, j);
         const int vb = Tqv / KIVI_VBLK, tt = Tqv % KIVI_VBLK;
+        __half *vsz = vsz_halves(g, dv.blk, i, j, vb);
+        uint32_t *vc = vc_words(g, dv.blk, i, j, vb);
         if (tt == 0) {   // a fresh value block: clear it so untouched fields read zero
-            for (int e = threadIdx.x; e < g.vc_blk; e += blockDim.x) vc[(size_t)vb * g.vc_blk + e] = 0u;
-            for (int e = threadIdx.x; e < g.vsz_blk; e += blockDim.x)
-                vsz[(size_t)vb * g.vsz_blk + e] = __float2half_rn(0.f);
+            for (int e = threadIdx.x; e < g.vc_blk; e += blockDim.x) vc[e] = 0u;
+            for (int e = threadIdx.x; e < g.vsz_blk; e += blockDim.x) vsz[e] = __float2half_rn(0.f);
         }
         __shared__ float s_sf[16], s_zf[16];   // d / G <= 16
         __syncthreads();
@@ -282,8 +273,8 @@ __global__ void __launch_bounds__(256) append_kernel(KiviGeom g, KiviDev dv,
                 mx = fmaxf(mx, v);
             }
             QParams p = qparams(mn, mx, g.vbits);
-            vsz[vsz_locate(g, Tqv, gi, 0)] = p.s16;
-            vsz[vsz_locate(g, Tqv, gi, 1)] = p.z16;
+            vsz[vsz_in_block(g, Tqv, gi, 0)] = p.s16;
+            vsz[vsz_in_block(g, Tqv, gi, 1)] = p.z16;
             s_sf[gi] = p.sf;
             s_zf[gi] = p.zf;
         }
@@ -300,7 +291,7 @@ __global__ void __launch_bounds__(256) append_kernel(KiviGeom g, KiviDev dv,
                 bits |= qcode(__half2float(x[c]), s_sf[gi], s_zf[gi], g.vbits) << (r * g.vbits);
             }
             int L = 4 * gg + tq, u = p * nwv + w;
-            size_t wd = (size_t)vb * g.vc_blk + (size_t)(u / cs) * 32 * cs + (size_t)L * cs + (u % cs);
+            size_t wd = (size_t)(u / cs) * 32 * cs + (size_t)L * cs + (u % cs);
             reinterpret_cast<uint16_t *>(vc + wd)[half] = (uint16_t)bits;
         }
     }

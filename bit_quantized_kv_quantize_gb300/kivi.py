@@ -22,7 +22,7 @@ EXPORTS = ["kivi_cache_create", "kivi_cache_destroy", "kivi_prefill", "kivi_appe
            "kivi_decode_attn", "kivi_cache_lengths", "kivi_cache_export_sizes",
            "kivi_cache_export", "kivi_cache_check", "kivi_profile_enable", "kivi_profile_read",
            "kivi_decode_plan", "kivi_status_str", "kivi_last_error", "kivi_abi_version",
-           "kivi_decode_attn_noalloc"]
+           "kivi_decode_attn_noalloc", "kivi_cache_export_records"]
 
 
 class KiviError(RuntimeError):
@@ -156,6 +156,14 @@ class KiviCache:
         arrs = [np.zeros(int(n) // np.dtype(t).itemsize, t) for n, t in zip(sz, dt)]
         _check(lib.kivi_cache_export(self._h, *[a.ctypes.data for a in arrs], _stream(stream)))
         return dict(zip(["Kc", "Ksz", "Vc", "Vsz", "Kf", "Vf"], arrs))
+
+    def export_records(self, stream=None) -> np.ndarray:
+        """The packed arrays as the device stores them (block records, uint8)."""
+        n = ctypes.c_size_t(0)
+        _check(lib.kivi_cache_export_records(self._h, None, ctypes.byref(n), _stream(stream)))
+        buf = np.zeros(int(n.value), np.uint8)
+        _check(lib.kivi_cache_export_records(self._h, buf.ctypes.data, ctypes.byref(n), _stream(stream)))
+        return buf
 
     def check(self, stream=None) -> int:
         f = ctypes.c_uint32(0)

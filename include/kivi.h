@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define KIVI_ABI_VERSION 1
+#define KIVI_ABI_VERSION 2
 
 typedef struct kivi_cache *kivi_cache_t;   /* opaque, library-owned */
 typedef struct CUstream_st *kivi_stream_t; /* the same type as cudaStream_t */
@@ -110,9 +110,11 @@ kivi_status kivi_cache_lengths(kivi_cache_t c, int32_t *T, int32_t *Tqk, int32_t
 /* Byte sizes of the six arrays kivi_cache_export writes, in its order. */
 kivi_status kivi_cache_export_sizes(kivi_cache_t c, size_t sizes[6]);
 
-/* Copy the cache's device arrays into HOST buffers (sizes from
+/* Copy the cache's contents into HOST buffers (sizes from
  * kivi_cache_export_sizes), in the packed format below, then synchronize
- * `stream`.  Any pointer may be NULL to skip that array.
+ * `stream`.  Any pointer may be NULL to skip that array.  (On the device
+ * the first four arrays are stored interleaved as block records, see
+ * kivi_cache_export_records; this call splits them apart on the host.)
  *   Kc  uint32 [b][h_kv][fcap/64][2 d k_bits]  key codes, 64-token blocks
  *   Ksz fp16   [b][h_kv][fcap/G][2][d]          key scale (row 0), zero (row 1)
  *   Vc  uint32 [b][h_kv][fcap/16][d v_bits / 2] value codes, 16-token blocks
@@ -135,6 +137,22 @@ kivi_status kivi_cache_export_sizes(kivi_cache_t c, size_t sizes[6]);
 kivi_status kivi_cache_export(kivi_cache_t c, void *Kc, void *Ksz, void *Vc, void *Vsz, void *Kf,
                               void *Vf, kivi_stream_t stream);
 
+/* The packed arrays as the device stores them: one record per 64-token
+ * block kb of each (sequence i, kv head j), records ordered [b][h_kv][fcap/64],
+ * each record holding, back to back, in the element formats above:
+ *   Kc block kb                      2 d k_bits words
+ *   Ksz rows of the block's groups   [max(1, 64/G)][2][d] fp16 (G = 128: the
+ *                                    rows of group kb/2, in both its records)
+ *   Vc value blocks 4kb .. 4kb+3     4 (d v_bits / 2) words
+ *   Vsz value blocks 4kb .. 4kb+3    4 [2][d/G][16] fp16
+ * With records == NULL, writes the byte size of all records to *bytes.
+ * Otherwise copies them into `records` (host or device memory, *bytes at
+ * least that size; cudaMemcpyDefault), synchronizes `stream` and sets *bytes
+ * to the size copied.  Errors: KIVI_ERR_INVALID_ARG (bytes NULL, buffer too
+ * small). */
+kivi_status kivi_cache_export_records(kivi_cache_t c, void *records, size_t *bytes,
+                                      kivi_stream_t stream);
+
 /* Synchronize `stream` and read the device status word into *flags (HOST).
  * 0 means no kernel recorded an anomaly; bit 0: a counter out of range,
  * bit 1: a bounded wait for a shared-memory copy ran out.  Clears it. */
@@ -151,13 +169,14 @@ kivi_status kivi_profile_read(kivi_cache_t c, double *total_ms, int *launches);
  * NULL): persistent CTAs of the decode kernel and kernel launches per call. */
 kivi_status kivi_decode_plan(kivi_cache_t c, int *splits, int *launches);
 
-/* A packed cache held in caller-owned device memory, in the format that
- * kivi_cache_export documents (arrays and fcap as there), with the
- * per-sequence counters as DEVICE int32 arrays of b entries. */
+/* A packed cache held in caller-owned device memory: the block records
+ * that kivi_cache_export_records documents, the fp16 windows Kf and Vf as
+ * kivi_cache_export documents them (fcap as there), and the per-sequence
+ * counters as DEVICE int32 arrays of b entries. */
 typedef struct {
     int b, h_kv, d, k_bits, v_bits, G, R, max_tokens;
-    const void *Kc, *Ksz, *Vc, *Vsz, *Kf, *Vf;   /* device, 16-byte aligned */
-    const int32_t *T, *Tqk, *Tqv;                 /* device counters */
+    const void *blocks, *Kf, *Vf;   /* device, 16-byte aligned */
+    const int32_t *T, *Tqk, *Tqv;   /* device counters */
 } kivi_packed_cache;
 
 /* Decode attention that allocates nothing.  (The pages have no counterpart:
@@ -169,7 +188,8 @@ typedef struct {
  * Its scratch (split partials, merge tickets, status word) lives in one
  * fixed 16 MiB __device__ array inside the library, which every GPU that
  * loads the library holds until the process exits; shapes whose scratch
- * b * h_q * (splits + tails) * (d + 2) * 4 bytes plus tickets exceed it are
+ * b * h_q * P * (d + 2) * 4 bytes plus tickets exceed it (P: the most
+ * persistent CTAs sharing one (sequence, kv head, head group)) are
  * rejected with KIVI_ERR_UNSUPPORTED and a kivi_last_error() message.  The
  * call launches on `stream` and clears the tickets itself; all calls share
  * the array, so calls whose kernels overlap on the GPU race and must not be

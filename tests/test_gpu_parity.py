@@ -170,6 +170,42 @@ def test_decode_is_read_only_and_repeatable():
         assert np.array_equal(before[k], after[k])
 
 
+@pytest.mark.parametrize("G,kb,vb,d", [(32, 2, 2, 128), (16, 4, 2, 64), (64, 2, 4, 128), (128, 4, 4, 256)])
+def test_block_records_match_the_packed_arrays(G, kb, vb, d):
+    """The device's block records, split by the documented record layout,
+    equal the four packed arrays of kivi_cache_export."""
+    b, h, R, cap = 2, 2, max(G, 128), 800
+    gpu = K.KiviCache(b, h, d, kb, vb, G, R, cap)
+    rng = np.random.default_rng(G * 31 + kb)
+    Kh, Vh = _rand_kv(rng, b, h, 600, d)
+    gpu.prefill(_dev(Kh), _dev(Vh), [600, 437])
+    for s in range(R + 3):   # crosses a key flush and value pops
+        k, v = _rand_kv(rng, b, h, 1, d)
+        gpu.append(_dev(k[:, :, 0]), _dev(v[:, :, 0]))
+    ex = gpu.export()
+    rec = gpu.export_records()
+    g = U.geometry(b, h, d, kb, vb, G, R, cap)
+    kgr = max(1, 64 // G)
+    sizes = [g["kc_blk"] * 4, kgr * 2 * d * 2, 4 * g["vc_blk"] * 4, 4 * g["vsz_blk"] * 2]
+    rb = sum(sizes)
+    assert rec.size == b * h * g["nkb"] * rb
+    rec = rec.reshape(b, h, g["nkb"], rb)
+    o = np.cumsum([0] + sizes)
+    Kc = rec[..., o[0]:o[1]].copy().view(np.uint32).reshape(-1)
+    Vc = rec[..., o[2]:o[3]].copy().view(np.uint32).reshape(-1)
+    Vsz = rec[..., o[3]:o[4]].copy().view(np.uint16).reshape(-1)
+    rows = rec[..., o[1]:o[2]].copy().view(np.uint16).reshape(b, h, g["nkb"], kgr, 2, d)
+    if G <= 64:
+        Ksz = rows.reshape(-1)
+    else:   # both records of a group carry its rows
+        assert np.array_equal(rows[:, :, 0::2], rows[:, :, 1::2])
+        Ksz = rows[:, :, 0::2].reshape(-1)
+    assert np.array_equal(Kc, ex["Kc"])
+    assert np.array_equal(Ksz, ex["Ksz"])
+    assert np.array_equal(Vc, ex["Vc"])
+    assert np.array_equal(Vsz, ex["Vsz"])
+
+
 def test_non_default_stream():
     w = W.small(W.WORKLOADS["tiny_kivi2"], prefill=100)
     p = Pair(w.b, w.h_kv, w.d, w.kbits, w.vbits, w.G, w.R, 200)

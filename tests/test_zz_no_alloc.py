@@ -23,8 +23,7 @@ pytestmark = pytest.mark.gpu
 class PackedCache(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("b", "h_kv", "d", "k_bits", "v_bits", "G", "R",
                                             "max_tokens")] + \
-               [(n, ctypes.c_void_p) for n in ("Kc", "Ksz", "Vc", "Vsz", "Kf", "Vf", "T", "Tqk",
-                                               "Tqv")]
+               [(n, ctypes.c_void_p) for n in ("blocks", "Kf", "Vf", "T", "Tqk", "Tqv")]
 
 
 @pytest.mark.parametrize("name,b,prefill,steps", [("llama3_8b_gqa_32k", 2, 3000, 3),
@@ -40,13 +39,15 @@ def test_noalloc_matches_decode_attn(name, b, prefill, steps):
         k, v = W.step_kv(w, s)
         cache.append(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
 
-    # the same cache in caller-owned device memory (the documented packed format)
+    # the same cache in caller-owned device memory (the documented block
+    # records and fp16 windows)
     ex = cache.export()
-    dev = {key: torch.from_numpy(arr.view(np.uint8).copy()).cuda() for key, arr in ex.items()}
+    dev = {key: torch.from_numpy(ex[key].view(np.uint8).copy()).cuda() for key in ("Kf", "Vf")}
+    dev["blocks"] = torch.from_numpy(cache.export_records()).cuda()
     T, Tqk, Tqv = cache.lengths()
     cnt = {n: torch.from_numpy(x.astype(np.int32)).cuda() for n, x in (("T", T), ("Tqk", Tqk), ("Tqv", Tqv))}
     pc = PackedCache(w.b, w.h_kv, w.d, w.kbits, w.vbits, w.G, w.R, cap,
-                     *[dev[key].data_ptr() for key in ("Kc", "Ksz", "Vc", "Vsz", "Kf", "Vf")],
+                     *[dev[key].data_ptr() for key in ("blocks", "Kf", "Vf")],
                      *[cnt[n].data_ptr() for n in ("T", "Tqk", "Tqv")])
     fn = K.lib.kivi_decode_attn_noalloc
     fn.argtypes = [ctypes.POINTER(PackedCache), ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
@@ -69,7 +70,7 @@ def test_noalloc_rejects_oversized_scratch():
     buf = torch.zeros(1 << 12, dtype=torch.uint8, device="cuda")
     p = buf.data_ptr()
     # 1024 sequences x 64 query heads x 128k tokens needs far more than 16 MiB of partials
-    pc = PackedCache(1024, 8, 128, 2, 2, 32, 128, 131072, p, p, p, p, p, p, p, p, p)
+    pc = PackedCache(1024, 8, 128, 2, 2, 32, 128, 131072, p, p, p, p, p, p)
     fn = K.lib.kivi_decode_attn_noalloc
     fn.argtypes = [ctypes.POINTER(PackedCache), ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                    ctypes.c_void_p]
