@@ -6,8 +6,8 @@
 // work units of all (sequence, kv head, head group) pairs evenly, so every
 // CTA streams about the same number of bytes whatever the batch and context
 // lengths (no partial last wave).  A unit is one 64-token block; blocks that
-// hold fp16 window tokens (the last few of each sequence) read their window
-// rows through a chain of dependent loads and count MW units each.
+// hold fp16 window tokens (the last few of each sequence) are staged by the
+// whole CTA with one round trip each and count MW units.
 #include <cstdlib>
 
 #include "kivi_internal.cuh"
@@ -57,7 +57,7 @@ DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *T, const int *
     while (p.stages > 2 && (size_t)p.warps * p.stages * sb > 220 * 1024) --p.stages;
 
     // units per pair of each sequence
-    const int MW = env_int("KIVI_DECODE_MIXED_WEIGHT", 8);
+    const int MW = env_int("KIVI_DECODE_MIXED_WEIGHT", 12);
     units->mixed_weight = MW;
     units->start[0] = 0;
     for (int i = 0; i < g.b; ++i) {

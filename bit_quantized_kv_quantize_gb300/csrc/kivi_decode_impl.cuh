@@ -87,6 +87,27 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned by
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
+// L2 eviction-priority policies: the streamed records are read once
+// (evict first); the tail data prefetched long before its use is kept
+// (evict last)
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, unsigned bytes, uint64_t *bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -213,10 +234,10 @@ __host__ __device__ __forceinline__ StageGeom stage_geom(const KiviGeom &g) {
     s.bytes = g.rec_bytes;
     return s;
 }
-// One warp's region of dynamic shared memory: its ring of stages (a mixed
-// block's 16 x d fp16 tile goes into the next slot, which is kept free then);
-// at the end of a segment it also holds the warp's result (m[4], l[4],
-// o[4][d] in fp32).
+// One warp's region of dynamic shared memory: its ring of stages; at the end
+// of a segment it also holds the warp's result (m[4], l[4], o[4][d] in
+// fp32).  Between the two, the CTA stages its mixed blocks across the
+// regions.
 __host__ __device__ __forceinline__ size_t warp_region(const KiviGeom &g, int stages) {
     const size_t sb = stage_geom(g).bytes;
     size_t ring = (size_t)(stages >= 2 ? stages : 2) * sb;
@@ -224,34 +245,57 @@ __host__ __device__ __forceinline__ size_t warp_region(const KiviGeom &g, int st
     size_t m = ring > res ? ring : res;
     return (m + 127) / 128 * 128;
 }
+// the warps' ring barriers and the CTA's mixed-block barrier
 __host__ __device__ __forceinline__ size_t bar_region(int warps, int stages) {
-    return ((size_t)warps * stages * 8 + 127) / 128 * 128;
+    return ((size_t)(warps * stages + 1) * 8 + 127) / 128 * 128;
+}
+// bytes a mixed block stages in the ring: its record, up to 64 key and 64
+// value rows of 2 d bytes, and a zero row
+__host__ __device__ __forceinline__ size_t mixed_region(const KiviGeom &g) {
+    return (size_t)g.rec_bytes + (size_t)(2 * KIVI_KBLK + 1) * (2 * g.d);
+}
+// Rows of tokens [a, b) a block stages from a window ring of `ring` rows (a
+// well-formed cache never holds more than the ring; the clamp keeps reads
+// inside it whatever the counters say).
+__device__ __forceinline__ int rows_to_stage(int a, int b, int ring) { return max(0, min(b - a, ring)); }
+// Copy those rows into consecutive rows at dst: at most two bulk copies (the
+// ring may wrap once); the bytes land on `bar`.
+template <int D>
+__device__ __forceinline__ void copy_rows(unsigned char *dst, const __half *win, int ring, int a, int b,
+                                          uint64_t *bar) {
+    const int n = rows_to_stage(a, b, ring);
+    if (n == 0) return;
+    const int r0 = a % ring;
+    const int n1 = min(n, ring - r0);
+    bulk_g2s(dst, win + (size_t)r0 * D, (unsigned)n1 * D * 2, bar);
+    if (n > n1) bulk_g2s(dst + (size_t)n1 * D * 2, win, (unsigned)(n - n1) * D * 2, bar);
 }
 
 // Stage block kb: one bulk copy of its record (packed keys, key scale/zero
 // rows, packed values, value scale/zero rows, back to back).  Lane 0 issues.
 __device__ __forceinline__ void issue_block(const StageGeom &sg, unsigned char *st, uint64_t *bar,
-                                            const unsigned char *recs, int kb) {
+                                            const unsigned char *recs, int kb, uint64_t policy) {
     if ((threadIdx.x & 31) == 0) {
         mbar_expect_tx(bar, (unsigned)sg.bytes);
-        bulk_g2s(st, recs + (size_t)kb * sg.bytes, (unsigned)sg.bytes, bar);
+        bulk_g2s_hint(st, recs + (size_t)kb * sg.bytes, (unsigned)sg.bytes, bar, policy);
     }
 }
 
 // L2 prefetches for a block that will be read late: its packed data, and the
 // fp16 window rows [a, b) of a ring of `ring` rows (at most `ring` rows, so
 // at most one wrap).
-__device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+__device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes), "l"(policy)
+                 : "memory");
 }
 
 template <int D>
-__device__ __forceinline__ void prefetch_rows(const __half *win, int ring, int a, int b) {
+__device__ __forceinline__ void prefetch_rows(const __half *win, int ring, int a, int b, uint64_t policy) {
     if (a >= b) return;
-    const int r0 = a % ring, n = b - a;
+    const int r0 = a % ring, n = min(b - a, ring);
     const int n1 = min(n, ring - r0);
-    prefetch_l2(win + (size_t)r0 * D, (unsigned)n1 * D * 2);
-    if (n > n1) prefetch_l2(win, (unsigned)(n - n1) * D * 2);
+    prefetch_l2(win + (size_t)r0 * D, (unsigned)n1 * D * 2, policy);
+    if (n > n1) prefetch_l2(win, (unsigned)(n - n1) * D * 2, policy);
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p) {
@@ -348,48 +392,31 @@ __device__ __forceinline__ PFrag p_fragments(float p0, float p1, int tq, int eB)
 
 // ---------------------------------------------------------------------------
 // One 64-token block, read from a shared-memory stage that a bulk TMA copy
-// filled with the block's packed codes and scale/zero rows.
+// filled with the block's record (packed codes and scale/zero rows).
 //
 // MIXED blocks also hold tokens of the fp16 windows (keys >= Tqk, values >=
-// Tqv) or run past the end T.  Their quantized tokens still go through the
-// packed path (value weights masked to the quantized tokens); each 16-token
-// tile with window tokens is copied as fp16 rows (swizzled 16-byte chunks,
-// other rows zero) into a free ring slot and multiplied from there with
-// ldmatrix fragments; scores past T are masked.
+// Tqv) or run past the end T; they are taken one 16-token tile at a time
+// (tmask).  Their quantized tokens still go through the packed path (value
+// weights masked to the quantized tokens); their window tokens are
+// multiplied from fp16 rows in shared memory with ldmatrix fragments (a row
+// of zeros stands in for tokens outside the window); scores past T are
+// masked.
 // ---------------------------------------------------------------------------
 struct MixCtx {
-    int tb;                      // first token of the block
-    int T, Tqk, Tqv, R;
-    const __half *kwin, *vwin;   // fp16 windows of this (sequence, kv head)
-    __half *tile;                // 16 x d fp16 scratch in shared memory
+    int tb;                              // first token of the block
+    int tmask;                           // its 16-token tiles to take (bit t: tile t)
+    int T, Tqk, Tqv;
+    const unsigned char *krows, *vrows;  // window rows of tokens ka.., va.. (stride RS bytes)
+    int ka, va, RS;
+    const unsigned char *zrow;           // 2 d zero bytes
 };
-
-// Copy rows [tau0, tau0 + 16) of an fp16 window into the swizzled tile: row r,
-// 16-byte chunk c lands at chunk c ^ (r & 7); rows outside [lo, T) are zero.
-// The copies are asynchronous (cp.async, zero-filled outside the rows), so
-// all of a lane's chunks are in flight together; the caller's __syncwarp
-// after the return publishes the tile to the other lanes.
-__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-                 "r"(valid ? 16 : 0)
-                 : "memory");
+__device__ __forceinline__ const __half *key_row(const MixCtx &m, int tau) {
+    return reinterpret_cast<const __half *>(tau >= m.Tqk && tau < m.T ? m.krows + (size_t)(tau - m.ka) * m.RS
+                                                                        : m.zrow);
 }
-template <int D>
-__device__ __forceinline__ void stage_window(__half *tile, const __half *win, int ring, int tau0, int lo,
-                                             int T) {
-    constexpr int CPR = D / 8;
-    const int lane = threadIdx.x & 31;
-    const int r0 = tau0 >= 0 ? tau0 % ring : 0;
-#pragma unroll
-    for (int e = lane; e < 16 * CPR; e += 32) {
-        const int r = e / CPR, c = e % CPR;
-        const int tau = tau0 + r;
-        const bool ok = tau >= lo && tau < T;
-        int slot = r0 + r;
-        slot = slot >= ring ? slot - ring : slot;   // ring >= 16 rows: at most one wrap
-        cp_async16(tile + r * D + 8 * (c ^ (r & 7)), win + (size_t)(ok ? slot : 0) * D + 8 * c, ok);
-    }
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+__device__ __forceinline__ const __half *value_row(const MixCtx &m, int tau) {
+    return reinterpret_cast<const __half *>(tau >= m.Tqv && tau < m.T ? m.vrows + (size_t)(tau - m.va) * m.RS
+                                                                        : m.zrow);
 }
 __device__ __forceinline__ uint32_t keep_halves(uint32_t x, bool lo, bool hi) {
     return x & ((lo ? 0x0000FFFFu : 0u) | (hi ? 0xFFFF0000u : 0u));
@@ -455,6 +482,9 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
             W[1][0] = w4.z;
             W[1][NWK - 1] = w4.w;
         }
+        // B = q s split exactly: hi columns RN(q s), lo columns q s - RN(q s)
+        // (fma(q, s, RN(-q s)) with -q on lo lanes, 0 on hi lanes)
+        const uint32_t qn0 = hmul2u(qB[jj][0], nm), qn1 = hmul2u(qB[jj][1], nm);
         uint32_t b0[4], b1[4];
 #pragma unroll
         for (int rp = 0; rp < 4; ++rp) {
@@ -462,12 +492,12 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
             if (rp > (3 >> sh)) continue;   // groups present in this block
             const uint32_t s0 = *reinterpret_cast<const uint32_t *>(sKsz + 2 * rp * D + 16 * jj + 2 * tq);
             const uint32_t s1 = *reinterpret_cast<const uint32_t *>(sKsz + 2 * rp * D + 16 * jj + 8 + 2 * tq);
-            const uint32_t h0 = hmul2u(qB[jj][0], s0), h1 = hmul2u(qB[jj][1], s1);
-            b0[rp] = hfma2u(qB[jj][0], s0, hmul2u(h0, nm));
-            b1[rp] = hfma2u(qB[jj][1], s1, hmul2u(h1, nm));
+            b0[rp] = hfma2u(qB[jj][0], s0, hmul2u(qn0, s0));
+            b1[rp] = hfma2u(qB[jj][1], s1, hmul2u(qn1, s1));
         }
 #pragma unroll
         for (int mm = 0; mm < 4; ++mm) {
+            if (MIXED && !((mx.tmask >> mm) & 1)) continue;
             const int rp = mm >> sh;
             const int wi = (2 * mm) / CPHK, r0 = (2 * mm) % CPHK;
             const uint32_t a0 = unpack<KB, true>(W[0][wi], r0), a1 = unpack<KB, true>(W[0][wi], r0 + 1);
@@ -489,16 +519,17 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
 #pragma unroll
         for (int mm = 0; mm < 4; ++mm) {
             const int tau0 = mx.tb + 16 * mm;
+            if (!((mx.tmask >> mm) & 1)) {   // not taken now
+                p[mm][0] = p[mm][1] = -INFINITY;
+                continue;
+            }
             if (tau0 >= mx.Tqk && tau0 < mx.T) {
-                __syncwarp();
-                stage_window<D>(mx.tile, mx.kwin, mx.R, tau0, mx.Tqk, mx.T);
-                __syncwarp();
+                const __half *krow = key_row(mx, tau0 + rr + 8 * (mi & 1));
                 float f[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int jj = 0; jj < NJ; ++jj) {
-                    const int row = rr + 8 * (mi & 1), ch = 2 * jj + (mi >> 1);
                     uint32_t a[4];
-                    ldsm_x4(a, mx.tile + row * D + 8 * (ch ^ (row & 7)));
+                    ldsm_x4(a, krow + 8 * (2 * jj + (mi >> 1)));
                     mma16816(f, a[0], a[1], a[2], a[3], odd ? 0u : qB[jj][0], odd ? 0u : qB[jj][1]);
                 }
                 p[mm][0] = f[0] * alpha;
@@ -513,6 +544,7 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
     // ---- weights times values, 16 tokens at a time ----
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
+        if (MIXED && !((mx.tmask >> kk) & 1)) continue;
         const PFrag f = p_fragments(p[kk][0], p[kk][1], tq, eB);
         // weights of quantized value tokens (tokens 2tq, 2tq+1 | 2tq+8, 2tq+9)
         uint32_t PH0 = f.PH0, PH1 = f.PH1, PL0 = f.PL0, PL1 = f.PL1;
@@ -524,7 +556,9 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
             PH1 = keep_halves(PH1, q8, q9);
             PL1 = keep_halves(PL1, q8, q9);
         }
+        // B = p s split: hi columns RN(ph s), lo columns (ph s - RN(ph s)) + pl s
         const uint32_t PL0m = hmul2u(PL0, m1), PL1m = hmul2u(PL1, m1);
+        const uint32_t PH0n = hmul2u(PH0, nm), PH1n = hmul2u(PH1, nm);
         const __half *vszk = sVsz + kk * g.vsz_blk;
         uint32_t b0[16], b1[16];
 #pragma unroll
@@ -533,9 +567,8 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
             if (gi >= ngi) continue;
             const uint32_t v0 = *reinterpret_cast<const uint32_t *>(vszk + gi * 16 + 2 * tq);
             const uint32_t v1 = *reinterpret_cast<const uint32_t *>(vszk + gi * 16 + 2 * tq + 8);
-            const uint32_t h0 = hmul2u(PH0, v0), hh1 = hmul2u(PH1, v1);
-            b0[gi] = hfma2u(PL0m, v0, hfma2u(PH0, v0, hmul2u(h0, nm)));
-            b1[gi] = hfma2u(PL1m, v1, hfma2u(PH1, v1, hmul2u(hh1, nm)));
+            b0[gi] = hfma2u(PL0m, v0, hfma2u(PH0, v0, hmul2u(PH0n, v0)));
+            b1[gi] = hfma2u(PL1m, v1, hfma2u(PH1, v1, hmul2u(PH1n, v1)));
         }
         uint32_t Wv[WLV];
         const uint32_t *sVk = sV + kk * g.vc_blk;
@@ -579,15 +612,12 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
             // window value tokens of this tile: fp16 rows, A = rows transposed
             const int tau0 = mx.tb + 16 * kk;
             if (tau0 + 15 >= mx.Tqv && tau0 < mx.T) {
-                __syncwarp();
-                stage_window<D>(mx.tile, mx.vwin, mx.R + 1, tau0, mx.Tqv, mx.T);
-                __syncwarp();
+                const __half *vrow = value_row(mx, tau0 + rr + 8 * (mi >> 1));
                 const uint32_t c0 = odd ? f.PL0 : f.PH0, c1 = odd ? f.PL1 : f.PH1;
 #pragma unroll
                 for (int mm = 0; mm < NJ; ++mm) {
-                    const int row = rr + 8 * (mi >> 1), ch = 2 * mm + (mi & 1);
                     uint32_t a[4];
-                    ldsm_x4_t(a, mx.tile + row * D + 8 * (ch ^ (row & 7)));
+                    ldsm_x4_t(a, vrow + 8 * (2 * mm + (mi & 1)));
                     mma16816(A.oacc[mm], a[0], a[1], a[2], a[3], c0, c1);
                 }
             }
@@ -631,9 +661,12 @@ __device__ __forceinline__ void warp_result(WarpAcc<D> &A, float *wres) {
 // group qg), its blocks whose keys and values are all quantized (one unit
 // each) and its remaining blocks (MW units each), laid end to end; CTA c
 // takes units [c U / C, (c+1) U / C).  Each stretch of one (i, j, qg) inside
-// a CTA is a segment: the CTA's warps share its blocks, merge in shared
-// memory and write one partial; the last CTA to finish a segment of that
-// (i, j, qg) merges all of its partials.
+// a CTA is a segment.  Its fully quantized blocks stream through the warps'
+// rings; its other blocks (those holding fp16 window tokens, at the end of
+// the sequence) are then staged one at a time by the whole CTA, record and
+// window rows with one round trip, and split into 16-token tiles over the
+// warps.  The warps merge in shared memory and write one partial; the last
+// CTA to finish a segment of that (i, j, qg) merges all of its partials.
 // ---------------------------------------------------------------------------
 __host__ __device__ __forceinline__ long long cta_of_unit(long long u, long long U, int C) {
     return ((u + 1) * C - 1) / U;
@@ -667,11 +700,18 @@ __global__ void __launch_bounds__(256, 2)
     // The barriers live for the whole kernel: a warp numbers the blocks it
     // streams across all its segments (seq), block n goes to slot n % stages
     // and completes phase n / stages of that slot's barrier.
-    if (threadIdx.x < nw * plan.stages) mbar_init(bars + threadIdx.x, 1);
+    if (threadIdx.x <= nw * plan.stages) mbar_init(bars + threadIdx.x, 1);
     fence_mbar_init();
     __syncthreads();
     unsigned seq = 0;
-    bool dead = false;   // a wait of this warp timed out: it streams no more blocks
+    bool dead = false;    // a wait of this warp timed out: it streams no more blocks
+    bool cdead = false;   // a wait of the CTA's mixed-block barrier timed out
+    uint64_t *cbar = bars + nw * plan.stages;   // the CTA's mixed-block barrier
+    unsigned cphase = 0;
+    const uint64_t pol_stream = policy_evict_first();
+    // mixed blocks staged per round: as many regions as the ring holds (<= 2)
+    const size_t mreg = mixed_region(g);
+    const int mper = max(1, min(2, (int)(max((size_t)nw * wstride, mreg) / mreg)));
 
     while (u < u_end) {
         if (threadIdx.x == 0) {
@@ -732,89 +772,49 @@ __global__ void __launch_bounds__(256, 2)
         };
         const int nD = first_at_least(nblk);            // blocks with data
         const int xm = min(first_at_least(nfull), nD);  // mixed blocks: [xm, nD)
-        const int nP = xm, nM = nD - xm;
-        // Warps by cost: a mixed block costs MW packed blocks (its window
-        // loads are a chain of dependent reads).  Mixed block k goes to warp
-        // k % nw; the packed blocks fill the warps up to an equal cost, as
-        // contiguous runs.
-        auto packed_of = [&](int w) {
-            const int n1 = nM % nw, nl = nw - n1;   // warps w < n1 hold one more mixed block
-            if (n1 == 0) return nP / nw + (w < nP % nw ? 1 : 0);
-            if (nP <= nl * MW) return w < n1 ? 0 : nP / nl + (w - n1 < nP % nl ? 1 : 0);
-            const int tot = nP + n1 * MW;
-            return tot / nw + (w < tot % nw ? 1 : 0) - (w < n1 ? MW : 0);
-        };
-        int ps = 0;
-        for (int w = 0; w < warp; ++w) ps += packed_of(w);
-        const int pw = dead ? 0 : packed_of(warp);
-        const int cm = dead ? 0 : (nM > warp ? (nM - warp + nw - 1) / nw : 0);
-        const int nb = pw + cm;   // this warp's blocks: pw packed, then cm mixed
-        auto kb_of = [&](int it) { return it < pw ? blk(ps + it) : blk(xm + warp + (it - pw) * nw); };
-        auto mixed = [&](int it) { return it >= pw; };
-        MixCtx mc;
-        mc.tb = 0;
-        mc.T = T;
-        mc.Tqk = Tqk;
-        mc.Tqv = Tqv;
-        mc.R = g.R;
-        mc.kwin = dv.Kf + kf_slice(g, i, j);
-        mc.vwin = dv.Vf + vf_slice(g, i, j);
-        mc.tile = nullptr;
-        // A block is issued ahead only if the block before it is not mixed: a
-        // mixed block uses the next block's slot as its fp16 scratch.
+        // Packed blocks [0, xm) stream through the warps' rings, as
+        // contiguous runs; mixed blocks [xm, nD) follow, one at a time, with
+        // the whole CTA (below).
+        const int pw = dead ? 0 : xm / nw + (warp < xm % nw ? 1 : 0);
+        const int ps = warp * (xm / nw) + min(warp, xm % nw);
+        const int nb = pw;
+        auto kb_of = [&](int it) { return blk(ps + it); };
+        const __half *kwin = dv.Kf + kf_slice(g, i, j), *vwin = dv.Vf + vf_slice(g, i, j);
+        if (threadIdx.x == 0) {
+            // the mixed blocks are read last: bring their records and window
+            // rows into L2 now
+            const uint64_t keep = policy_evict_last();
+            for (int x = xm; x < nD; ++x) {
+                const int kb = blk(x), tb = kb * KIVI_KBLK, te = min(tb + KIVI_KBLK, T);
+                prefetch_l2(recs + (size_t)kb * sg.bytes, (unsigned)sg.bytes, keep);
+                prefetch_rows<D>(kwin, g.R, max(tb, Tqk), te, keep);
+                prefetch_rows<D>(vwin, g.R + 1, max(tb, Tqv), te, keep);
+            }
+        }
         int issued = 0;
         auto ring_slot = [&](int it) { return (int)((seq + (unsigned)it) % (unsigned)plan.stages); };
         auto parity = [&](int it) { return ((seq + (unsigned)it) / (unsigned)plan.stages) & 1u; };
-        while (issued < nb && issued < plan.stages && (issued == 0 || !mixed(issued - 1))) {
+        while (issued < nb && issued < plan.stages) {
             issue_block(sg, myregion + (size_t)ring_slot(issued) * sg.bytes, mybars + ring_slot(issued), recs,
-                        kb_of(issued));
+                        kb_of(issued), pol_stream);
             ++issued;
         }
         __syncwarp();
-        // Mixed blocks come last in a warp's list and are not read ahead: two
-        // blocks before the first of them, bring their packed data and window
-        // rows into L2 so that their loads do not wait on HBM.
-        int first_mixed = nb;
-        while (first_mixed > 0 && mixed(first_mixed - 1)) --first_mixed;
-        const int pf_at = first_mixed - 2 > 0 ? first_mixed - 2 : 0;
+        MixCtx mc;   // unused by the packed path
         int timed_out_at = -1;
         for (int it = 0; it < nb; ++it) {
-            if (it == pf_at && lane == 0) {
-                for (int x = first_mixed; x < nb; ++x) {
-                    const int kb = kb_of(x), tb = kb * KIVI_KBLK, te = min(tb + KIVI_KBLK, T);
-                    prefetch_l2(recs + (size_t)kb * sg.bytes, (unsigned)sg.bytes);
-                    prefetch_rows<D>(mc.kwin, g.R, max(tb, Tqk), te);
-                    prefetch_rows<D>(mc.vwin, g.R + 1, max(tb, Tqv), te);
-                }
-            }
             const int st = ring_slot(it);
-            if (issued <= it) {   // deferred behind a mixed block
-                // the slot held the mixed block's fp16 tiles (generic and
-                // cp.async writes): order them before the bulk copies
-                fence_proxy_async();
-                __syncwarp();
-                issue_block(sg, myregion + (size_t)st * sg.bytes, mybars + st, recs, kb_of(it));
-                issued = it + 1;
-                __syncwarp();
-            }
             if (!__all_sync(0xffffffffu, mbar_wait(mybars + st, parity(it)))) {
                 timed_out_at = it;
                 break;
             }
-            const unsigned char *sb = myregion + (size_t)st * sg.bytes;
-            if (!mixed(it)) {
-                do_block<D, KB, VB, SH, false>(A, qB, sb, sg, g, alpha, mc);
-            } else {
-                mc.tb = kb_of(it) * KIVI_KBLK;
-                mc.tile = reinterpret_cast<__half *>(myregion + (size_t)ring_slot(it + 1) * sg.bytes);
-                do_block<D, KB, VB, SH, true>(A, qB, sb, sg, g, alpha, mc);
-            }
+            do_block<D, KB, VB, SH, false>(A, qB, myregion + (size_t)st * sg.bytes, sg, g, alpha, mc);
             __syncwarp();
             // Refill the slot just read.  Its packed data was only read (by
             // loads whose values the block has consumed): no proxy fence.
-            while (issued < nb && issued <= it + plan.stages && !mixed(issued - 1)) {
+            if (issued < nb) {
                 issue_block(sg, myregion + (size_t)ring_slot(issued) * sg.bytes, mybars + ring_slot(issued), recs,
-                            kb_of(issued));
+                            kb_of(issued), pol_stream);
                 ++issued;
             }
         }
@@ -827,6 +827,69 @@ __global__ void __launch_bounds__(256, 2)
             dead = true;
         }
         seq += (unsigned)nb;
+
+        // ---- mixed blocks: per round the CTA stages up to mper of them,
+        // each block's record and fp16 window rows (a few bulk copies: the
+        // rows are consecutive in their rings) in a region of the ring, with
+        // one round trip; then the warps take their 16-token tiles (tile t
+        // of the round's block k goes to warp (4 k + t) mod nw).  The rows
+        // are not padded: the tiles' ldmatrix reads conflict on banks, a
+        // small cost next to more copies.
+        const int RS = 2 * D;
+        for (int x0 = xm; x0 < nD && !cdead; x0 += mper) {
+            const int nrb = min(mper, nD - x0);
+            fence_proxy_async();   // earlier generic reads and writes of the ring
+            __syncthreads();
+            if (warp == 0) {
+                unsigned bytes = 0;
+                for (int k = 0; k < nrb; ++k) {
+                    const int kb = blk(x0 + k), tb = kb * KIVI_KBLK, te = min(tb + KIVI_KBLK, T);
+                    bytes += sg.bytes + (rows_to_stage(max(tb, Tqk), te, g.R) +
+                                         rows_to_stage(max(tb, Tqv), te, g.R + 1)) * 2 * D;
+                }
+                if (lane == 0) mbar_expect_tx(cbar, bytes);
+                for (int k = 0; k < nrb && lane == 0; ++k) {
+                    const int kb = blk(x0 + k), tb = kb * KIVI_KBLK, te = min(tb + KIVI_KBLK, T);
+                    unsigned char *reg = ring + (size_t)k * mreg;
+                    bulk_g2s(reg, recs + (size_t)kb * sg.bytes, (unsigned)sg.bytes, cbar);
+                    copy_rows<D>(reg + sg.bytes, kwin, g.R, max(tb, Tqk), te, cbar);
+                    copy_rows<D>(reg + sg.bytes + (size_t)KIVI_KBLK * RS, vwin, g.R + 1, max(tb, Tqv), te, cbar);
+                }
+            }
+            for (int k = 0; k < nrb; ++k) {
+                unsigned char *zrow = ring + (size_t)k * mreg + sg.bytes + (size_t)2 * KIVI_KBLK * RS;
+                for (int e = threadIdx.x; e < 2 * D / 16; e += blockDim.x)
+                    reinterpret_cast<uint4 *>(zrow)[e] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncthreads();
+            const bool ok = mbar_wait(cbar, cphase);
+            cphase ^= 1u;
+            if (!__syncthreads_and(ok)) {
+                if (threadIdx.x == 0) atomicOr(dv.status, KIVI_FLAG_WAIT);
+                mbar_wait(cbar, cphase ^ 1u);   // bounded: let the copies land before the ring is reused
+                cdead = true;
+                break;
+            }
+            for (int w4 = warp; w4 < 4 * nrb; w4 += nw) {
+                const int k = w4 >> 2, t = w4 & 3;
+                const int kb = blk(x0 + k), tb = kb * KIVI_KBLK;
+                if (tb + 16 * t >= T || dead) continue;
+                unsigned char *reg = ring + (size_t)k * mreg;
+                mc.tb = tb;
+                mc.tmask = 1 << t;
+                mc.T = T;
+                mc.Tqk = Tqk;
+                mc.Tqv = Tqv;
+                mc.krows = reg + sg.bytes;
+                mc.vrows = reg + sg.bytes + (size_t)KIVI_KBLK * RS;
+                mc.ka = max(tb, Tqk);
+                mc.va = max(tb, Tqv);
+                mc.zrow = reg + sg.bytes + (size_t)2 * KIVI_KBLK * RS;
+                mc.RS = RS;
+                do_block<D, KB, VB, SH, true>(A, qB, reg, sg, g, alpha, mc);
+            }
+        }
+        __syncthreads();   // the ring holds mixed data no longer needed
 
         // ---- merge the warps into this CTA's partial of (i, j, qg) ----
         __syncwarp();
@@ -898,7 +961,9 @@ __global__ void __launch_bounds__(256, 2)
 template <int D, int KB, int VB, int SH>
 cudaError_t launch_t(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, __half *out,
                      const DecodePlan &plan, const DecodeUnits &units, cudaStream_t st) {
-    const size_t smem = bar_region(plan.warps, plan.stages) + (size_t)plan.warps * warp_region(g, plan.stages);
+    size_t rings = (size_t)plan.warps * warp_region(g, plan.stages);
+    if (rings < mixed_region(g)) rings = mixed_region(g);
+    const size_t smem = bar_region(plan.warps, plan.stages) + rings;
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, KB, VB, SH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
