@@ -41,8 +41,9 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) of one decode-attention launch, from an ncu
 # capture of the kernel whose source hash is recorded beside it; reported
-# only while the kernel source is unchanged.
-NCU_TRAFFIC = {}
+# only while the kernel source is unchanged.  (llama3_8b_gqa_32k, the
+# default workload: profiles/decode_kernel_llama3_8b_gqa_32k.md.)
+NCU_TRAFFIC = {"6968604a5ef5bfa4": 205751040 + 3219968}
 
 
 def algorithmic_bytes(w: W.Workload, T, Tqk, Tqv) -> int:
@@ -70,7 +71,7 @@ def load_peaks():
 def source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("kivi_decode.cu", "kivi_internal.cuh"):
+    for f in ("kivi_decode.cu", "kivi_decode_impl.cuh", "kivi_internal.cuh"):
         with open(os.path.join(ROOT, "bit_quantized_kv_quantize_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -375,7 +376,7 @@ def run_ours(args, w):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": "decode_kernel (tensor-core split-K + fp16 tail + last-CTA merge)",
+                     "kernel": "decode_kernel (persistent stream-K over TMA-staged block records, mma.sync, last-CTA merge)",
                      "traffic": NCU_TRAFFIC.get(source_hash())},
         "e2e": {"value": round(e2e_per * 1e3, 3), "unit": "us/step",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
