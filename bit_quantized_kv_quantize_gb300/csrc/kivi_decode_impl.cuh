@@ -697,14 +697,15 @@ __global__ void __launch_bounds__(256, 2)
     __shared__ int s_seg[5];
     __shared__ int s_last;
     __shared__ float sML[8];
-    // The barriers live for the whole kernel: a warp numbers the blocks it
-    // streams across all its segments (seq), block n goes to slot n % stages
-    // and completes phase n / stages of that slot's barrier.
+    // The barriers live for the whole kernel: a warp's n-th block (counted
+    // across all its segments) goes to slot n % stages and completes phase
+    // n / stages of that slot's barrier.
     if (threadIdx.x <= nw * plan.stages) mbar_init(bars + threadIdx.x, 1);
     fence_mbar_init();
     __syncthreads();
-    unsigned seq = 0;
-    bool dead = false;    // a wait of this warp timed out: it streams no more blocks
+    int rslot = 0;         // this warp's next ring slot to consume ...
+    unsigned rphase = 0;   // ... and the phase its barrier completes next
+    bool dead = false;     // a wait of this warp timed out: it streams no more blocks
     bool cdead = false;   // a wait of the CTA's mixed-block barrier timed out
     uint64_t *cbar = bars + nw * plan.stages;   // the CTA's mixed-block barrier
     unsigned cphase = 0;
@@ -791,42 +792,49 @@ __global__ void __launch_bounds__(256, 2)
                 prefetch_rows<D>(vwin, g.R + 1, max(tb, Tqv), te, keep);
             }
         }
+        // Slots and phases advance incrementally: the ring position (rslot,
+        // rphase) of the next block to consume and the slot of the next
+        // block to issue carry over from segment to segment.
         int issued = 0;
-        auto ring_slot = [&](int it) { return (int)((seq + (unsigned)it) % (unsigned)plan.stages); };
-        auto parity = [&](int it) { return ((seq + (unsigned)it) / (unsigned)plan.stages) & 1u; };
+        int islot = rslot;
+        auto next_slot = [&](int sl) { return sl + 1 == plan.stages ? 0 : sl + 1; };
         while (issued < nb && issued < plan.stages) {
-            issue_block(sg, myregion + (size_t)ring_slot(issued) * sg.bytes, mybars + ring_slot(issued), recs,
-                        kb_of(issued), pol_stream);
+            issue_block(sg, myregion + (size_t)islot * sg.bytes, mybars + islot, recs, kb_of(issued), pol_stream);
+            islot = next_slot(islot);
             ++issued;
         }
         __syncwarp();
         MixCtx mc;   // unused by the packed path
         int timed_out_at = -1;
         for (int it = 0; it < nb; ++it) {
-            const int st = ring_slot(it);
-            if (!__all_sync(0xffffffffu, mbar_wait(mybars + st, parity(it)))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(mybars + rslot, rphase))) {
                 timed_out_at = it;
                 break;
             }
-            do_block<D, KB, VB, SH, false>(A, qB, myregion + (size_t)st * sg.bytes, sg, g, alpha, mc);
+            do_block<D, KB, VB, SH, false>(A, qB, myregion + (size_t)rslot * sg.bytes, sg, g, alpha, mc);
             __syncwarp();
             // Refill the slot just read.  Its packed data was only read (by
             // loads whose values the block has consumed): no proxy fence.
             if (issued < nb) {
-                issue_block(sg, myregion + (size_t)ring_slot(issued) * sg.bytes, mybars + ring_slot(issued), recs,
-                            kb_of(issued), pol_stream);
+                issue_block(sg, myregion + (size_t)islot * sg.bytes, mybars + islot, recs, kb_of(issued), pol_stream);
+                islot = next_slot(islot);
                 ++issued;
             }
+            rslot = next_slot(rslot);
+            rphase ^= rslot == 0 ? 1u : 0u;
         }
         if (timed_out_at >= 0) {
             if (lane == 0) atomicOr(dv.status, KIVI_FLAG_WAIT);
             // wait (bounded) for this warp's copies still in flight before
             // its region is reused; the warp then streams nothing more
-            for (int it = timed_out_at; it < issued; ++it) mbar_wait(mybars + ring_slot(it), parity(it));
+            for (int it = timed_out_at; it < issued; ++it) {
+                mbar_wait(mybars + rslot, rphase);
+                rslot = next_slot(rslot);
+                rphase ^= rslot == 0 ? 1u : 0u;
+            }
             acc_reset<D>(A);
             dead = true;
         }
-        seq += (unsigned)nb;
 
         // ---- mixed blocks: per round the CTA stages up to mper of them,
         // each block's record and fp16 window rows (a few bulk copies: the
