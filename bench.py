@@ -233,9 +233,10 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w):
+def workload_config(w, unfused=True):
     T = int(w.lengths().max()) + 1
-    return {"workload": w.name, "b": w.b, "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d,
+    return {"workload": w.name,
+            "step": "kivi_append + kivi_decode_attn" if unfused else "kivi_append_decode (one launch)", "b": w.b, "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d,
             "k_bits": w.kbits, "v_bits": w.vbits, "G": w.G, "R": w.R,
             "context": T if not w.ragged else f"ragged {w.ragged[0]}-{w.ragged[1]}",
             "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)",
@@ -288,8 +289,11 @@ def run_ours(args, w):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
     def step(s):
-        cache.append(kd[s], vd[s])
-        cache.decode(qd[s], out)
+        if (not args.fused):
+            cache.append(kd[s], vd[s])
+            cache.decode(qd[s], out)
+        else:
+            cache.append_decode(kd[s], vd[s], qd[s], out)
 
     for s in range(args.warmup):
         flush.fill_(s)
@@ -341,8 +345,11 @@ def run_ours(args, w):
         kbuf.copy_(pin_k[s], non_blocking=True)
         vbuf.copy_(pin_v[s], non_blocking=True)
         qbuf.copy_(pin_q[s], non_blocking=True)
-        cache.append(kbuf, vbuf)
-        cache.decode(qbuf, out)
+        if (not args.fused):
+            cache.append(kbuf, vbuf)
+            cache.decode(qbuf, out)
+        else:
+            cache.append_decode(kbuf, vbuf, qbuf, out)
         out_h.copy_(out, non_blocking=True)
         b.record(stream)
         e2e_ms.append((a, b))
@@ -368,7 +375,7 @@ def run_ours(args, w):
         "vs_baseline": None,
         "dtype": "u2/u4 codes, f16 in, f32 accumulate",
         "data": "synthetic",
-        "config": workload_config(w),
+        "config": workload_config(w, (not args.fused)),
         "attn_us": round(attn_ms * 1e3, 3),
         "cache_gbs": round(bytes_per / (attn_ms * 1e-3) / 1e9, 1),
         "bytes_per_step": int(bytes_per),
@@ -380,7 +387,7 @@ def run_ours(args, w):
                      "traffic": NCU_TRAFFIC.get(source_hash())},
         "e2e": {"value": round(e2e_per * 1e3, 3), "unit": "us/step",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * (1 + launches),
+        "gpu_launches": args.steps * (launches + (1 if (not args.fused) else 0)),
         "splits": splits,
         "clocks": clk.summary(),
         "source_hash": source_hash(),
@@ -436,6 +443,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused", action="store_true",
+                    help="time a step as kivi_append_decode (one launch) instead of kivi_append + "
+                         "kivi_decode_attn")
     ap.add_argument("--ncu", action="store_true",
                     help="run only prefill, one append and --steps decode calls (profiler captures)")
     args = ap.parse_args(argv)

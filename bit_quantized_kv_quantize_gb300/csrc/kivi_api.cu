@@ -47,6 +47,7 @@ struct kivi_cache {
     bool profiling;
     std::vector<cudaEvent_t> ev;   // pairs
     int nprof;
+    unsigned epoch;   // fused append + decode calls so far (the slices' mflag value)
 };
 
 namespace {
@@ -83,11 +84,88 @@ kivi_status check_handle(kivi_cache_t c) {
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 void free_dev(KiviDev &d) {
-    void *ps[] = {d.blk, d.Kf, d.Vf, d.T, d.Tqk, d.Tqv, d.ticket, d.status, d.part, d.merge_ticket};
+    void *ps[] = {d.blk, d.Kf, d.Vf, d.T, d.Tqk, d.Tqv, d.ticket, d.status, d.part, d.merge_ticket, d.mflag,
+                  d.grid_ticket};
     for (void *p : ps)
         if (p) cudaFree(p);
     memset(&d, 0, sizeof d);
 }
+
+kivi_status check_decode_args(kivi_cache *c, const void *q, int h_q, const void *out) {
+    if (!q || !out) {
+        set_err("q or out is null");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (h_q < 1 || h_q % c->g.h != 0) {
+        set_err("h_q must be a positive multiple of h_kv");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (h_q / c->g.h > KIVI_MAX_QPERKV) {
+        set_err("h_q / h_kv above 8");
+        return KIVI_ERR_UNSUPPORTED;
+    }
+    if (!aligned16(q) || !aligned16(out)) {
+        set_err("q and out must be 16-byte aligned");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    return KIVI_OK;
+}
+
+kivi_status check_append_args(kivi_cache *c, const void *k, const void *v) {
+    if (!k || !v) {
+        set_err("k or v is null");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (!aligned16(k) || !aligned16(v)) {
+        set_err("k and v must be 16-byte aligned");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    for (int i = 0; i < c->g.b; ++i)
+        if (c->T[i] + 1 > c->max_tokens) {
+            set_err("sequence %s%ld is full", "", i);
+            return KIVI_ERR_CAPACITY;
+        }
+    return KIVI_OK;
+}
+
+// host mirror of one append (item 4's lazy maintenance, then the token)
+void advance_mirror(kivi_cache *c) {
+    const int R = c->g.R;
+    for (int i = 0; i < c->g.b; ++i) {
+        if (c->T[i] - c->Tqk[i] == R) c->Tqk[i] += R;
+        if (c->T[i] - c->Tqv[i] == R + 1) c->Tqv[i] += 1;
+        c->T[i] += 1;
+    }
+}
+
+// Plan and launch the decode kernel; units come from (T, Tqk, Tqv).
+kivi_status launch_decode(kivi_cache *c, const void *q, int h_q, void *out, kivi_stream_t stream,
+                          const AppendStep &ap, const int *T, const int *Tqk, const int *Tqv,
+                          const char *what) {
+    DecodeUnits units;
+    DecodePlan plan = kivi_plan_decode(c->g, h_q, T, Tqk, Tqv, c->num_sms, &units);
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (c->profiling && c->nprof < kMaxProfile) {
+        if ((int)c->ev.size() < 2 * (c->nprof + 1)) {
+            cudaEvent_t a, b;
+            if (cudaEventCreate(&a) == cudaSuccess && cudaEventCreate(&b) == cudaSuccess) {
+                c->ev.push_back(a);
+                c->ev.push_back(b);
+            }
+        }
+        if ((int)c->ev.size() >= 2 * (c->nprof + 1)) {
+            e0 = c->ev[2 * c->nprof];
+            e1 = c->ev[2 * c->nprof + 1];
+            c->nprof++;
+        }
+    }
+    cudaError_t e = kivi_launch_decode(c->g, c->dv, (const __half *)q, h_q, (__half *)out, plan, units, ap,
+                                       (cudaStream_t)stream, e0, e1);
+    if (e != cudaSuccess) return fail_cuda(c, e, what);
+    c->last_plan = plan;
+    return KIVI_OK;
+}
+
 
 }  // namespace
 
@@ -157,6 +235,7 @@ kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, in
     c->max_tokens = max_tokens;
     c->profiling = false;
     c->nprof = 0;
+    c->epoch = 0;
     memset(&c->last_plan, 0, sizeof c->last_plan);
     KiviGeom &g = c->g;
     g.b = b; g.h = h_kv; g.d = d; g.kbits = k_bits; g.vbits = v_bits; g.G = G; g.R = R;
@@ -189,6 +268,8 @@ kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, in
         {(void **)&dv.status, 4},
         {(void **)&dv.part, bh * KIVI_MAX_QPERKV * g.smax * (d + 2) * 4},
         {(void **)&dv.merge_ticket, bh * 4 * 4},
+        {(void **)&dv.mflag, bh * 4},
+        {(void **)&dv.grid_ticket, 4},
     };
     for (auto &r : reqs) {
         e = cudaMalloc(r.p, r.bytes);
@@ -284,28 +365,12 @@ kivi_status kivi_append(kivi_cache_t c, const void *k, const void *v, kivi_strea
     g_err[0] = 0;
     kivi_status s = check_handle(c);
     if (s != KIVI_OK) return s;
-    if (!k || !v) {
-        set_err("k or v is null");
-        return KIVI_ERR_INVALID_ARG;
-    }
-    if (!aligned16(k) || !aligned16(v)) {
-        set_err("k and v must be 16-byte aligned");
-        return KIVI_ERR_INVALID_ARG;
-    }
-    for (int i = 0; i < c->g.b; ++i)
-        if (c->T[i] + 1 > c->max_tokens) {
-            set_err("sequence %s%ld is full", "", i);
-            return KIVI_ERR_CAPACITY;
-        }
+    s = check_append_args(c, k, v);
+    if (s != KIVI_OK) return s;
     cudaError_t e = kivi_launch_append(c->g, c->dv, (const __half *)k, (const __half *)v,
                                        (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(c, e, "append");
-    const int R = c->g.R;
-    for (int i = 0; i < c->g.b; ++i) {
-        if (c->T[i] - c->Tqk[i] == R) c->Tqk[i] += R;
-        if (c->T[i] - c->Tqv[i] == R + 1) c->Tqv[i] += 1;
-        c->T[i] += 1;
-    }
+    advance_mirror(c);
     return KIVI_OK;
 }
 
@@ -314,44 +379,32 @@ kivi_status kivi_decode_attn(kivi_cache_t c, const void *q, int h_q, void *out,
     g_err[0] = 0;
     kivi_status s = check_handle(c);
     if (s != KIVI_OK) return s;
-    if (!q || !out) {
-        set_err("q or out is null");
-        return KIVI_ERR_INVALID_ARG;
-    }
-    if (h_q < 1 || h_q % c->g.h != 0) {
-        set_err("h_q must be a positive multiple of h_kv");
-        return KIVI_ERR_INVALID_ARG;
-    }
-    if (h_q / c->g.h > KIVI_MAX_QPERKV) {
-        set_err("h_q / h_kv above 8");
-        return KIVI_ERR_UNSUPPORTED;
-    }
-    if (!aligned16(q) || !aligned16(out)) {
-        set_err("q and out must be 16-byte aligned");
-        return KIVI_ERR_INVALID_ARG;
-    }
-    DecodeUnits units;
-    DecodePlan plan = kivi_plan_decode(c->g, h_q, c->T.data(), c->Tqk.data(), c->Tqv.data(),
-                                       c->num_sms, &units);
-    cudaEvent_t e0 = nullptr, e1 = nullptr;
-    if (c->profiling && c->nprof < kMaxProfile) {
-        if ((int)c->ev.size() < 2 * (c->nprof + 1)) {
-            cudaEvent_t a, b;
-            if (cudaEventCreate(&a) == cudaSuccess && cudaEventCreate(&b) == cudaSuccess) {
-                c->ev.push_back(a);
-                c->ev.push_back(b);
-            }
-        }
-        if ((int)c->ev.size() >= 2 * (c->nprof + 1)) {
-            e0 = c->ev[2 * c->nprof];
-            e1 = c->ev[2 * c->nprof + 1];
-            c->nprof++;
-        }
-    }
-    cudaError_t e = kivi_launch_decode(c->g, c->dv, (const __half *)q, h_q, (__half *)out, plan,
-                                       units, (cudaStream_t)stream, e0, e1);
-    if (e != cudaSuccess) return fail_cuda(c, e, "decode_attn");
-    c->last_plan = plan;
+    s = check_decode_args(c, q, h_q, out);
+    if (s != KIVI_OK) return s;
+    const AppendStep no_append = {nullptr, nullptr, 0u, 0};
+    return launch_decode(c, q, h_q, out, stream, no_append, c->T.data(), c->Tqk.data(), c->Tqv.data(),
+                         "decode_attn");
+}
+
+kivi_status kivi_append_decode(kivi_cache_t c, const void *k, const void *v, const void *q, int h_q,
+                               void *out, kivi_stream_t stream) {
+    g_err[0] = 0;
+    kivi_status s = check_handle(c);
+    if (s != KIVI_OK) return s;
+    s = check_append_args(c, k, v);
+    if (s != KIVI_OK) return s;
+    s = check_decode_args(c, q, h_q, out);
+    if (s != KIVI_OK) return s;
+    // Plan with the blocks the append leaves alone (min(Tqk, Tqv) before it)
+    // as fully quantized and the lengths after it.
+    std::vector<int> Tpost(c->T);
+    for (int i = 0; i < c->g.b; ++i) Tpost[i] += 1;
+    if (++c->epoch == 0) c->epoch = 1;   // mflag words start at 0
+    const AppendStep ap = {(const __half *)k, (const __half *)v, c->epoch, 1};
+    s = launch_decode(c, q, h_q, out, stream, ap, Tpost.data(), c->Tqk.data(), c->Tqv.data(),
+                      "append_decode");
+    if (s != KIVI_OK) return s;
+    advance_mirror(c);
     return KIVI_OK;
 }
 

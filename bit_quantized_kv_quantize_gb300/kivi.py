@@ -22,7 +22,7 @@ EXPORTS = ["kivi_cache_create", "kivi_cache_destroy", "kivi_prefill", "kivi_appe
            "kivi_decode_attn", "kivi_cache_lengths", "kivi_cache_export_sizes",
            "kivi_cache_export", "kivi_cache_check", "kivi_profile_enable", "kivi_profile_read",
            "kivi_decode_plan", "kivi_status_str", "kivi_last_error", "kivi_abi_version",
-           "kivi_decode_attn_noalloc", "kivi_cache_export_records"]
+           "kivi_decode_attn_noalloc", "kivi_cache_export_records", "kivi_append_decode"]
 
 
 class KiviError(RuntimeError):
@@ -138,6 +138,19 @@ class KiviCache:
             out = torch.empty_like(q)
         op = _dev_fp16(out, (self.b, hq, self.d), "out")
         _check(lib.kivi_decode_attn(self._h, qp, hq, op, _stream(stream)))
+        return out
+
+    def append_decode(self, k, v, q, out=None, stream=None):
+        """append(k, v) then decode(q) in one launch; returns out."""
+        import torch
+        hq = q.shape[1]
+        kp = _dev_fp16(k, (self.b, self.h_kv, self.d), "k")
+        vp = _dev_fp16(v, (self.b, self.h_kv, self.d), "v")
+        qp = _dev_fp16(q, (self.b, hq, self.d), "q")
+        if out is None:
+            out = torch.empty_like(q)
+        op = _dev_fp16(out, (self.b, hq, self.d), "out")
+        _check(lib.kivi_append_decode(self._h, kp, vp, qp, hq, op, _stream(stream)))
         return out
 
     # -- inspection ----------------------------------------------------------

@@ -56,6 +56,12 @@ class Pair:
                                 int(Tqv[i]), what=f"{what} seq {i} head {j}")
         assert self.gpu.check() == 0
 
+    def step_fused(self, k, v, q, what=""):
+        """One fused append + decode on the GPU against append then decode in the oracle."""
+        out = self.gpu.append_decode(_dev(k), _dev(v), _dev(q)).float().cpu().numpy()
+        self.ora.append(k, v)
+        return U.compare_output(out, self.ora.decode(q), what)
+
     def check_decode(self, q, what="", pairs=None):
         out = self.gpu.decode(_dev(q)).float().cpu().numpy()
         ref = self.ora.decode(q, pairs=pairs)
@@ -87,6 +93,73 @@ def test_tiny_kivi2_every_step():
         p.append(k, v)
         p.check_state(f"step {s}")
         p.check_decode(W.step_q(w, s), f"step {s}")
+
+
+# ---------------------------------------------------------------------------
+# The fused step (kivi_append_decode): the append's maintenance runs inside
+# the attention kernel.
+# ---------------------------------------------------------------------------
+
+def test_fused_step_tiny_every_step():
+    w = W.WORKLOADS["tiny_kivi2"]
+    p = Pair(w.b, w.h_kv, w.d, w.kbits, w.vbits, w.G, w.R, w.capacity())
+    Kh, Vh, lens = W.prefill_kv(w)
+    p.prefill(Kh, Vh, lens)
+    for s in range(w.steps):
+        k, v = W.step_kv(w, s)
+        p.step_fused(k, v, W.step_q(w, s), f"fused step {s}")
+        p.check_state(f"fused step {s}")
+
+
+FUSED = [
+    # b, h, hq, d, kb, vb, G, R, lens, steps
+    (8, 2, 8, 128, 4, 4, 32, 128, [300, 317, 512, 640, 700, 767, 800, 899], 200),
+    (3, 2, 2, 64, 2, 2, 32, 32, [0, 1, 31], 70),
+    (2, 1, 3, 256, 2, 2, 64, 128, [300, 64], 135),
+    (2, 2, 4, 128, 2, 2, 128, 128, [511, 128], 130),
+]
+
+
+@pytest.mark.parametrize("case", FUSED, ids=[f"fused{i}" for i in range(len(FUSED))])
+def test_fused_step_ragged(case):
+    """Ragged batches over enough fused steps to cross key flushes and value
+    pops in every sequence; outputs every step, the cache every 9th."""
+    b, h, hq, d, kb, vb, G, R, lens, steps = case
+    rng = np.random.default_rng(zlib.crc32(str(case).encode()))
+    p = Pair(b, h, d, kb, vb, G, R, max(lens) + steps + 3)
+    Kh, Vh = _rand_kv(rng, b, h, max(lens), d, kscale=3.0)
+    p.prefill(Kh, Vh, np.array(lens, np.int32))
+    for s in range(steps):
+        k = (rng.standard_normal((b, h, d)) * 3).astype(np.float16)
+        v = rng.standard_normal((b, h, d)).astype(np.float16)
+        q = rng.standard_normal((b, hq, d)).astype(np.float16)
+        p.step_fused(k, v, q, f"fused step {s}")
+        if s % 9 == 0 or s == steps - 1:
+            p.check_state(f"fused step {s}")
+
+
+def test_fused_step_matches_two_calls():
+    """Same inputs through kivi_append_decode and through kivi_append +
+    kivi_decode_attn: identical caches, outputs within the tolerance."""
+    w = W.small(W.WORKLOADS["llama3_8b_gqa_32k"], b=2, prefill=3000)
+    caches = [K.KiviCache(w.b, w.h_kv, w.d, w.kbits, w.vbits, w.G, w.R, 3200) for _ in range(2)]
+    Kh, Vh, lens = W.prefill_kv(w)
+    for c in caches:
+        c.prefill(_dev(Kh), _dev(Vh), lens)
+    for s in range(140):
+        k, v = W.step_kv(w, s)
+        q = _dev(W.step_q(w, s))
+        a = caches[0].append_decode(_dev(k), _dev(v), q).float().cpu().numpy()
+        caches[1].append(_dev(k), _dev(v))
+        b_ = caches[1].decode(q).float().cpu().numpy()
+        U.compare_output(a, b_, f"step {s}")
+    ea, eb = caches[0].export(), caches[1].export()
+    for key in ea:
+        assert np.array_equal(ea[key], eb[key]), key
+    assert all(np.array_equal(x, y) for x, y in zip(caches[0].lengths(), caches[1].lengths()))
+    assert caches[0].check() == 0 and caches[1].check() == 0
+    for c in caches:
+        c.close()
 
 
 # ---------------------------------------------------------------------------
