@@ -47,7 +47,6 @@ struct kivi_cache {
     bool profiling;
     std::vector<cudaEvent_t> ev;   // pairs
     int nprof;
-    unsigned epoch;   // fused append + decode calls so far (the slices' mflag value)
 };
 
 namespace {
@@ -84,8 +83,7 @@ kivi_status check_handle(kivi_cache_t c) {
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 void free_dev(KiviDev &d) {
-    void *ps[] = {d.blk, d.Kf, d.Vf, d.T, d.Tqk, d.Tqv, d.ticket, d.status, d.part, d.merge_ticket, d.mflag,
-                  d.grid_ticket};
+    void *ps[] = {d.blk, d.Kf, d.Vf, d.T, d.Tqk, d.Tqv, d.ticket, d.status, d.part, d.merge_ticket};
     for (void *p : ps)
         if (p) cudaFree(p);
     memset(&d, 0, sizeof d);
@@ -140,8 +138,7 @@ void advance_mirror(kivi_cache *c) {
 
 // Plan and launch the decode kernel; units come from (T, Tqk, Tqv).
 kivi_status launch_decode(kivi_cache *c, const void *q, int h_q, void *out, kivi_stream_t stream,
-                          const AppendStep &ap, const int *T, const int *Tqk, const int *Tqv,
-                          const char *what) {
+                          const int *T, const int *Tqk, const int *Tqv, const char *what) {
     DecodeUnits units;
     DecodePlan plan = kivi_plan_decode(c->g, h_q, T, Tqk, Tqv, c->num_sms, &units);
     cudaEvent_t e0 = nullptr, e1 = nullptr;
@@ -159,7 +156,7 @@ kivi_status launch_decode(kivi_cache *c, const void *q, int h_q, void *out, kivi
             c->nprof++;
         }
     }
-    cudaError_t e = kivi_launch_decode(c->g, c->dv, (const __half *)q, h_q, (__half *)out, plan, units, ap,
+    cudaError_t e = kivi_launch_decode(c->g, c->dv, (const __half *)q, h_q, (__half *)out, plan, units,
                                        (cudaStream_t)stream, e0, e1);
     if (e != cudaSuccess) return fail_cuda(c, e, what);
     c->last_plan = plan;
@@ -235,7 +232,6 @@ kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, in
     c->max_tokens = max_tokens;
     c->profiling = false;
     c->nprof = 0;
-    c->epoch = 0;
     memset(&c->last_plan, 0, sizeof c->last_plan);
     KiviGeom &g = c->g;
     g.b = b; g.h = h_kv; g.d = d; g.kbits = k_bits; g.vbits = v_bits; g.G = G; g.R = R;
@@ -268,8 +264,6 @@ kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, in
         {(void **)&dv.status, 4},
         {(void **)&dv.part, bh * KIVI_MAX_QPERKV * g.smax * (d + 2) * 4},
         {(void **)&dv.merge_ticket, bh * 4 * 4},
-        {(void **)&dv.mflag, bh * 4},
-        {(void **)&dv.grid_ticket, 4},
     };
     for (auto &r : reqs) {
         e = cudaMalloc(r.p, r.bytes);
@@ -381,9 +375,7 @@ kivi_status kivi_decode_attn(kivi_cache_t c, const void *q, int h_q, void *out,
     if (s != KIVI_OK) return s;
     s = check_decode_args(c, q, h_q, out);
     if (s != KIVI_OK) return s;
-    const AppendStep no_append = {nullptr, nullptr, 0u, 0};
-    return launch_decode(c, q, h_q, out, stream, no_append, c->T.data(), c->Tqk.data(), c->Tqv.data(),
-                         "decode_attn");
+    return launch_decode(c, q, h_q, out, stream, c->T.data(), c->Tqk.data(), c->Tqv.data(), "decode_attn");
 }
 
 kivi_status kivi_append_decode(kivi_cache_t c, const void *k, const void *v, const void *q, int h_q,
@@ -395,17 +387,11 @@ kivi_status kivi_append_decode(kivi_cache_t c, const void *k, const void *v, con
     if (s != KIVI_OK) return s;
     s = check_decode_args(c, q, h_q, out);
     if (s != KIVI_OK) return s;
-    // Plan with the blocks the append leaves alone (min(Tqk, Tqv) before it)
-    // as fully quantized and the lengths after it.
-    std::vector<int> Tpost(c->T);
-    for (int i = 0; i < c->g.b; ++i) Tpost[i] += 1;
-    if (++c->epoch == 0) c->epoch = 1;   // mflag words start at 0
-    const AppendStep ap = {(const __half *)k, (const __half *)v, c->epoch, 1};
-    s = launch_decode(c, q, h_q, out, stream, ap, Tpost.data(), c->Tqk.data(), c->Tqv.data(),
-                      "append_decode");
-    if (s != KIVI_OK) return s;
+    cudaError_t e = kivi_launch_append(c->g, c->dv, (const __half *)k, (const __half *)v,
+                                       (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail_cuda(c, e, "append_decode");
     advance_mirror(c);
-    return KIVI_OK;
+    return launch_decode(c, q, h_q, out, stream, c->T.data(), c->Tqk.data(), c->Tqv.data(), "append_decode");
 }
 
 kivi_status kivi_cache_lengths(kivi_cache_t c, int32_t *T, int32_t *Tqk, int32_t *Tqv) {

@@ -1,6 +1,5 @@
-// kivi_append_impl.cuh -- the append step of one (sequence, kv head): the
-// lazy maintenance of the residual windows, then the new token.  Shared by
-// the append kernel and the fused append + decode kernel.
+// kivi_append_impl.cuh -- the append step of one (sequence, kv head) slice:
+// the lazy maintenance of the residual windows, then the new token.
 //
 // Method: "Literature audit -- Group 2", section 1 KIVI, core algorithm
 // item 4: when the key window holds R tokens it is quantized as R / G
@@ -28,6 +27,18 @@ __device__ __forceinline__ void append_pair(const KiviGeom &g, const KiviDev &dv
     const int d = g.d, R = g.R;
     const bool flush = (T - Tqk) == R;
     const bool pop = (T - Tqv) == R + 1;
+    // One round trip for the rows this step needs: the new key and value
+    // (kept in registers, written last) and the value leaving the queue.
+    const int nv8 = d / 8;   // 16-byte chunks per row
+    __shared__ __align__(16) __half s_row[256];   // d <= 256
+    uint4 kn_c = make_uint4(0u, 0u, 0u, 0u), vn_c = kn_c;
+    if ((int)threadIdx.x < nv8) {
+        kn_c = reinterpret_cast<const uint4 *>(knew + ((size_t)i * g.h + j) * d)[threadIdx.x];
+        vn_c = reinterpret_cast<const uint4 *>(vnew + ((size_t)i * g.h + j) * d)[threadIdx.x];
+        if (pop)
+            reinterpret_cast<uint4 *>(s_row)[threadIdx.x] = reinterpret_cast<const uint4 *>(
+                dv.Vf + vf_slice(g, i, j) + (size_t)(Tqv % (R + 1)) * d)[threadIdx.x];
+    }
     const __half *kf = dv.Kf + kf_slice(g, i, j);
     __half *kfw = dv.Kf + kf_slice(g, i, j);
     __half *vfw = dv.Vf + vf_slice(g, i, j);
@@ -77,8 +88,8 @@ __device__ __forceinline__ void append_pair(const KiviGeom &g, const KiviDev &dv
     }
 
     if (pop) {
-        // value token Tqv, slot Tqv % (R + 1)
-        const __half *x = dv.Vf + vf_slice(g, i, j) + (size_t)(Tqv % (R + 1)) * d;
+        // value token Tqv (slot Tqv % (R + 1)), staged in s_row
+        const __half *x = s_row;
         const int ngi = d / g.G;
         const int vb = Tqv / KIVI_VBLK, tt = Tqv % KIVI_VBLK;
         __half *vsz = vsz_halves(g, dv.blk, i, j, vb);
@@ -121,10 +132,8 @@ __device__ __forceinline__ void append_pair(const KiviGeom &g, const KiviDev &dv
     }
     __syncthreads();   // maintenance has read the slots the new token overwrites
 
-    const __half *kn = knew + ((size_t)i * g.h + j) * d;
-    const __half *vn = vnew + ((size_t)i * g.h + j) * d;
-    for (int c = threadIdx.x; c < d / 8; c += blockDim.x) {
-        reinterpret_cast<uint4 *>(kfw + (size_t)(T % R) * d)[c] = reinterpret_cast<const uint4 *>(kn)[c];
-        reinterpret_cast<uint4 *>(vfw + (size_t)(T % (R + 1)) * d)[c] = reinterpret_cast<const uint4 *>(vn)[c];
+    if ((int)threadIdx.x < nv8) {
+        reinterpret_cast<uint4 *>(kfw + (size_t)(T % R) * d)[threadIdx.x] = kn_c;
+        reinterpret_cast<uint4 *>(vfw + (size_t)(T % (R + 1)) * d)[threadIdx.x] = vn_c;
     }
 }

@@ -13,14 +13,11 @@
 #include "kivi_internal.cuh"
 
 cudaError_t kivi_launch_decode_d64(const KiviGeom &, const KiviDev &, const __half *, int, __half *,
-                                   const DecodePlan &, const DecodeUnits &, const AppendStep &,
-                                    cudaStream_t);
+                                   const DecodePlan &, const DecodeUnits &, cudaStream_t);
 cudaError_t kivi_launch_decode_d128(const KiviGeom &, const KiviDev &, const __half *, int, __half *,
-                                    const DecodePlan &, const DecodeUnits &, const AppendStep &,
-                                    cudaStream_t);
+                                    const DecodePlan &, const DecodeUnits &, cudaStream_t);
 cudaError_t kivi_launch_decode_d256(const KiviGeom &, const KiviDev &, const __half *, int, __half *,
-                                    const DecodePlan &, const DecodeUnits &, const AppendStep &,
-                                    cudaStream_t);
+                                    const DecodePlan &, const DecodeUnits &, cudaStream_t);
 
 namespace {
 int env_int(const char *name, int dflt) {
@@ -100,13 +97,13 @@ DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *T, const int *
 
 cudaError_t kivi_launch_decode(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq,
                                __half *out, const DecodePlan &plan, const DecodeUnits &units,
-                               const AppendStep &ap, cudaStream_t st, cudaEvent_t ev0, cudaEvent_t ev1) {
+                               cudaStream_t st, cudaEvent_t ev0, cudaEvent_t ev1) {
     if (ev0) cudaEventRecord(ev0, st);
     cudaError_t e;
     switch (g.d) {
-    case 64: e = kivi_launch_decode_d64(g, dv, q, hq, out, plan, units, ap, st); break;
-    case 128: e = kivi_launch_decode_d128(g, dv, q, hq, out, plan, units, ap, st); break;
-    default: e = kivi_launch_decode_d256(g, dv, q, hq, out, plan, units, ap, st); break;
+    case 64: e = kivi_launch_decode_d64(g, dv, q, hq, out, plan, units, st); break;
+    case 128: e = kivi_launch_decode_d128(g, dv, q, hq, out, plan, units, st); break;
+    default: e = kivi_launch_decode_d256(g, dv, q, hq, out, plan, units, st); break;
     }
     if (ev1) cudaEventRecord(ev1, st);
     return e;

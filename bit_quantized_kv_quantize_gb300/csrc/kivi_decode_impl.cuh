@@ -29,7 +29,7 @@
 // log2(e) / sqrt(d)); the last CTA to finish a pair merges its partials with
 // log-sum-exp weights and writes the fp16 output.
 #pragma once
-#include "kivi_append_impl.cuh"
+#include "kivi_internal.cuh"
 
 namespace {
 
@@ -672,40 +672,10 @@ __host__ __device__ __forceinline__ long long cta_of_unit(long long u, long long
     return ((u + 1) * C - 1) / U;
 }
 
-// Fused append (ap.on): CTA c first appends the token to the slices p = c,
-// c + C, ... (append_pair) and publishes each with mflag[p] = epoch.  The
-// device counters keep their pre-append values during the launch; every CTA
-// derives the post-append ones, and the last CTA to finish writes them.
-// The append only touches blocks from min(Tqk, Tqv) / 64 on (before the
-// append) and the fp16 windows, so fully quantized blocks below that stream
-// at once; the others go through the CTA's window-block phase, which waits
-// (bounded) for the slice's flag first.
-__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// bounded: false if the flag did not reach `epoch`
-__device__ __forceinline__ bool wait_flag(const unsigned *p, unsigned epoch) {
-    for (int it = 0; it < (1 << 22); ++it) {
-        if (ld_acquire(p) == epoch) {
-            // the slice was written through the generic proxy; the bulk
-            // copies that read it next go through the async proxy
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            return true;
-        }
-        __nanosleep(64);
-    }
-    return false;
-}
-
 template <int D, int KB, int VB, int SH>
 __global__ void __launch_bounds__(256, 2)
     decode_kernel(KiviGeom g, KiviDev dv, const __half *__restrict__ q, int hq,
-                  __half *__restrict__ out, DecodePlan plan, DecodeUnits units, AppendStep ap) {
+                  __half *__restrict__ out, DecodePlan plan, DecodeUnits units) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int NJ = D / 16;
     const int nw = blockDim.x >> 5;
@@ -733,21 +703,6 @@ __global__ void __launch_bounds__(256, 2)
     if (threadIdx.x <= nw * plan.stages) mbar_init(bars + threadIdx.x, 1);
     fence_mbar_init();
     __syncthreads();
-    if (ap.on) {
-        for (int p = c; p < g.b * g.h; p += C) {
-            const int ai = p / g.h, aj = p % g.h;
-            const int T0 = dv.T[ai], Tqk0 = dv.Tqk[ai], Tqv0 = dv.Tqv[ai];
-            if (append_counters_ok(g, T0, Tqk0, Tqv0))
-                append_pair(g, dv, ap.k, ap.v, ai, aj, T0, Tqk0, Tqv0);
-            else if (threadIdx.x == 0)
-                atomicOr(dv.status, KIVI_FLAG_COUNTER);
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                __threadfence();
-                st_release(dv.mflag + p, ap.epoch);
-            }
-        }
-    }
     int rslot = 0;         // this warp's next ring slot to consume ...
     unsigned rphase = 0;   // ... and the phase its barrier completes next
     bool dead = false;     // a wait of this warp timed out: it streams no more blocks
@@ -781,15 +736,8 @@ __global__ void __launch_bounds__(256, 2)
         const int i = s_seg[0], jq = s_seg[1], o0 = s_seg[2], o1 = s_seg[3], Wi = s_seg[4];
         const int j = jq / QG, qg = jq % QG;
         const int e0 = qg * 4, nh = min(4, hg - e0);
-        int T = dv.T[i], Tqk = dv.Tqk[i], Tqv = dv.Tqv[i];
-        // blocks below nfull stream through the warps (fused append: those
-        // below the pre-append count, which the append leaves alone)
+        const int T = dv.T[i], Tqk = dv.Tqk[i], Tqv = dv.Tqv[i];
         const int nfull = min(Tqk, Tqv) / KIVI_KBLK;
-        if (ap.on && append_counters_ok(g, T, Tqk, Tqv)) {
-            Tqk += (T - Tqk) == g.R ? g.R : 0;
-            Tqv += (T - Tqv) == g.R + 1 ? 1 : 0;
-            T += 1;
-        }
         const int nblk = (T + KIVI_KBLK - 1) / KIVI_KBLK;
         const int nfh = units.full[i];
         const int MW = units.mixed_weight;
@@ -899,9 +847,6 @@ __global__ void __launch_bounds__(256, 2)
         for (int x0 = xm; x0 < nD && !cdead; x0 += mper) {
             const int nrb = min(mper, nD - x0);
             fence_proxy_async();   // earlier generic reads and writes of the ring
-            __syncthreads();
-            if (ap.on && threadIdx.x == 0 && !wait_flag(dv.mflag + (size_t)i * g.h + j, ap.epoch))
-                atomicOr(dv.status, KIVI_FLAG_WAIT);
             __syncthreads();
             if (warp == 0) {
                 unsigned bytes = 0;
@@ -1019,60 +964,41 @@ __global__ void __launch_bounds__(256, 2)
         __syncthreads();
         u += o1 - o0;
     }
-    if (ap.on) {   // the last CTA to finish writes the post-append counters
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            __threadfence();
-            s_last = atomicAdd(dv.grid_ticket, 1u) == (unsigned)C - 1u;
-        }
-        __syncthreads();
-        if (s_last) {
-            __threadfence();
-            for (int si = threadIdx.x; si < g.b; si += blockDim.x) {
-                const int T0 = dv.T[si], Tqk0 = dv.Tqk[si], Tqv0 = dv.Tqv[si];
-                if (!append_counters_ok(g, T0, Tqk0, Tqv0)) continue;
-                dv.Tqk[si] = Tqk0 + ((T0 - Tqk0) == g.R ? g.R : 0);
-                dv.Tqv[si] = Tqv0 + ((T0 - Tqv0) == g.R + 1 ? 1 : 0);
-                dv.T[si] = T0 + 1;
-            }
-            if (threadIdx.x == 0) *dv.grid_ticket = 0u;
-        }
-    }
 }
 
 template <int D, int KB, int VB, int SH>
 cudaError_t launch_t(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, __half *out,
-                     const DecodePlan &plan, const DecodeUnits &units, const AppendStep &ap, cudaStream_t st) {
+                     const DecodePlan &plan, const DecodeUnits &units, cudaStream_t st) {
     size_t rings = (size_t)plan.warps * warp_region(g, plan.stages);
     if (rings < mixed_region(g)) rings = mixed_region(g);
     const size_t smem = bar_region(plan.warps, plan.stages) + rings;
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, KB, VB, SH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    decode_kernel<D, KB, VB, SH><<<plan.ctas, plan.warps * 32, smem, st>>>(g, dv, q, hq, out, plan, units, ap);
+    decode_kernel<D, KB, VB, SH><<<plan.ctas, plan.warps * 32, smem, st>>>(g, dv, q, hq, out, plan, units);
     return cudaGetLastError();
 }
 
 template <int D, int KB, int VB>
 cudaError_t launch_g(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, __half *out,
-                     const DecodePlan &plan, const DecodeUnits &units, const AppendStep &ap, cudaStream_t st) {
+                     const DecodePlan &plan, const DecodeUnits &units, cudaStream_t st) {
     switch (g.G) {
-    case 16: return launch_t<D, KB, VB, 0>(g, dv, q, hq, out, plan, units, ap, st);
-    case 32: return launch_t<D, KB, VB, 1>(g, dv, q, hq, out, plan, units, ap, st);
-    case 64: return launch_t<D, KB, VB, 2>(g, dv, q, hq, out, plan, units, ap, st);
+    case 16: return launch_t<D, KB, VB, 0>(g, dv, q, hq, out, plan, units, st);
+    case 32: return launch_t<D, KB, VB, 1>(g, dv, q, hq, out, plan, units, st);
+    case 64: return launch_t<D, KB, VB, 2>(g, dv, q, hq, out, plan, units, st);
     default:
-        if constexpr (D >= 128) return launch_t<D, KB, VB, 3>(g, dv, q, hq, out, plan, units, ap, st);
+        if constexpr (D >= 128) return launch_t<D, KB, VB, 3>(g, dv, q, hq, out, plan, units, st);
         return cudaErrorInvalidValue;
     }
 }
 
 template <int D>
 cudaError_t launch_d(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, __half *out,
-                     const DecodePlan &plan, const DecodeUnits &units, const AppendStep &ap, cudaStream_t st) {
-    if (g.kbits == 2 && g.vbits == 2) return launch_g<D, 2, 2>(g, dv, q, hq, out, plan, units, ap, st);
-    if (g.kbits == 2 && g.vbits == 4) return launch_g<D, 2, 4>(g, dv, q, hq, out, plan, units, ap, st);
-    if (g.kbits == 4 && g.vbits == 2) return launch_g<D, 4, 2>(g, dv, q, hq, out, plan, units, ap, st);
-    return launch_g<D, 4, 4>(g, dv, q, hq, out, plan, units, ap, st);
+                     const DecodePlan &plan, const DecodeUnits &units, cudaStream_t st) {
+    if (g.kbits == 2 && g.vbits == 2) return launch_g<D, 2, 2>(g, dv, q, hq, out, plan, units, st);
+    if (g.kbits == 2 && g.vbits == 4) return launch_g<D, 2, 4>(g, dv, q, hq, out, plan, units, st);
+    if (g.kbits == 4 && g.vbits == 2) return launch_g<D, 4, 2>(g, dv, q, hq, out, plan, units, st);
+    return launch_g<D, 4, 4>(g, dv, q, hq, out, plan, units, st);
 }
 
 }  // namespace

@@ -73,17 +73,6 @@ struct KiviDev {
     unsigned *status;       // anomaly flags
     float *part;            // decode partials [b][h * KIVI_MAX_QPERKV][smax][d + 2]
     unsigned *merge_ticket; // [b][h] arrivals of decode CTAs (split-K merge)
-    unsigned *mflag;        // [b][h] epoch of the last fused append done for the slice
-    unsigned *grid_ticket;  // CTAs of a fused append + decode launch that have finished
-};
-
-// The append a fused append + decode launch performs before its attention
-// (on = 0: a plain decode).  k, v: fp16 [b][h][d] device; epoch: the value
-// the slices' mflag words take once their append is done (never 0).
-struct AppendStep {
-    const __half *k, *v;
-    unsigned epoch;
-    int on;
 };
 
 struct SeqLens {
@@ -254,4 +243,4 @@ DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *T, const int *
 int kivi_partial_slots(int b, int h, int num_sms);
 cudaError_t kivi_launch_decode(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq,
                                __half *out, const DecodePlan &plan, const DecodeUnits &units,
-                               const AppendStep &ap, cudaStream_t st, cudaEvent_t ev0, cudaEvent_t ev1);
+                               cudaStream_t st, cudaEvent_t ev0, cudaEvent_t ev1);

@@ -115,8 +115,7 @@ extern "C" kivi_status kivi_decode_attn_noalloc(const kivi_packed_cache *pc, con
     dv.part = reinterpret_cast<float *>(scratch);
     dv.merge_ticket = reinterpret_cast<unsigned *>(scratch + ticket_off);
     dv.status = reinterpret_cast<unsigned *>(scratch + status_off);
-    const AppendStep no_append = {nullptr, nullptr, 0u, 0};
-    e = kivi_launch_decode(g, dv, (const __half *)q, h_q, (__half *)out, plan, units, no_append, st, nullptr,
+    e = kivi_launch_decode(g, dv, (const __half *)q, h_q, (__half *)out, plan, units, st, nullptr,
                            nullptr);
     if (e != cudaSuccess) return fail(KIVI_ERR_CUDA, cudaGetErrorString(e));
     return KIVI_OK;

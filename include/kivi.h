@@ -102,17 +102,10 @@ kivi_status kivi_append(kivi_cache_t c, const void *k, const void *v, kivi_strea
 kivi_status kivi_decode_attn(kivi_cache_t c, const void *q, int h_q, void *out,
                              kivi_stream_t stream);
 
-/* One decode step in one launch: the effect of kivi_append(k, v) followed by
- * kivi_decode_attn(q, h_q, out) -- the attention sees the appended token and
- * the step's maintenance.  ("Literature audit -- Group 2", section 1 KIVI,
- * stated limitations: the quantization work of decode is not fused with the
- * neighbouring operations; here the append's maintenance runs inside the
- * attention kernel, overlapped with the streaming of the blocks it does not
- * touch.)  Arguments, layouts and preconditions as those two calls; both
- * sets of arguments are validated before any work, so a failed call changes
- * nothing (KIVI_ERR_CAPACITY if a sequence is full).  Outputs agree with the
- * two-call sequence within the attention tolerance (the work split, hence
- * the fp32 summation order, may differ); the cache is bit-identical. */
+/* One decode step in one call: kivi_append(k, v) then kivi_decode_attn(q,
+ * h_q, out), launched back to back on `stream` once both sets of arguments
+ * have been validated (a failed call changes nothing; KIVI_ERR_CAPACITY if a
+ * sequence is full).  Results are those of the two calls. */
 kivi_status kivi_append_decode(kivi_cache_t c, const void *k, const void *v, const void *q, int h_q,
                                void *out, kivi_stream_t stream);
 
