@@ -773,13 +773,12 @@ __global__ void __launch_bounds__(256, 2)
         };
         const int nD = first_at_least(nblk);            // blocks with data
         const int xm = min(first_at_least(nfull), nD);  // mixed blocks: [xm, nD)
-        // Packed blocks [0, xm) stream through the warps' rings, as
-        // contiguous runs; mixed blocks [xm, nD) follow, one at a time, with
-        // the whole CTA (below).
-        const int pw = dead ? 0 : xm / nw + (warp < xm % nw ? 1 : 0);
-        const int ps = warp * (xm / nw) + min(warp, xm % nw);
-        const int nb = pw;
-        auto kb_of = [&](int it) { return blk(ps + it); };
+        // Packed blocks [0, xm) stream through the warps' rings, interleaved
+        // (warp w takes blocks w, w + nw, ...: the CTA's warps read adjacent
+        // records together); mixed blocks [xm, nD) follow, one at a time,
+        // with the whole CTA (below).
+        int taken = 0;   // blocks this warp has taken
+        auto grab = [&]() { return warp + nw * taken++; };
         const __half *kwin = dv.Kf + kf_slice(g, i, j), *vwin = dv.Vf + vf_slice(g, i, j);
         if (threadIdx.x == 0) {
             // the mixed blocks are read last: bring their records and window
@@ -795,39 +794,43 @@ __global__ void __launch_bounds__(256, 2)
         // Slots and phases advance incrementally: the ring position (rslot,
         // rphase) of the next block to consume and the slot of the next
         // block to issue carry over from segment to segment.
-        int issued = 0;
+        int issued = 0, consumed = 0;
+        bool more = !dead;   // blocks may be left to take
         int islot = rslot;
         auto next_slot = [&](int sl) { return sl + 1 == plan.stages ? 0 : sl + 1; };
-        while (issued < nb && issued < plan.stages) {
-            issue_block(sg, myregion + (size_t)islot * sg.bytes, mybars + islot, recs, kb_of(issued), pol_stream);
+        auto take_and_issue = [&]() {
+            const int x = grab();
+            if (x >= xm) {
+                more = false;
+                return;
+            }
+            issue_block(sg, myregion + (size_t)islot * sg.bytes, mybars + islot, recs, blk(x), pol_stream);
             islot = next_slot(islot);
             ++issued;
-        }
+        };
+        while (more && issued < plan.stages) take_and_issue();
         __syncwarp();
         MixCtx mc;   // unused by the packed path
-        int timed_out_at = -1;
-        for (int it = 0; it < nb; ++it) {
+        bool timed_out = false;
+        while (consumed < issued) {
             if (!__all_sync(0xffffffffu, mbar_wait(mybars + rslot, rphase))) {
-                timed_out_at = it;
+                timed_out = true;
                 break;
             }
             do_block<D, KB, VB, SH, false>(A, qB, myregion + (size_t)rslot * sg.bytes, sg, g, alpha, mc);
             __syncwarp();
             // Refill the slot just read.  Its packed data was only read (by
             // loads whose values the block has consumed): no proxy fence.
-            if (issued < nb) {
-                issue_block(sg, myregion + (size_t)islot * sg.bytes, mybars + islot, recs, kb_of(issued), pol_stream);
-                islot = next_slot(islot);
-                ++issued;
-            }
+            if (more) take_and_issue();
             rslot = next_slot(rslot);
             rphase ^= rslot == 0 ? 1u : 0u;
+            ++consumed;
         }
-        if (timed_out_at >= 0) {
+        if (timed_out) {
             if (lane == 0) atomicOr(dv.status, KIVI_FLAG_WAIT);
             // wait (bounded) for this warp's copies still in flight before
             // its region is reused; the warp then streams nothing more
-            for (int it = timed_out_at; it < issued; ++it) {
+            for (; consumed < issued; ++consumed) {
                 mbar_wait(mybars + rslot, rphase);
                 rslot = next_slot(rslot);
                 rphase ^= rslot == 0 ? 1u : 0u;
@@ -934,30 +937,42 @@ __global__ void __launch_bounds__(256, 2)
         }
         __syncthreads();
         if (s_last) {
+            // Merge the pair's partials: their (m, l) come into shared memory
+            // with one round trip, the log-sum-exp weights are formed there,
+            // then each output reads its accumulators once.  The ring is
+            // free: the warps' results were merged above.
             __threadfence();
+            float *sm_m = reinterpret_cast<float *>(ring);   // [nh][np]
+            float *sm_w = sm_m + 4 * np;                      // [nh][np]
+            for (int x = threadIdx.x; x < nh * np; x += blockDim.x) {
+                const int e = x / np, y = x % np;
+                const float *pp = part + (((size_t)i * hq + j * hg + e0 + e) * g.smax + y) * (D + 2);
+                sm_m[x] = __ldcg(pp);
+                sm_w[x] = __ldcg(pp + 1);
+            }
+            __syncthreads();
             if (threadIdx.x < nh) {
                 const int e = threadIdx.x;
-                const float *pp = part + ((size_t)i * hq + j * hg + e0 + e) * g.smax * (D + 2);
                 float M = -INFINITY;
-                for (int x = 0; x < np; ++x) M = fmaxf(M, __ldcg(pp + (size_t)x * (D + 2)));
+                for (int y = 0; y < np; ++y) M = fmaxf(M, sm_m[e * np + y]);
                 float L = 0.f;
                 if (M != -INFINITY)
-                    for (int x = 0; x < np; ++x)
-                        L += ex2(__ldcg(pp + (size_t)x * (D + 2)) - M) * __ldcg(pp + (size_t)x * (D + 2) + 1);
+                    for (int y = 0; y < np; ++y) L += ex2(sm_m[e * np + y] - M) * sm_w[e * np + y];
                 sML[e] = M;
                 sML[4 + e] = L;
             }
             __syncthreads();
+            for (int x = threadIdx.x; x < nh * np; x += blockDim.x) {
+                const int e = x / np;
+                const float M = sML[e];
+                sm_w[x] = M == -INFINITY ? 0.f : ex2(sm_m[x] - M) / sML[4 + e];
+            }
+            __syncthreads();
             for (int x = threadIdx.x; x < nh * D; x += blockDim.x) {
                 const int e = x / D, cc = x % D;
-                const float M = sML[e], L = sML[4 + e];
-                const float *pp = part + ((size_t)i * hq + j * hg + e0 + e) * g.smax * (D + 2);
+                const float *pp = part + ((size_t)i * hq + j * hg + e0 + e) * g.smax * (D + 2) + 2 + cc;
                 float a = 0.f;
-                if (M != -INFINITY) {
-                    for (int y = 0; y < np; ++y)
-                        a += ex2(__ldcg(pp + (size_t)y * (D + 2)) - M) * __ldcg(pp + (size_t)y * (D + 2) + 2 + cc);
-                    a = a / L;
-                }
+                for (int y = 0; y < np; ++y) a = fmaf(sm_w[e * np + y], __ldcg(pp + (size_t)y * (D + 2)), a);
                 out[((size_t)i * hq + j * hg + e0 + e) * D + cc] = __float2half_rn(a);
             }
         }

@@ -96,7 +96,7 @@ kivi_status kivi_append(kivi_cache_t c, const void *k, const void *v, kivi_strea
  * over the quantized keys followed by the fp16 keys, one softmax over both,
  * weights applied to the quantized then fp16 values; fp32 accumulation.
  * A sequence with no tokens gets an all-zero output.  Read-only on the
- * cache (the call can be repeated).  Preconditions: inputs finite and
+ * cache (the call can be repeated, with bitwise identical results).  Preconditions: inputs finite and
  * |q_c| * s < 65504 for every key scale s (the scaled query is staged in
  * fp16 for the tensor-core contraction). */
 kivi_status kivi_decode_attn(kivi_cache_t c, const void *q, int h_q, void *out,
