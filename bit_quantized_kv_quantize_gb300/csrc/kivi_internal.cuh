@@ -208,6 +208,22 @@ __device__ __forceinline__ uint32_t qcode(float x, float sf, float zf, int bits)
     return (uint32_t)q;
 }
 
+// The same code from a precomputed rs = RN(1 / sf).  (x - z) * rs lies
+// within a few ulps of the correctly rounded quotient, so both round to the
+// same integer unless they sit next to a rounding tie (k + 1/2); there the
+// IEEE division decides.  Bit-identical to qcode, without a division per
+// code.
+__device__ __forceinline__ uint32_t qcode_rcp(float x, float sf, float zf, float rs, int bits) {
+    if (sf == 0.0f) return 0u;
+    const float dlt = __fsub_rn(x, zf);
+    float q = __fmul_rn(dlt, rs);
+    if (fabsf(q - (floorf(q) + 0.5f)) < 1.0e-5f * fmaxf(1.0f, fabsf(q))) q = __fdiv_rn(dlt, sf);
+    int k = __float2int_rn(q);
+    const int qmax = (1 << bits) - 1;
+    k = k < 0 ? 0 : (k > qmax ? qmax : k);
+    return (uint32_t)k;
+}
+
 // ---- host-side launchers (kivi_pack.cu, kivi_decode.cu) ----------------------------
 struct DecodePlan {
     int ctas;        // persistent CTAs (grid size)

@@ -15,67 +15,78 @@ namespace {
 
 __device__ __forceinline__ void flag(unsigned *status, unsigned f) { atomicOr(status, f); }
 
+// Shared-memory tiles keep each token row padded by 16 bytes, so reads of
+// one channel across tokens fall in different banks.
+__host__ __device__ __forceinline__ int xs_stride(int d) { return d + 8; }
+
 // ---------------------------------------------------------------------------
 // Prefill keys: one CTA per (super block of TB = max(64, G) tokens, kv head,
 // sequence).  Quantizes tokens [0, nqk), nqk = t - t mod R.
 // ---------------------------------------------------------------------------
+template <int KBITS, int G>
 __global__ void __launch_bounds__(256) prefill_keys_kernel(KiviGeom g, KiviDev dv,
                                                            const __half *__restrict__ K,
                                                            SeqLens lens, int t_stride) {
     extern __shared__ __align__(16) unsigned char smem[];
-    const int TB = g.G > KIVI_KBLK ? g.G : KIVI_KBLK;
+    constexpr int TB = G > KIVI_KBLK ? G : KIVI_KBLK;
     const int sb = blockIdx.x, j = blockIdx.y, i = blockIdx.z;
     const int t = lens.t[i];
     const int nqk = t - t % g.R;
     const int tok0 = sb * TB;
     if (tok0 >= nqk) return;
-    const int d = g.d;
+    const int d = g.d, xsd = xs_stride(d);
     const int ntok = min(TB, nqk - tok0);   // a multiple of G
-    const int ngr = ntok / g.G;
+    const int ngr = ntok / G;
 
-    __half *xs = reinterpret_cast<__half *>(smem);                     // [TB][d]
-    float *sfz = reinterpret_cast<float *>(smem + (size_t)TB * d * 2); // [TB/G][2][d]
+    __half *xs = reinterpret_cast<__half *>(smem);                        // [TB][xsd]
+    float *sfz = reinterpret_cast<float *>(smem + (size_t)TB * xsd * 2);  // [TB/G][3][d]: s, z, 1/s
 
     // stage the tile (16-byte vectors)
     const __half *src = K + (((size_t)i * g.h + j) * t_stride + tok0) * d;
-    const int nvec = ntok * d / 8;
-    for (int e = threadIdx.x; e < nvec; e += blockDim.x)
-        reinterpret_cast<uint4 *>(xs)[e] = reinterpret_cast<const uint4 *>(src)[e];
+    const int vpr = d / 8;   // vectors per row
+    for (int e = threadIdx.x; e < ntok * vpr; e += blockDim.x) {
+        const int r = e / vpr, c = e - r * vpr;
+        reinterpret_cast<uint4 *>(xs + (size_t)r * xsd)[c] = reinterpret_cast<const uint4 *>(src)[e];
+    }
     __syncthreads();
 
     // scale and zero per (group, channel)
     for (int e = threadIdx.x; e < ngr * d; e += blockDim.x) {
-        int gr = e / d, c = e - gr * d;
-        float mn = __half2float(xs[(size_t)gr * g.G * d + c]), mx = mn;
-        for (int k = 1; k < g.G; ++k) {
-            float x = __half2float(xs[((size_t)gr * g.G + k) * d + c]);
+        const int gr = e / d, c = e - gr * d;
+        float mn = __half2float(xs[(size_t)gr * G * xsd + c]), mx = mn;
+#pragma unroll 8
+        for (int k = 1; k < G; ++k) {
+            const float x = __half2float(xs[((size_t)gr * G + k) * xsd + c]);
             mn = fminf(mn, x);
             mx = fmaxf(mx, x);
         }
-        QParams p = qparams(mn, mx, g.kbits);
-        ksz_store(g, dv.blk, i, j, tok0 / g.G + gr, c, p.s16, p.z16);
-        sfz[(gr * 2 + 0) * d + c] = p.sf;
-        sfz[(gr * 2 + 1) * d + c] = p.zf;
+        const QParams p = qparams(mn, mx, KBITS);
+        ksz_store(g, dv.blk, i, j, tok0 / G + gr, c, p.s16, p.z16);
+        sfz[(gr * 3 + 0) * d + c] = p.sf;
+        sfz[(gr * 3 + 1) * d + c] = p.zf;
+        sfz[(gr * 3 + 2) * d + c] = p.sf == 0.0f ? 0.0f : __frcp_rn(p.sf);
     }
     __syncthreads();
 
     // packed words of every 64-token block that starts inside [tok0, nqk)
+    constexpr int cph = 16 / KBITS;
+    const int kc_blk = g.kc_blk;
     const int nblk = (ntok + KIVI_KBLK - 1) / KIVI_KBLK;
-    const int cph = 16 / g.kbits;
-    for (int e = threadIdx.x; e < nblk * g.kc_blk; e += blockDim.x) {
-        int kbl = e / g.kc_blk, wb = e - kbl * g.kc_blk;
-        KWord kw = kword_decode(wb, g.kbits);
+    for (int e = threadIdx.x; e < nblk * kc_blk; e += blockDim.x) {
+        const int kbl = e / kc_blk, wb = e - kbl * kc_blk;
+        const KWord kw = kword_decode(wb, KBITS);
         uint32_t word = 0;
-#pragma unroll 2
+#pragma unroll
         for (int half = 0; half < 2; ++half) {
-            int c = kw.c0 + half;
+            const int c = kw.c0 + half;
+#pragma unroll
             for (int r = 0; r < cph; ++r) {
-                int tl = kbl * KIVI_KBLK + 8 * (kw.pos0 + r) + kw.g;   // token within the tile
+                const int tl = kbl * KIVI_KBLK + 8 * (kw.pos0 + r) + kw.g;   // token within the tile
                 if (tl < ntok) {
-                    int gr = tl / g.G;
-                    float x = __half2float(xs[(size_t)tl * d + c]);
-                    uint32_t q = qcode(x, sfz[(gr * 2) * d + c], sfz[(gr * 2 + 1) * d + c], g.kbits);
-                    word |= q << (16 * half + r * g.kbits);
+                    const int gr = tl / G;
+                    const float x = __half2float(xs[(size_t)tl * xsd + c]);
+                    const float *f = sfz + (size_t)gr * 3 * d + c;
+                    word |= qcode_rcp(x, f[0], f[d], f[2 * d], KBITS) << (16 * half + r * KBITS);
                 }
             }
         }
@@ -87,6 +98,7 @@ __global__ void __launch_bounds__(256) prefill_keys_kernel(KiviGeom g, KiviDev d
 // Prefill values: one CTA per (64 tokens = 4 value blocks, kv head,
 // sequence).  Quantizes tokens [0, nqv), nqv = max(t - R, 0).
 // ---------------------------------------------------------------------------
+template <int VBITS, int G>
 __global__ void __launch_bounds__(256) prefill_values_kernel(KiviGeom g, KiviDev dv,
                                                              const __half *__restrict__ V,
                                                              SeqLens lens, int t_stride) {
@@ -96,34 +108,42 @@ __global__ void __launch_bounds__(256) prefill_values_kernel(KiviGeom g, KiviDev
     const int nqv = t > g.R ? t - g.R : 0;
     const int tok0 = sb * 64;
     if (tok0 >= nqv) return;
-    const int d = g.d, ngi = d / g.G;
+    const int d = g.d, ngi = d / G, xsd = xs_stride(d);
     const int ntok = min(64, nqv - tok0);
-    __half *xs = reinterpret_cast<__half *>(smem);                          // [64][d]
-    float *sfz = reinterpret_cast<float *>(smem + (size_t)64 * d * 2);     // [64][2][ngi]
+    __half *xs = reinterpret_cast<__half *>(smem);                         // [64][xsd]
+    float *sfz = reinterpret_cast<float *>(smem + (size_t)64 * xsd * 2);   // [64][3][ngi]: s, z, 1/s
 
     const __half *src = V + (((size_t)i * g.h + j) * t_stride + tok0) * d;
-    for (int e = threadIdx.x; e < ntok * d / 8; e += blockDim.x)
-        reinterpret_cast<uint4 *>(xs)[e] = reinterpret_cast<const uint4 *>(src)[e];
+    const int vpr = d / 8;
+    for (int e = threadIdx.x; e < ntok * vpr; e += blockDim.x) {
+        const int r = e / vpr, c = e - r * vpr;
+        reinterpret_cast<uint4 *>(xs + (size_t)r * xsd)[c] = reinterpret_cast<const uint4 *>(src)[e];
+    }
     __syncthreads();
 
     const int nvblk = (ntok + KIVI_VBLK - 1) / KIVI_VBLK;   // value blocks touched
     for (int e = threadIdx.x; e < nvblk * KIVI_VBLK * ngi; e += blockDim.x) {
-        int tl = e / ngi, gi = e - tl * ngi;
-        int tau = tok0 + tl;
+        const int tl = e / ngi, gi = e - tl * ngi;
+        const int tau = tok0 + tl;
         __half s16 = __float2half_rn(0.f), z16 = s16;
         if (tl < ntok) {
-            const __half *x = xs + (size_t)tl * d + gi * g.G;
-            float mn = __half2float(x[0]), mx = mn;
-            for (int k = 1; k < g.G; ++k) {
-                float v = __half2float(x[k]);
+            // the scan starts at a token-dependent offset: the warp's threads
+            // read different banks
+            const __half *x = xs + (size_t)tl * xsd + gi * G;
+            const int rot = (2 * tl) & (G - 1);
+            float mn = __half2float(x[rot]), mx = mn;
+#pragma unroll 8
+            for (int k = 1; k < G; ++k) {
+                const float v = __half2float(x[(k + rot) & (G - 1)]);
                 mn = fminf(mn, v);
                 mx = fmaxf(mx, v);
             }
-            QParams p = qparams(mn, mx, g.vbits);
+            const QParams p = qparams(mn, mx, VBITS);
             s16 = p.s16;
             z16 = p.z16;
-            sfz[(tl * 2 + 0) * ngi + gi] = p.sf;
-            sfz[(tl * 2 + 1) * ngi + gi] = p.zf;
+            sfz[(tl * 3 + 0) * ngi + gi] = p.sf;
+            sfz[(tl * 3 + 1) * ngi + gi] = p.zf;
+            sfz[(tl * 3 + 2) * ngi + gi] = p.sf == 0.0f ? 0.0f : __frcp_rn(p.sf);
         }
         __half *vsz = vsz_halves(g, dv.blk, i, j, tau >> 4);
         vsz[vsz_in_block(g, tau, gi, 0)] = s16;   // tokens past nqv: zero
@@ -131,24 +151,61 @@ __global__ void __launch_bounds__(256) prefill_values_kernel(KiviGeom g, KiviDev
     }
     __syncthreads();
 
-    const int cs = v_cs(g), cph = 16 / g.vbits;
-    for (int e = threadIdx.x; e < nvblk * g.vc_blk; e += blockDim.x) {
-        int vbl = e / g.vc_blk, wb = e - vbl * g.vc_blk;
-        VWord vw = vword_decode(wb, d, g.vbits, cs);
+    const int cs = v_cs(g);
+    constexpr int cph = 16 / VBITS;
+    const int vc_blk = g.vc_blk;
+    for (int e = threadIdx.x; e < nvblk * vc_blk; e += blockDim.x) {
+        const int vbl = e / vc_blk, wb = e - vbl * vc_blk;
+        const VWord vw = vword_decode(wb, d, VBITS, cs);
         uint32_t word = 0;
+#pragma unroll
         for (int half = 0; half < 2; ++half) {
-            int tl = vbl * KIVI_VBLK + vw.tt0 + half;
+            const int tl = vbl * KIVI_VBLK + vw.tt0 + half;
             if (tl >= ntok) continue;
+#pragma unroll
             for (int r = 0; r < cph; ++r) {
-                int c = 8 * (vw.ci0 + r) + vw.g;
-                int gi = c / g.G;
-                float x = __half2float(xs[(size_t)tl * d + c]);
-                uint32_t q = qcode(x, sfz[(tl * 2) * ngi + gi], sfz[(tl * 2 + 1) * ngi + gi], g.vbits);
-                word |= q << (16 * half + r * g.vbits);
+                const int c = 8 * (vw.ci0 + r) + vw.g;
+                const int gi = c / G;
+                const float x = __half2float(xs[(size_t)tl * xsd + c]);
+                const float *f = sfz + (size_t)tl * 3 * ngi + gi;
+                word |= qcode_rcp(x, f[0], f[ngi], f[2 * ngi], VBITS) << (16 * half + r * VBITS);
             }
         }
         vc_words(g, dv.blk, i, j, tok0 / KIVI_VBLK + vbl)[wb] = word;
     }
+}
+
+template <int BITS, int G>
+cudaError_t launch_prefill_kv(const KiviGeom &g, const KiviDev &dv, const __half *K, const __half *V,
+                              const SeqLens &lens, int t_stride, int maxt, cudaStream_t st) {
+    constexpr int TB = G > KIVI_KBLK ? G : KIVI_KBLK;
+    const int xsd = xs_stride(g.d);
+    cudaError_t e = cudaSuccess;
+    if (g.kbits == BITS) {
+        const size_t smk = (size_t)TB * xsd * 2 + (size_t)(TB / G) * 3 * g.d * 4;
+        e = cudaFuncSetAttribute(prefill_keys_kernel<BITS, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smk);
+        if (e != cudaSuccess) return e;
+        prefill_keys_kernel<BITS, G><<<dim3((maxt + TB - 1) / TB, g.h, g.b), 256, smk, st>>>(g, dv, K, lens,
+                                                                                           t_stride);
+    }
+    if (g.vbits == BITS) {
+        const size_t smv = (size_t)64 * xsd * 2 + (size_t)64 * 3 * (g.d / G) * 4;
+        e = cudaFuncSetAttribute(prefill_values_kernel<BITS, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smv);
+        if (e != cudaSuccess) return e;
+        prefill_values_kernel<BITS, G><<<dim3((maxt + 63) / 64, g.h, g.b), 256, smv, st>>>(g, dv, V, lens,
+                                                                                         t_stride);
+    }
+    return cudaGetLastError();
+}
+
+template <int G>
+cudaError_t launch_prefill_g(const KiviGeom &g, const KiviDev &dv, const __half *K, const __half *V,
+                             const SeqLens &lens, int t_stride, int maxt, cudaStream_t st) {
+    cudaError_t e = launch_prefill_kv<2, G>(g, dv, K, V, lens, t_stride, maxt, st);
+    if (e != cudaSuccess) return e;
+    return launch_prefill_kv<4, G>(g, dv, K, V, lens, t_stride, maxt, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -222,19 +279,14 @@ cudaError_t kivi_launch_prefill(const KiviGeom &g, const KiviDev &dv, const __ha
     int maxt = 0;
     for (int i = 0; i < g.b; ++i) maxt = lens.t[i] > maxt ? lens.t[i] : maxt;
     if (maxt > 0) {
-        const int TB = g.G > KIVI_KBLK ? g.G : KIVI_KBLK;
-        size_t smk = (size_t)TB * g.d * 2 + (size_t)(TB / g.G) * 2 * g.d * 4;
-        cudaError_t e = cudaFuncSetAttribute(prefill_keys_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smk);
+        cudaError_t e;
+        switch (g.G) {
+        case 16: e = launch_prefill_g<16>(g, dv, K, V, lens, t_stride, maxt, st); break;
+        case 32: e = launch_prefill_g<32>(g, dv, K, V, lens, t_stride, maxt, st); break;
+        case 64: e = launch_prefill_g<64>(g, dv, K, V, lens, t_stride, maxt, st); break;
+        default: e = launch_prefill_g<128>(g, dv, K, V, lens, t_stride, maxt, st); break;
+        }
         if (e != cudaSuccess) return e;
-        dim3 gk((maxt + TB - 1) / TB, g.h, g.b);
-        prefill_keys_kernel<<<gk, 256, smk, st>>>(g, dv, K, lens, t_stride);
-        size_t smv = (size_t)64 * g.d * 2 + (size_t)64 * 2 * (g.d / g.G) * 4;
-        e = cudaFuncSetAttribute(prefill_values_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smv);
-        if (e != cudaSuccess) return e;
-        dim3 gv((maxt + 63) / 64, g.h, g.b);
-        prefill_values_kernel<<<gv, 256, smv, st>>>(g, dv, V, lens, t_stride);
     }
     prefill_residual_kernel<<<dim3(g.h, g.b), 256, 0, st>>>(g, dv, K, V, lens, t_stride);
     return cudaGetLastError();
