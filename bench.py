@@ -236,7 +236,7 @@ def run_reference(args, w):
 def workload_config(w, unfused=True):
     T = int(w.lengths().max()) + 1
     return {"workload": w.name,
-            "step": "kivi_append + kivi_decode_attn" if unfused else "kivi_append_decode (one launch)", "b": w.b, "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d,
+            "step": "kivi_append + kivi_decode_attn" if unfused else "kivi_append_decode", "b": w.b, "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d,
             "k_bits": w.kbits, "v_bits": w.vbits, "G": w.G, "R": w.R,
             "context": T if not w.ragged else f"ragged {w.ragged[0]}-{w.ragged[1]}",
             "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)",
@@ -442,9 +442,13 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--k-bits", type=int, choices=(2, 4), help="override the workload's key bits")
+    ap.add_argument("--v-bits", type=int, choices=(2, 4), help="override the workload's value bits")
+    ap.add_argument("--group", type=int, choices=(16, 32, 64, 128), help="override the group size G")
+    ap.add_argument("--residual", type=int, help="override the residual length R (a multiple of G)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fused", action="store_true",
-                    help="time a step as kivi_append_decode (one launch) instead of kivi_append + "
+                    help="time a step as one kivi_append_decode call instead of kivi_append + "
                          "kivi_decode_attn")
     ap.add_argument("--ncu", action="store_true",
                     help="run only prefill, one append and --steps decode calls (profiler captures)")
@@ -452,6 +456,12 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     w = W.WORKLOADS[args.workload]
+    over = {k: v for k, v in (("kbits", args.k_bits), ("vbits", args.v_bits), ("G", args.group),
+                              ("R", args.residual)) if v is not None}
+    if over:   # a variant of the workload (bits / group / residual sweep)
+        w = W.small(w, **over)
+        if w.R % w.G or w.d % w.G:
+            ap.error("need R % G == 0 and d % G == 0")
     if args.impl == "reference":
         return run_reference(args, w)
     if args.ncu:

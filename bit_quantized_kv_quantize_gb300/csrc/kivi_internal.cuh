@@ -217,10 +217,11 @@ __device__ __forceinline__ uint32_t qcode_rcp(float x, float sf, float zf, float
     if (sf == 0.0f) return 0u;
     const float dlt = __fsub_rn(x, zf);
     float q = __fmul_rn(dlt, rs);
-    if (fabsf(q - (floorf(q) + 0.5f)) < 1.0e-5f * fmaxf(1.0f, fabsf(q))) q = __fdiv_rn(dlt, sf);
-    int k = __float2int_rn(q);
-    const int qmax = (1 << bits) - 1;
-    k = k < 0 ? 0 : (k > qmax ? qmax : k);
+    float k = rintf(q);
+    // |q - k| close to 1/2: q lies next to a tie
+    if (fabsf(q - k) > 0.5f - 1.0e-5f * fmaxf(1.0f, fabsf(q))) k = rintf(__fdiv_rn(dlt, sf));
+    const float qmax = (float)((1 << bits) - 1);
+    k = fminf(fmaxf(k, 0.0f), qmax);
     return (uint32_t)k;
 }
 

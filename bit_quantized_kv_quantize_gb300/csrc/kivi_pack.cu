@@ -77,17 +77,15 @@ __global__ void __launch_bounds__(256) prefill_keys_kernel(KiviGeom g, KiviDev d
         const KWord kw = kword_decode(wb, KBITS);
         uint32_t word = 0;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int c = kw.c0 + half;
-#pragma unroll
-            for (int r = 0; r < cph; ++r) {
-                const int tl = kbl * KIVI_KBLK + 8 * (kw.pos0 + r) + kw.g;   // token within the tile
-                if (tl < ntok) {
-                    const int gr = tl / G;
-                    const float x = __half2float(xs[(size_t)tl * xsd + c]);
-                    const float *f = sfz + (size_t)gr * 3 * d + c;
-                    word |= qcode_rcp(x, f[0], f[d], f[2 * d], KBITS) << (16 * half + r * KBITS);
-                }
+        for (int r = 0; r < cph; ++r) {
+            // slot r of both halves: token tl, channels c0 and c0 + 1
+            const int tl = kbl * KIVI_KBLK + 8 * (kw.pos0 + r) + kw.g;   // token within the tile
+            if (tl < ntok) {
+                const int gr = tl / G;
+                const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(xs + (size_t)tl * xsd + kw.c0));
+                const float *f = sfz + (size_t)gr * 3 * d + kw.c0;
+                word |= qcode_rcp(x.x, f[0], f[d], f[2 * d], KBITS) << (r * KBITS);
+                word |= qcode_rcp(x.y, f[1], f[d + 1], f[2 * d + 1], KBITS) << (16 + r * KBITS);
             }
         }
         kc_words(g, dv.blk, i, j, tok0 / KIVI_KBLK + kbl)[wb] = word;
