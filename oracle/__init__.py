@@ -75,6 +75,7 @@ def lib():
             L.ko_append.argtypes = [vp, vp, vp]
             L.ko_decode.argtypes = [vp, vp, ctypes.c_int, vp]
             L.ko_decode_subset.argtypes = [vp, vp, ctypes.c_int, vp, vp, ctypes.c_int]
+            L.ko_decode_probs.argtypes = [vp, vp, ctypes.c_int, vp, vp, ctypes.c_longlong, vp, ctypes.c_int]
             L.ko_set_threads.argtypes = [ctypes.c_int]
             L.ko_lengths.argtypes = [vp, vp, vp, vp]
             L.ko_dequant_kv.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, vp]
@@ -184,6 +185,25 @@ class Cache:
         if rc != 0:
             raise ValueError(f"oracle decode failed ({rc})")
         return out
+
+    def decode_probs(self, q, ld=None, pairs=None):
+        """(out fp32 [b, hq, d], probs fp32 [b, hq, ld]): the attention output and
+        each token's softmax weight (row (i, h) holds T_i weights, zeros after)."""
+        q = _f16(q)
+        hq = q.shape[1]
+        T = self.lengths()[0]
+        ld = int(max(1, T.max())) if ld is None else int(ld)
+        out = np.zeros((self.b, hq, self.d), np.float32)
+        probs = np.zeros((self.b, hq, ld), np.float32)
+        pr, npr = None, 0
+        if pairs is not None:
+            pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+            npr = pr.shape[0]
+        rc = lib().ko_decode_probs(self._h, q.ctypes.data, hq, out.ctypes.data, probs.ctypes.data, ld,
+                                   None if pr is None else pr.ctypes.data, npr)
+        if rc != 0:
+            raise ValueError(f"oracle decode failed ({rc})")
+        return out, probs
 
     def lengths(self):
         T = np.zeros(self.b, np.int32)

@@ -347,9 +347,13 @@ void ko_dequant_kv(const ko_cache *o, int i, int j, float *Khat, float *Vhat)
 }
 
 /* Item 5: decode attention for every (sequence, query head).
- * q is fp16 [b][hq][d]; out is fp32 [b][hq][d]. */
+ * q is fp16 [b][hq][d]; out is fp32 [b][hq][d].  When prow is not NULL it
+ * receives the softmax weights themselves, prow[tok] = p[tok] / l for the T
+ * tokens (the per-token attention that an accumulated-attention eviction
+ * score, H2O's in the same survey's section on token eviction, sums over
+ * decode steps). */
 static void decode_one(const ko_cache *o, int i, int j, const uint16_t *q,
-                       float *outp, float *Khat, float *Vhat, float *p)
+                       float *outp, float *Khat, float *Vhat, float *p, float *prow)
 {
     int d = o->d, T = o->T[i];
     if (T == 0) {
@@ -375,6 +379,8 @@ static void decode_one(const ko_cache *o, int i, int j, const uint16_t *q,
         for (int tok = 0; tok < T; ++tok) acc += p[tok] * Vhat[(size_t)tok * d + c];
         outp[c] = acc / l;
     }
+    if (prow)
+        for (int tok = 0; tok < T; ++tok) prow[tok] = p[tok] / l;
 }
 
 int ko_decode(const ko_cache *o, const uint16_t *q, int hq, float *out)
@@ -402,8 +408,19 @@ int ko_set_threads(int n)
 int ko_decode_subset(const ko_cache *o, const uint16_t *q, int hq, float *out,
                      const int *pairs, int npairs)
 {
+    return ko_decode_probs(o, q, hq, out, NULL, 0, pairs, npairs);
+}
+
+/* As ko_decode_subset; probs (may be NULL) is fp32 [b][hq][ld] and row
+ * (i, qh) of a listed pair receives its T_i softmax weights in [0, T_i);
+ * the rest of the row is untouched.  ld >= max T_i. */
+int ko_decode_probs(const ko_cache *o, const uint16_t *q, int hq, float *out,
+                    float *probs, long long ld, const int *pairs, int npairs)
+{
     int d = o->d;
     if (hq < o->h || hq % o->h != 0) return 1;
+    if (probs)
+        for (int i = 0; i < o->b; ++i) if (o->T[i] > ld) return 1;
     int maxT = 1;
     for (int i = 0; i < o->b; ++i) if (o->T[i] > maxT) maxT = o->T[i];
     int nt = g_threads;
@@ -432,7 +449,8 @@ int ko_decode_subset(const ko_cache *o, const uint16_t *q, int hq, float *out,
             if (i < 0 || i >= o->b || qh < 0 || qh >= hq) continue;
             decode_one(o, i, qh / grp, q + ((size_t)i * hq + qh) * d,
                        out + ((size_t)i * hq + qh) * d,
-                       bufs[3 * w], bufs[3 * w + 1], bufs[3 * w + 2]);
+                       bufs[3 * w], bufs[3 * w + 1], bufs[3 * w + 2],
+                       probs ? probs + ((size_t)i * hq + qh) * (size_t)ld : NULL);
         }
     }
     for (int w = 0; w < nt; ++w) {

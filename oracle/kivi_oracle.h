@@ -35,6 +35,8 @@ int ko_append(ko_cache *o, const uint16_t *k, const uint16_t *v);
 int ko_decode(const ko_cache *o, const uint16_t *q, int hq, float *out);
 int ko_decode_subset(const ko_cache *o, const uint16_t *q, int hq, float *out,
                      const int *pairs, int npairs);
+int ko_decode_probs(const ko_cache *o, const uint16_t *q, int hq, float *out,
+                    float *probs, long long ld, const int *pairs, int npairs);
 int ko_set_threads(int n);
 void ko_f32_to_f16_n(const float *x, uint16_t *y, size_t n);
 void ko_f16_to_f32_n(const uint16_t *x, float *y, size_t n);

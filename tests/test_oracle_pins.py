@@ -457,6 +457,76 @@ def test_attention_special_cases():
                                atol=1e-7)
 
 
+def _dense_weights(q, K):
+    """Textbook softmax(q K^T / sqrt(d)) weights in fp64."""
+    s = np.asarray(K, np.float64) @ np.asarray(q, np.float64) / np.sqrt(K.shape[1])
+    p = np.exp(s - s.max())
+    return p / p.sum()
+
+
+def test_probs_unquantized_equal_dense_weights():
+    """With R >= T nothing is quantized: each row of weights is the plain
+    softmax over the raw keys, summing to 1, zeros after T_i."""
+    b, h, hq, d, G, R, t = 2, 2, 4, 64, 32, 256, 200
+    lens = [t, 57]
+    c, K, V = _cache_with(b, h, d, 2, 2, G, R, t + 8, lens)
+    q = np.random.default_rng(2).standard_normal((b, hq, d)).astype(np.float16)
+    out, probs = c.decode_probs(q, ld=t + 5)
+    assert np.array_equal(out, c.decode(q))
+    for i in range(b):
+        for qh in range(hq):
+            j = qh // (hq // h)
+            ref = _dense_weights(q[i, qh], K[i, j, :lens[i]])
+            np.testing.assert_allclose(probs[i, qh, :lens[i]], ref, rtol=2e-5, atol=1e-9)
+            assert abs(float(probs[i, qh, :lens[i]].astype(np.float64).sum()) - 1.0) < 1e-5
+            assert not probs[i, qh, lens[i]:].any()
+
+
+@pytest.mark.parametrize("kb,vb", [(2, 2), (4, 2)])
+def test_probs_over_dequantized_and_consistent_with_output(kb, vb):
+    """After prefill and appends (quantized and fp16 tokens mixed): the
+    weights are the dense softmax over the dequantized keys, and weights
+    times dequantized values give the attention output (token by token, so
+    a shifted or swapped token index fails)."""
+    b, h, hq, d, G, R = 2, 2, 8, 64, 32, 32
+    lens = [300, 77]
+    c, K, V = _cache_with(b, h, d, kb, vb, G, R, 400, lens, seed=5)
+    rng = np.random.default_rng(9)
+    for _ in range(37):
+        c.append(rng.standard_normal((b, h, d)).astype(np.float16),
+                 rng.standard_normal((b, h, d)).astype(np.float16))
+    q = rng.standard_normal((b, hq, d)).astype(np.float16)
+    out, probs = c.decode_probs(q)
+    T = c.lengths()[0]
+    for i in range(b):
+        for qh in range(hq):
+            Kh, Vh = c.dequant_kv(i, qh // (hq // h))
+            ref = _dense_weights(q[i, qh], Kh)
+            np.testing.assert_allclose(probs[i, qh, :T[i]], ref, rtol=3e-5, atol=1e-9)
+            np.testing.assert_allclose(probs[i, qh, :T[i]].astype(np.float64) @ Vh, out[i, qh],
+                                       rtol=1e-4, atol=1e-5)
+
+
+def test_probs_special_cases():
+    d = 64
+    q = np.ones((1, 1, d), np.float16)
+    # one token: weight 1
+    c = oracle.Cache(1, 1, d, 2, 2, 32, 32, 8)
+    c.prefill(np.zeros((1, 1, 1, d), np.float16), np.ones((1, 1, 1, d), np.float16), [1])
+    assert c.decode_probs(q)[1].tolist() == [[[1.0]]]
+    # equal keys: uniform weights 1 / T
+    c2 = oracle.Cache(1, 1, d, 2, 2, 32, 32, 80)
+    c2.prefill(np.ones((1, 1, 70, d), np.float16), np.ones((1, 1, 70, d), np.float16), [70])
+    np.testing.assert_allclose(c2.decode_probs(q)[1][0, 0], np.full(70, 1 / 70), rtol=1e-6)
+    # no tokens: the row is left as it was (zeros)
+    e = oracle.Cache(1, 1, d, 2, 2, 32, 32, 8)
+    e.prefill(np.zeros((1, 1, 1, d), np.float16), np.zeros((1, 1, 1, d), np.float16), [0])
+    assert not e.decode_probs(q, ld=4)[1].any()
+    # a row narrower than a sequence is refused
+    with pytest.raises(ValueError):
+        c2.decode_probs(q, ld=69)
+
+
 # --------------------------------------------------------------------------
 # Packed device format.
 # --------------------------------------------------------------------------
