@@ -46,16 +46,19 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {"132e5299ad230a05": 205726208 + 3175424}
 
 
-def algorithmic_bytes(w: W.Workload, T, Tqk, Tqv) -> int:
+def algorithmic_bytes(w: W.Workload, T, Tqk, Tqv, scores: bool = False) -> int:
     """Cache bytes one decode-attention call must read, plus q and out:
     packed codes and fp16 scale/zero of the quantized tokens and the fp16
-    residual tokens, per (sequence, kv head)."""
+    residual tokens, per (sequence, kv head); with scores, also the fp32
+    score of every (sequence, query head, token) the kernel writes for the
+    attention-weight output."""
     d, G = w.d, w.G
     per_qk = d * w.kbits // 8 + 4 * d // G
     per_qv = d * w.vbits // 8 + 4 * d // G
     T, Tqk, Tqv = (np.asarray(x, np.int64) for x in (T, Tqk, Tqv))
     cache = w.h_kv * int(np.sum(Tqk * per_qk + Tqv * per_qv + ((T - Tqk) + (T - Tqv)) * 2 * d))
-    return cache + 2 * w.b * w.h_q * d * 2
+    extra = 4 * w.h_q * int(np.sum(T)) if scores else 0
+    return cache + 2 * w.b * w.h_q * d * 2 + extra
 
 
 def load_peaks():
@@ -233,10 +236,18 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w, unfused=True):
+STEP_NAMES = {"two": "kivi_append + kivi_decode_attn", "fused": "kivi_append_decode",
+              "probs": "kivi_append + kivi_decode_attn_probs (weights, accumulated mass)"}
+
+
+def step_mode(args) -> str:
+    return "probs" if getattr(args, "probs", False) else ("fused" if getattr(args, "fused", False) else "two")
+
+
+def workload_config(w, mode="two"):
     T = int(w.lengths().max()) + 1
     return {"workload": w.name,
-            "step": "kivi_append + kivi_decode_attn" if unfused else "kivi_append_decode", "b": w.b, "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d,
+            "step": STEP_NAMES[mode], "b": w.b, "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d,
             "k_bits": w.kbits, "v_bits": w.vbits, "G": w.G, "R": w.R,
             "context": T if not w.ragged else f"ragged {w.ragged[0]}-{w.ragged[1]}",
             "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)",
@@ -287,13 +298,23 @@ def run_ours(args, w):
     qd = [torch.from_numpy(x).to(dev) for x in host_q]
     out = torch.empty((w.b, w.h_q, w.d), dtype=torch.float16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    mode = step_mode(args)
+    if mode == "probs":   # per-token weights and their running sum, one row per query head
+        probs = torch.zeros((w.b, w.h_q, cap), dtype=torch.float32, device=dev)
+        mass = torch.zeros_like(probs)
+
+    def run_step(k, v, q):
+        if mode == "two":
+            cache.append(k, v)
+            cache.decode(q, out)
+        elif mode == "fused":
+            cache.append_decode(k, v, q, out)
+        else:
+            cache.append(k, v)
+            cache.decode_probs(q, probs, mass=mass, out=out)
 
     def step(s):
-        if (not args.fused):
-            cache.append(kd[s], vd[s])
-            cache.decode(qd[s], out)
-        else:
-            cache.append_decode(kd[s], vd[s], qd[s], out)
+        run_step(kd[s], vd[s], qd[s])
 
     for s in range(args.warmup):
         flush.fill_(s)
@@ -316,7 +337,7 @@ def run_ours(args, w):
             step(s)
             ends[n].record(stream)
             T, Tqk, Tqv = cache.lengths()
-            bytes_steps.append(algorithmic_bytes(w, T, Tqk, Tqv))
+            bytes_steps.append(algorithmic_bytes(w, T, Tqk, Tqv, scores=mode == "probs"))
         torch.cuda.synchronize(dev)
     barrier(dist, dev)
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
@@ -345,11 +366,7 @@ def run_ours(args, w):
         kbuf.copy_(pin_k[s], non_blocking=True)
         vbuf.copy_(pin_v[s], non_blocking=True)
         qbuf.copy_(pin_q[s], non_blocking=True)
-        if (not args.fused):
-            cache.append(kbuf, vbuf)
-            cache.decode(qbuf, out)
-        else:
-            cache.append_decode(kbuf, vbuf, qbuf, out)
+        run_step(kbuf, vbuf, qbuf)
         out_h.copy_(out, non_blocking=True)
         b.record(stream)
         e2e_ms.append((a, b))
@@ -375,7 +392,7 @@ def run_ours(args, w):
         "vs_baseline": None,
         "dtype": "u2/u4 codes, f16 in, f32 accumulate",
         "data": "synthetic",
-        "config": workload_config(w, (not args.fused)),
+        "config": workload_config(w, mode),
         "attn_us": round(attn_ms * 1e3, 3),
         "cache_gbs": round(bytes_per / (attn_ms * 1e-3) / 1e9, 1),
         "bytes_per_step": int(bytes_per),
@@ -384,10 +401,10 @@ def run_ours(args, w):
                      "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "kernel": "decode_kernel (persistent stream-K over TMA-staged block records, mma.sync, last-CTA merge)",
-                     "traffic": NCU_TRAFFIC.get(source_hash())},
+                     "traffic": NCU_TRAFFIC.get(source_hash()) if mode != "probs" else None},
         "e2e": {"value": round(e2e_per * 1e3, 3), "unit": "us/step",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * (launches + (1 if (not args.fused) else 0)),
+        "gpu_launches": args.steps * (launches + {"two": 1, "fused": 0, "probs": 2}[mode]),
         "splits": splits,
         "clocks": clk.summary(),
         "source_hash": source_hash(),
@@ -450,6 +467,9 @@ def main(argv=None):
     ap.add_argument("--fused", action="store_true",
                     help="time a step as one kivi_append_decode call instead of kivi_append + "
                          "kivi_decode_attn")
+    ap.add_argument("--probs", action="store_true",
+                    help="time a step as kivi_append + kivi_decode_attn_probs (per-token weights "
+                         "and their accumulated mass)")
     ap.add_argument("--ncu", action="store_true",
                     help="run only prefill, one append and --steps decode calls (profiler captures)")
     args = ap.parse_args(argv)

@@ -83,7 +83,7 @@ kivi_status check_handle(kivi_cache_t c) {
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 void free_dev(KiviDev &d) {
-    void *ps[] = {d.blk, d.Kf, d.Vf, d.T, d.Tqk, d.Tqv, d.ticket, d.status, d.part, d.merge_ticket};
+    void *ps[] = {d.blk, d.Kf, d.Vf, d.T, d.Tqk, d.Tqv, d.ticket, d.status, d.part, d.merge_ticket, d.ml};
     for (void *p : ps)
         if (p) cudaFree(p);
     memset(&d, 0, sizeof d);
@@ -138,7 +138,8 @@ void advance_mirror(kivi_cache *c) {
 
 // Plan and launch the decode kernel; units come from (T, Tqk, Tqv).
 kivi_status launch_decode(kivi_cache *c, const void *q, int h_q, void *out, kivi_stream_t stream,
-                          const int *T, const int *Tqk, const int *Tqv, const char *what) {
+                          const int *T, const int *Tqk, const int *Tqv, const char *what,
+                          const ProbsOut *po = nullptr) {
     DecodeUnits units;
     DecodePlan plan = kivi_plan_decode(c->g, h_q, T, Tqk, Tqv, c->num_sms, &units);
     cudaEvent_t e0 = nullptr, e1 = nullptr;
@@ -156,8 +157,10 @@ kivi_status launch_decode(kivi_cache *c, const void *q, int h_q, void *out, kivi
             c->nprof++;
         }
     }
+    int maxT = 0;
+    for (int i = 0; i < c->g.b; ++i) maxT = T[i] > maxT ? T[i] : maxT;
     cudaError_t e = kivi_launch_decode(c->g, c->dv, (const __half *)q, h_q, (__half *)out, plan, units,
-                                       (cudaStream_t)stream, e0, e1);
+                                       (cudaStream_t)stream, e0, e1, po, maxT);
     if (e != cudaSuccess) return fail_cuda(c, e, what);
     c->last_plan = plan;
     return KIVI_OK;
@@ -264,6 +267,7 @@ kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, in
         {(void **)&dv.status, 4},
         {(void **)&dv.part, bh * KIVI_MAX_QPERKV * g.smax * (d + 2) * 4},
         {(void **)&dv.merge_ticket, bh * 4 * 4},
+        {(void **)&dv.ml, bh * KIVI_MAX_QPERKV * 2 * 4},
     };
     for (auto &r : reqs) {
         e = cudaMalloc(r.p, r.bytes);
@@ -376,6 +380,32 @@ kivi_status kivi_decode_attn(kivi_cache_t c, const void *q, int h_q, void *out,
     s = check_decode_args(c, q, h_q, out);
     if (s != KIVI_OK) return s;
     return launch_decode(c, q, h_q, out, stream, c->T.data(), c->Tqk.data(), c->Tqv.data(), "decode_attn");
+}
+
+kivi_status kivi_decode_attn_probs(kivi_cache_t c, const void *q, int h_q, void *out, float *probs,
+                                   float *mass, int64_t ld, kivi_stream_t stream) {
+    g_err[0] = 0;
+    kivi_status s = check_handle(c);
+    if (s != KIVI_OK) return s;
+    s = check_decode_args(c, q, h_q, out);
+    if (s != KIVI_OK) return s;
+    if (!probs || probs == mass) {
+        set_err("probs is null or the same buffer as mass");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (((uintptr_t)probs & 3u) || ((uintptr_t)mass & 3u)) {
+        set_err("probs and mass must be 4-byte aligned");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    int maxT = 0;
+    for (int i = 0; i < c->g.b; ++i) maxT = c->T[i] > maxT ? c->T[i] : maxT;
+    if (ld < 1 || ld < maxT) {
+        set_err("ld must be at least 1 and at least every sequence's token count");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    const ProbsOut po{probs, mass, (long long)ld};
+    return launch_decode(c, q, h_q, out, stream, c->T.data(), c->Tqk.data(), c->Tqv.data(), "decode_attn_probs",
+                         &po);
 }
 
 kivi_status kivi_append_decode(kivi_cache_t c, const void *k, const void *v, const void *q, int h_q,

@@ -5,5 +5,5 @@
 cudaError_t kivi_launch_decode_d256(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq,
                                    __half *out, const DecodePlan &plan, const DecodeUnits &units,
                                    cudaStream_t st) {
-    return launch_d<256>(g, dv, q, hq, out, plan, units, st);
+    return launch_d<256, false>(g, dv, q, hq, out, plan, units, ProbsOut{nullptr, nullptr, 0}, st);
 }

@@ -422,10 +422,12 @@ __device__ __forceinline__ uint32_t keep_halves(uint32_t x, bool lo, bool hi) {
     return x & ((lo ? 0x0000FFFFu : 0u) | (hi ? 0xFFFF0000u : 0u));
 }
 
-template <int D, int KB, int VB, int SH, bool MIXED>
+// PROBS: the block's scores (log2 units) of head tq also go to srow[0..63]
+// (tokens tb.. of that head's weights row; null for absent heads).
+template <int D, int KB, int VB, int SH, bool MIXED, bool PROBS>
 __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D / 16][2],
                                          const unsigned char *sb, const StageGeom &sg, const KiviGeom &g,
-                                         float alpha, const MixCtx &mx) {
+                                         float alpha, const MixCtx &mx, float *srow) {
     constexpr int NJ = D / 16;
     constexpr int CPHK = 16 / KB, NWK = KB / 2;
     constexpr int CPHV = 16 / VB, NWV = D * VB / 128;
@@ -537,6 +539,17 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
             }
             if (tau0 + gq >= mx.T) p[mm][0] = -INFINITY;
             if (tau0 + gq + 8 >= mx.T) p[mm][1] = -INFINITY;
+        }
+    }
+    if constexpr (PROBS) {
+        if (srow) {
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+                if (MIXED && !((mx.tmask >> mm) & 1)) continue;
+                const int t0 = 16 * mm + gq;
+                if (!MIXED || mx.tb + t0 < mx.T) srow[t0] = p[mm][0];
+                if (!MIXED || mx.tb + t0 + 8 < mx.T) srow[t0 + 8] = p[mm][1];
+            }
         }
     }
     softmax_update<D>(A, p);
@@ -672,10 +685,10 @@ __host__ __device__ __forceinline__ long long cta_of_unit(long long u, long long
     return ((u + 1) * C - 1) / U;
 }
 
-template <int D, int KB, int VB, int SH>
+template <int D, int KB, int VB, int SH, bool PROBS>
 __global__ void __launch_bounds__(256, 2)
     decode_kernel(KiviGeom g, KiviDev dv, const __half *__restrict__ q, int hq,
-                  __half *__restrict__ out, DecodePlan plan, DecodeUnits units) {
+                  __half *__restrict__ out, DecodePlan plan, DecodeUnits units, ProbsOut po) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int NJ = D / 16;
     const int nw = blockDim.x >> 5;
@@ -753,6 +766,10 @@ __global__ void __launch_bounds__(256, 2)
                                      : 0u;
         WarpAcc<D> A;
         acc_reset<D>(A);
+        // PROBS: this lane's head's row of scores (null for absent heads)
+        float *prow = nullptr;
+        if constexpr (PROBS)
+            if (tq < nh) prow = po.p + ((size_t)i * hq + j * hg + e0 + tq) * (size_t)po.ld;
 
         // Blocks of the segment: units [o0, min(o1, nfh)) are blocks of the
         // same index, units nfh + MW m in [o0, o1) are block nfh + m; blocks
@@ -817,7 +834,11 @@ __global__ void __launch_bounds__(256, 2)
                 timed_out = true;
                 break;
             }
-            do_block<D, KB, VB, SH, false>(A, qB, myregion + (size_t)rslot * sg.bytes, sg, g, alpha, mc);
+            float *srow = nullptr;
+            if constexpr (PROBS)   // the warp's consumed-th block is its grab of that index
+                if (prow) srow = prow + (size_t)blk(warp + nw * consumed) * KIVI_KBLK;
+            do_block<D, KB, VB, SH, false, PROBS>(A, qB, myregion + (size_t)rslot * sg.bytes, sg, g, alpha,
+                                                  mc, srow);
             __syncwarp();
             // Refill the slot just read.  Its packed data was only read (by
             // loads whose values the block has consumed): no proxy fence.
@@ -897,7 +918,8 @@ __global__ void __launch_bounds__(256, 2)
                 mc.va = max(tb, Tqv);
                 mc.zrow = reg + sg.bytes + (size_t)2 * KIVI_KBLK * RS;
                 mc.RS = RS;
-                do_block<D, KB, VB, SH, true>(A, qB, reg, sg, g, alpha, mc);
+                do_block<D, KB, VB, SH, true, PROBS>(A, qB, reg, sg, g, alpha, mc,
+                                                     PROBS && prow ? prow + tb : nullptr);
             }
         }
         __syncthreads();   // the ring holds mixed data no longer needed
@@ -960,6 +982,11 @@ __global__ void __launch_bounds__(256, 2)
                     for (int y = 0; y < np; ++y) L += ex2(sm_m[e * np + y] - M) * sm_w[e * np + y];
                 sML[e] = M;
                 sML[4 + e] = L;
+                if constexpr (PROBS) {
+                    float *ml = dv.ml + ((size_t)i * hq + j * hg + e0 + e) * 2;
+                    ml[0] = M;
+                    ml[1] = L > 0.f ? 1.f / L : 0.f;
+                }
             }
             __syncthreads();
             for (int x = threadIdx.x; x < nh * np; x += blockDim.x) {
@@ -981,39 +1008,40 @@ __global__ void __launch_bounds__(256, 2)
     }
 }
 
-template <int D, int KB, int VB, int SH>
+template <int D, int KB, int VB, int SH, bool PROBS>
 cudaError_t launch_t(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, __half *out,
-                     const DecodePlan &plan, const DecodeUnits &units, cudaStream_t st) {
+                     const DecodePlan &plan, const DecodeUnits &units, const ProbsOut &po, cudaStream_t st) {
     size_t rings = (size_t)plan.warps * warp_region(g, plan.stages);
     if (rings < mixed_region(g)) rings = mixed_region(g);
     const size_t smem = bar_region(plan.warps, plan.stages) + rings;
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, KB, VB, SH>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, KB, VB, SH, PROBS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    decode_kernel<D, KB, VB, SH><<<plan.ctas, plan.warps * 32, smem, st>>>(g, dv, q, hq, out, plan, units);
+    decode_kernel<D, KB, VB, SH, PROBS><<<plan.ctas, plan.warps * 32, smem, st>>>(g, dv, q, hq, out, plan,
+                                                                                 units, po);
     return cudaGetLastError();
 }
 
-template <int D, int KB, int VB>
+template <int D, int KB, int VB, bool PROBS>
 cudaError_t launch_g(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, __half *out,
-                     const DecodePlan &plan, const DecodeUnits &units, cudaStream_t st) {
+                     const DecodePlan &plan, const DecodeUnits &units, const ProbsOut &po, cudaStream_t st) {
     switch (g.G) {
-    case 16: return launch_t<D, KB, VB, 0>(g, dv, q, hq, out, plan, units, st);
-    case 32: return launch_t<D, KB, VB, 1>(g, dv, q, hq, out, plan, units, st);
-    case 64: return launch_t<D, KB, VB, 2>(g, dv, q, hq, out, plan, units, st);
+    case 16: return launch_t<D, KB, VB, 0, PROBS>(g, dv, q, hq, out, plan, units, po, st);
+    case 32: return launch_t<D, KB, VB, 1, PROBS>(g, dv, q, hq, out, plan, units, po, st);
+    case 64: return launch_t<D, KB, VB, 2, PROBS>(g, dv, q, hq, out, plan, units, po, st);
     default:
-        if constexpr (D >= 128) return launch_t<D, KB, VB, 3>(g, dv, q, hq, out, plan, units, st);
+        if constexpr (D >= 128) return launch_t<D, KB, VB, 3, PROBS>(g, dv, q, hq, out, plan, units, po, st);
         return cudaErrorInvalidValue;
     }
 }
 
-template <int D>
+template <int D, bool PROBS>
 cudaError_t launch_d(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, __half *out,
-                     const DecodePlan &plan, const DecodeUnits &units, cudaStream_t st) {
-    if (g.kbits == 2 && g.vbits == 2) return launch_g<D, 2, 2>(g, dv, q, hq, out, plan, units, st);
-    if (g.kbits == 2 && g.vbits == 4) return launch_g<D, 2, 4>(g, dv, q, hq, out, plan, units, st);
-    if (g.kbits == 4 && g.vbits == 2) return launch_g<D, 4, 2>(g, dv, q, hq, out, plan, units, st);
-    return launch_g<D, 4, 4>(g, dv, q, hq, out, plan, units, st);
+                     const DecodePlan &plan, const DecodeUnits &units, const ProbsOut &po, cudaStream_t st) {
+    if (g.kbits == 2 && g.vbits == 2) return launch_g<D, 2, 2, PROBS>(g, dv, q, hq, out, plan, units, po, st);
+    if (g.kbits == 2 && g.vbits == 4) return launch_g<D, 2, 4, PROBS>(g, dv, q, hq, out, plan, units, po, st);
+    if (g.kbits == 4 && g.vbits == 2) return launch_g<D, 4, 2, PROBS>(g, dv, q, hq, out, plan, units, po, st);
+    return launch_g<D, 4, 4, PROBS>(g, dv, q, hq, out, plan, units, po, st);
 }
 
 }  // namespace

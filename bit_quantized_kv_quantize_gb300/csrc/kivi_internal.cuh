@@ -73,6 +73,17 @@ struct KiviDev {
     unsigned *status;       // anomaly flags
     float *part;            // decode partials [b][h * KIVI_MAX_QPERKV][smax][d + 2]
     unsigned *merge_ticket; // [b][h] arrivals of decode CTAs (split-K merge)
+    float *ml;              // [b][h * KIVI_MAX_QPERKV][2] softmax max and 1 / sum (weights output)
+};
+
+// Optional per-token attention-weight output of a decode call: p[i][h][t]
+// (row stride ld) receives the raw scores during the decode kernel and the
+// softmax weights after the finalizing kernel; mass (may be null, same
+// layout) accumulates the weights.
+struct ProbsOut {
+    float *p;
+    float *mass;
+    long long ld;
 };
 
 struct SeqLens {
@@ -258,6 +269,9 @@ DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *T, const int *
                             int num_sms, DecodeUnits *units);
 // partial slots per (sequence, query head) a cache of this shape allocates
 int kivi_partial_slots(int b, int h, int num_sms);
+// po (may be null): also write the per-token weights (launches the
+// finalizing kernel after the decode kernel; maxT = max_i T_i).
 cudaError_t kivi_launch_decode(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq,
                                __half *out, const DecodePlan &plan, const DecodeUnits &units,
-                               cudaStream_t st, cudaEvent_t ev0, cudaEvent_t ev1);
+                               cudaStream_t st, cudaEvent_t ev0, cudaEvent_t ev1,
+                               const ProbsOut *po = nullptr, int maxT = 0);

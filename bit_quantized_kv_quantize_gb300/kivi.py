@@ -22,7 +22,8 @@ EXPORTS = ["kivi_cache_create", "kivi_cache_destroy", "kivi_prefill", "kivi_appe
            "kivi_decode_attn", "kivi_cache_lengths", "kivi_cache_export_sizes",
            "kivi_cache_export", "kivi_cache_check", "kivi_profile_enable", "kivi_profile_read",
            "kivi_decode_plan", "kivi_status_str", "kivi_last_error", "kivi_abi_version",
-           "kivi_decode_attn_noalloc", "kivi_cache_export_records", "kivi_append_decode"]
+           "kivi_decode_attn_noalloc", "kivi_cache_export_records", "kivi_append_decode",
+           "kivi_decode_attn_probs"]
 
 
 class KiviError(RuntimeError):
@@ -46,6 +47,7 @@ def _load():
     L.kivi_prefill.argtypes = [vp, vp, vp, vp, i32, vp]
     L.kivi_append.argtypes = [vp, vp, vp, vp]
     L.kivi_decode_attn.argtypes = [vp, vp, i32, vp, vp]
+    L.kivi_decode_attn_probs.argtypes = [vp, vp, i32, vp, vp, vp, ctypes.c_int64, vp]
     L.kivi_cache_lengths.argtypes = [vp, vp, vp, vp]
     L.kivi_cache_export_sizes.argtypes = [vp, ctypes.POINTER(ctypes.c_size_t)]
     L.kivi_cache_export.argtypes = [vp] * 8
@@ -76,6 +78,16 @@ def _stream(stream):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev_f32_rows(x, lead, name):
+    """Pointer of a contiguous CUDA fp32 tensor [*lead, ld]."""
+    import torch
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.float32):
+        raise TypeError(f"{name} must be a CUDA float32 tensor")
+    if x.dim() != len(lead) + 1 or tuple(x.shape[:-1]) != tuple(lead) or not x.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous [{', '.join(map(str, lead))}, ld] tensor")
+    return x.data_ptr()
 
 
 def _dev_fp16(x, shape, name):
@@ -138,6 +150,27 @@ class KiviCache:
             out = torch.empty_like(q)
         op = _dev_fp16(out, (self.b, hq, self.d), "out")
         _check(lib.kivi_decode_attn(self._h, qp, hq, op, _stream(stream)))
+        return out
+
+    def decode_probs(self, q, probs, mass=None, out=None, stream=None):
+        """decode(q), and each token's softmax weight into probs (CUDA fp32
+        [b, h_q, ld], ld >= every sequence's length; entries past a
+        sequence's length untouched); mass (same shape, optional) += probs.
+        Returns out."""
+        import torch
+        hq = q.shape[1]
+        qp = _dev_fp16(q, (self.b, hq, self.d), "q")
+        if out is None:
+            out = torch.empty_like(q)
+        op = _dev_fp16(out, (self.b, hq, self.d), "out")
+        pp = _dev_f32_rows(probs, (self.b, hq), "probs")
+        mp = 0
+        if mass is not None:
+            if tuple(mass.shape) != tuple(probs.shape):
+                raise ValueError("mass must have the shape of probs")
+            mp = _dev_f32_rows(mass, (self.b, hq), "mass")
+        _check(lib.kivi_decode_attn_probs(self._h, qp, hq, op, pp, mp or None, probs.shape[2],
+                                          _stream(stream)))
         return out
 
     def append_decode(self, k, v, q, out=None, stream=None):

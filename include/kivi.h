@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define KIVI_ABI_VERSION 3
+#define KIVI_ABI_VERSION 4
 
 typedef struct kivi_cache *kivi_cache_t;   /* opaque, library-owned */
 typedef struct CUstream_st *kivi_stream_t; /* the same type as cudaStream_t */
@@ -101,6 +101,26 @@ kivi_status kivi_append(kivi_cache_t c, const void *k, const void *v, kivi_strea
  * fp16 for the tensor-core contraction). */
 kivi_status kivi_decode_attn(kivi_cache_t c, const void *q, int h_q, void *out,
                              kivi_stream_t stream);
+
+/* Decode attention with each token's attention weight: out as
+ * kivi_decode_attn computes it (bitwise the same), and, for sequence i,
+ * query head h and token t < T_i, probs[(i h_q + h) ld + t] = the softmax
+ * weight of token t in that head's attention (fp32, device; tokens in
+ * sequence order, quantized and fp16 alike; a row's weights sum to 1).
+ * Entries t >= T_i are left as they were.  mass (device, same layout, may
+ * be NULL) accumulates the weights: mass[...] += probs[...] for t < T_i, so
+ * that repeated steps sum each token's attention over decode steps.  That
+ * sum is H2O's eviction score ("Literature audit -- Group 2 (KV-cache
+ * compression primary sources)", section 4 "H2O (Heavy-Hitter Oracle)":
+ * per head, each key's softmax weights added over the query rows seen so
+ * far), and section 1 "KIVI" counts KIVI as orthogonal to, and combinable
+ * with, such eviction.  Token positions are stable across appends, so mass
+ * rows stay aligned.
+ * ld >= 1 and ld >= every T_i; probs and mass 4-byte aligned and distinct
+ * (KIVI_ERR_INVALID_ARG otherwise).  Two launches: the decode kernel writes
+ * raw scores into probs, a second kernel turns them into weights. */
+kivi_status kivi_decode_attn_probs(kivi_cache_t c, const void *q, int h_q, void *out, float *probs,
+                                   float *mass, int64_t ld, kivi_stream_t stream);
 
 /* One decode step in one call: kivi_append(k, v) then kivi_decode_attn(q,
  * h_q, out), launched back to back on `stream` once both sets of arguments
