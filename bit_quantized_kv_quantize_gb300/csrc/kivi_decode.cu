@@ -1,8 +1,8 @@
 // kivi_decode.cu -- launch planning and dispatch of the decode-attention
 // kernel (kivi_decode_impl.cuh, instantiated per head dimension in
 // kivi_decode_d{64,128,256}.cu, and with the score output for the
-// attention weights in kivi_decode_probs_d{64,128,256}.cu), and the kernel
-// that turns those scores into weights.
+// attention weights in kivi_decode_probs_d{64,128,256}.cu; kivi_probs.cu
+// turns those scores into weights).
 //
 // The kernel is persistent: a fixed grid of CTAs (two per SM) splits the
 // work units of all (sequence, kv head, head group) pairs evenly, so every
@@ -10,7 +10,6 @@
 // lengths (no partial last wave).  A unit is one 64-token block; blocks that
 // hold fp16 window tokens (the last few of each sequence) are staged by the
 // whole CTA with one round trip each and count MW units.
-#include <cstdint>
 #include <cstdlib>
 
 #include "kivi_internal.cuh"
@@ -44,56 +43,6 @@ long long cta_of(long long u, long long U, int C) { return ((u + 1) * C - 1) / U
 
 constexpr int kCtasPerSm = 2;   // the kernel is compiled for <= 128 registers a thread
 
-// Tokens of one weights row a CTA of the finalizing kernel covers.
-constexpr int kProbsChunk = 4096;
-
-__device__ __forceinline__ float weight_of(float s, float M, float inv) { return exp2f(s - M) * inv; }
-
-// The attention-weight output, after the decode kernel: each (sequence i,
-// query head) row holds the T_i raw scores s (log2 units) and the merge left
-// the row's softmax max M and 1 / sum; the weight is 2^(s - M) / sum, and
-// mass (if any) accumulates it.  CTA x covers chunk x % chunks of row
-// x / chunks.  VEC: rows start on 16-byte boundaries (ld % 4 == 0, aligned
-// buffers), so four tokens move per access.
-template <bool VEC>
-__global__ void __launch_bounds__(256) probs_finalize_kernel(const int *__restrict__ T,
-                                                             const float *__restrict__ ml, int hq,
-                                                             int chunks, ProbsOut po) {
-    const int row = blockIdx.x / chunks, ch = blockIdx.x % chunks;
-    const int t0 = ch * kProbsChunk, t1 = min(T[row / hq], t0 + kProbsChunk);
-    if (t0 >= t1) return;
-    const float M = ml[2 * row], inv = ml[2 * row + 1];
-    float *p = po.p + (size_t)row * po.ld;
-    float *mass = po.mass ? po.mass + (size_t)row * po.ld : nullptr;
-    int tail = t0;
-    if constexpr (VEC) {
-        const int n4 = (t1 - t0) >> 2;
-        float4 *p4 = reinterpret_cast<float4 *>(p + t0);
-        float4 *m4 = mass ? reinterpret_cast<float4 *>(mass + t0) : nullptr;
-        for (int k = threadIdx.x; k < n4; k += blockDim.x) {
-            float4 w = p4[k];
-            w.x = weight_of(w.x, M, inv);
-            w.y = weight_of(w.y, M, inv);
-            w.z = weight_of(w.z, M, inv);
-            w.w = weight_of(w.w, M, inv);
-            p4[k] = w;
-            if (m4) {
-                float4 a = m4[k];
-                a.x += w.x;
-                a.y += w.y;
-                a.z += w.z;
-                a.w += w.w;
-                m4[k] = a;
-            }
-        }
-        tail = t0 + 4 * n4;
-    }
-    for (int t = tail + threadIdx.x; t < t1; t += blockDim.x) {
-        const float w = weight_of(p[t], M, inv);
-        p[t] = w;
-        if (mass) mass[t] += w;
-    }
-}
 }  // namespace
 
 int kivi_partial_slots(int b, int h, int num_sms) {
@@ -178,13 +127,6 @@ cudaError_t kivi_launch_decode(const KiviGeom &g, const KiviDev &dv, const __hal
         }
     }
     if (ev1) cudaEventRecord(ev1, st);
-    if (e == cudaSuccess && po && maxT > 0) {
-        const int chunks = (maxT + kProbsChunk - 1) / kProbsChunk;
-        const unsigned grid = (unsigned)(g.b * hq) * chunks;
-        const bool vec = po->ld % 4 == 0 && ((uintptr_t)po->p & 15u) == 0 && ((uintptr_t)po->mass & 15u) == 0;
-        if (vec) probs_finalize_kernel<true><<<grid, 256, 0, st>>>(dv.T, dv.ml, hq, chunks, *po);
-        else probs_finalize_kernel<false><<<grid, 256, 0, st>>>(dv.T, dv.ml, hq, chunks, *po);
-        e = cudaGetLastError();
-    }
+    if (e == cudaSuccess && po && maxT > 0) e = kivi_launch_probs_finalize(g, dv, hq, *po, maxT, st);
     return e;
 }

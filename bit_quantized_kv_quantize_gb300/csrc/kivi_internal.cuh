@@ -269,6 +269,10 @@ DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *T, const int *
                             int num_sms, DecodeUnits *units);
 // partial slots per (sequence, query head) a cache of this shape allocates
 int kivi_partial_slots(int b, int h, int num_sms);
+// Scores left in po.p by the decode kernel's weights variant -> weights
+// (and mass += weights), for rows of up to maxT tokens (kivi_probs.cu).
+cudaError_t kivi_launch_probs_finalize(const KiviGeom &g, const KiviDev &dv, int hq, const ProbsOut &po,
+                                       int maxT, cudaStream_t st);
 // po (may be null): also write the per-token weights (launches the
 // finalizing kernel after the decode kernel; maxT = max_i T_i).
 cudaError_t kivi_launch_decode(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq,

@@ -200,3 +200,27 @@ def test_probs_argument_errors():
     gpu.decode_probs(q, p)
     np.testing.assert_allclose(p.sum(2).cpu().numpy(), 1.0, rtol=1e-5)
     gpu.close()
+
+
+def test_probs_unaligned_buffers():
+    """Buffers that start off a 16-byte boundary (a view one float in) take
+    the one-token-at-a-time path and give the same weights and mass."""
+    b, h, hq, d = 2, 2, 4, 128
+    rng = np.random.default_rng(77)
+    gpu = K.KiviCache(b, h, d, 2, 2, 32, 128, 5000)
+    Kh = rng.standard_normal((b, h, 4500, d)).astype(np.float16)
+    Vh = rng.standard_normal((b, h, 4500, d)).astype(np.float16)
+    gpu.prefill(_dev(Kh), _dev(Vh), [4500, 4099])
+    q = _dev(rng.standard_normal((b, hq, d)).astype(np.float16))
+    ld = 4502
+    n = b * hq * ld
+    pa = torch.zeros((b, hq, ld), dtype=torch.float32, device="cuda")
+    ma = torch.ones_like(pa)
+    pu = torch.zeros(n + 1, dtype=torch.float32, device="cuda")[1:].view(b, hq, ld)
+    mu = torch.ones(n + 1, dtype=torch.float32, device="cuda")[1:].view(b, hq, ld)
+    assert pu.data_ptr() % 16 and mu.data_ptr() % 16
+    gpu.decode_probs(q, pa, mass=ma)
+    gpu.decode_probs(q, pu, mass=mu)
+    assert torch.equal(pa, pu) and torch.equal(ma, mu)
+    np.testing.assert_allclose(pa.sum(2).cpu().numpy(), 1.0, rtol=1e-5)
+    gpu.close()
