@@ -42,6 +42,11 @@ struct kivi_cache {
     int num_sms;
     KiviGeom g;
     KiviDev dv;
+    // Two device counter sets [2][3][b] (T, Tqk, Tqv): dv points at set
+    // `parity`; an append reads the host mirror and writes the other set,
+    // which then becomes current (no CTA of the append waits for another).
+    int *cnt;
+    int parity;
     std::vector<int> T, Tqk, Tqv;   // host mirror
     DecodePlan last_plan;
     bool profiling;
@@ -82,11 +87,21 @@ kivi_status check_handle(kivi_cache_t c) {
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-void free_dev(KiviDev &d) {
-    void *ps[] = {d.blk, d.Kf, d.Vf, d.T, d.Tqk, d.Tqv, d.ticket, d.status, d.part, d.merge_ticket, d.ml};
+void free_dev(kivi_cache *c) {
+    KiviDev &d = c->dv;
+    void *ps[] = {d.blk, d.Kf, d.Vf, c->cnt, d.status, d.part, d.merge_ticket, d.ml};
     for (void *p : ps)
         if (p) cudaFree(p);
     memset(&d, 0, sizeof d);
+    c->cnt = nullptr;
+}
+
+void point_counters(kivi_cache *c) {
+    const int b = c->g.b;
+    int *set = c->cnt + (size_t)c->parity * 3 * b;
+    c->dv.T = set;
+    c->dv.Tqk = set + b;
+    c->dv.Tqv = set + 2 * b;
 }
 
 kivi_status check_decode_args(kivi_cache *c, const void *q, int h_q, const void *out) {
@@ -134,6 +149,25 @@ void advance_mirror(kivi_cache *c) {
         if (c->T[i] - c->Tqv[i] == R + 1) c->Tqv[i] += 1;
         c->T[i] += 1;
     }
+}
+
+// Launch the append kernel from the host mirror, then make the counter set
+// it writes current and advance the mirror.
+kivi_status launch_append(kivi_cache *c, const void *k, const void *v, kivi_stream_t stream,
+                          const char *what) {
+    const int b = c->g.b;
+    AppendCounters ac;   // entries past b are never read
+    memcpy(ac.T, c->T.data(), (size_t)b * sizeof(int));
+    memcpy(ac.Tqk, c->Tqk.data(), (size_t)b * sizeof(int));
+    memcpy(ac.Tqv, c->Tqv.data(), (size_t)b * sizeof(int));
+    int *nxt = c->cnt + (size_t)(1 - c->parity) * 3 * b;
+    cudaError_t e = kivi_launch_append(c->g, c->dv, (const __half *)k, (const __half *)v, ac, nxt,
+                                       (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail_cuda(c, e, what);
+    c->parity ^= 1;
+    point_counters(c);
+    advance_mirror(c);
+    return KIVI_OK;
 }
 
 // Plan and launch the decode kernel; units come from (T, Tqk, Tqv).
@@ -260,10 +294,7 @@ kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, in
         {(void **)&dv.blk, bh * g.nkb * g.rec_bytes},
         {(void **)&dv.Kf, bh * R * d * 2},
         {(void **)&dv.Vf, bh * (R + 1) * d * 2},
-        {(void **)&dv.T, (size_t)b * 4},
-        {(void **)&dv.Tqk, (size_t)b * 4},
-        {(void **)&dv.Tqv, (size_t)b * 4},
-        {(void **)&dv.ticket, (size_t)b * 4},
+        {(void **)&c->cnt, (size_t)2 * 3 * b * 4},
         {(void **)&dv.status, 4},
         {(void **)&dv.part, bh * KIVI_MAX_QPERKV * g.smax * (d + 2) * 4},
         {(void **)&dv.merge_ticket, bh * 4 * 4},
@@ -273,16 +304,18 @@ kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, in
         e = cudaMalloc(r.p, r.bytes);
         if (e == cudaSuccess) e = cudaMemset(*r.p, 0, r.bytes);
         if (e != cudaSuccess) {
-            free_dev(dv);
+            free_dev(c);
             delete c;
             cudaGetLastError();
             snprintf(g_err, sizeof g_err, "device allocation failed: %s", cudaGetErrorString(e));
             return e == cudaErrorMemoryAllocation ? KIVI_ERR_OOM : KIVI_ERR_CUDA;
         }
     }
+    c->parity = 0;
+    point_counters(c);
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
-        free_dev(dv);
+        free_dev(c);
         delete c;
         snprintf(g_err, sizeof g_err, "create: %s", cudaGetErrorString(e));
         return KIVI_ERR_CUDA;
@@ -310,7 +343,7 @@ kivi_status kivi_cache_destroy(kivi_cache_t c) {
     }
     cudaDeviceSynchronize();
     cudaGetLastError();
-    free_dev(c->dv);
+    free_dev(c);
     for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
     c->magic = 0;
     delete c;
@@ -365,11 +398,7 @@ kivi_status kivi_append(kivi_cache_t c, const void *k, const void *v, kivi_strea
     if (s != KIVI_OK) return s;
     s = check_append_args(c, k, v);
     if (s != KIVI_OK) return s;
-    cudaError_t e = kivi_launch_append(c->g, c->dv, (const __half *)k, (const __half *)v,
-                                       (cudaStream_t)stream);
-    if (e != cudaSuccess) return fail_cuda(c, e, "append");
-    advance_mirror(c);
-    return KIVI_OK;
+    return launch_append(c, k, v, stream, "append");
 }
 
 kivi_status kivi_decode_attn(kivi_cache_t c, const void *q, int h_q, void *out,
@@ -417,10 +446,8 @@ kivi_status kivi_append_decode(kivi_cache_t c, const void *k, const void *v, con
     if (s != KIVI_OK) return s;
     s = check_decode_args(c, q, h_q, out);
     if (s != KIVI_OK) return s;
-    cudaError_t e = kivi_launch_append(c->g, c->dv, (const __half *)k, (const __half *)v,
-                                       (cudaStream_t)stream);
-    if (e != cudaSuccess) return fail_cuda(c, e, "append_decode");
-    advance_mirror(c);
+    s = launch_append(c, k, v, stream, "append_decode");
+    if (s != KIVI_OK) return s;
     return launch_decode(c, q, h_q, out, stream, c->T.data(), c->Tqk.data(), c->Tqv.data(), "append_decode");
 }
 

@@ -43,19 +43,29 @@ __device__ __forceinline__ void append_pair(const KiviGeom &g, const KiviDev &dv
     __half *kfw = dv.Kf + kf_slice(g, i, j);
     __half *vfw = dv.Vf + vf_slice(g, i, j);
 
+    // the flushed groups' scale and zero (fp32), when they fit
+    constexpr int kSzCap = 2048;
+    __shared__ float s_ks[kSzCap], s_kz[kSzCap];
     if (flush) {
         // keys [Tqk, Tqk + R): token tau lives in slot tau - Tqk (Tqk % R == 0)
         const int ngr = R / g.G;
+        const bool sz_smem = ngr * d <= kSzCap;
         for (int e = threadIdx.x; e < ngr * d; e += blockDim.x) {
             int gr = e / d, c = e - gr * d;
-            float mn = __half2float(kf[(size_t)gr * g.G * d + c]), mx = mn;
-            for (int k = 1; k < g.G; ++k) {
-                float x = __half2float(kf[((size_t)gr * g.G + k) * d + c]);
+            const __half *col = kf + (size_t)gr * g.G * d + c;
+            float mn = __half2float(col[0]), mx = mn;
+#pragma unroll 8
+            for (int k = 1; k < g.G; ++k) {   // independent loads: several in flight
+                float x = __half2float(col[(size_t)k * d]);
                 mn = fminf(mn, x);
                 mx = fmaxf(mx, x);
             }
             QParams p = qparams(mn, mx, g.kbits);
             ksz_store(g, dv.blk, i, j, Tqk / g.G + gr, c, p.s16, p.z16);
+            if (sz_smem) {
+                s_ks[e] = p.sf;
+                s_kz[e] = p.zf;
+            }
         }
         __syncthreads();
         const int kb0 = Tqk / KIVI_KBLK, kb1 = (Tqk + R - 1) / KIVI_KBLK;
@@ -68,6 +78,7 @@ __device__ __forceinline__ void append_pair(const KiviGeom &g, const KiviDev &dv
             uint32_t word = 0;
             for (int half = 0; half < 2; ++half) {
                 int c = kw.c0 + half;
+#pragma unroll 8
                 for (int r = 0; r < cph; ++r) {
                     int tau = kb * KIVI_KBLK + 8 * (kw.pos0 + r) + kw.g;
                     int sh = 16 * half + r * g.kbits;
@@ -76,8 +87,14 @@ __device__ __forceinline__ void append_pair(const KiviGeom &g, const KiviDev &dv
                         word |= old & mask;                     // earlier tokens stay
                     } else if (tau < Tqk + R) {
                         int grp = tau / g.G;
-                        float sf = __half2float(ksz_load(g, dv.blk, i, j, grp, c, 0));
-                        float zf = __half2float(ksz_load(g, dv.blk, i, j, grp, c, 1));
+                        float sf, zf;
+                        if (sz_smem) {   // the value ksz_store just wrote, as fp32
+                            sf = s_ks[(grp - Tqk / g.G) * d + c];
+                            zf = s_kz[(grp - Tqk / g.G) * d + c];
+                        } else {
+                            sf = __half2float(ksz_load(g, dv.blk, i, j, grp, c, 0));
+                            zf = __half2float(ksz_load(g, dv.blk, i, j, grp, c, 1));
+                        }
                         float x = __half2float(kf[(size_t)(tau - Tqk) * d + c]);
                         word |= qcode(x, sf, zf, g.kbits) << sh;
                     }                                           // later tokens: zero

@@ -716,6 +716,13 @@ __global__ void __launch_bounds__(256, 2)
     if (threadIdx.x <= nw * plan.stages) mbar_init(bars + threadIdx.x, 1);
     fence_mbar_init();
     __syncthreads();
+    // The kernel is launched as a programmatic dependent of the one before
+    // it on the stream (usually the append): the set-up above touched only
+    // shared memory and parameters; nothing in global memory is read before
+    // that kernel has finished.  A dependent launched after this one (the
+    // weights' finalizing kernel) may in turn start its own set-up.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     int rslot = 0;         // this warp's next ring slot to consume ...
     unsigned rphase = 0;   // ... and the phase its barrier completes next
     bool dead = false;     // a wait of this warp timed out: it streams no more blocks
@@ -1017,9 +1024,19 @@ cudaError_t launch_t(const KiviGeom &g, const KiviDev &dv, const __half *q, int 
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, KB, VB, SH, PROBS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    decode_kernel<D, KB, VB, SH, PROBS><<<plan.ctas, plan.warps * 32, smem, st>>>(g, dv, q, hq, out, plan,
-                                                                                 units, po);
-    return cudaGetLastError();
+    // programmatic dependent launch: the CTAs may be placed while the
+    // previous kernel (the append) finishes; the kernel waits for it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.ctas);
+    cfg.blockDim = dim3(plan.warps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_kernel<D, KB, VB, SH, PROBS>, g, dv, q, hq, out, plan, units, po);
 }
 
 template <int D, int KB, int VB, bool PROBS>

@@ -68,8 +68,7 @@ struct KiviDev {
     unsigned char *blk;     // block records [b][h][nkb][rec_bytes]
     __half *Kf;
     __half *Vf;
-    int *T, *Tqk, *Tqv;     // device counters [b]
-    unsigned *ticket;       // [b] arrivals of the append kernel's CTAs
+    int *T, *Tqk, *Tqv;     // device counters [b] (the current one of the cache's two sets)
     unsigned *status;       // anomaly flags
     float *part;            // decode partials [b][h * KIVI_MAX_QPERKV][smax][d + 2]
     unsigned *merge_ticket; // [b][h] arrivals of decode CTAs (split-K merge)
@@ -88,6 +87,12 @@ struct ProbsOut {
 
 struct SeqLens {
     int t[KIVI_MAX_BATCH];
+};
+
+// Every sequence's counters before an append, from the host mirror (kernel
+// parameters: the append needs no device read before its row loads).
+struct AppendCounters {
+    int T[KIVI_MAX_BATCH], Tqk[KIVI_MAX_BATCH], Tqv[KIVI_MAX_BATCH];
 };
 
 // ---- records and slice bases ----------------------------------------------------
@@ -263,8 +268,10 @@ void kivi_set_last_error(const char *msg);
 cudaError_t kivi_launch_prefill(const KiviGeom &g, const KiviDev &dv, const __half *K,
                                 const __half *V, const SeqLens &lens, int t_stride,
                                 cudaStream_t st);
+// nxt: the other counter set ([3][b]: T, Tqk, Tqv), which receives the
+// counters after the append (dv's set is left as it was).
 cudaError_t kivi_launch_append(const KiviGeom &g, const KiviDev &dv, const __half *k,
-                               const __half *v, cudaStream_t st);
+                               const __half *v, const AppendCounters &ac, int *nxt, cudaStream_t st);
 DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *T, const int *Tqk, const int *Tqv,
                             int num_sms, DecodeUnits *units);
 // partial slots per (sequence, query head) a cache of this shape allocates

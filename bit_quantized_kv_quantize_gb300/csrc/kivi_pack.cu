@@ -233,7 +233,6 @@ __global__ void prefill_residual_kernel(KiviGeom g, KiviDev dv, const __half *__
         dv.T[i] = t;
         dv.Tqk[i] = nqk;
         dv.Tqv[i] = nqv;
-        dv.ticket[i] = 0u;
     }
 }
 
@@ -242,29 +241,37 @@ __global__ void prefill_residual_kernel(KiviGeom g, KiviDev dv, const __half *__
 // then the last CTA of a sequence to finish advances that sequence's
 // counters (all CTAs read them first).
 // ---------------------------------------------------------------------------
+// One CTA per (kv head j, sequence i).  The counters before the append come
+// from the host mirror (ac); the device's current set is read only to check
+// that the two agree.  CTA j = 0 of each sequence writes the counters after
+// the append into the other set (nxt), so no CTA waits for another.
 __global__ void __launch_bounds__(256) append_kernel(KiviGeom g, KiviDev dv,
                                                      const __half *__restrict__ knew,
-                                                     const __half *__restrict__ vnew) {
+                                                     const __half *__restrict__ vnew, AppendCounters ac,
+                                                     int *__restrict__ nxt) {
+    // the decode launch that usually follows may start its set-up now: it
+    // waits for this whole grid before it reads anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int j = blockIdx.x, i = blockIdx.y;
     const int R = g.R;
-    const int T = dv.T[i], Tqk = dv.Tqk[i], Tqv = dv.Tqv[i];
+    const int T = ac.T[i], Tqk = ac.Tqk[i], Tqv = ac.Tqv[i];
+    int dT = T, dTqk = Tqk, dTqv = Tqv;
+    if (threadIdx.x == 0) {
+        dT = dv.T[i];
+        dTqk = dv.Tqk[i];
+        dTqv = dv.Tqv[i];
+    }
     if (!append_counters_ok(g, T, Tqk, Tqv)) {
         if (threadIdx.x == 0) flag(dv.status, KIVI_FLAG_COUNTER);
         return;
     }
     append_pair(g, dv, knew, vnew, i, j, T, Tqk, Tqv);
-
-    // last CTA of this sequence advances the counters
-    __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        unsigned prev = atomicAdd(&dv.ticket[i], 1u);
-        if (prev == (unsigned)g.h - 1u) {
-            dv.T[i] = T + 1;
-            dv.Tqk[i] = Tqk + ((T - Tqk) == R ? R : 0);
-            dv.Tqv[i] = Tqv + ((T - Tqv) == R + 1 ? 1 : 0);
-            dv.ticket[i] = 0u;
-            __threadfence();
+        if (dT != T || dTqk != Tqk || dTqv != Tqv) flag(dv.status, KIVI_FLAG_COUNTER);
+        if (j == 0) {
+            nxt[i] = T + 1;
+            nxt[g.b + i] = Tqk + ((T - Tqk) == R ? R : 0);
+            nxt[2 * g.b + i] = Tqv + ((T - Tqv) == R + 1 ? 1 : 0);
         }
     }
 }
@@ -291,7 +298,7 @@ cudaError_t kivi_launch_prefill(const KiviGeom &g, const KiviDev &dv, const __ha
 }
 
 cudaError_t kivi_launch_append(const KiviGeom &g, const KiviDev &dv, const __half *k,
-                               const __half *v, cudaStream_t st) {
-    append_kernel<<<dim3(g.h, g.b), 256, 0, st>>>(g, dv, k, v);
+                               const __half *v, const AppendCounters &ac, int *nxt, cudaStream_t st) {
+    append_kernel<<<dim3(g.h, g.b), 256, 0, st>>>(g, dv, k, v, ac, nxt);
     return cudaGetLastError();
 }

@@ -27,6 +27,8 @@ template <bool VEC>
 __global__ void __launch_bounds__(256) probs_finalize_kernel(const int *__restrict__ T,
                                                              const float *__restrict__ ml, int hq,
                                                              int chunks, ProbsOut po) {
+    // a programmatic dependent of the decode kernel: wait for it to finish
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int row = blockIdx.x / chunks, ch = blockIdx.x % chunks;
     const int t0 = ch * kChunk, t1 = min(T[row / hq], t0 + kChunk);
     if (t0 >= t1) return;
@@ -71,7 +73,17 @@ cudaError_t kivi_launch_probs_finalize(const KiviGeom &g, const KiviDev &dv, int
     const int chunks = (maxT + kChunk - 1) / kChunk;
     const unsigned grid = (unsigned)(g.b * hq) * chunks;
     const bool vec = ((uintptr_t)po.p & 15u) == 0 && ((uintptr_t)po.mass & 15u) == 0;
-    if (vec) probs_finalize_kernel<true><<<grid, 256, 0, st>>>(dv.T, dv.ml, hq, chunks, po);
-    else probs_finalize_kernel<false><<<grid, 256, 0, st>>>(dv.T, dv.ml, hq, chunks, po);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (vec) return cudaLaunchKernelEx(&cfg, probs_finalize_kernel<true>, (const int *)dv.T, (const float *)dv.ml, hq,
+                                       chunks, po);
+    return cudaLaunchKernelEx(&cfg, probs_finalize_kernel<false>, (const int *)dv.T, (const float *)dv.ml, hq, chunks,
+                              po);
 }
