@@ -43,64 +43,77 @@ __device__ __forceinline__ void append_pair(const KiviGeom &g, const KiviDev &dv
     __half *kfw = dv.Kf + kf_slice(g, i, j);
     __half *vfw = dv.Vf + vf_slice(g, i, j);
 
-    // the flushed groups' scale and zero (fp32), when they fit
-    constexpr int kSzCap = 2048;
-    __shared__ float s_ks[kSzCap], s_kz[kSzCap];
     if (flush) {
-        // keys [Tqk, Tqk + R): token tau lives in slot tau - Tqk (Tqk % R == 0)
-        const int ngr = R / g.G;
-        const bool sz_smem = ngr * d <= kSzCap;
-        for (int e = threadIdx.x; e < ngr * d; e += blockDim.x) {
-            int gr = e / d, c = e - gr * d;
-            const __half *col = kf + (size_t)gr * g.G * d + c;
-            float mn = __half2float(col[0]), mx = mn;
-#pragma unroll 8
-            for (int k = 1; k < g.G; ++k) {   // independent loads: several in flight
-                float x = __half2float(col[(size_t)k * d]);
-                mn = fminf(mn, x);
-                mx = fmaxf(mx, x);
+        // Keys [Tqk, Tqk + R) (token tau in window slot tau - Tqk, as
+        // Tqk % R == 0), one round of CH aligned tokens at a time
+        // (flush_round_tokens: whole groups and 64-token blocks): the
+        // round's window rows come into shared memory with one round trip,
+        // then its groups get their scale and zero and its blocks their
+        // code words.  Shared memory (dynamic, flush_smem_bytes): rows
+        // [CH][d] fp16, then s, z and RN(1 / s) [CH/G][d] fp32.  G, d and
+        // the block's word count are powers of two: indices are shifts and
+        // masks.
+        extern __shared__ __align__(16) unsigned char flush_smem[];
+        const int G = g.G, CH = flush_round_tokens(g);
+        const int CA = G > KIVI_KBLK ? G : KIVI_KBLK;   // alignment of a round's start
+        const int lgG = __ffs(G) - 1, lgd = __ffs(d) - 1, lgw = __ffs(g.kc_blk) - 1;
+        __half *xs = reinterpret_cast<__half *>(flush_smem);
+        float *s_ks = reinterpret_cast<float *>(flush_smem + (size_t)CH * d * 2);
+        float *s_kz = s_ks + (CH / G) * d;
+        float *s_kr = s_kz + (CH / G) * d;
+        const int nv = d / 8;   // 16-byte pieces per row
+        const int cph = 16 / g.kbits;
+        for (int cs = Tqk / CA * CA; cs < Tqk + R; cs += CH) {
+            const int ta = max(cs, Tqk), tb = min(cs + CH, Tqk + R);   // multiples of G
+            for (int e = threadIdx.x; e < (tb - ta) * nv; e += blockDim.x) {
+                const int tau = ta + e / nv, c8 = e % nv;
+                reinterpret_cast<uint4 *>(xs + (size_t)(tau - cs) * d)[c8] =
+                    reinterpret_cast<const uint4 *>(kf + (size_t)(tau - Tqk) * d)[c8];
             }
-            QParams p = qparams(mn, mx, g.kbits);
-            ksz_store(g, dv.blk, i, j, Tqk / g.G + gr, c, p.s16, p.z16);
-            if (sz_smem) {
+            __syncthreads();
+            const int gr0 = ta >> lgG, ngr = (tb - ta) >> lgG;
+            for (int e = threadIdx.x; e < ngr * d; e += blockDim.x) {
+                const int gr = e >> lgd, c = e & (d - 1);
+                const __half *col = xs + (size_t)((gr0 + gr) * G - cs) * d + c;
+                float mn = __half2float(col[0]), mx = mn;
+                for (int k = 1; k < G; ++k) {
+                    const float x = __half2float(col[(size_t)k * d]);
+                    mn = fminf(mn, x);
+                    mx = fmaxf(mx, x);
+                }
+                const QParams p = qparams(mn, mx, g.kbits);
+                ksz_store(g, dv.blk, i, j, gr0 + gr, c, p.s16, p.z16);
                 s_ks[e] = p.sf;
                 s_kz[e] = p.zf;
+                s_kr[e] = p.sf == 0.0f ? 0.0f : __frcp_rn(p.sf);
             }
-        }
-        __syncthreads();
-        const int kb0 = Tqk / KIVI_KBLK, kb1 = (Tqk + R - 1) / KIVI_KBLK;
-        const int cph = 16 / g.kbits;
-        for (int e = threadIdx.x; e < (kb1 - kb0 + 1) * g.kc_blk; e += blockDim.x) {
-            int kb = kb0 + e / g.kc_blk, wb = e % g.kc_blk;
-            KWord kw = kword_decode(wb, g.kbits);
-            uint32_t *kc = kc_words(g, dv.blk, i, j, kb);
-            uint32_t old = kc[wb];
-            uint32_t word = 0;
-            for (int half = 0; half < 2; ++half) {
-                int c = kw.c0 + half;
-#pragma unroll 8
-                for (int r = 0; r < cph; ++r) {
-                    int tau = kb * KIVI_KBLK + 8 * (kw.pos0 + r) + kw.g;
-                    int sh = 16 * half + r * g.kbits;
-                    uint32_t mask = ((1u << g.kbits) - 1u) << sh;
-                    if (tau < Tqk) {
-                        word |= old & mask;                     // earlier tokens stay
-                    } else if (tau < Tqk + R) {
-                        int grp = tau / g.G;
-                        float sf, zf;
-                        if (sz_smem) {   // the value ksz_store just wrote, as fp32
-                            sf = s_ks[(grp - Tqk / g.G) * d + c];
-                            zf = s_kz[(grp - Tqk / g.G) * d + c];
-                        } else {
-                            sf = __half2float(ksz_load(g, dv.blk, i, j, grp, c, 0));
-                            zf = __half2float(ksz_load(g, dv.blk, i, j, grp, c, 1));
+            __syncthreads();
+            const int kb0 = cs / KIVI_KBLK, nkb = CH / KIVI_KBLK;
+            for (int e = threadIdx.x; e < nkb * g.kc_blk; e += blockDim.x) {
+                const int kb = kb0 + (e >> lgw), wb = e & (g.kc_blk - 1);
+                const int t0 = kb * KIVI_KBLK;
+                if (t0 >= tb || t0 + KIVI_KBLK <= ta) continue;   // no window token in this block
+                const KWord kw = kword_decode(wb, g.kbits);
+                uint32_t *kc = kc_words(g, dv.blk, i, j, kb);
+                const uint32_t old = t0 < Tqk ? kc[wb] : 0u;   // earlier tokens' codes stay
+                uint32_t word = 0;
+                for (int half = 0; half < 2; ++half) {
+                    const int c = kw.c0 + half;
+                    for (int r = 0; r < cph; ++r) {
+                        const int tau = t0 + 8 * (kw.pos0 + r) + kw.g;
+                        const int sh = 16 * half + r * g.kbits;
+                        if (tau < Tqk) {
+                            word |= old & (((1u << g.kbits) - 1u) << sh);
+                        } else if (tau < tb) {   // later tokens: zero
+                            const int sz = (((tau >> lgG) - gr0) << lgd) + c;
+                            word |= qcode_rcp(__half2float(xs[((tau - cs) << lgd) + c]), s_ks[sz], s_kz[sz],
+                                              s_kr[sz], g.kbits) << sh;
                         }
-                        float x = __half2float(kf[(size_t)(tau - Tqk) * d + c]);
-                        word |= qcode(x, sf, zf, g.kbits) << sh;
-                    }                                           // later tokens: zero
+                    }
                 }
+                kc[wb] = word;
             }
-            kc[wb] = word;
+            __syncthreads();   // the next chunk reuses the rows
         }
     }
 

@@ -89,6 +89,23 @@ struct SeqLens {
     int t[KIVI_MAX_BATCH];
 };
 
+// Key-window flush staging: a round covers this many aligned tokens (a
+// multiple of max(64, G), so it holds whole groups and whole 64-token
+// blocks), as many as keep the fp16 rows within 48 KB of shared memory and
+// no more than a window can touch; and the round's shared-memory bytes
+// (rows, then scale, zero and reciprocal per group and channel, fp32).
+__host__ __device__ __forceinline__ int flush_round_tokens(const KiviGeom &g) {
+    const int ch = g.G > 64 ? g.G : 64;
+    int n = 48 * 1024 / (g.d * 2) / ch;
+    if (n < 1) n = 1;
+    const int need = (g.R + ch - 1) / ch + 1;
+    return ch * (n < need ? n : need);
+}
+__host__ __device__ __forceinline__ size_t flush_smem_bytes(const KiviGeom &g) {
+    const int r = flush_round_tokens(g);
+    return (size_t)r * g.d * 2 + 3 * (size_t)(r / g.G) * g.d * 4;
+}
+
 // Every sequence's counters before an append, from the host mirror (kernel
 // parameters: the append needs no device read before its row loads).
 struct AppendCounters {

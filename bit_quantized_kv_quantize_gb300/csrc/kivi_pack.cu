@@ -245,7 +245,7 @@ __global__ void prefill_residual_kernel(KiviGeom g, KiviDev dv, const __half *__
 // from the host mirror (ac); the device's current set is read only to check
 // that the two agree.  CTA j = 0 of each sequence writes the counters after
 // the append into the other set (nxt), so no CTA waits for another.
-__global__ void __launch_bounds__(256) append_kernel(KiviGeom g, KiviDev dv,
+__global__ void __launch_bounds__(1024) append_kernel(KiviGeom g, KiviDev dv,
                                                      const __half *__restrict__ knew,
                                                      const __half *__restrict__ vnew, AppendCounters ac,
                                                      int *__restrict__ nxt) {
@@ -299,6 +299,17 @@ cudaError_t kivi_launch_prefill(const KiviGeom &g, const KiviDev &dv, const __ha
 
 cudaError_t kivi_launch_append(const KiviGeom &g, const KiviDev &dv, const __half *k,
                                const __half *v, const AppendCounters &ac, int *nxt, cudaStream_t st) {
-    append_kernel<<<dim3(g.h, g.b), 256, 0, st>>>(g, dv, k, v, ac, nxt);
+    // When some sequence flushes its key window now: shared memory for the
+    // staged window rows and their groups' scale, zero and reciprocal, and
+    // four times the threads (the flush is latency-bound arithmetic over
+    // R x d keys; the other steps move one token).
+    bool flush = false;
+    for (int i = 0; i < g.b; ++i) flush |= ac.T[i] - ac.Tqk[i] == g.R;
+    const size_t smem = flush ? flush_smem_bytes(g) : 0;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    append_kernel<<<dim3(g.h, g.b), flush ? 1024 : 256, smem, st>>>(g, dv, k, v, ac, nxt);
     return cudaGetLastError();
 }
