@@ -75,15 +75,20 @@ __global__ void __launch_bounds__(256) prefill_keys_kernel(KiviGeom g, KiviDev d
     for (int e = threadIdx.x; e < nblk * kc_blk; e += blockDim.x) {
         const int kbl = e / kc_blk, wb = e - kbl * kc_blk;
         const KWord kw = kword_decode(wb, KBITS);
+        // Slot r holds token trow + 8 r + g (g < 8).  trow is a multiple of
+        // 32, and of G whenever G <= 32; for G >= 64 the word's tokens lie
+        // in one group.  So slot r's group is trow / G + (8 r) / G: a
+        // compile-time step, and slots of one group share their loads.
+        const int trow = kbl * KIVI_KBLK + 8 * kw.pos0;
+        const float *fw = sfz + (size_t)(trow / G) * 3 * d + kw.c0;
         uint32_t word = 0;
 #pragma unroll
         for (int r = 0; r < cph; ++r) {
             // slot r of both halves: token tl, channels c0 and c0 + 1
-            const int tl = kbl * KIVI_KBLK + 8 * (kw.pos0 + r) + kw.g;   // token within the tile
+            const int tl = trow + 8 * r + kw.g;   // token within the tile
             if (tl < ntok) {
-                const int gr = tl / G;
                 const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(xs + (size_t)tl * xsd + kw.c0));
-                const float *f = sfz + (size_t)gr * 3 * d + kw.c0;
+                const float *f = fw + (size_t)((8 * r) / G) * 3 * d;
                 word |= qcode_rcp(x.x, f[0], f[d], f[2 * d], KBITS) << (r * KBITS);
                 word |= qcode_rcp(x.y, f[1], f[d + 1], f[2 * d + 1], KBITS) << (16 + r * KBITS);
             }
@@ -155,17 +160,21 @@ __global__ void __launch_bounds__(256) prefill_values_kernel(KiviGeom g, KiviDev
     for (int e = threadIdx.x; e < nvblk * vc_blk; e += blockDim.x) {
         const int vbl = e / vc_blk, wb = e - vbl * vc_blk;
         const VWord vw = vword_decode(wb, d, VBITS, cs);
+        // Slot r holds channel 8 (ci0 + r) + g (g < 8); 8 ci0 is a multiple
+        // of 32, and of G whenever G <= 32; for G >= 64 the word's channels
+        // lie in one group.  So slot r's group is 8 ci0 / G + (8 r) / G.
+        const int gi0 = 8 * vw.ci0 / G;
         uint32_t word = 0;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const int tl = vbl * KIVI_VBLK + vw.tt0 + half;
             if (tl >= ntok) continue;
+            const float *ft = sfz + (size_t)tl * 3 * ngi + gi0;
 #pragma unroll
             for (int r = 0; r < cph; ++r) {
                 const int c = 8 * (vw.ci0 + r) + vw.g;
-                const int gi = c / G;
                 const float x = __half2float(xs[(size_t)tl * xsd + c]);
-                const float *f = sfz + (size_t)tl * 3 * ngi + gi;
+                const float *f = ft + (8 * r) / G;
                 word |= qcode_rcp(x, f[0], f[ngi], f[2 * ngi], VBITS) << (16 * half + r * VBITS);
             }
         }
