@@ -19,6 +19,22 @@ __device__ __forceinline__ void flag(unsigned *status, unsigned f) { atomicOr(st
 // one channel across tokens fall in different banks.
 __host__ __device__ __forceinline__ int xs_stride(int d) { return d + 8; }
 
+// qcode_rcp for a bit width known at compile time, where rs is 0 whenever
+// sf is 0 (then (x - z) * rs = 0 gives code 0, as qcode does).  For a
+// group member the quotient lies in [0, 2 * 2^BITS) (below 2^BITS unless a
+// subnormal fp16 scale rounded down), so the single margin 1e-5 * 2^BITS
+// is at least the few ulps of |q| by which the product can miss the
+// quotient: the IEEE division still decides every code next to a tie.
+template <int BITS>
+__device__ __forceinline__ uint32_t qcode_rcp_t(float x, float sf, float zf, float rs) {
+    const float dlt = __fsub_rn(x, zf);
+    const float q = __fmul_rn(dlt, rs);
+    float k = rintf(q);
+    if (fabsf(q - k) > 0.5f - 1.0e-5f * (float)(1 << BITS)) k = rintf(__fdiv_rn(dlt, sf));
+    k = fminf(fmaxf(k, 0.0f), (float)((1 << BITS) - 1));
+    return (uint32_t)k;
+}
+
 // ---------------------------------------------------------------------------
 // Prefill keys: one CTA per (super block of TB = max(64, G) tokens, kv head,
 // sequence).  Quantizes tokens [0, nqk), nqk = t - t mod R.
@@ -89,8 +105,8 @@ __global__ void __launch_bounds__(256) prefill_keys_kernel(KiviGeom g, KiviDev d
             if (tl < ntok) {
                 const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(xs + (size_t)tl * xsd + kw.c0));
                 const float *f = fw + (size_t)((8 * r) / G) * 3 * d;
-                word |= qcode_rcp(x.x, f[0], f[d], f[2 * d], KBITS) << (r * KBITS);
-                word |= qcode_rcp(x.y, f[1], f[d + 1], f[2 * d + 1], KBITS) << (16 + r * KBITS);
+                word |= qcode_rcp_t<KBITS>(x.x, f[0], f[d], f[2 * d]) << (r * KBITS);
+                word |= qcode_rcp_t<KBITS>(x.y, f[1], f[d + 1], f[2 * d + 1]) << (16 + r * KBITS);
             }
         }
         kc_words(g, dv.blk, i, j, tok0 / KIVI_KBLK + kbl)[wb] = word;
@@ -175,7 +191,7 @@ __global__ void __launch_bounds__(256) prefill_values_kernel(KiviGeom g, KiviDev
                 const int c = 8 * (vw.ci0 + r) + vw.g;
                 const float x = __half2float(xs[(size_t)tl * xsd + c]);
                 const float *f = ft + (8 * r) / G;
-                word |= qcode_rcp(x, f[0], f[ngi], f[2 * ngi], VBITS) << (16 * half + r * VBITS);
+                word |= qcode_rcp_t<VBITS>(x, f[0], f[ngi], f[2 * ngi]) << (16 * half + r * VBITS);
             }
         }
         vc_words(g, dv.blk, i, j, tok0 / KIVI_VBLK + vbl)[wb] = word;
