@@ -66,21 +66,28 @@ __global__ void __launch_bounds__(256) prefill_keys_kernel(KiviGeom g, KiviDev d
     }
     __syncthreads();
 
-    // scale and zero per (group, channel)
-    for (int e = threadIdx.x; e < ngr * d; e += blockDim.x) {
-        const int gr = e / d, c = e - gr * d;
-        float mn = __half2float(xs[(size_t)gr * G * xsd + c]), mx = mn;
+    // scale and zero per (group, channel): the min / max of fp16 values is
+    // exact in fp16, taken two channels at a time
+    const int dp = d / 2;
+    for (int e = threadIdx.x; e < ngr * dp; e += blockDim.x) {
+        const int gr = e / dp, c = 2 * (e - gr * dp);
+        const __half2 *col = reinterpret_cast<const __half2 *>(xs + (size_t)gr * G * xsd + c);
+        __half2 mn = col[0], mx = mn;
 #pragma unroll 8
         for (int k = 1; k < G; ++k) {
-            const float x = __half2float(xs[((size_t)gr * G + k) * xsd + c]);
-            mn = fminf(mn, x);
-            mx = fmaxf(mx, x);
+            const __half2 x = col[(size_t)k * (xsd / 2)];
+            mn = __hmin2(mn, x);
+            mx = __hmax2(mx, x);
         }
-        const QParams p = qparams(mn, mx, KBITS);
-        ksz_store(g, dv.blk, i, j, tok0 / G + gr, c, p.s16, p.z16);
-        sfz[(gr * 3 + 0) * d + c] = p.sf;
-        sfz[(gr * 3 + 1) * d + c] = p.zf;
-        sfz[(gr * 3 + 2) * d + c] = p.sf == 0.0f ? 0.0f : __frcp_rn(p.sf);
+        const float2 mnf = __half22float2(mn), mxf = __half22float2(mx);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const QParams p = qparams(h ? mnf.y : mnf.x, h ? mxf.y : mxf.x, KBITS);
+            ksz_store(g, dv.blk, i, j, tok0 / G + gr, c + h, p.s16, p.z16);
+            sfz[(gr * 3 + 0) * d + c + h] = p.sf;
+            sfz[(gr * 3 + 1) * d + c + h] = p.zf;
+            sfz[(gr * 3 + 2) * d + c + h] = p.sf == 0.0f ? 0.0f : __frcp_rn(p.sf);
+        }
     }
     __syncthreads();
 
@@ -146,17 +153,21 @@ __global__ void __launch_bounds__(256) prefill_values_kernel(KiviGeom g, KiviDev
         const int tau = tok0 + tl;
         __half s16 = __float2half_rn(0.f), z16 = s16;
         if (tl < ntok) {
-            // the scan starts at a token-dependent offset: the warp's threads
+            // fp16 min / max (exact), two channels at a time; the scan
+            // starts at a token-dependent offset so that the warp's threads
             // read different banks
-            const __half *x = xs + (size_t)tl * xsd + gi * G;
-            const int rot = (2 * tl) & (G - 1);
-            float mn = __half2float(x[rot]), mx = mn;
+            const __half2 *x = reinterpret_cast<const __half2 *>(xs + (size_t)tl * xsd + gi * G);
+            constexpr int GP = G / 2;
+            const int rot = tl & (GP - 1);
+            __half2 mn2 = x[rot], mx2 = mn2;
 #pragma unroll 8
-            for (int k = 1; k < G; ++k) {
-                const float v = __half2float(x[(k + rot) & (G - 1)]);
-                mn = fminf(mn, v);
-                mx = fmaxf(mx, v);
+            for (int k = 1; k < GP; ++k) {
+                const __half2 v = x[(k + rot) & (GP - 1)];
+                mn2 = __hmin2(mn2, v);
+                mx2 = __hmax2(mx2, v);
             }
+            const float mn = fminf(__low2float(mn2), __high2float(mn2));
+            const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
             const QParams p = qparams(mn, mx, VBITS);
             s16 = p.s16;
             z16 = p.z16;
