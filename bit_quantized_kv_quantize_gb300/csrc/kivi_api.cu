@@ -87,6 +87,40 @@ kivi_status check_handle(kivi_cache_t c) {
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+// The cache shapes the library supports (kivi_cache_create's rules).
+kivi_status check_shape(int b, int h_kv, int d, int k_bits, int v_bits, int G, int R, int max_tokens) {
+    if (b < 1 || h_kv < 1 || d < 1 || G < 1 || R < 1 || max_tokens < 1) {
+        set_err("sizes must be positive");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (b > KIVI_MAX_BATCH) {
+        set_err("b above %s%ld", "", KIVI_MAX_BATCH);
+        return KIVI_ERR_UNSUPPORTED;
+    }
+    if ((k_bits != 2 && k_bits != 4) || (v_bits != 2 && v_bits != 4)) {
+        set_err("bits must be 2 or 4");
+        return KIVI_ERR_UNSUPPORTED;
+    }
+    if (G != 16 && G != 32 && G != 64 && G != 128) {
+        set_err("G must be 16, 32, 64 or 128");
+        return KIVI_ERR_UNSUPPORTED;
+    }
+    if (d != 64 && d != 128 && d != 256) {
+        set_err("d must be 64, 128 or 256");
+        return KIVI_ERR_UNSUPPORTED;
+    }
+    if (d % G != 0 || R % G != 0 || R > 4096) {
+        set_err("need d %% G == 0, R %% G == 0 and R <= 4096");
+        return KIVI_ERR_UNSUPPORTED;
+    }
+    const int q = G > KIVI_KBLK ? G : KIVI_KBLK;
+    if ((long)max_tokens + q > (1L << 30)) {
+        set_err("max_tokens too large");
+        return KIVI_ERR_UNSUPPORTED;
+    }
+    return KIVI_OK;
+}
+
 void free_dev(kivi_cache *c) {
     KiviDev &d = c->dv;
     void *ps[] = {d.blk, d.Kf, d.Vf, c->cnt, d.status, d.part, d.merge_ticket, d.ml};
@@ -230,35 +264,8 @@ kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, in
         return KIVI_ERR_INVALID_ARG;
     }
     *out = nullptr;
-    if (b < 1 || h_kv < 1 || d < 1 || G < 1 || R < 1 || max_tokens < 1) {
-        set_err("sizes must be positive");
-        return KIVI_ERR_INVALID_ARG;
-    }
-    if (b > KIVI_MAX_BATCH) {
-        set_err("b above %s%ld", "", KIVI_MAX_BATCH);
-        return KIVI_ERR_UNSUPPORTED;
-    }
-    if ((k_bits != 2 && k_bits != 4) || (v_bits != 2 && v_bits != 4)) {
-        set_err("bits must be 2 or 4");
-        return KIVI_ERR_UNSUPPORTED;
-    }
-    if (G != 16 && G != 32 && G != 64 && G != 128) {
-        set_err("G must be 16, 32, 64 or 128");
-        return KIVI_ERR_UNSUPPORTED;
-    }
-    if (d != 64 && d != 128 && d != 256) {
-        set_err("d must be 64, 128 or 256");
-        return KIVI_ERR_UNSUPPORTED;
-    }
-    if (d % G != 0 || R % G != 0 || R > 4096) {
-        set_err("need d %% G == 0, R %% G == 0 and R <= 4096");
-        return KIVI_ERR_UNSUPPORTED;
-    }
-    const int q = G > KIVI_KBLK ? G : KIVI_KBLK;
-    if ((long)max_tokens + q > (1L << 30)) {
-        set_err("max_tokens too large");
-        return KIVI_ERR_UNSUPPORTED;
-    }
+    kivi_status sc = check_shape(b, h_kv, d, k_bits, v_bits, G, R, max_tokens);
+    if (sc != KIVI_OK) return sc;
     kivi_cache *c = new (std::nothrow) kivi_cache();
     if (!c) {
         set_err("host allocation failed");
@@ -596,6 +603,50 @@ kivi_status kivi_profile_read(kivi_cache_t c, double *total_ms, int *launches) {
     if (total_ms) *total_ms = tot;
     if (launches) *launches = c->nprof;
     c->nprof = 0;
+    return KIVI_OK;
+}
+
+kivi_status kivi_plan_preview(int b, int h_kv, int d, int k_bits, int v_bits, int G, int R, int max_tokens,
+                              int h_q, const int32_t *T, const int32_t *Tqk, const int32_t *Tqv, int num_sms,
+                              int64_t out[6]) {
+    g_err[0] = 0;
+    kivi_status s = check_shape(b, h_kv, d, k_bits, v_bits, G, R, max_tokens);
+    if (s != KIVI_OK) return s;
+    if (!T || !Tqk || !Tqv || !out) {
+        set_err("a pointer argument is null");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (h_q < 1 || h_q % h_kv != 0 || num_sms < 1) {
+        set_err("need h_q a positive multiple of h_kv and num_sms >= 1");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (h_q / h_kv > KIVI_MAX_QPERKV) {
+        set_err("h_q / h_kv above 8");
+        return KIVI_ERR_UNSUPPORTED;
+    }
+    for (int i = 0; i < b; ++i)
+        if (T[i] < 0 || T[i] > max_tokens || Tqk[i] < 0 || Tqk[i] > T[i] || Tqv[i] < 0 || Tqv[i] > T[i]) {
+            set_err("need 0 <= Tqk, Tqv <= T <= max_tokens (i = %s%ld)", "", i);
+            return KIVI_ERR_INVALID_ARG;
+        }
+    KiviGeom g;
+    g.b = b;
+    g.h = h_kv;
+    g.d = d;
+    g.kbits = k_bits;
+    g.vbits = v_bits;
+    g.G = G;
+    g.R = R;
+    kivi_geom_init(g, max_tokens);
+    g.smax = kivi_partial_slots(b, h_kv, num_sms);
+    DecodeUnits units;
+    const DecodePlan plan = kivi_plan_decode(g, h_q, T, Tqk, Tqv, num_sms, &units);
+    out[0] = plan.ctas;
+    out[1] = plan.warps;
+    out[2] = plan.stages;
+    out[3] = plan.max_parts;
+    out[4] = g.smax;
+    out[5] = units.total;
     return KIVI_OK;
 }
 

@@ -23,7 +23,7 @@ EXPORTS = ["kivi_cache_create", "kivi_cache_destroy", "kivi_prefill", "kivi_appe
            "kivi_cache_export", "kivi_cache_check", "kivi_profile_enable", "kivi_profile_read",
            "kivi_decode_plan", "kivi_status_str", "kivi_last_error", "kivi_abi_version",
            "kivi_decode_attn_noalloc", "kivi_cache_export_records", "kivi_append_decode",
-           "kivi_decode_attn_probs"]
+           "kivi_decode_attn_probs", "kivi_plan_preview"]
 
 
 class KiviError(RuntimeError):
@@ -48,6 +48,7 @@ def _load():
     L.kivi_append.argtypes = [vp, vp, vp, vp]
     L.kivi_decode_attn.argtypes = [vp, vp, i32, vp, vp]
     L.kivi_decode_attn_probs.argtypes = [vp, vp, i32, vp, vp, vp, ctypes.c_int64, vp]
+    L.kivi_plan_preview.argtypes = [i32] * 9 + [vp, vp, vp, i32, vp]
     L.kivi_cache_lengths.argtypes = [vp, vp, vp, vp]
     L.kivi_cache_export_sizes.argtypes = [vp, ctypes.POINTER(ctypes.c_size_t)]
     L.kivi_cache_export.argtypes = [vp] * 8

@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define KIVI_ABI_VERSION 4
+#define KIVI_ABI_VERSION 5
 
 typedef struct kivi_cache *kivi_cache_t;   /* opaque, library-owned */
 typedef struct CUstream_st *kivi_stream_t; /* the same type as cudaStream_t */
@@ -226,6 +226,20 @@ typedef struct {
  * routine is called. */
 kivi_status kivi_decode_attn_noalloc(const kivi_packed_cache *cache, const void *q, int h_q,
                                      void *out, kivi_stream_t stream);
+
+/* The launch plan kivi_decode_attn would use for a cache of this shape
+ * (kivi_cache_create's rules; max_tokens sets the capacity) holding these
+ * per-sequence counters (HOST arrays of b int32, 0 <= Tqk, Tqv <= T <=
+ * max_tokens) for h_q query heads, on a GPU with num_sms SMs.  Host-only:
+ * no CUDA call is made, so it runs without a GPU.  out (HOST, 6 int64):
+ * persistent CTAs, warps per CTA, ring stages per warp, the most split
+ * partials any (sequence, kv head, group of up to 4 query heads) receives,
+ * the partial slots a cache of this shape holds for each, and the total
+ * work units (a fully quantized 64-token block is one unit, any other
+ * block a fixed larger weight).  The kernel requires partials <= slots. */
+kivi_status kivi_plan_preview(int b, int h_kv, int d, int k_bits, int v_bits, int G, int R, int max_tokens,
+                              int h_q, const int32_t *T, const int32_t *Tqk, const int32_t *Tqv, int num_sms,
+                              int64_t out[6]);
 
 const char *kivi_status_str(kivi_status s);
 /* Text of the last error on the calling thread ("" if none). */
