@@ -98,7 +98,10 @@ kivi_status kivi_append(kivi_cache_t c, const void *k, const void *v, kivi_strea
  * A sequence with no tokens gets an all-zero output.  Read-only on the
  * cache (the call can be repeated, with bitwise identical results).  Preconditions: inputs finite and
  * |q_c| * s < 65504 for every key scale s (the scaled query is staged in
- * fp16 for the tensor-core contraction). */
+ * fp16 for the tensor-core contraction).  The kernel is launched as a
+ * programmatic dependent of the previous kernel on the stream: its blocks
+ * may be placed and set up while that kernel finishes, but nothing in
+ * global memory is read before it has completed, so stream order holds. */
 kivi_status kivi_decode_attn(kivi_cache_t c, const void *q, int h_q, void *out,
                              kivi_stream_t stream);
 
