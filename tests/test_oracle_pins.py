@@ -561,6 +561,37 @@ def test_layout_single_code_placement(row):
     assert int(words[word]) == 3 << bit
 
 
+def _read_layout_golden_d128():
+    rows = []
+    with open(os.path.join(GOLDEN, "layout_placements_d128.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                a, bits, ch, tok, word, bit = line.split()
+                rows.append((a, int(bits), int(ch), int(tok), int(word), int(bit)))
+    return rows
+
+
+@pytest.mark.parametrize("row", _read_layout_golden_d128())
+def test_layout_single_code_placement_d128(row):
+    """d = 128 (value words four to a lane group, cs = 4) at 2 and 4 bits: a
+    single entry 1.0 in an all-zero cache is the top code 2^B - 1 of its
+    group {0, 1}; the export holds exactly that field at the hand-derived
+    word and bit."""
+    arr, bits, ch, tok, word, bit = row
+    d, G, R, t = 128, 32, 32, 256
+    K = np.zeros((1, 1, t, d), np.float16)
+    V = np.zeros((1, 1, t, d), np.float16)
+    (K if arr == "K" else V)[0, 0, tok, ch] = 1.0
+    c = oracle.Cache(1, 1, d, bits, bits, G, R, t)
+    c.prefill(K, V, [t])
+    ex = c.export()
+    words = ex["Kc"] if arr == "K" else ex["Vc"]
+    nz = np.nonzero(words)[0]
+    assert nz.tolist() == [word]
+    assert int(words[word]) == ((1 << bits) - 1) << bit
+
+
 @pytest.mark.parametrize("kb,vb,d", [(2, 2, 64), (4, 4, 128), (2, 4, 128), (4, 2, 256)])
 def test_layout_is_a_packing(kb, vb, d):
     """All-maximal codes fill every bit of every full word exactly once (the
@@ -646,3 +677,37 @@ def test_workload_slices_are_reproducible():
     w4 = W.WORKLOADS["kivi4_serving"]
     L = w4.lengths()
     assert L.min() >= 1024 and L.max() <= 4096 and L.shape == (64,)
+
+
+def test_threaded_decode_equals_serial():
+    """The GPU tests run the oracle's decode with one (sequence, query head)
+    row per host thread; each row is computed exactly as in the serial loop,
+    so outputs and weights must agree bit for bit with one thread, for all
+    rows and for a listed subset."""
+    rng = np.random.default_rng(11)
+    b, h, hq, d, G, R = 3, 2, 8, 64, 16, 32
+    lens = np.array([0, 77, 150], np.int32)
+    K = (rng.standard_normal((b, h, 150, d)) * 2).astype(np.float16)
+    V = rng.standard_normal((b, h, 150, d)).astype(np.float16)
+    c = oracle.Cache(b, h, d, 4, 2, G, R, 200)
+    c.prefill(K, V, lens)
+    for s in range(5):
+        c.append(rng.standard_normal((b, h, d)).astype(np.float16),
+                 rng.standard_normal((b, h, d)).astype(np.float16))
+    q = rng.standard_normal((b, hq, d)).astype(np.float16)
+    pairs = [(2, 7), (1, 0), (2, 3), (0, 5)]
+    try:
+        assert oracle.set_threads(1) == 1
+        o1, p1 = c.decode_probs(q)
+        s1 = c.decode(q, pairs=pairs)
+        nt = oracle.set_threads(max(4, os.cpu_count() or 1))
+        on, pn = c.decode_probs(q)
+        sn = c.decode(q, pairs=pairs)
+    finally:
+        oracle.set_threads(os.cpu_count() or 1)
+    if nt == 1:
+        pytest.skip("the oracle was built without OpenMP")
+    assert np.array_equal(o1.view(np.uint32), on.view(np.uint32))
+    assert np.array_equal(p1.view(np.uint32), pn.view(np.uint32))
+    assert np.array_equal(s1.view(np.uint32), sn.view(np.uint32))
+    assert np.all(np.isfinite(o1)) and np.count_nonzero(o1) == o1.size
