@@ -96,8 +96,8 @@ def test_tiny_kivi2_every_step():
 
 
 # ---------------------------------------------------------------------------
-# The fused step (kivi_append_decode): the append's maintenance runs inside
-# the attention kernel.
+# The one-call step (kivi_append_decode): the append kernel, then the
+# decode kernel launched as its programmatic dependent.
 # ---------------------------------------------------------------------------
 
 def test_fused_step_tiny_every_step():
@@ -322,7 +322,13 @@ def test_errors_leave_state_unchanged():
 # Full-size workloads, sampled: the launch configuration the benchmark times.
 # ---------------------------------------------------------------------------
 
-def _full_size_sampled(name, samples):
+def _full_size(name):
+    """The workload at full size, as the benchmark runs it: prefill, one
+    append, one decode.  Every (sequence, kv head) slice of the cache is
+    compared bit-exact with an oracle of that slice, and the whole output
+    (every sequence and query head) with the oracle's, within the tolerance
+    over the whole output."""
+    from concurrent.futures import ThreadPoolExecutor
     w = W.WORKLOADS[name]
     cap = w.capacity()
     gpu = K.KiviCache(w.b, w.h_kv, w.d, w.kbits, w.vbits, w.G, w.R, cap)
@@ -336,33 +342,40 @@ def _full_size_sampled(name, samples):
     gex = gpu.export()
     assert gpu.check() == 0
     gg = U.geometry(w.b, w.h_kv, w.d, w.kbits, w.vbits, w.G, w.R, cap)
+    og = U.geometry(1, 1, w.d, w.kbits, w.vbits, w.G, w.R, cap)
     T, Tqk, Tqv = gpu.lengths()
     hg = w.group
-    for (i, j) in samples:
+    ref = np.zeros_like(out)
+
+    def one(ij):
+        i, j = ij
         n = int(lens[i])
         ora = oracle.Cache(1, 1, w.d, w.kbits, w.vbits, w.G, w.R, cap)
         ora.prefill(W.prefill_slice(w, "K", i, j, n)[None, None], W.prefill_slice(w, "V", i, j, n)[None, None],
                     [n])
-        ora.append(k[i:i + 1, j:j + 1], v[i:i + 1, j:j + 1])
-        og = U.geometry(1, 1, w.d, w.kbits, w.vbits, w.G, w.R, cap)
+        ora.append(np.ascontiguousarray(k[i:i + 1, j:j + 1]), np.ascontiguousarray(v[i:i + 1, j:j + 1]))
         U.compare_slice(gex, gg, i, j, ora.export(), og, 0, 0, int(T[i]), int(Tqk[i]), int(Tqv[i]),
                         what=f"{name} seq {i} head {j}")
-        qs = q[i:i + 1, j * hg:(j + 1) * hg]
-        ref = ora.decode(np.ascontiguousarray(qs))
-        U.compare_output(out[i, j * hg:(j + 1) * hg], ref[0], what=f"{name} seq {i} head {j}")
+        ref[i, j * hg:(j + 1) * hg] = ora.decode(np.ascontiguousarray(q[i:i + 1, j * hg:(j + 1) * hg]))[0]
+        ora.close()
+
+    slices = [(i, j) for i in range(w.b) for j in range(w.h_kv)]
+    with ThreadPoolExecutor(max(1, min(len(slices), (os.cpu_count() or 1) // 2))) as ex:
+        list(ex.map(one, slices))
+    U.compare_output(out, ref, what=f"{name} whole output")
     gpu.close()
 
 
 def test_full_llama2_7b_4k():
-    _full_size_sampled("llama2_7b_4k", [(0, 0), (0, 13), (0, 31)])
+    _full_size("llama2_7b_4k")
 
 
 def test_full_llama3_8b_gqa_32k():
-    _full_size_sampled("llama3_8b_gqa_32k", [(0, 0), (3, 5), (7, 7)])
+    _full_size("llama3_8b_gqa_32k")
 
 
 def test_full_long_128k():
-    _full_size_sampled("long_128k", [(0, 2), (0, 7)])
+    _full_size("long_128k")
 
 
 def test_kivi4_serving_ragged_256_steps():

@@ -26,11 +26,19 @@ class PackedCache(ctypes.Structure):
                [(n, ctypes.c_void_p) for n in ("blocks", "Kf", "Vf", "T", "Tqk", "Tqv")]
 
 
-@pytest.mark.parametrize("name,b,prefill,steps", [("llama3_8b_gqa_32k", 2, 3000, 3),
-                                                  ("kivi4_serving", 6, 0, 2)])
-def test_noalloc_matches_decode_attn(name, b, prefill, steps):
+CASES = [
+    # workload, b, prefill (0: ragged 300-900), steps, field overrides
+    ("llama3_8b_gqa_32k", 2, 3000, 3, {}),
+    ("kivi4_serving", 6, 0, 2, {}),
+    ("tiny_kivi2", 3, 0, 5, dict(h_q=8, h_kv=2, kbits=4, vbits=2, G=16, R=32)),
+]
+
+
+@pytest.mark.parametrize("name,b,prefill,steps,over", CASES, ids=[c[0] for c in CASES])
+def test_noalloc_matches_decode_attn(name, b, prefill, steps, over):
     from bit_quantized_kv_quantize_gb300 import kivi as K
-    w = W.small(W.WORKLOADS[name], b=b, prefill=prefill or 900, ragged=(300, 900) if prefill == 0 else ())
+    w = W.small(W.WORKLOADS[name], b=b, prefill=prefill or 900, ragged=(300, 900) if prefill == 0 else (),
+                **over)
     cap = int(w.lengths().max()) + steps + 4
     cache = K.KiviCache(w.b, w.h_kv, w.d, w.kbits, w.vbits, w.G, w.R, cap)
     Kh, Vh, lens = W.prefill_kv(w)
@@ -58,9 +66,16 @@ def test_noalloc_matches_decode_attn(name, b, prefill, steps):
         q = torch.from_numpy(W.step_q(w, 10 + call)).cuda()
         ref = cache.decode(q).float().cpu().numpy()
         out = torch.full_like(q, float("nan"))
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
         rc = fn(ctypes.byref(pc), q.data_ptr(), w.h_q, out.data_ptr(), stream.cuda_stream)
         assert rc == 0, K.lib.kivi_last_error().decode()
         torch.cuda.synchronize()
+        free1 = torch.cuda.mem_get_info()[0]
+        # the first call of a shape may load the array and the kernel's code
+        # (lazy module loading); a later call takes no device memory
+        if call == 1:
+            assert free1 == free0, f"second no-alloc call took {free0 - free1} bytes of device memory"
         U.compare_output(out.float().cpu().numpy(), ref, f"{name} no-alloc call {call}")
     cache.close()
 
