@@ -175,7 +175,10 @@ class KiviCache:
         return out
 
     def append_decode(self, k, v, q, out=None, stream=None):
-        """append(k, v) then decode(q) in one launch; returns out."""
+        """append(k, v) then decode(q) in one call; returns out.
+
+        Two launches on the stream: the append kernel, then the decode
+        kernel as its programmatic dependent."""
         import torch
         hq = q.shape[1]
         kp = _dev_fp16(k, (self.b, self.h_kv, self.d), "k")

@@ -27,7 +27,7 @@
  * Arithmetic: fp32 with IEEE division, rintf (round half to even), no FMA
  * contraction (build with -ffp-contract=off, never -ffast-math).
  *
- * Readings where the pages are silent (each listed in the design notes):
+ * Readings where the pages are silent:
  *   - "round" is round-half-to-even (rintf).
  *   - the scale is stored as fp16 (round-to-nearest-even of the fp32
  *     scale); the zero is min(X), which is exact in fp16.  Codes are
