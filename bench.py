@@ -12,8 +12,8 @@ context (batch 8, 32 query / 8 kv heads, d 128, 2-bit K/V, G 32, R 128).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--no-cpu-baseline]
 
---impl reference times the CPU oracle (plain C, fp32) on the host cores on
-a bounded sample of the same workload.  Under torchrun (N > 1) every rank
+--impl reference times the CPU oracle (plain C, fp32) on the host cores over
+the same workload (--warmup untimed and --steps timed steps).  Under torchrun (N > 1) every rank
 runs an independent replica of the workload on its own GPU (the path has no
 exchange step); rank 0 prints the max over ranks.
 """
@@ -41,8 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) of one decode-attention launch, from an ncu
 # capture of the kernel whose source hash is recorded beside it; reported
-# only while the kernel source is unchanged.  (llama3_8b_gqa_32k, the
-# default workload: profiles/decode_kernel_llama3_8b_gqa_32k.md.)
+# only while the kernel source is unchanged (llama3_8b_gqa_32k, the
+# default workload).
 NCU_TRAFFIC = {"4e7c25cb0e81b994": 205740032 + 2805504}
 
 
@@ -168,22 +168,33 @@ def barrier(dist, device=None):
 # CPU oracle timing (the reference arm and the cpu_baseline object)
 # ---------------------------------------------------------------------------
 
-def oracle_time(w: W.Workload, budget_s: float = 15.0, max_pairs: int = 8):
-    """Time the oracle's decode step (append + attention) on a sample of the
-    workload: the first b' sequences x h' kv heads (b' h' <= max_pairs) with
-    all their query heads, in one oracle cache whose attention rows spread
-    over the host cores.  Returns (us per full step, cores, sample text),
-    scaled to all b x h_kv (sequence, kv head) pairs by token count."""
+def cpu_model() -> str:
+    """The host CPU's model name (or the architecture when none is listed)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                key = ln.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
+
+
+def _oracle_sample(w: W.Workload, bs: int, hs: int, cap: int):
+    """An oracle cache of the first bs sequences x hs kv heads of the
+    workload, and (K, V, lengths) to prefill it with."""
     import oracle
-    cores = os.cpu_count() or 1
-    oracle.set_threads(cores)
-    lens = w.lengths()
-    bs = min(w.b, max_pairs)
-    hs = min(w.h_kv, max(1, max_pairs // bs))
-    max_steps = 400
-    cap = int(lens.max()) + max_steps + 8
-    c = oracle.Cache(bs, hs, w.d, w.kbits, w.vbits, w.G, w.R, cap)
-    ts = int(lens[:bs].max())
+    lens = w.lengths()[:bs]
+    ts = int(max(1, lens.max()))
     Kh = np.zeros((bs, hs, ts, w.d), np.float16)
     Vh = np.zeros_like(Kh)
     for i in range(bs):
@@ -191,35 +202,87 @@ def oracle_time(w: W.Workload, budget_s: float = 15.0, max_pairs: int = 8):
             n = int(lens[i])
             Kh[i, j, :n] = W.prefill_slice(w, "K", i, j, n)
             Vh[i, j, :n] = W.prefill_slice(w, "V", i, j, n)
-    c.prefill(Kh, Vh, lens[:bs])
+    return oracle.Cache(bs, hs, w.d, w.kbits, w.vbits, w.G, w.R, cap), Kh, Vh, lens
+
+
+def _oracle_step(c, w, s, bs, hs):
+    k, v = W.step_kv(w, s)
+    q = W.step_q(w, s)
+    k = np.ascontiguousarray(k[:bs, :hs])
+    v = np.ascontiguousarray(v[:bs, :hs])
+    q = np.ascontiguousarray(q[:bs, :hs * w.group])
+    t0 = time.perf_counter()
+    c.append(k, v)
+    c.decode(q)
+    return time.perf_counter() - t0
+
+
+def oracle_time(w: W.Workload, budget_s: float = 15.0, max_pairs: int = 8):
+    """The oracle (as it stands) on a bounded sample of the workload: the
+    first b' sequences x h' kv heads (b' h' <= max_pairs) with all their
+    query heads, timed per decode step (append + attention) on all host
+    threads and on one, and its prefill (quantize + pack) once; each scaled
+    to all b x h_kv (sequence, kv head) pairs by token count.  Returns the
+    cpu_baseline fields."""
+    import oracle
+    cores = os.cpu_count() or 1
+    lens = w.lengths()
+    bs = min(w.b, max_pairs)
+    hs = min(w.h_kv, max(1, max_pairs // bs))
+    max_steps = 400
+    c, Kh, Vh, lp = _oracle_sample(w, bs, hs, int(lens.max()) + max_steps + 8)
+    t0 = time.perf_counter()
+    c.prefill(Kh, Vh, lp)
+    prefill_s = time.perf_counter() - t0
     del Kh, Vh
-    hg = w.group
+    scale = float(lens.sum() * w.h_kv) / float(max(1, lp.sum()) * hs)
+    oracle.set_threads(cores)
     steps, elapsed = 0, 0.0
     while steps < max_steps and elapsed < budget_s:
-        k, v = W.step_kv(w, steps)
-        q = W.step_q(w, steps)
-        k = np.ascontiguousarray(k[:bs, :hs])
-        v = np.ascontiguousarray(v[:bs, :hs])
-        q = np.ascontiguousarray(q[:bs, :hs * hg])
-        t0 = time.perf_counter()
-        c.append(k, v)
-        c.decode(q)
-        elapsed += time.perf_counter() - t0
+        elapsed += _oracle_step(c, w, steps, bs, hs)
         steps += 1
-    scale = float(lens.sum() * w.h_kv) / float(lens[:bs].sum() * hs)
+    oracle.set_threads(1)
+    steps1, elapsed1 = 0, 0.0
+    while steps1 < max_steps and elapsed1 < budget_s / 3:
+        elapsed1 += _oracle_step(c, w, steps + steps1, bs, hs)
+        steps1 += 1
+    oracle.set_threads(cores)
+    c.close()
     us = elapsed / steps * scale * 1e6
     sample = (f"{bs} sequence(s) x {hs} kv head(s) of {w.b} x {w.h_kv}, {steps} step(s) of "
-              f"append + attention over {hg} query heads per kv head, scaled by token count "
-              f"to the whole batch; {elapsed:.1f} s of oracle time on {cores} threads")
-    return us, cores, sample
+              f"append + attention over {w.group} query heads per kv head on {cores} threads "
+              f"({elapsed:.1f} s) and {steps1} on one ({elapsed1:.1f} s), prefill once; "
+              f"scaled by token count to the whole batch")
+    return {"value": round(us, 3), "unit": "us/step", "cores": cores, "kind": "oracle",
+            "sample": sample, "cpu_model": cpu_model(),
+            "single_thread_us_per_step": round(elapsed1 / max(1, steps1) * scale * 1e6, 3),
+            "prefill_us": round(prefill_s * scale * 1e6, 1)}
 
 
 def run_reference(args, w):
-    rank, ws, dist = 0, int(os.environ.get("WORLD_SIZE", "1")), None
-    if ws > 1 and int(os.environ.get("RANK", "0")) != 0:
+    """The reference arm: the oracle, as it stands, on the host cores, over
+    the whole workload (every sequence and kv head): prefill once, --warmup
+    untimed steps, then --steps timed steps of append + attention."""
+    import oracle
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1 and int(os.environ.get("RANK", "0")) != 0:
         return 0
     t0 = time.time()
-    us, cores, sample = oracle_time(w, budget_s=float(os.environ.get("KIVI_ORACLE_BUDGET_S", "20")))
+    cores = os.cpu_count() or 1
+    lens = w.lengths()
+    n = args.warmup + args.steps
+    c, Kh, Vh, lp = _oracle_sample(w, w.b, w.h_kv, int(lens.max()) + n + 8)
+    tp = time.perf_counter()
+    c.prefill(Kh, Vh, lp)
+    prefill_s = time.perf_counter() - tp
+    del Kh, Vh
+    oracle.set_threads(cores)
+    for s in range(args.warmup):
+        _oracle_step(c, w, s, w.b, w.h_kv)
+    times = [_oracle_step(c, w, args.warmup + s, w.b, w.h_kv) for s in range(args.steps)]
+    c.close()
+    us = sum(times) / len(times) * 1e6
+    sample = (f"the whole workload ({w.b} x {w.h_kv} (sequence, kv head) pairs), {args.steps} timed "
+              f"step(s) of append + attention after {args.warmup} untimed, on {cores} threads")
     line = {
         "metric": METRIC, "value": round(us, 3), "unit": "us/step", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 6),
@@ -227,7 +290,8 @@ def run_reference(args, w):
         "data": "synthetic", "impl": "reference",
         "config": workload_config(w),
         "cpu_baseline": {"value": round(us, 3), "unit": "us/step", "cores": cores,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "cpu_model": cpu_model(),
+                         "prefill_us": round(prefill_s * 1e6, 1)},
         "e2e": {"value": round(us, 3), "unit": "us/step", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "wall_s": round(time.time() - t0, 1),
@@ -421,9 +485,7 @@ def run_ours(args, w):
         "source_hash": source_hash(),
     }
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
-        us, cores, sample = oracle_time(w, budget_s=float(os.environ.get("KIVI_ORACLE_BUDGET_S", "15")))
-        line["cpu_baseline"] = {"value": round(us, 3), "unit": "us/step", "cores": cores,
-                                "kind": "oracle", "sample": sample}
+        line["cpu_baseline"] = oracle_time(w, budget_s=float(os.environ.get("KIVI_ORACLE_BUDGET_S", "15")))
     line["wall_s"] = round(time.time() - t_start, 1)
     cache.close()
     if rank == 0:
