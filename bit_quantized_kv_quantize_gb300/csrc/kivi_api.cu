@@ -87,8 +87,11 @@ kivi_status check_handle(kivi_cache_t c) {
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-// The cache shapes the library supports (kivi_cache_create's rules).
-kivi_status check_shape(int b, int h_kv, int d, int k_bits, int v_bits, int G, int R, int max_tokens) {
+}  // namespace
+
+// The cache shapes the library supports (kivi_cache_create's rules); also
+// used by the allocation-free decode (kivi_noalloc.cu).
+int kivi_check_shape(int b, int h_kv, int d, int k_bits, int v_bits, int G, int R, int max_tokens) {
     if (b < 1 || h_kv < 1 || d < 1 || G < 1 || R < 1 || max_tokens < 1) {
         set_err("sizes must be positive");
         return KIVI_ERR_INVALID_ARG;
@@ -121,9 +124,15 @@ kivi_status check_shape(int b, int h_kv, int d, int k_bits, int v_bits, int G, i
     return KIVI_OK;
 }
 
+namespace {
+
+kivi_status check_shape(int b, int h_kv, int d, int k_bits, int v_bits, int G, int R, int max_tokens) {
+    return (kivi_status)kivi_check_shape(b, h_kv, d, k_bits, v_bits, G, R, max_tokens);
+}
+
 void free_dev(kivi_cache *c) {
     KiviDev &d = c->dv;
-    void *ps[] = {d.blk, d.Kf, d.Vf, c->cnt, d.status, d.part, d.merge_ticket, d.ml};
+    void *ps[] = {d.blk, d.Kf, d.Vf, c->cnt, d.status, d.part, d.ml};
     for (void *p : ps)
         if (p) cudaFree(p);
     memset(&d, 0, sizeof d);
@@ -304,7 +313,6 @@ kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, in
         {(void **)&c->cnt, (size_t)2 * 3 * b * 4},
         {(void **)&dv.status, 4},
         {(void **)&dv.part, bh * KIVI_MAX_QPERKV * g.smax * (d + 2) * 4},
-        {(void **)&dv.merge_ticket, bh * 4 * 4},
         {(void **)&dv.ml, bh * KIVI_MAX_QPERKV * 2 * 4},
     };
     for (auto &r : reqs) {

@@ -26,8 +26,9 @@
 // that also hold tokens of the fp16 windows add, for those tokens, MMAs over
 // fp16 rows copied into shared memory.  Each CTA merges its warps per pair
 // and writes (m, l, acc[d]) in base 2 (scores pre-multiplied by
-// log2(e) / sqrt(d)); the last CTA to finish a pair merges its partials with
-// log-sum-exp weights and writes the fp16 output.
+// log2(e) / sqrt(d)); merge_kernel (kivi_merge.cu), launched next on the
+// stream, merges each pair's partials with log-sum-exp weights and writes
+// the fp16 output.
 #pragma once
 #include "kivi_internal.cuh"
 
@@ -209,37 +210,81 @@ __device__ __forceinline__ uint32_t unpack(uint32_t w, int r) {
     default: return unpack_t<BITS, KEY, (BITS == 2 ? 7 : 3)>(w);
     }
 }
-// value fields: the exact code as fp16 (offset subtracted, exact)
-template <int BITS>
-__device__ __forceinline__ uint32_t unpack_exact(uint32_t w, int r) {
-    const View v = view_of<BITS, false>(r);
-    return h2u(__hsub2(u2h(unpack<BITS, false>(w, r)), u2h(v.magic)));
-}
 template <int BITS, bool KEY>
 __host__ __device__ constexpr float slot_offset(int r) { return view_of<BITS, KEY>(r).off; }
+
+// Value fields for the P.V contraction, centred: code - c0 with c0 =
+// (2^B - 1) / 2, exact in fp16.  The field is unpacked at a position whose
+// offset off is at most 64 (2-bit: the keys' positions 4, 6, 8; 4-bit:
+// position 4), so that off + c0 is itself an fp16 value and one HSUB2
+// leaves the exact centred code.  The value's midpoint z + c0 s goes into
+// the zero-point accumulator.  Centring keeps both accumulators near the
+// size of the output instead of near c0 s sum(p) (N(0, 1) values put the
+// group midpoints near 0), which is what bounds the fp32 accumulation error
+// at long contexts.
+__host__ __device__ constexpr View view_val(int bits, int r);
+// mantissa position p of a view (its magic constant's exponent field is 25 - p)
+__host__ __device__ constexpr int view_pos(int bits, int r) { return 25 - (int)((view_val(bits, r).magic >> 10) & 31u); }
+__host__ __device__ constexpr View view_val(int bits, int r) {
+    if (bits == 4) return r == 0 ? at_pos(4, 4, 4, 0) : (r == 1 ? at_pos(4, 4, 0, 0) : at_pos(4, 4, 0, 4 * r - 4));
+    return view_of<2, true>(r);
+}
+template <int BITS, int R>
+__device__ __forceinline__ uint32_t unpack_val_t(uint32_t w) {
+    constexpr View v = view_val(BITS, R);
+    const uint32_t x = v.shl ? (w << v.shl) : (v.shr ? (w >> v.shr) : w);
+    return and_or<v.mask, v.magic>(x);
+}
+template <int BITS>
+__device__ __forceinline__ uint32_t unpack_val_raw(uint32_t w, int r) {
+    switch (r) {
+    case 0: return unpack_val_t<BITS, 0>(w);
+    case 1: return unpack_val_t<BITS, 1>(w);
+    case 2: return unpack_val_t<BITS, 2>(w);
+    case 3: return unpack_val_t<BITS, 3>(w);
+    case 4: return unpack_val_t<BITS, (BITS == 2 ? 4 : 3)>(w);
+    case 5: return unpack_val_t<BITS, (BITS == 2 ? 5 : 3)>(w);
+    case 6: return unpack_val_t<BITS, (BITS == 2 ? 6 : 3)>(w);
+    default: return unpack_val_t<BITS, (BITS == 2 ? 7 : 3)>(w);
+    }
+}
+// off + c0 of value field r as an fp16 bit pattern in both halves: off =
+// 2^(10 - p) has exponent field 25 - p; c0 = (2^B - 1) / 2 adds mantissa
+// c0 * 2^(p) (exact: c0 < off and c0 has one fractional bit, p >= 2)
+__host__ __device__ constexpr uint32_t val_centre(int bits, int r) {
+    return (view_val(bits, r).magic & 0xFFFFu) + (uint32_t)(((1 << bits) - 1) << (view_pos(bits, r) - 1));
+}
+template <int BITS>
+__device__ __forceinline__ uint32_t unpack_val(uint32_t w, int r) {
+    const uint32_t c = val_centre(BITS, r) * 0x10001u;
+    return h2u(__hsub2(u2h(unpack_val_raw<BITS>(w, r)), u2h(c)));
+}
 
 
 // ---------------------------------------------------------------------------
 // Shared-memory geometry
 // ---------------------------------------------------------------------------
-struct StageGeom {
-    int kc_bytes, ksz_bytes, vc_bytes, vsz_bytes, bytes;
+// The block record's layout for a kernel variant, at compile time (the same
+// numbers kivi_geom_init derives at run time; the launcher checks they agree).
+template <int D, int KB, int VB, int SH>
+struct Rec {
+    static constexpr int G = 16 << SH;
+    static constexpr int KGR = G >= 64 ? 1 : 64 / G;
+    static constexpr int KC = 2 * D * KB * 4;           // key code bytes
+    static constexpr int KSZ = KGR * 2 * D * 2;         // key scale/zero bytes
+    static constexpr int VC_BLK = D * VB / 2;           // words per value block
+    static constexpr int VSZ_BLK = 2 * (D / G) * 16;    // halves per value block
+    static constexpr int VC = 4 * VC_BLK * 4;
+    static constexpr int VSZ = 4 * VSZ_BLK * 2;
+    static constexpr int OFF_KSZ = KC, OFF_VC = KC + KSZ, OFF_VSZ = KC + KSZ + VC;
+    static constexpr int BYTES = KC + KSZ + VC + VSZ;
 };
-__host__ __device__ __forceinline__ StageGeom stage_geom(const KiviGeom &g) {
-    StageGeom s;   // a stage holds one block record
-    s.kc_bytes = g.off_ksz;
-    s.ksz_bytes = g.off_vc - g.off_ksz;
-    s.vc_bytes = g.off_vsz - g.off_vc;
-    s.vsz_bytes = g.rec_bytes - g.off_vsz;
-    s.bytes = g.rec_bytes;
-    return s;
-}
 // One warp's region of dynamic shared memory: its ring of stages; at the end
 // of a segment it also holds the warp's result (m[4], l[4], o[4][d] in
 // fp32).  Between the two, the CTA stages its mixed blocks across the
 // regions.
 __host__ __device__ __forceinline__ size_t warp_region(const KiviGeom &g, int stages) {
-    const size_t sb = stage_geom(g).bytes;
+    const size_t sb = (size_t)g.rec_bytes;   // a stage holds one block record
     size_t ring = (size_t)(stages >= 2 ? stages : 2) * sb;
     size_t res = (size_t)(8 + 4 * g.d) * 4;
     size_t m = ring > res ? ring : res;
@@ -273,11 +318,12 @@ __device__ __forceinline__ void copy_rows(unsigned char *dst, const __half *win,
 
 // Stage block kb: one bulk copy of its record (packed keys, key scale/zero
 // rows, packed values, value scale/zero rows, back to back).  Lane 0 issues.
-__device__ __forceinline__ void issue_block(const StageGeom &sg, unsigned char *st, uint64_t *bar,
-                                            const unsigned char *recs, int kb, uint64_t policy) {
+template <int BYTES>
+__device__ __forceinline__ void issue_block(unsigned char *st, uint64_t *bar, const unsigned char *recs, int kb,
+                                            uint64_t policy) {
     if ((threadIdx.x & 31) == 0) {
-        mbar_expect_tx(bar, (unsigned)sg.bytes);
-        bulk_g2s_hint(st, recs + (size_t)kb * sg.bytes, (unsigned)sg.bytes, bar, policy);
+        mbar_expect_tx(bar, (unsigned)BYTES);
+        bulk_g2s_hint(st, recs + (size_t)kb * BYTES, (unsigned)BYTES, bar, policy);
     }
 }
 
@@ -426,8 +472,8 @@ __device__ __forceinline__ uint32_t keep_halves(uint32_t x, bool lo, bool hi) {
 // (tokens tb.. of that head's weights row; null for absent heads).
 template <int D, int KB, int VB, int SH, bool MIXED, bool PROBS>
 __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D / 16][2],
-                                         const unsigned char *sb, const StageGeom &sg, const KiviGeom &g,
-                                         float alpha, const MixCtx &mx, float *srow) {
+                                         const unsigned char *sb, float alpha, const MixCtx &mx, float *srow) {
+    using RG = Rec<D, KB, VB, SH>;
     constexpr int NJ = D / 16;
     constexpr int CPHK = 16 / KB, NWK = KB / 2;
     constexpr int CPHV = 16 / VB, NWV = D * VB / 128;
@@ -443,19 +489,18 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
     const uint32_t nm = odd ? 0xBC00BC00u : 0u;   // -1 for lo columns, 0 for hi
     const uint32_t m1 = odd ? 0x3C003C00u : 0u;   // 1 for lo columns, 0 for hi
     const uint32_t *sK = reinterpret_cast<const uint32_t *>(sb);
-    const __half *sKsz = reinterpret_cast<const __half *>(sb + sg.kc_bytes);
-    const uint32_t *sV = reinterpret_cast<const uint32_t *>(sb + sg.kc_bytes + sg.ksz_bytes);
-    const __half *sVsz = reinterpret_cast<const __half *>(sb + sg.kc_bytes + sg.ksz_bytes + sg.vc_bytes);
+    const __half *sKsz = reinterpret_cast<const __half *>(sb + RG::OFF_KSZ);
+    const uint32_t *sV = reinterpret_cast<const uint32_t *>(sb + RG::OFF_VC);
+    const __half *sVsz = reinterpret_cast<const __half *>(sb + RG::OFF_VSZ);
 
     // ---- key zero points: sum_c q_c z_c and sum_c q_c s_c per group ----
+    // (rows gq >= nkrows repeat a present row: their results are not used)
     float dc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int zkrow = gq & (nkrows - 1);
 #pragma unroll
     for (int jj = 0; jj < NJ; ++jj) {
-        uint32_t a0 = 0, a2 = 0;
-        if (gq < nkrows) {
-            a0 = *reinterpret_cast<const uint32_t *>(sKsz + gq * D + 16 * jj + 2 * tq);
-            a2 = *reinterpret_cast<const uint32_t *>(sKsz + gq * D + 16 * jj + 8 + 2 * tq);
-        }
+        const uint32_t a0 = *reinterpret_cast<const uint32_t *>(sKsz + zkrow * D + 16 * jj + 2 * tq);
+        const uint32_t a2 = *reinterpret_cast<const uint32_t *>(sKsz + zkrow * D + 16 * jj + 8 + 2 * tq);
         mma16816(dc, a0, 0u, a2, 0u, qB[jj][0], qB[jj][1]);
     }
     float kz[4], ks[4];
@@ -555,6 +600,9 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
     softmax_update<D>(A, p);
 
     // ---- weights times values, 16 tokens at a time ----
+    // sacc: the block's sum_t p_t s_t per (value group, column), for the
+    // midpoint term at the end (rows = groups, like zacc)
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
         if (MIXED && !((mx.tmask >> kk) & 1)) continue;
@@ -572,7 +620,7 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
         // B = p s split: hi columns RN(ph s), lo columns (ph s - RN(ph s)) + pl s
         const uint32_t PL0m = hmul2u(PL0, m1), PL1m = hmul2u(PL1, m1);
         const uint32_t PH0n = hmul2u(PH0, nm), PH1n = hmul2u(PH1, nm);
-        const __half *vszk = sVsz + kk * g.vsz_blk;
+        const __half *vszk = sVsz + kk * RG::VSZ_BLK;
         uint32_t b0[16], b1[16];
 #pragma unroll
         for (int gi = 0; gi < 16; ++gi) {
@@ -584,7 +632,7 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
             b1[gi] = hfma2u(PL1m, v1, hfma2u(PH1, v1, hmul2u(PH1n, v1)));
         }
         uint32_t Wv[WLV];
-        const uint32_t *sVk = sV + kk * g.vc_blk;
+        const uint32_t *sVk = sV + kk * RG::VC_BLK;
 #pragma unroll
         for (int ch = 0; ch < WLV / CSV; ++ch) {
             if (CSV == 4) {
@@ -604,23 +652,36 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
             const int ci0 = 2 * mm;
             const int w = ci0 / CPHV, r0 = ci0 % CPHV;
             const uint32_t Wp0 = Wv[0 * NWV + w], Wp1 = Wv[1 * NWV + w];
-            const uint32_t a0 = unpack_exact<VB>(Wp0, r0), a1 = unpack_exact<VB>(Wp0, r0 + 1);
-            const uint32_t a2 = unpack_exact<VB>(Wp1, r0), a3 = unpack_exact<VB>(Wp1, r0 + 1);
+            const uint32_t a0 = unpack_val<VB>(Wp0, r0), a1 = unpack_val<VB>(Wp0, r0 + 1);
+            const uint32_t a2 = unpack_val<VB>(Wp1, r0), a3 = unpack_val<VB>(Wp1, r0 + 1);
             mma16816(A.oacc[mm], a0, a1, a2, a3, b0[mm >> sh], b1[mm >> sh]);
         }
-        // value zero points: rows [z][gi][16 tokens] (the codes entered exactly)
+        // value zero points and scales: rows [z or s][gi][16 tokens] (rows
+        // gq >= ngi repeat a present row, rows gq + 8 only exist with 16 groups)
         const uint32_t bz0 = odd ? PL0 : PH0, bz1 = odd ? PL1 : PH1;
-        const __half *zrow = vszk + ngi * 16;
-        uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-        if (gq < ngi) {
-            a0 = *reinterpret_cast<const uint32_t *>(zrow + gq * 16 + 2 * tq);
-            a2 = *reinterpret_cast<const uint32_t *>(zrow + gq * 16 + 2 * tq + 8);
+        const int zvrow = ngi >= 8 ? gq : (gq & (ngi - 1));
+        {
+            const __half *zrow = vszk + ngi * 16;
+            const uint32_t a0 = *reinterpret_cast<const uint32_t *>(zrow + zvrow * 16 + 2 * tq);
+            const uint32_t a2 = *reinterpret_cast<const uint32_t *>(zrow + zvrow * 16 + 2 * tq + 8);
+            uint32_t a1 = 0, a3 = 0;
+            if (ngi > 8) {
+                a1 = *reinterpret_cast<const uint32_t *>(zrow + (gq + 8) * 16 + 2 * tq);
+                a3 = *reinterpret_cast<const uint32_t *>(zrow + (gq + 8) * 16 + 2 * tq + 8);
+            }
+            mma16816(A.zacc, a0, a1, a2, a3, bz0, bz1);
         }
-        if (gq + 8 < ngi) {
-            a1 = *reinterpret_cast<const uint32_t *>(zrow + (gq + 8) * 16 + 2 * tq);
-            a3 = *reinterpret_cast<const uint32_t *>(zrow + (gq + 8) * 16 + 2 * tq + 8);
+        {
+            const __half *srw = vszk;
+            const uint32_t a0 = *reinterpret_cast<const uint32_t *>(srw + zvrow * 16 + 2 * tq);
+            const uint32_t a2 = *reinterpret_cast<const uint32_t *>(srw + zvrow * 16 + 2 * tq + 8);
+            uint32_t a1 = 0, a3 = 0;
+            if (ngi > 8) {
+                a1 = *reinterpret_cast<const uint32_t *>(srw + (gq + 8) * 16 + 2 * tq);
+                a3 = *reinterpret_cast<const uint32_t *>(srw + (gq + 8) * 16 + 2 * tq + 8);
+            }
+            mma16816(sacc, a0, a1, a2, a3, bz0, bz1);
         }
-        mma16816(A.zacc, a0, a1, a2, a3, bz0, bz1);
         if (MIXED) {
             // window value tokens of this tile: fp16 rows, A = rows transposed
             const int tau0 = mx.tb + 16 * kk;
@@ -636,6 +697,11 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
             }
         }
     }
+    // the values' midpoints: zacc += c0 * (the block's sum_t p_t s_t), row
+    // for row (both accumulators hold rows = groups)
+    constexpr float c0 = 0.5f * (float)((1 << VB) - 1);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) A.zacc[k] = fmaf(c0, sacc[k], A.zacc[k]);
 }
 
 // Per-warp result: m, l per head and o[head][d] = sum p v (value zero points
@@ -678,8 +744,8 @@ __device__ __forceinline__ void warp_result(WarpAcc<D> &A, float *wres) {
 // rings; its other blocks (those holding fp16 window tokens, at the end of
 // the sequence) are then staged one at a time by the whole CTA, record and
 // window rows with one round trip, and split into 16-token tiles over the
-// warps.  The warps merge in shared memory and write one partial; the last
-// CTA to finish a segment of that (i, j, qg) merges all of its partials.
+// warps.  The warps merge in shared memory and write one partial per
+// segment; merge_kernel merges the partials of each (i, j, qg).
 // ---------------------------------------------------------------------------
 __host__ __device__ __forceinline__ long long cta_of_unit(long long u, long long U, int C) {
     return ((u + 1) * C - 1) / U;
@@ -687,8 +753,8 @@ __host__ __device__ __forceinline__ long long cta_of_unit(long long u, long long
 
 template <int D, int KB, int VB, int SH, bool PROBS>
 __global__ void __launch_bounds__(256, 2)
-    decode_kernel(KiviGeom g, KiviDev dv, const __half *__restrict__ q, int hq,
-                  __half *__restrict__ out, DecodePlan plan, DecodeUnits units, ProbsOut po) {
+    decode_kernel(KiviGeom g, KiviDev dv, const __half *__restrict__ q, int hq, DecodePlan plan,
+                  DecodeUnits units, ProbsOut po) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int NJ = D / 16;
     const int nw = blockDim.x >> 5;
@@ -696,7 +762,7 @@ __global__ void __launch_bounds__(256, 2)
     const int gq = lane >> 2, tq = lane & 3;
     const int eB = gq >> 1;
     const int hg = hq / g.h, QG = plan.qgroups, HQG = g.h * QG;
-    const StageGeom sg = stage_geom(g);
+    using RG = Rec<D, KB, VB, SH>;
     const size_t wstride = warp_region(g, plan.stages);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
     unsigned char *ring = smem + bar_region(nw, plan.stages);
@@ -708,8 +774,8 @@ __global__ void __launch_bounds__(256, 2)
     long long u = (long long)c * U / C;
     const long long u_end = (long long)(c + 1) * U / C;
     __shared__ int s_seg[5];
-    __shared__ int s_last;
-    __shared__ float sML[8];
+    __shared__ float sML[8];    // per head: max over the warps, then the weighted sum of l
+    __shared__ float sWt[32];   // [warp][head]: the warp's weight
     // The barriers live for the whole kernel: a warp's n-th block (counted
     // across all its segments) goes to slot n % stages and completes phase
     // n / stages of that slot's barrier.
@@ -810,7 +876,7 @@ __global__ void __launch_bounds__(256, 2)
             const uint64_t keep = policy_evict_last();
             for (int x = xm; x < nD; ++x) {
                 const int kb = blk(x), tb = kb * KIVI_KBLK, te = min(tb + KIVI_KBLK, T);
-                prefetch_l2(recs + (size_t)kb * sg.bytes, (unsigned)sg.bytes, keep);
+                prefetch_l2(recs + (size_t)kb * RG::BYTES, (unsigned)RG::BYTES, keep);
                 prefetch_rows<D>(kwin, g.R, max(tb, Tqk), te, keep);
                 prefetch_rows<D>(vwin, g.R + 1, max(tb, Tqv), te, keep);
             }
@@ -828,7 +894,7 @@ __global__ void __launch_bounds__(256, 2)
                 more = false;
                 return;
             }
-            issue_block(sg, myregion + (size_t)islot * sg.bytes, mybars + islot, recs, blk(x), pol_stream);
+            issue_block<RG::BYTES>(myregion + (size_t)islot * RG::BYTES, mybars + islot, recs, blk(x), pol_stream);
             islot = next_slot(islot);
             ++issued;
         };
@@ -844,8 +910,7 @@ __global__ void __launch_bounds__(256, 2)
             float *srow = nullptr;
             if constexpr (PROBS)   // the warp's consumed-th block is its grab of that index
                 if (prow) srow = prow + (size_t)blk(warp + nw * consumed) * KIVI_KBLK;
-            do_block<D, KB, VB, SH, false, PROBS>(A, qB, myregion + (size_t)rslot * sg.bytes, sg, g, alpha,
-                                                  mc, srow);
+            do_block<D, KB, VB, SH, false, PROBS>(A, qB, myregion + (size_t)rslot * RG::BYTES, alpha, mc, srow);
             __syncwarp();
             // Refill the slot just read.  Its packed data was only read (by
             // loads whose values the block has consumed): no proxy fence.
@@ -883,20 +948,20 @@ __global__ void __launch_bounds__(256, 2)
                 unsigned bytes = 0;
                 for (int k = 0; k < nrb; ++k) {
                     const int kb = blk(x0 + k), tb = kb * KIVI_KBLK, te = min(tb + KIVI_KBLK, T);
-                    bytes += sg.bytes + (rows_to_stage(max(tb, Tqk), te, g.R) +
+                    bytes += RG::BYTES + (rows_to_stage(max(tb, Tqk), te, g.R) +
                                          rows_to_stage(max(tb, Tqv), te, g.R + 1)) * 2 * D;
                 }
                 if (lane == 0) mbar_expect_tx(cbar, bytes);
                 for (int k = 0; k < nrb && lane == 0; ++k) {
                     const int kb = blk(x0 + k), tb = kb * KIVI_KBLK, te = min(tb + KIVI_KBLK, T);
                     unsigned char *reg = ring + (size_t)k * mreg;
-                    bulk_g2s(reg, recs + (size_t)kb * sg.bytes, (unsigned)sg.bytes, cbar);
-                    copy_rows<D>(reg + sg.bytes, kwin, g.R, max(tb, Tqk), te, cbar);
-                    copy_rows<D>(reg + sg.bytes + (size_t)KIVI_KBLK * RS, vwin, g.R + 1, max(tb, Tqv), te, cbar);
+                    bulk_g2s(reg, recs + (size_t)kb * RG::BYTES, (unsigned)RG::BYTES, cbar);
+                    copy_rows<D>(reg + RG::BYTES, kwin, g.R, max(tb, Tqk), te, cbar);
+                    copy_rows<D>(reg + RG::BYTES + (size_t)KIVI_KBLK * RS, vwin, g.R + 1, max(tb, Tqv), te, cbar);
                 }
             }
             for (int k = 0; k < nrb; ++k) {
-                unsigned char *zrow = ring + (size_t)k * mreg + sg.bytes + (size_t)2 * KIVI_KBLK * RS;
+                unsigned char *zrow = ring + (size_t)k * mreg + RG::BYTES + (size_t)2 * KIVI_KBLK * RS;
                 for (int e = threadIdx.x; e < 2 * D / 16; e += blockDim.x)
                     reinterpret_cast<uint4 *>(zrow)[e] = make_uint4(0u, 0u, 0u, 0u);
             }
@@ -919,96 +984,58 @@ __global__ void __launch_bounds__(256, 2)
                 mc.T = T;
                 mc.Tqk = Tqk;
                 mc.Tqv = Tqv;
-                mc.krows = reg + sg.bytes;
-                mc.vrows = reg + sg.bytes + (size_t)KIVI_KBLK * RS;
+                mc.krows = reg + RG::BYTES;
+                mc.vrows = reg + RG::BYTES + (size_t)KIVI_KBLK * RS;
                 mc.ka = max(tb, Tqk);
                 mc.va = max(tb, Tqv);
-                mc.zrow = reg + sg.bytes + (size_t)2 * KIVI_KBLK * RS;
+                mc.zrow = reg + RG::BYTES + (size_t)2 * KIVI_KBLK * RS;
                 mc.RS = RS;
-                do_block<D, KB, VB, SH, true, PROBS>(A, qB, reg, sg, g, alpha, mc,
-                                                     PROBS && prow ? prow + tb : nullptr);
+                do_block<D, KB, VB, SH, true, PROBS>(A, qB, reg, alpha, mc, PROBS && prow ? prow + tb : nullptr);
             }
         }
         __syncthreads();   // the ring holds mixed data no longer needed
 
         // ---- merge the warps into this CTA's partial of (i, j, qg) ----
+        // (the partials of all CTAs are merged by merge_kernel, launched
+        // after this kernel)
         __syncwarp();
         warp_result<D, SH>(A, reinterpret_cast<float *>(myregion));
         __syncthreads();
+        if (threadIdx.x < 32) {
+            // lane 4 w + e: warp w's weight for head e, relative to the max
+            // over the warps; lanes 0-3 also hold the sum of the weighted l
+            const int w = lane >> 2, e = lane & 3;
+            const float *r = reinterpret_cast<const float *>(ring + (size_t)w * wstride);
+            const float m = w < nw ? r[e] : -INFINITY;
+            float M = m;
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 8));
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 16));
+            const float wt = M == -INFINITY ? 0.f : ex2(m - M);
+            float L = w < nw ? wt * r[4 + e] : 0.f;
+            L += __shfl_xor_sync(0xffffffffu, L, 4);
+            L += __shfl_xor_sync(0xffffffffu, L, 8);
+            L += __shfl_xor_sync(0xffffffffu, L, 16);
+            sWt[lane] = wt;
+            if (lane < 4) {
+                sML[lane] = M;
+                sML[4 + lane] = L;
+            }
+        }
+        __syncthreads();
         const long long Pp = (long long)HQG * units.start[i] + (long long)jq * Wi;
-        const int cfirst = (int)cta_of_unit(Pp, U, C);
-        const int np = (int)cta_of_unit(Pp + Wi - 1, U, C) - cfirst + 1;
-        const int slot = c - cfirst;
-        float *part = dv.part;
+        const int slot = c - (int)cta_of_unit(Pp, U, C);
         for (int x = threadIdx.x; x < nh * (D + 2); x += blockDim.x) {
             const int e = x / (D + 2), cc = x % (D + 2);
-            float M = -INFINITY;
-            for (int w = 0; w < nw; ++w) M = fmaxf(M, reinterpret_cast<const float *>(ring + w * wstride)[e]);
-            float val = 0.f;
-            if (cc == 0) {
-                val = M;
-            } else if (M != -INFINITY) {
-                for (int w = 0; w < nw; ++w) {
-                    const float *r = reinterpret_cast<const float *>(ring + w * wstride);
-                    const float fw = ex2(r[e] - M);
-                    val += fw * (cc == 1 ? r[4 + e] : r[8 + e * D + (cc - 2)]);
-                }
+            float val;
+            if (cc < 2) {
+                val = sML[4 * cc + e];
+            } else {
+                val = 0.f;
+                for (int w = 0; w < nw; ++w)
+                    val = fmaf(sWt[4 * w + e], reinterpret_cast<const float *>(ring + (size_t)w * wstride)[8 + e * D + (cc - 2)], val);
             }
-            part[(((size_t)i * hq + j * hg + e0 + e) * g.smax + slot) * (D + 2) + cc] = val;
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            __threadfence();
-            unsigned *tk = dv.merge_ticket + ((size_t)i * g.h + j) * 4 + qg;
-            const unsigned prev = atomicAdd(tk, 1u);
-            s_last = prev == (unsigned)np - 1u;
-            if (s_last) *tk = 0u;
-        }
-        __syncthreads();
-        if (s_last) {
-            // Merge the pair's partials: their (m, l) come into shared memory
-            // with one round trip, the log-sum-exp weights are formed there,
-            // then each output reads its accumulators once.  The ring is
-            // free: the warps' results were merged above.
-            __threadfence();
-            float *sm_m = reinterpret_cast<float *>(ring);   // [nh][np]
-            float *sm_w = sm_m + 4 * np;                      // [nh][np]
-            for (int x = threadIdx.x; x < nh * np; x += blockDim.x) {
-                const int e = x / np, y = x % np;
-                const float *pp = part + (((size_t)i * hq + j * hg + e0 + e) * g.smax + y) * (D + 2);
-                sm_m[x] = __ldcg(pp);
-                sm_w[x] = __ldcg(pp + 1);
-            }
-            __syncthreads();
-            if (threadIdx.x < nh) {
-                const int e = threadIdx.x;
-                float M = -INFINITY;
-                for (int y = 0; y < np; ++y) M = fmaxf(M, sm_m[e * np + y]);
-                float L = 0.f;
-                if (M != -INFINITY)
-                    for (int y = 0; y < np; ++y) L += ex2(sm_m[e * np + y] - M) * sm_w[e * np + y];
-                sML[e] = M;
-                sML[4 + e] = L;
-                if constexpr (PROBS) {
-                    float *ml = dv.ml + ((size_t)i * hq + j * hg + e0 + e) * 2;
-                    ml[0] = M;
-                    ml[1] = L > 0.f ? 1.f / L : 0.f;
-                }
-            }
-            __syncthreads();
-            for (int x = threadIdx.x; x < nh * np; x += blockDim.x) {
-                const int e = x / np;
-                const float M = sML[e];
-                sm_w[x] = M == -INFINITY ? 0.f : ex2(sm_m[x] - M) / sML[4 + e];
-            }
-            __syncthreads();
-            for (int x = threadIdx.x; x < nh * D; x += blockDim.x) {
-                const int e = x / D, cc = x % D;
-                const float *pp = part + ((size_t)i * hq + j * hg + e0 + e) * g.smax * (D + 2) + 2 + cc;
-                float a = 0.f;
-                for (int y = 0; y < np; ++y) a = fmaf(sm_w[e * np + y], __ldcg(pp + (size_t)y * (D + 2)), a);
-                out[((size_t)i * hq + j * hg + e0 + e) * D + cc] = __float2half_rn(a);
-            }
+            dv.part[(((size_t)i * hq + j * hg + e0 + e) * g.smax + slot) * (D + 2) + cc] = val;
         }
         __syncthreads();
         u += o1 - o0;
@@ -1018,6 +1045,10 @@ __global__ void __launch_bounds__(256, 2)
 template <int D, int KB, int VB, int SH, bool PROBS>
 cudaError_t launch_t(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, __half *out,
                      const DecodePlan &plan, const DecodeUnits &units, const ProbsOut &po, cudaStream_t st) {
+    using RG = Rec<D, KB, VB, SH>;
+    if (g.rec_bytes != RG::BYTES || g.off_ksz != RG::OFF_KSZ || g.off_vc != RG::OFF_VC ||
+        g.off_vsz != RG::OFF_VSZ || g.vc_blk != RG::VC_BLK || g.vsz_blk != RG::VSZ_BLK)
+        return cudaErrorInvalidValue;   // the record layout the kernel was compiled for
     size_t rings = (size_t)plan.warps * warp_region(g, plan.stages);
     if (rings < mixed_region(g)) rings = mixed_region(g);
     const size_t smem = bar_region(plan.warps, plan.stages) + rings;
@@ -1036,7 +1067,7 @@ cudaError_t launch_t(const KiviGeom &g, const KiviDev &dv, const __half *q, int 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<D, KB, VB, SH, PROBS>, g, dv, q, hq, out, plan, units, po);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<D, KB, VB, SH, PROBS>, g, dv, q, hq, plan, units, po);
 }
 
 template <int D, int KB, int VB, bool PROBS>

@@ -70,9 +70,8 @@ struct KiviDev {
     __half *Vf;
     int *T, *Tqk, *Tqv;     // device counters [b] (the current one of the cache's two sets)
     unsigned *status;       // anomaly flags
-    float *part;            // decode partials [b][h * KIVI_MAX_QPERKV][smax][d + 2]
-    unsigned *merge_ticket; // [b][h] arrivals of decode CTAs (split-K merge)
-    float *ml;              // [b][h * KIVI_MAX_QPERKV][2] softmax max and 1 / sum (weights output)
+    float *part;            // decode partials [b][h_q][smax][d + 2] (row stride smax (d + 2))
+    float *ml;              // [b][h_q][2] softmax max and 1 / sum (weights output)
 };
 
 // Optional per-token attention-weight output of a decode call: p[i][h][t]
@@ -281,6 +280,9 @@ struct DecodeUnits {
 
 // Sets the calling thread's text for kivi_last_error() (kivi_api.cu).
 void kivi_set_last_error(const char *msg);
+// Validates a cache shape by kivi_cache_create's rules: returns a
+// kivi_status value (0 = supported) and sets the error text (kivi_api.cu).
+int kivi_check_shape(int b, int h_kv, int d, int k_bits, int v_bits, int G, int R, int max_tokens);
 
 cudaError_t kivi_launch_prefill(const KiviGeom &g, const KiviDev &dv, const __half *K,
                                 const __half *V, const SeqLens &lens, int t_stride,
@@ -297,8 +299,14 @@ int kivi_partial_slots(int b, int h, int num_sms);
 // (and mass += weights), for rows of up to maxT tokens (kivi_probs.cu).
 cudaError_t kivi_launch_probs_finalize(const KiviGeom &g, const KiviDev &dv, int hq, const ProbsOut &po,
                                        int maxT, cudaStream_t st);
-// po (may be null): also write the per-token weights (launches the
-// finalizing kernel after the decode kernel; maxT = max_i T_i).
+// Merges the decode kernel's split-K partials of every (sequence, query
+// head) row into out (kivi_merge.cu); probs: also the row's softmax max
+// and 1 / sum for the weights' finalizing kernel.
+cudaError_t kivi_launch_merge(const KiviGeom &g, const KiviDev &dv, int hq, __half *out, const DecodePlan &plan,
+                              const DecodeUnits &units, bool probs, cudaStream_t st);
+// Launches the decode kernel, then the merge kernel; po (may be null):
+// also write the per-token weights (launches the finalizing kernel after
+// them; maxT = max_i T_i).
 cudaError_t kivi_launch_decode(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq,
                                __half *out, const DecodePlan &plan, const DecodeUnits &units,
                                cudaStream_t st, cudaEvent_t ev0, cudaEvent_t ev1,

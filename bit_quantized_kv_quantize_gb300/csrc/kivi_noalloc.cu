@@ -4,15 +4,21 @@
 // memory pool owns all device memory, inside an allocator callback, or under
 // a real-time budget that forbids allocation after start-up.  For them,
 // kivi_decode_attn_noalloc reads a packed cache that lives in memory the
-// caller already owns and keeps its own scratch (the split-K partials, the
-// merge tickets and the status word) in one file-scope __device__ array of
-// fixed size, instead of the per-cache buffers kivi_cache_create allocates.
+// caller already owns and keeps its own scratch (the split-K partials and
+// the status word) in one file-scope __device__ array of fixed size,
+// instead of the per-cache buffers kivi_cache_create allocates.
 //
-// The array is part of the loaded module: every GPU that loads libkivi holds
-// KIVI_NOALLOC_SCRATCH_BYTES of it until the process exits.  All calls share
-// it, so calls whose kernels overlap on the GPU (different streams, or
-// different host threads) race on it; the tickets that must start at zero are
-// cleared by each call, the partials are fully rewritten before they are read.
+// CUDA loads a library's device code and __device__ arrays lazily, on first
+// use: the array (KIVI_NOALLOC_SCRATCH_BYTES) takes device memory on a device
+// from the first call there (the address look-up loads it), and the decode
+// kernel's code when a call first launches that kernel variant (head
+// dimension, bit widths, G); both stay until the process exits.  Later calls
+// of an already-used shape take no device memory.  All calls share the
+// array, so calls whose kernels overlap on the GPU (different streams, or
+// different host threads) race on it; the status word is cleared by each
+// call, the partials are fully rewritten before they are read.
+// The status word in the array is cleared by each call and never read back:
+// this path reports no device-side anomaly (a bounded wait that ran out).
 #include <cstring>
 #include <mutex>
 
@@ -35,7 +41,9 @@ kivi_status fail(kivi_status s, const char *msg) {
 }
 
 // The array's name is only a host-side stand-in in host code; the kernel
-// needs its device address, looked up once per device with that device current.
+// needs its device address, looked up once per device with that device
+// current.  A cudaDeviceReset unloads the module and makes the cached
+// address stale: the entry point is not to be used after a reset.
 kivi_status scratch_address(unsigned char **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= KIVI_NOALLOC_MAX_DEVICES)
@@ -58,13 +66,10 @@ extern "C" kivi_status kivi_decode_attn_noalloc(const kivi_packed_cache *pc, con
     kivi_set_last_error("");
     if (!pc || !q || !out) return fail(KIVI_ERR_INVALID_ARG, "cache, q or out is null");
     const int b = pc->b, h = pc->h_kv, d = pc->d, G = pc->G, R = pc->R;
-    if (b < 1 || h < 1 || pc->max_tokens < 1 || R < 1) return fail(KIVI_ERR_INVALID_ARG, "sizes must be positive");
-    if (b > KIVI_MAX_BATCH) return fail(KIVI_ERR_UNSUPPORTED, "b above 1024");
-    if ((pc->k_bits != 2 && pc->k_bits != 4) || (pc->v_bits != 2 && pc->v_bits != 4))
-        return fail(KIVI_ERR_UNSUPPORTED, "bits must be 2 or 4");
-    if ((G != 16 && G != 32 && G != 64 && G != 128) || (d != 64 && d != 128 && d != 256) || d % G ||
-        R % G || R > 4096)
-        return fail(KIVI_ERR_UNSUPPORTED, "unsupported G, d or R");
+    // the same shape rules as kivi_cache_create (they also bound max_tokens,
+    // so the capacity arithmetic below stays in range)
+    const int sc = kivi_check_shape(b, h, d, pc->k_bits, pc->v_bits, G, R, pc->max_tokens);
+    if (sc != KIVI_OK) return (kivi_status)sc;   // the error text is set
     if (h_q < 1 || h_q % h != 0) return fail(KIVI_ERR_INVALID_ARG, "h_q must be a positive multiple of h_kv");
     if (h_q / h > KIVI_MAX_QPERKV) return fail(KIVI_ERR_UNSUPPORTED, "h_q / h_kv above 8");
     const void *ptrs[] = {pc->blocks, pc->Kf, pc->Vf, q, out};
@@ -89,9 +94,7 @@ extern "C" kivi_status kivi_decode_attn_noalloc(const kivi_packed_cache *pc, con
     g.smax = plan.max_parts;   // partial stride: exactly what this plan writes
 
     const size_t part_bytes = (size_t)b * h_q * g.smax * (d + 2) * sizeof(float);
-    const size_t ticket_off = (part_bytes + 255) / 256 * 256;
-    const size_t ticket_bytes = (size_t)b * h * 4 * sizeof(unsigned);
-    const size_t status_off = ticket_off + (ticket_bytes + 255) / 256 * 256;
+    const size_t status_off = (part_bytes + 255) / 256 * 256;
     if (status_off + 256 > KIVI_NOALLOC_SCRATCH_BYTES)
         return fail(KIVI_ERR_UNSUPPORTED,
                     "decode scratch for this shape exceeds the fixed 16 MiB no-alloc array");
@@ -100,8 +103,8 @@ extern "C" kivi_status kivi_decode_attn_noalloc(const kivi_packed_cache *pc, con
     kivi_status s = scratch_address(&scratch);
     if (s != KIVI_OK) return s;
     cudaStream_t st = (cudaStream_t)stream;
-    // merge tickets and the status word must start at zero
-    cudaError_t e = cudaMemsetAsync(scratch + ticket_off, 0, status_off + 256 - ticket_off, st);
+    // the status word must start at zero
+    cudaError_t e = cudaMemsetAsync(scratch + status_off, 0, 256, st);
     if (e != cudaSuccess) return fail(KIVI_ERR_CUDA, cudaGetErrorString(e));
 
     KiviDev dv;
@@ -113,7 +116,6 @@ extern "C" kivi_status kivi_decode_attn_noalloc(const kivi_packed_cache *pc, con
     dv.Tqk = (int *)pc->Tqk;
     dv.Tqv = (int *)pc->Tqv;
     dv.part = reinterpret_cast<float *>(scratch);
-    dv.merge_ticket = reinterpret_cast<unsigned *>(scratch + ticket_off);
     dv.status = reinterpret_cast<unsigned *>(scratch + status_off);
     e = kivi_launch_decode(g, dv, (const __half *)q, h_q, (__half *)out, plan, units, st, nullptr,
                            nullptr);

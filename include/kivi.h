@@ -214,19 +214,27 @@ typedef struct {
  * code running while a framework's memory pool owns the device memory, in
  * an allocator callback, or under a real-time budget that forbids device
  * allocation after start-up.)  Computes exactly what kivi_decode_attn
- * computes, over the cache described by *cache; q and out as there.
- * Its scratch (split partials, merge tickets, status word) lives in one
- * fixed 16 MiB __device__ array inside the library, which every GPU that
- * loads the library holds until the process exits; shapes whose scratch
- * b * h_q * P * (d + 2) * 4 bytes plus tickets exceed it (P: the most
- * persistent CTAs sharing one (sequence, kv head, head group)) are
- * rejected with KIVI_ERR_UNSUPPORTED and a kivi_last_error() message.  The
- * call launches on `stream` and clears the tickets itself; all calls share
+ * computes, over the cache described by *cache; q and out as there; the
+ * shape rules are kivi_cache_create's.
+ * Its scratch (split partials, status word) lives in one fixed 16 MiB
+ * __device__ array inside the library; shapes whose scratch
+ * b * h_q * P * (d + 2) * 4 bytes exceed it (P: the most persistent CTAs
+ * sharing one (sequence, kv head, head group)) are rejected with
+ * KIVI_ERR_UNSUPPORTED and a kivi_last_error() message.  The call launches
+ * on `stream` (the decode and merge kernels) and clears the status word
+ * itself; all calls share
  * the array, so calls whose kernels overlap on the GPU race and must not be
- * issued.  The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  No cudaMalloc, cudaFree or other allocating
- * routine is called. */
+ * issued.  CUDA loads device code and __device__ arrays lazily: the first
+ * call on a device loads the array (16 MiB of device memory, held until the
+ * process exits) and looks up its device address (cudaGetSymbolAddress)
+ * with that device current, and the first call of each shape (d, k_bits,
+ * v_bits, G) loads that kernel's code.  So make one warm-up call per device
+ * and shape before a memory pool takes the device memory, and before any
+ * stream capture; later calls take no device memory.  After a
+ * cudaDeviceReset the entry point must not be used (the looked-up address
+ * is stale).  The kernel's status word is cleared by each call and not
+ * reported: this path has no counterpart of kivi_cache_check.  No
+ * cudaMalloc, cudaFree or other allocating routine is called. */
 kivi_status kivi_decode_attn_noalloc(const kivi_packed_cache *cache, const void *q, int h_q,
                                      void *out, kivi_stream_t stream);
 
