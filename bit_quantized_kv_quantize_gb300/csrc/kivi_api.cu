@@ -132,7 +132,7 @@ kivi_status check_shape(int b, int h_kv, int d, int k_bits, int v_bits, int G, i
 
 void free_dev(kivi_cache *c) {
     KiviDev &d = c->dv;
-    void *ps[] = {d.blk, d.Kf, d.Vf, c->cnt, d.status, d.part, d.ml};
+    void *ps[] = {d.blk, d.Kf, d.Vf, c->cnt, d.status, d.part, d.merge_ticket, d.ml};
     for (void *p : ps)
         if (p) cudaFree(p);
     memset(&d, 0, sizeof d);
@@ -312,7 +312,8 @@ kivi_status kivi_cache_create(int b, int h_kv, int d, int k_bits, int v_bits, in
         {(void **)&dv.Vf, bh * (R + 1) * d * 2},
         {(void **)&c->cnt, (size_t)2 * 3 * b * 4},
         {(void **)&dv.status, 4},
-        {(void **)&dv.part, bh * KIVI_MAX_QPERKV * g.smax * (d + 2) * 4},
+        {(void **)&dv.part, bh * KIVI_MAX_QPERKV * g.smax * (d + 4) * 4},
+        {(void **)&dv.merge_ticket, bh * 4 * 4},
         {(void **)&dv.ml, bh * KIVI_MAX_QPERKV * 2 * 4},
     };
     for (auto &r : reqs) {

@@ -55,7 +55,7 @@ DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *T, const int *
     DecodePlan p;
     const int hg = hq / g.h;
     p.qgroups = (hg + 3) / 4;
-    p.launches = 2;   // the decode kernel, then the merge kernel
+    p.launches = 1;
     // shared memory: two CTAs per SM, ~110 KB each for the warps' rings of at
     // least two stages
     const int sb = g.rec_bytes;   // a stage holds one block record
@@ -126,7 +126,6 @@ cudaError_t kivi_launch_decode(const KiviGeom &g, const KiviDev &dv, const __hal
         default: e = kivi_launch_decode_d256(g, dv, q, hq, out, plan, units, st); break;
         }
     }
-    if (e == cudaSuccess) e = kivi_launch_merge(g, dv, hq, out, plan, units, po != nullptr, st);
     if (ev1) cudaEventRecord(ev1, st);
     if (e == cudaSuccess && po && maxT > 0) e = kivi_launch_probs_finalize(g, dv, hq, *po, maxT, st);
     return e;

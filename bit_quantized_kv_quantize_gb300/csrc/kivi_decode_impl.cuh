@@ -26,9 +26,8 @@
 // that also hold tokens of the fp16 windows add, for those tokens, MMAs over
 // fp16 rows copied into shared memory.  Each CTA merges its warps per pair
 // and writes (m, l, acc[d]) in base 2 (scores pre-multiplied by
-// log2(e) / sqrt(d)); merge_kernel (kivi_merge.cu), launched next on the
-// stream, merges each pair's partials with log-sum-exp weights and writes
-// the fp16 output.
+// log2(e) / sqrt(d)); the last CTA to finish a pair merges its partials
+// with log-sum-exp weights and writes the fp16 output.
 #pragma once
 #include "kivi_internal.cuh"
 
@@ -745,7 +744,8 @@ __device__ __forceinline__ void warp_result(WarpAcc<D> &A, float *wres) {
 // the sequence) are then staged one at a time by the whole CTA, record and
 // window rows with one round trip, and split into 16-token tiles over the
 // warps.  The warps merge in shared memory and write one partial per
-// segment; merge_kernel merges the partials of each (i, j, qg).
+// segment; the last CTA to finish a segment of that (i, j, qg) merges all
+// of its partials.
 // ---------------------------------------------------------------------------
 __host__ __device__ __forceinline__ long long cta_of_unit(long long u, long long U, int C) {
     return ((u + 1) * C - 1) / U;
@@ -753,8 +753,8 @@ __host__ __device__ __forceinline__ long long cta_of_unit(long long u, long long
 
 template <int D, int KB, int VB, int SH, bool PROBS>
 __global__ void __launch_bounds__(256, 2)
-    decode_kernel(KiviGeom g, KiviDev dv, const __half *__restrict__ q, int hq, DecodePlan plan,
-                  DecodeUnits units, ProbsOut po) {
+    decode_kernel(KiviGeom g, KiviDev dv, const __half *__restrict__ q, int hq,
+                  __half *__restrict__ out, DecodePlan plan, DecodeUnits units, ProbsOut po) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int NJ = D / 16;
     const int nw = blockDim.x >> 5;
@@ -774,7 +774,8 @@ __global__ void __launch_bounds__(256, 2)
     long long u = (long long)c * U / C;
     const long long u_end = (long long)(c + 1) * U / C;
     __shared__ int s_seg[5];
-    __shared__ float sML[8];    // per head: max over the warps, then the weighted sum of l
+    __shared__ int s_last;
+    __shared__ float sML[8];    // per head: max over the warps (or partials), then the weighted sum of l
     __shared__ float sWt[32];   // [warp][head]: the warp's weight
     // The barriers live for the whole kernel: a warp's n-th block (counted
     // across all its segments) goes to slot n % stages and completes phase
@@ -996,8 +997,9 @@ __global__ void __launch_bounds__(256, 2)
         __syncthreads();   // the ring holds mixed data no longer needed
 
         // ---- merge the warps into this CTA's partial of (i, j, qg) ----
-        // (the partials of all CTAs are merged by merge_kernel, launched
-        // after this kernel)
+        // A partial is PS = D + 4 floats: m, l, two unused, acc[D] (rows
+        // 16-byte aligned for the vector loads of the final merge).
+        constexpr int PS = D + 4, NC4 = D / 4;
         __syncwarp();
         warp_result<D, SH>(A, reinterpret_cast<float *>(myregion));
         __syncthreads();
@@ -1024,18 +1026,128 @@ __global__ void __launch_bounds__(256, 2)
         }
         __syncthreads();
         const long long Pp = (long long)HQG * units.start[i] + (long long)jq * Wi;
-        const int slot = c - (int)cta_of_unit(Pp, U, C);
-        for (int x = threadIdx.x; x < nh * (D + 2); x += blockDim.x) {
-            const int e = x / (D + 2), cc = x % (D + 2);
-            float val;
-            if (cc < 2) {
-                val = sML[4 * cc + e];
+        const int cfirst = (int)cta_of_unit(Pp, U, C);
+        const int np = (int)cta_of_unit(Pp + Wi - 1, U, C) - cfirst + 1;
+        const int slot = c - cfirst;
+        float *const prow0 = dv.part + ((size_t)i * hq + j * hg + e0) * g.smax * PS;   // head e: + e smax PS
+        for (int x = threadIdx.x; x < nh * (NC4 + 1); x += blockDim.x) {
+            const int e = x / (NC4 + 1), c4 = x % (NC4 + 1);
+            float *dst = prow0 + ((size_t)e * g.smax + slot) * PS;
+            if (c4 == NC4) {
+                *reinterpret_cast<float2 *>(dst) = make_float2(sML[e], sML[4 + e]);
             } else {
-                val = 0.f;
-                for (int w = 0; w < nw; ++w)
-                    val = fmaf(sWt[4 * w + e], reinterpret_cast<const float *>(ring + (size_t)w * wstride)[8 + e * D + (cc - 2)], val);
+                float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int w = 0; w < nw; ++w) {
+                    const float wt = sWt[4 * w + e];
+                    const float4 o4 = *reinterpret_cast<const float4 *>(
+                        reinterpret_cast<const float *>(ring + (size_t)w * wstride) + 8 + e * D + 4 * c4);
+                    a4.x = fmaf(wt, o4.x, a4.x);
+                    a4.y = fmaf(wt, o4.y, a4.y);
+                    a4.z = fmaf(wt, o4.z, a4.z);
+                    a4.w = fmaf(wt, o4.w, a4.w);
+                }
+                *reinterpret_cast<float4 *>(dst + 4 + 4 * c4) = a4;
             }
-            dv.part[(((size_t)i * hq + j * hg + e0 + e) * g.smax + slot) * (D + 2) + cc] = val;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            unsigned *tk = dv.merge_ticket + ((size_t)i * g.h + j) * 4 + qg;
+            const unsigned prev = atomicAdd(tk, 1u);
+            s_last = prev == (unsigned)np - 1u;
+            if (s_last) *tk = 0u;
+        }
+        __syncthreads();
+        if (s_last) {
+            // Merge the pair's partials: their (m, l) come into shared memory
+            // with one round trip, each head's weights are formed there by
+            // one warp, then the accumulators are read as float4 columns,
+            // S partials in flight per column (S threads a column, summed in
+            // shared memory).  The ring is free: the warps' results were
+            // merged above.
+            __threadfence();
+            float *sm_m = reinterpret_cast<float *>(ring);   // [nh][np]
+            float *sm_w = sm_m + 4 * np;                      // [nh][np]: l, then the weights
+            float4 *sm_a = reinterpret_cast<float4 *>(sm_w + 4 * np);   // [S][nh NC4] (16-byte aligned)
+            for (int x = threadIdx.x; x < nh * np; x += blockDim.x) {
+                const int e = x / np, y = x % np;
+                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(prow0 + ((size_t)e * g.smax + y) * PS));
+                sm_m[x] = ml.x;
+                sm_w[x] = ml.y;
+            }
+            __syncthreads();
+            if (warp < nh) {
+                const int e = warp;
+                float M = -INFINITY;
+                for (int y = lane; y < np; y += 32) M = fmaxf(M, sm_m[e * np + y]);
+                for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+                float L = 0.f;
+                if (M != -INFINITY)
+                    for (int y = lane; y < np; y += 32) L = fmaf(ex2(sm_m[e * np + y] - M), sm_w[e * np + y], L);
+                for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                __syncwarp();
+                for (int y = lane; y < np; y += 32)
+                    sm_w[e * np + y] = M == -INFINITY ? 0.f : ex2(sm_m[e * np + y] - M) * inv;
+                if constexpr (PROBS) {
+                    if (lane == 0) {
+                        float *ml = dv.ml + ((size_t)i * hq + j * hg + e0 + e) * 2;
+                        ml[0] = M;
+                        ml[1] = inv;
+                    }
+                }
+            }
+            __syncthreads();
+            // (column, subset) items: S subsets of the partials per float4
+            // column when the CTA has threads for them, else one; each
+            // thread takes items in turn
+            const int ncol = nh * NC4;
+            const int S = max(1, min(8, (int)blockDim.x / ncol));
+            for (int it = threadIdx.x; it < ncol * S; it += blockDim.x) {
+                const int col = it % ncol, sub = it / ncol;
+                const int e = col / NC4, c4 = col % NC4;
+                const float *src = prow0 + (size_t)e * g.smax * PS + 4 + 4 * c4;
+                const float *wr = sm_w + e * np;
+                float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                int y = sub;
+                for (; y + 3 * S < np; y += 4 * S) {   // four partials in flight
+                    const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(src + (size_t)y * PS));
+                    const float4 v1 = __ldcg(reinterpret_cast<const float4 *>(src + (size_t)(y + S) * PS));
+                    const float4 v2 = __ldcg(reinterpret_cast<const float4 *>(src + (size_t)(y + 2 * S) * PS));
+                    const float4 v3 = __ldcg(reinterpret_cast<const float4 *>(src + (size_t)(y + 3 * S) * PS));
+                    const float w0 = wr[y], w1 = wr[y + S], w2 = wr[y + 2 * S], w3 = wr[y + 3 * S];
+                    a4.x = fmaf(w0, v0.x, fmaf(w1, v1.x, fmaf(w2, v2.x, fmaf(w3, v3.x, a4.x))));
+                    a4.y = fmaf(w0, v0.y, fmaf(w1, v1.y, fmaf(w2, v2.y, fmaf(w3, v3.y, a4.y))));
+                    a4.z = fmaf(w0, v0.z, fmaf(w1, v1.z, fmaf(w2, v2.z, fmaf(w3, v3.z, a4.z))));
+                    a4.w = fmaf(w0, v0.w, fmaf(w1, v1.w, fmaf(w2, v2.w, fmaf(w3, v3.w, a4.w))));
+                }
+                for (; y < np; y += S) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + (size_t)y * PS));
+                    const float w0 = wr[y];
+                    a4.x = fmaf(w0, v.x, a4.x);
+                    a4.y = fmaf(w0, v.y, a4.y);
+                    a4.z = fmaf(w0, v.z, a4.z);
+                    a4.w = fmaf(w0, v.w, a4.w);
+                }
+                sm_a[it] = a4;
+            }
+            __syncthreads();
+            for (int col = threadIdx.x; col < ncol; col += blockDim.x) {
+                const int e = col / NC4, c4 = col % NC4;
+                float4 a4 = sm_a[col];
+                for (int k = 1; k < S; ++k) {
+                    const float4 b4 = sm_a[k * ncol + col];
+                    a4.x += b4.x;
+                    a4.y += b4.y;
+                    a4.z += b4.z;
+                    a4.w += b4.w;
+                }
+                const __half2 lo = __floats2half2_rn(a4.x, a4.y), hi = __floats2half2_rn(a4.z, a4.w);
+                uint2 o2;
+                o2.x = h2u(lo);
+                o2.y = h2u(hi);
+                *reinterpret_cast<uint2 *>(out + ((size_t)i * hq + j * hg + e0 + e) * D + 4 * c4) = o2;
+            }
         }
         __syncthreads();
         u += o1 - o0;
@@ -1067,7 +1179,7 @@ cudaError_t launch_t(const KiviGeom &g, const KiviDev &dv, const __half *q, int 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<D, KB, VB, SH, PROBS>, g, dv, q, hq, plan, units, po);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<D, KB, VB, SH, PROBS>, g, dv, q, hq, out, plan, units, po);
 }
 
 template <int D, int KB, int VB, bool PROBS>

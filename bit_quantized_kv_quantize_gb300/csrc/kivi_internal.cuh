@@ -70,7 +70,8 @@ struct KiviDev {
     __half *Vf;
     int *T, *Tqk, *Tqv;     // device counters [b] (the current one of the cache's two sets)
     unsigned *status;       // anomaly flags
-    float *part;            // decode partials [b][h_q][smax][d + 2] (row stride smax (d + 2))
+    float *part;            // decode partials [b][h_q][smax][d + 4]: m, l, 2 unused, acc[d]
+    unsigned *merge_ticket; // [b][h][4] arrivals of decode CTAs (split-K merge)
     float *ml;              // [b][h_q][2] softmax max and 1 / sum (weights output)
 };
 
@@ -299,14 +300,8 @@ int kivi_partial_slots(int b, int h, int num_sms);
 // (and mass += weights), for rows of up to maxT tokens (kivi_probs.cu).
 cudaError_t kivi_launch_probs_finalize(const KiviGeom &g, const KiviDev &dv, int hq, const ProbsOut &po,
                                        int maxT, cudaStream_t st);
-// Merges the decode kernel's split-K partials of every (sequence, query
-// head) row into out (kivi_merge.cu); probs: also the row's softmax max
-// and 1 / sum for the weights' finalizing kernel.
-cudaError_t kivi_launch_merge(const KiviGeom &g, const KiviDev &dv, int hq, __half *out, const DecodePlan &plan,
-                              const DecodeUnits &units, bool probs, cudaStream_t st);
-// Launches the decode kernel, then the merge kernel; po (may be null):
-// also write the per-token weights (launches the finalizing kernel after
-// them; maxT = max_i T_i).
+// po (may be null): also write the per-token weights (launches the
+// finalizing kernel after the decode kernel; maxT = max_i T_i).
 cudaError_t kivi_launch_decode(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq,
                                __half *out, const DecodePlan &plan, const DecodeUnits &units,
                                cudaStream_t st, cudaEvent_t ev0, cudaEvent_t ev1,

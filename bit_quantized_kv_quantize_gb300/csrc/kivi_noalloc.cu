@@ -4,9 +4,9 @@
 // memory pool owns all device memory, inside an allocator callback, or under
 // a real-time budget that forbids allocation after start-up.  For them,
 // kivi_decode_attn_noalloc reads a packed cache that lives in memory the
-// caller already owns and keeps its own scratch (the split-K partials and
-// the status word) in one file-scope __device__ array of fixed size,
-// instead of the per-cache buffers kivi_cache_create allocates.
+// caller already owns and keeps its own scratch (the split-K partials, the
+// merge tickets and the status word) in one file-scope __device__ array of
+// fixed size, instead of the per-cache buffers kivi_cache_create allocates.
 //
 // CUDA loads a library's device code and __device__ arrays lazily, on first
 // use: the array (KIVI_NOALLOC_SCRATCH_BYTES) takes device memory on a device
@@ -15,8 +15,9 @@
 // dimension, bit widths, G); both stay until the process exits.  Later calls
 // of an already-used shape take no device memory.  All calls share the
 // array, so calls whose kernels overlap on the GPU (different streams, or
-// different host threads) race on it; the status word is cleared by each
-// call, the partials are fully rewritten before they are read.
+// different host threads) race on it; the tickets that must start at zero
+// and the status word are cleared by each call, the partials are fully
+// rewritten before they are read.
 // The status word in the array is cleared by each call and never read back:
 // this path reports no device-side anomaly (a bounded wait that ran out).
 #include <cstring>
@@ -93,8 +94,10 @@ extern "C" kivi_status kivi_decode_attn_noalloc(const kivi_packed_cache *pc, con
     const DecodePlan plan = kivi_plan_decode(g, h_q, full, full, full, sms, &units);
     g.smax = plan.max_parts;   // partial stride: exactly what this plan writes
 
-    const size_t part_bytes = (size_t)b * h_q * g.smax * (d + 2) * sizeof(float);
-    const size_t status_off = (part_bytes + 255) / 256 * 256;
+    const size_t part_bytes = (size_t)b * h_q * g.smax * (d + 4) * sizeof(float);
+    const size_t ticket_off = (part_bytes + 255) / 256 * 256;
+    const size_t ticket_bytes = (size_t)b * h * 4 * sizeof(unsigned);
+    const size_t status_off = ticket_off + (ticket_bytes + 255) / 256 * 256;
     if (status_off + 256 > KIVI_NOALLOC_SCRATCH_BYTES)
         return fail(KIVI_ERR_UNSUPPORTED,
                     "decode scratch for this shape exceeds the fixed 16 MiB no-alloc array");
@@ -103,8 +106,8 @@ extern "C" kivi_status kivi_decode_attn_noalloc(const kivi_packed_cache *pc, con
     kivi_status s = scratch_address(&scratch);
     if (s != KIVI_OK) return s;
     cudaStream_t st = (cudaStream_t)stream;
-    // the status word must start at zero
-    cudaError_t e = cudaMemsetAsync(scratch + status_off, 0, 256, st);
+    // the merge tickets and the status word must start at zero
+    cudaError_t e = cudaMemsetAsync(scratch + ticket_off, 0, status_off + 256 - ticket_off, st);
     if (e != cudaSuccess) return fail(KIVI_ERR_CUDA, cudaGetErrorString(e));
 
     KiviDev dv;
@@ -116,6 +119,7 @@ extern "C" kivi_status kivi_decode_attn_noalloc(const kivi_packed_cache *pc, con
     dv.Tqk = (int *)pc->Tqk;
     dv.Tqv = (int *)pc->Tqv;
     dv.part = reinterpret_cast<float *>(scratch);
+    dv.merge_ticket = reinterpret_cast<unsigned *>(scratch + ticket_off);
     dv.status = reinterpret_cast<unsigned *>(scratch + status_off);
     e = kivi_launch_decode(g, dv, (const __half *)q, h_q, (__half *)out, plan, units, st, nullptr,
                            nullptr);

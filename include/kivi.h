@@ -216,13 +216,12 @@ typedef struct {
  * allocation after start-up.)  Computes exactly what kivi_decode_attn
  * computes, over the cache described by *cache; q and out as there; the
  * shape rules are kivi_cache_create's.
- * Its scratch (split partials, status word) lives in one fixed 16 MiB
- * __device__ array inside the library; shapes whose scratch
- * b * h_q * P * (d + 2) * 4 bytes exceed it (P: the most persistent CTAs
- * sharing one (sequence, kv head, head group)) are rejected with
- * KIVI_ERR_UNSUPPORTED and a kivi_last_error() message.  The call launches
- * on `stream` (the decode and merge kernels) and clears the status word
- * itself; all calls share
+ * Its scratch (split partials, merge tickets, status word) lives in one
+ * fixed 16 MiB __device__ array inside the library; shapes whose scratch
+ * b * h_q * P * (d + 4) * 4 bytes plus tickets exceed it (P: the most
+ * persistent CTAs sharing one (sequence, kv head, head group)) are
+ * rejected with KIVI_ERR_UNSUPPORTED and a kivi_last_error() message.  The
+ * call launches on `stream` and clears the tickets itself; all calls share
  * the array, so calls whose kernels overlap on the GPU race and must not be
  * issued.  CUDA loads device code and __device__ arrays lazily: the first
  * call on a device loads the array (16 MiB of device memory, held until the
