@@ -43,7 +43,7 @@ FALLBACK_HBM_GBS = 6800.0
 # capture of the kernel whose source hash is recorded beside it; reported
 # only while the kernel source is unchanged (llama3_8b_gqa_32k, the
 # default workload).
-NCU_TRAFFIC = {"4e7c25cb0e81b994": 205740032 + 2805504}
+NCU_TRAFFIC = {"4e7c25cb0e81b994": 205740032 + 2805504, "0c2edd1a35994eed": 205770240 + 3154944}
 
 
 def algorithmic_bytes(w: W.Workload, T, Tqk, Tqv, scores: bool = False) -> int:

@@ -533,14 +533,21 @@ kivi_status kivi_cache_export(kivi_cache_t c, void *Kc, void *Ksz, void *Vc, voi
                 const size_t slice = (size_t)i * g.h + j;
                 if (Kc) memcpy((unsigned char *)Kc + (slice * g.nkb + kb) * kcb, r, kcb);
                 if (Vc) memcpy((unsigned char *)Vc + (slice * g.nkb + kb) * vcb, r + g.off_vc, vcb);
-                if (Vsz) memcpy((unsigned char *)Vsz + (slice * g.nkb + kb) * vszb, r + g.off_vsz, vszb);
-                if (Ksz) {
-                    if (g.G <= KIVI_KBLK)
-                        memcpy((unsigned char *)Ksz + (slice * g.nkg + (size_t)kb * g.kgr) * rowsb, r + g.off_ksz,
-                               g.kgr * rowsb);
-                    else if (kb % (g.G / KIVI_KBLK) == 0)   // first of the group's records
-                        memcpy((unsigned char *)Ksz + (slice * g.nkg + kb / (g.G / KIVI_KBLK)) * rowsb,
-                               r + g.off_ksz, rowsb);
+                // scale / zero rows: undo the record's lane-major order
+                if (Vsz) {
+                    const uint16_t *src = reinterpret_cast<const uint16_t *>(r + g.off_vsz);
+                    uint16_t *dst = reinterpret_cast<uint16_t *>((unsigned char *)Vsz + (slice * g.nkb + kb) * vszb);
+                    for (int row = 0; row < 4 * g.vsz_blk / 16; ++row)
+                        for (int tau = 0; tau < 16; ++tau) dst[row * 16 + tau] = src[row * 16 + vsz_pos(tau)];
+                }
+                if (Ksz && (g.G <= KIVI_KBLK || kb % (g.G / KIVI_KBLK) == 0)) {
+                    // G > 64: the rows of group kb / (G / 64), from the first of its records
+                    const int nrow = g.G <= KIVI_KBLK ? 2 * g.kgr : 2;
+                    const size_t grp0 = g.G <= KIVI_KBLK ? (size_t)kb * g.kgr : (size_t)kb / (g.G / KIVI_KBLK);
+                    const uint16_t *src = reinterpret_cast<const uint16_t *>(r + g.off_ksz);
+                    uint16_t *dst = reinterpret_cast<uint16_t *>((unsigned char *)Ksz + (slice * g.nkg + grp0) * rowsb);
+                    for (int row = 0; row < nrow; ++row)
+                        for (int ch = 0; ch < g.d; ++ch) dst[(size_t)row * g.d + ch] = src[(size_t)row * g.d + ksz_pos(g.d, ch)];
                 }
             }
     return KIVI_OK;

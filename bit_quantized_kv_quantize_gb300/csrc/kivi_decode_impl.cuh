@@ -212,21 +212,30 @@ __device__ __forceinline__ uint32_t unpack(uint32_t w, int r) {
 template <int BITS, bool KEY>
 __host__ __device__ constexpr float slot_offset(int r) { return view_of<BITS, KEY>(r).off; }
 
-// Value fields for the P.V contraction, centred: code - c0 with c0 =
-// (2^B - 1) / 2, exact in fp16.  The field is unpacked at a position whose
-// offset off is at most 64 (2-bit: the keys' positions 4, 6, 8; 4-bit:
-// position 4), so that off + c0 is itself an fp16 value and one HSUB2
-// leaves the exact centred code.  The value's midpoint z + c0 s goes into
-// the zero-point accumulator.  Centring keeps both accumulators near the
-// size of the output instead of near c0 s sum(p) (N(0, 1) values put the
-// group midpoints near 0), which is what bounds the fp32 accumulation error
-// at long contexts.
-__host__ __device__ constexpr View view_val(int bits, int r);
-// mantissa position p of a view (its magic constant's exponent field is 25 - p)
-__host__ __device__ constexpr int view_pos(int bits, int r) { return 25 - (int)((view_val(bits, r).magic >> 10) & 31u); }
+// Value fields for the P.V contraction: off + code as fp16 (2-bit fields
+// at mantissa positions 6 and 8, offsets 16 and 4; 4-bit at position 4,
+// offset 64), no subtraction per code.  The accumulator is kept centred
+// instead: at the end of each block every row loses (off + c0) times the
+// block's sum_t p_t s_t of its group (c0 = (2^B - 1) / 2; a small MMA over
+// the scale rows gives those sums), and the group midpoints z + c0 s go
+// into the zero-point accumulator.  So the accumulators hold the centred
+// sums sum p s (code - c0) and sum p (z + c0 s), both near the size of the
+// output (N(0, 1) values put the group midpoints near 0), rather than
+// c0 s sum(p): that is what bounds the fp32 accumulation error at long
+// contexts.  The offset lives in the accumulator for one block only; small
+// offsets keep that transient small.
 __host__ __device__ constexpr View view_val(int bits, int r) {
     if (bits == 4) return r == 0 ? at_pos(4, 4, 4, 0) : (r == 1 ? at_pos(4, 4, 0, 0) : at_pos(4, 4, 0, 4 * r - 4));
-    return view_of<2, true>(r);
+    switch (r) {   // 2-bit field bits [2r, 2r + 2) -> mantissa bits 6 or 8
+    case 0: return at_pos(6, 2, 6, 0);
+    case 1: return at_pos(8, 2, 6, 0);
+    case 2: return at_pos(6, 2, 2, 0);
+    case 3: return at_pos(6, 2, 0, 0);
+    case 4: return at_pos(8, 2, 0, 0);
+    case 5: return at_pos(6, 2, 0, 4);
+    case 6: return at_pos(8, 2, 0, 4);
+    default: return at_pos(8, 2, 0, 6);
+    }
 }
 template <int BITS, int R>
 __device__ __forceinline__ uint32_t unpack_val_t(uint32_t w) {
@@ -246,17 +255,6 @@ __device__ __forceinline__ uint32_t unpack_val_raw(uint32_t w, int r) {
     case 6: return unpack_val_t<BITS, (BITS == 2 ? 6 : 3)>(w);
     default: return unpack_val_t<BITS, (BITS == 2 ? 7 : 3)>(w);
     }
-}
-// off + c0 of value field r as an fp16 bit pattern in both halves: off =
-// 2^(10 - p) has exponent field 25 - p; c0 = (2^B - 1) / 2 adds mantissa
-// c0 * 2^(p) (exact: c0 < off and c0 has one fractional bit, p >= 2)
-__host__ __device__ constexpr uint32_t val_centre(int bits, int r) {
-    return (view_val(bits, r).magic & 0xFFFFu) + (uint32_t)(((1 << bits) - 1) << (view_pos(bits, r) - 1));
-}
-template <int BITS>
-__device__ __forceinline__ uint32_t unpack_val(uint32_t w, int r) {
-    const uint32_t c = val_centre(BITS, r) * 0x10001u;
-    return h2u(__hsub2(u2h(unpack_val_raw<BITS>(w, r)), u2h(c)));
 }
 
 
@@ -498,8 +496,10 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
     const int zkrow = gq & (nkrows - 1);
 #pragma unroll
     for (int jj = 0; jj < NJ; ++jj) {
-        const uint32_t a0 = *reinterpret_cast<const uint32_t *>(sKsz + zkrow * D + 16 * jj + 2 * tq);
-        const uint32_t a2 = *reinterpret_cast<const uint32_t *>(sKsz + zkrow * D + 16 * jj + 8 + 2 * tq);
+        // rows are lane-major: lane t's channels 16 jj + 2 t (+1) and
+        // 16 jj + 8 + 2 t (+1) are the four halves at t d/4 + 4 jj
+        const uint2 za = *reinterpret_cast<const uint2 *>(sKsz + zkrow * D + tq * (D / 4) + 4 * jj);
+        const uint32_t a0 = za.x, a2 = za.y;
         mma16816(dc, a0, 0u, a2, 0u, qB[jj][0], qB[jj][1]);
     }
     float kz[4], ks[4];
@@ -536,8 +536,8 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
         for (int rp = 0; rp < 4; ++rp) {
             b0[rp] = b1[rp] = 0u;
             if (rp > (3 >> sh)) continue;   // groups present in this block
-            const uint32_t s0 = *reinterpret_cast<const uint32_t *>(sKsz + 2 * rp * D + 16 * jj + 2 * tq);
-            const uint32_t s1 = *reinterpret_cast<const uint32_t *>(sKsz + 2 * rp * D + 16 * jj + 8 + 2 * tq);
+            const uint2 sv = *reinterpret_cast<const uint2 *>(sKsz + 2 * rp * D + tq * (D / 4) + 4 * jj);
+            const uint32_t s0 = sv.x, s1 = sv.y;
             b0[rp] = hfma2u(qB[jj][0], s0, hmul2u(qn0, s0));
             b1[rp] = hfma2u(qB[jj][1], s1, hmul2u(qn1, s1));
         }
@@ -600,7 +600,7 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
 
     // ---- weights times values, 16 tokens at a time ----
     // sacc: the block's sum_t p_t s_t per (value group, column), for the
-    // midpoint term at the end (rows = groups, like zacc)
+    // centring at the end (rows = groups, like zacc)
     float sacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
@@ -625,8 +625,9 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
         for (int gi = 0; gi < 16; ++gi) {
             b0[gi] = b1[gi] = 0u;
             if (gi >= ngi) continue;
-            const uint32_t v0 = *reinterpret_cast<const uint32_t *>(vszk + gi * 16 + 2 * tq);
-            const uint32_t v1 = *reinterpret_cast<const uint32_t *>(vszk + gi * 16 + 2 * tq + 8);
+            // rows are lane-major: tokens 2 t, 2 t + 1, 2 t + 8, 2 t + 9 at 4 t
+            const uint2 vv = *reinterpret_cast<const uint2 *>(vszk + gi * 16 + 4 * tq);
+            const uint32_t v0 = vv.x, v1 = vv.y;
             b0[gi] = hfma2u(PL0m, v0, hfma2u(PH0, v0, hmul2u(PH0n, v0)));
             b1[gi] = hfma2u(PL1m, v1, hfma2u(PH1, v1, hmul2u(PH1n, v1)));
         }
@@ -651,8 +652,8 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
             const int ci0 = 2 * mm;
             const int w = ci0 / CPHV, r0 = ci0 % CPHV;
             const uint32_t Wp0 = Wv[0 * NWV + w], Wp1 = Wv[1 * NWV + w];
-            const uint32_t a0 = unpack_val<VB>(Wp0, r0), a1 = unpack_val<VB>(Wp0, r0 + 1);
-            const uint32_t a2 = unpack_val<VB>(Wp1, r0), a3 = unpack_val<VB>(Wp1, r0 + 1);
+            const uint32_t a0 = unpack_val_raw<VB>(Wp0, r0), a1 = unpack_val_raw<VB>(Wp0, r0 + 1);
+            const uint32_t a2 = unpack_val_raw<VB>(Wp1, r0), a3 = unpack_val_raw<VB>(Wp1, r0 + 1);
             mma16816(A.oacc[mm], a0, a1, a2, a3, b0[mm >> sh], b1[mm >> sh]);
         }
         // value zero points and scales: rows [z or s][gi][16 tokens] (rows
@@ -661,23 +662,25 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
         const int zvrow = ngi >= 8 ? gq : (gq & (ngi - 1));
         {
             const __half *zrow = vszk + ngi * 16;
-            const uint32_t a0 = *reinterpret_cast<const uint32_t *>(zrow + zvrow * 16 + 2 * tq);
-            const uint32_t a2 = *reinterpret_cast<const uint32_t *>(zrow + zvrow * 16 + 2 * tq + 8);
+            const uint2 za = *reinterpret_cast<const uint2 *>(zrow + zvrow * 16 + 4 * tq);
+            const uint32_t a0 = za.x, a2 = za.y;
             uint32_t a1 = 0, a3 = 0;
             if (ngi > 8) {
-                a1 = *reinterpret_cast<const uint32_t *>(zrow + (gq + 8) * 16 + 2 * tq);
-                a3 = *reinterpret_cast<const uint32_t *>(zrow + (gq + 8) * 16 + 2 * tq + 8);
+                const uint2 zb = *reinterpret_cast<const uint2 *>(zrow + (gq + 8) * 16 + 4 * tq);
+                a1 = zb.x;
+                a3 = zb.y;
             }
             mma16816(A.zacc, a0, a1, a2, a3, bz0, bz1);
         }
         {
             const __half *srw = vszk;
-            const uint32_t a0 = *reinterpret_cast<const uint32_t *>(srw + zvrow * 16 + 2 * tq);
-            const uint32_t a2 = *reinterpret_cast<const uint32_t *>(srw + zvrow * 16 + 2 * tq + 8);
+            const uint2 sa = *reinterpret_cast<const uint2 *>(srw + zvrow * 16 + 4 * tq);
+            const uint32_t a0 = sa.x, a2 = sa.y;
             uint32_t a1 = 0, a3 = 0;
             if (ngi > 8) {
-                a1 = *reinterpret_cast<const uint32_t *>(srw + (gq + 8) * 16 + 2 * tq);
-                a3 = *reinterpret_cast<const uint32_t *>(srw + (gq + 8) * 16 + 2 * tq + 8);
+                const uint2 sb2 = *reinterpret_cast<const uint2 *>(srw + (gq + 8) * 16 + 4 * tq);
+                a1 = sb2.x;
+                a3 = sb2.y;
             }
             mma16816(sacc, a0, a1, a2, a3, bz0, bz1);
         }
@@ -696,9 +699,26 @@ __device__ __forceinline__ void do_block(WarpAcc<D> &A, const uint32_t (&qB)[D /
             }
         }
     }
-    // the values' midpoints: zacc += c0 * (the block's sum_t p_t s_t), row
-    // for row (both accumulators hold rows = groups)
+    // centre the accumulators: rows of m-tile mm are value fields r0 (row
+    // gq) and r0 + 1 (row gq + 8) of group mm >> sh; sacc row g holds that
+    // group's sum over the block (lane 4 g' + tq holds rows g' and g' + 8)
     constexpr float c0 = 0.5f * (float)((1 << VB) - 1);
+#pragma unroll
+    for (int gi = 0; gi < ngi; ++gi) {
+        const int src = (gi & 7) * 4 + tq;
+        const float s0 = __shfl_sync(0xffffffffu, gi < 8 ? sacc[0] : sacc[2], src);
+        const float s1 = __shfl_sync(0xffffffffu, gi < 8 ? sacc[1] : sacc[3], src);
+#pragma unroll
+        for (int mm = 0; mm < NJ; ++mm) {
+            if ((mm >> sh) != gi) continue;
+            const int r0 = (2 * mm) % CPHV;
+            const float f0 = view_val(VB, r0).off + c0, f1 = view_val(VB, r0 + 1).off + c0;
+            A.oacc[mm][0] = fmaf(-f0, s0, A.oacc[mm][0]);
+            A.oacc[mm][1] = fmaf(-f0, s1, A.oacc[mm][1]);
+            A.oacc[mm][2] = fmaf(-f1, s0, A.oacc[mm][2]);
+            A.oacc[mm][3] = fmaf(-f1, s1, A.oacc[mm][3]);
+        }
+    }
 #pragma unroll
     for (int k = 0; k < 4; ++k) A.zacc[k] = fmaf(c0, sacc[k], A.zacc[k]);
 }

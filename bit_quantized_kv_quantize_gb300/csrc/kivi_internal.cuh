@@ -16,6 +16,14 @@
 //   value scale/zero of the same   4 vsz_blk fp16
 // so the decode kernel fetches a block with one bulk copy.  With G = 128 a
 // key group spans two blocks and both records carry its rows.
+//
+// Inside a record the scale and zero rows are stored lane-major, so that
+// the decode kernel's lane t (t < 4) reads its values with one vector load:
+//   key row (d halves): channel c = 16 jj + 8 hh + 2 t + lo sits at
+//     position t (d / 4) + 4 jj + 2 hh + lo;
+//   value row (16 halves, one per token of a 16-token block): token
+//     tau = 2 t + 8 p + lo sits at position 4 t + 2 p + lo.
+// kivi_cache_export undoes the permutation (its arrays are in natural order).
 #pragma once
 
 #include <cuda_fp16.h>
@@ -136,26 +144,36 @@ __host__ __device__ __forceinline__ __half *vsz_halves(const KiviGeom &g, unsign
                                                        int vb) {
     return reinterpret_cast<__half *>(blk + rec_off(g, i, j, vb >> 2) + g.off_vsz) + (size_t)(vb & 3) * g.vsz_blk;
 }
+// position of channel c inside a key scale / zero row (lane-major, above)
+__host__ __device__ __forceinline__ int ksz_pos(int d, int c) {
+    return ((c >> 1) & 3) * (d >> 2) + ((c >> 4) << 2) + (((c >> 3) & 1) << 1) + (c & 1);
+}
+// position of token tau (mod 16) inside a value scale / zero row
+__host__ __device__ __forceinline__ int vsz_pos(int tau) {
+    return (((tau >> 1) & 3) << 2) + (((tau >> 3) & 1) << 1) + (tau & 1);
+}
 // scale (sz = 0) or zero (sz = 1) of key group grp, channel c: written to
 // every record that holds the group, read from the first
 __device__ __forceinline__ void ksz_store(const KiviGeom &g, unsigned char *blk, int i, int j, int grp, int c,
                                           __half s16, __half z16) {
+    const int pc = ksz_pos(g.d, c);
     if (g.G <= 64) {
         __half *r = ksz_rows(g, blk, i, j, grp / g.kgr) + (size_t)(grp % g.kgr) * 2 * g.d;
-        r[c] = s16;
-        r[g.d + c] = z16;
+        r[pc] = s16;
+        r[g.d + pc] = z16;
     } else {
         for (int k = 0; k < g.G / 64; ++k) {
             __half *r = ksz_rows(g, blk, i, j, grp * (g.G / 64) + k);
-            r[c] = s16;
-            r[g.d + c] = z16;
+            r[pc] = s16;
+            r[g.d + pc] = z16;
         }
     }
 }
 __device__ __forceinline__ __half ksz_load(const KiviGeom &g, unsigned char *blk, int i, int j, int grp, int c,
                                            int sz) {
-    if (g.G <= 64) return ksz_rows(g, blk, i, j, grp / g.kgr)[((size_t)(grp % g.kgr) * 2 + sz) * g.d + c];
-    return ksz_rows(g, blk, i, j, grp * (g.G / 64))[(size_t)sz * g.d + c];
+    const int pc = ksz_pos(g.d, c);
+    if (g.G <= 64) return ksz_rows(g, blk, i, j, grp / g.kgr)[((size_t)(grp % g.kgr) * 2 + sz) * g.d + pc];
+    return ksz_rows(g, blk, i, j, grp * (g.G / 64))[(size_t)sz * g.d + pc];
 }
 __host__ __device__ __forceinline__ size_t kf_slice(const KiviGeom &g, int i, int j) {
     return ((size_t)i * g.h + j) * (size_t)g.R * g.d;
@@ -212,7 +230,7 @@ __device__ __forceinline__ VWord vword_decode(int wb, int d, int vbits, int cs) 
 // fp16 scale (sz = 0) or zero (sz = 1) of value token tau, channel group gi,
 // within its value block's scale/zero halves
 __device__ __forceinline__ int vsz_in_block(const KiviGeom &g, int tau, int gi, int sz) {
-    return (sz * (g.d / g.G) + gi) * 16 + (tau & 15);
+    return (sz * (g.d / g.G) + gi) * 16 + vsz_pos(tau & 15);
 }
 
 // ---- the quantizer (item 1), bit-exact with IEEE fp32 ---------------------------

@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define KIVI_ABI_VERSION 5
+#define KIVI_ABI_VERSION 6
 
 typedef struct kivi_cache *kivi_cache_t;   /* opaque, library-owned */
 typedef struct CUstream_st *kivi_stream_t; /* the same type as cudaStream_t */
@@ -175,6 +175,10 @@ kivi_status kivi_cache_export(kivi_cache_t c, void *Kc, void *Ksz, void *Vc, voi
  *                                    rows of group kb/2, in both its records)
  *   Vc value blocks 4kb .. 4kb+3     4 (d v_bits / 2) words
  *   Vsz value blocks 4kb .. 4kb+3    4 [2][d/G][16] fp16
+ * except that inside a record every scale or zero row is stored lane-major:
+ * in a key row (d halves) channel c = 16 jj + 8 hh + 2 t + lo (t < 4,
+ * lo < 2) sits at position t d/4 + 4 jj + 2 hh + lo, and in a value row (16
+ * halves) token tau = 2 t + 8 p + lo sits at 4 t + 2 p + lo.
  * With records == NULL, writes the byte size of all records to *bytes.
  * Otherwise copies them into `records` (host or device memory, *bytes at
  * least that size; cudaMemcpyDefault), synchronizes `stream` and sets *bytes

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings_and_version(lib):
     lib.kivi_status_str.restype = ctypes.c_char_p
-    assert lib.kivi_abi_version() == 5
+    assert lib.kivi_abi_version() == 6
     for s in range(7):
         assert lib.kivi_status_str(s)
     assert lib.kivi_status_str(0) == b"ok"

@@ -245,8 +245,9 @@ def test_decode_is_read_only_and_repeatable():
 
 @pytest.mark.parametrize("G,kb,vb,d", [(32, 2, 2, 128), (16, 4, 2, 64), (64, 2, 4, 128), (128, 4, 4, 256)])
 def test_block_records_match_the_packed_arrays(G, kb, vb, d):
-    """The device's block records, split by the documented record layout,
-    equal the four packed arrays of kivi_cache_export."""
+    """The device's block records, split by the documented record layout
+    (scale and zero rows lane-major), equal the four packed arrays of
+    kivi_cache_export."""
     b, h, R, cap = 2, 2, max(G, 128), 800
     gpu = K.KiviCache(b, h, d, kb, vb, G, R, cap)
     rng = np.random.default_rng(G * 31 + kb)
@@ -266,8 +267,15 @@ def test_block_records_match_the_packed_arrays(G, kb, vb, d):
     o = np.cumsum([0] + sizes)
     Kc = rec[..., o[0]:o[1]].copy().view(np.uint32).reshape(-1)
     Vc = rec[..., o[2]:o[3]].copy().view(np.uint32).reshape(-1)
-    Vsz = rec[..., o[3]:o[4]].copy().view(np.uint16).reshape(-1)
-    rows = rec[..., o[1]:o[2]].copy().view(np.uint16).reshape(b, h, g["nkb"], kgr, 2, d)
+    # scale / zero rows are lane-major inside a record: value token
+    # tau = 2t + 8p + lo at 4t + 2p + lo, key channel c = 16jj + 8hh + 2t + lo
+    # at t d/4 + 4jj + 2hh + lo
+    tau = np.arange(16)
+    vpos = 4 * ((tau >> 1) & 3) + 2 * ((tau >> 3) & 1) + (tau & 1)
+    Vsz = rec[..., o[3]:o[4]].copy().view(np.uint16).reshape(-1, 16)[:, vpos].reshape(-1)
+    ch = np.arange(d)
+    kpos = ((ch >> 1) & 3) * (d // 4) + 4 * (ch >> 4) + 2 * ((ch >> 3) & 1) + (ch & 1)
+    rows = rec[..., o[1]:o[2]].copy().view(np.uint16).reshape(b, h, g["nkb"], kgr, 2, d)[..., kpos]
     if G <= 64:
         Ksz = rows.reshape(-1)
     else:   # both records of a group carry its rows
