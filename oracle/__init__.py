@@ -77,6 +77,7 @@ def lib():
             L.ko_decode_subset.argtypes = [vp, vp, ctypes.c_int, vp, vp, ctypes.c_int]
             L.ko_decode_probs.argtypes = [vp, vp, ctypes.c_int, vp, vp, ctypes.c_longlong, vp, ctypes.c_int]
             L.ko_set_threads.argtypes = [ctypes.c_int]
+            L.ko_prefill_attn.argtypes = [vp, vp, vp, vp] + [ctypes.c_int] * 5 + [vp, ctypes.c_int, vp]
             L.ko_lengths.argtypes = [vp, vp, vp, vp]
             L.ko_dequant_kv.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, vp]
             L.ko_state.argtypes = [vp] * 9
@@ -121,6 +122,31 @@ def dequant(code: int, s16: int, z16: int) -> float:
 
 def set_threads(n: int) -> int:
     return int(lib().ko_set_threads(int(n)))
+
+
+def prefill_attention(Q, K, V, t, rows=None) -> np.ndarray:
+    """Causal attention of the prompt's queries over its raw fp16 keys and
+    values, in double (ko_prefill_attn).  Q: fp16 [b, hq, ts, d]; K, V: fp16
+    [b, h, ts, d]; t: tokens per sequence.  Returns float64 [b, hq, ts, d]
+    with every row tau < t[i] (zeros elsewhere), or, given ``rows`` (an
+    [n, 3] array of (i, qh, tau)), float64 [n, d]: those rows."""
+    Q, K, V = _f16(Q), _f16(K), _f16(V)
+    b, hq, ts, d = Q.shape
+    h = K.shape[1]
+    assert K.shape == (b, h, ts, d) and V.shape == K.shape
+    t = np.ascontiguousarray(np.broadcast_to(np.asarray(t, np.int32), (b,)))
+    if rows is None:
+        rp, n = None, 0
+        out = np.zeros((b, hq, ts, d), np.float64)
+    else:
+        rows = np.ascontiguousarray(np.asarray(rows, np.int32).reshape(-1, 3))
+        rp, n = rows.ctypes.data, rows.shape[0]
+        out = np.zeros((n, d), np.float64)
+    rc = lib().ko_prefill_attn(Q.ctypes.data, K.ctypes.data, V.ctypes.data, t.ctypes.data, b, hq, h, ts, d,
+                               rp, n, out.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"ko_prefill_attn failed ({rc})")
+    return out
 
 
 def _f16(a) -> np.ndarray:

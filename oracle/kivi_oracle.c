@@ -460,6 +460,101 @@ int ko_decode_probs(const ko_cache *o, const uint16_t *q, int hq, float *out,
     return bad ? 2 : 0;
 }
 
+/* Causal attention of a prompt's queries over its own raw fp16 keys and
+ * values: the full-precision prefill attention of "Literature audit --
+ * Group 2", section 1 KIVI (its backends list runs the prefill's attention
+ * on the unquantized K/V), i.e. core-algorithm item 5's softmax(q K^T /
+ * sqrt(d)) V with keys s <= tau only.  In double.  Q: fp16 [b][hq][ts][d];
+ * K, V: fp16 [b][h][ts][d] (query head qh reads kv head qh / (hq / h)).
+ * With rows == NULL, out is double [b][hq][ts][d] and receives every row
+ * tau < t[i] (the others untouched); else out is double [nrows][d] and row
+ * k receives (i, qh, tau) = rows[3k..3k+2]. */
+static void prefill_row(const uint16_t *q, const uint16_t *K, const uint16_t *V, int tau, int d,
+                        double *p, double *outp)
+{
+    double rs = sqrt((double)d), m = -INFINITY;
+    for (int s = 0; s <= tau; ++s) {
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c)
+            dot += (double)ko_f16_to_f32(q[c]) * (double)ko_f16_to_f32(K[(size_t)s * d + c]);
+        p[s] = dot / rs;
+        if (p[s] > m) m = p[s];
+    }
+    double l = 0.0;
+    for (int s = 0; s <= tau; ++s) {
+        p[s] = exp(p[s] - m);
+        l += p[s];
+    }
+    for (int c = 0; c < d; ++c) {
+        double acc = 0.0;
+        for (int s = 0; s <= tau; ++s) acc += p[s] * (double)ko_f16_to_f32(V[(size_t)s * d + c]);
+        outp[c] = acc / l;
+    }
+}
+
+int ko_prefill_attn(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int *t, int b, int hq,
+                    int h, int ts, int d, const int *rows, int nrows, double *out)
+{
+    if (h < 1 || hq < h || hq % h != 0) return 1;
+    int maxt = 1;
+    for (int i = 0; i < b; ++i) {
+        if (t[i] < 0 || t[i] > ts) return 1;
+        if (t[i] > maxt) maxt = t[i];
+    }
+    /* the work: (i, qh, tau) triples */
+    long long n = 0;
+    int *all = NULL;
+    const int compact = rows != NULL;
+    if (!rows) {
+        for (int i = 0; i < b; ++i) n += (long long)hq * t[i];
+        all = (int *)malloc((size_t)(n > 0 ? n : 1) * 3 * sizeof(int));
+        if (!all) return 2;
+        long long k = 0;
+        for (int i = 0; i < b; ++i)
+            for (int qh = 0; qh < hq; ++qh)
+                for (int tau = 0; tau < t[i]; ++tau) {
+                    all[3 * k] = i;
+                    all[3 * k + 1] = qh;
+                    all[3 * k + 2] = tau;
+                    ++k;
+                }
+        rows = all;
+    } else {
+        n = nrows;
+    }
+    int nt = g_threads, bad = 0;
+    double **bufs = (double **)calloc((size_t)nt, sizeof(double *));
+    if (!bufs) {
+        free(all);
+        return 2;
+    }
+    for (int w = 0; w < nt; ++w) {
+        bufs[w] = (double *)malloc((size_t)maxt * sizeof(double));
+        if (!bufs[w]) bad = 1;
+    }
+    if (!bad) {
+        int grp = hq / h;
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 16)
+#endif
+        for (long long k = 0; k < n; ++k) {
+            int w = 0;
+#ifdef _OPENMP
+            w = omp_get_thread_num();
+#endif
+            int i = rows[3 * k], qh = rows[3 * k + 1], tau = rows[3 * k + 2];
+            if (i < 0 || i >= b || qh < 0 || qh >= hq || tau < 0 || tau >= t[i]) continue;
+            size_t kv = ((size_t)i * h + qh / grp) * ts * d;
+            size_t qo = (((size_t)i * hq + qh) * ts + tau) * d;
+            prefill_row(Q + qo, K + kv, V + kv, tau, d, bufs[w], out + (compact ? (size_t)k * d : qo));
+        }
+    }
+    for (int w = 0; w < nt; ++w) free(bufs[w]);
+    free(bufs);
+    free(all);
+    return bad ? 2 : 0;
+}
+
 /* Bulk conversions, for tests and input preparation. */
 void ko_f32_to_f16_n(const float *x, uint16_t *y, size_t n)
 {

@@ -38,6 +38,8 @@ int ko_decode_subset(const ko_cache *o, const uint16_t *q, int hq, float *out,
 int ko_decode_probs(const ko_cache *o, const uint16_t *q, int hq, float *out,
                     float *probs, long long ld, const int *pairs, int npairs);
 int ko_set_threads(int n);
+int ko_prefill_attn(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int *t, int b, int hq,
+                    int h, int ts, int d, const int *rows, int nrows, double *out);
 void ko_f32_to_f16_n(const float *x, uint16_t *y, size_t n);
 void ko_f16_to_f32_n(const uint16_t *x, float *y, size_t n);
 void ko_lengths(const ko_cache *o, int *T, int *Tqk, int *Tqv);

@@ -711,3 +711,80 @@ def test_threaded_decode_equals_serial():
     assert np.array_equal(p1.view(np.uint32), pn.view(np.uint32))
     assert np.array_equal(s1.view(np.uint32), sn.view(np.uint32))
     assert np.all(np.isfinite(o1)) and np.count_nonzero(o1) == o1.size
+
+
+# ---------------------------------------------------------------------------
+# Prefill attention (the full-precision causal attention of the prompt,
+# "Literature audit -- Group 2", section 1 KIVI, backends list; item 5's
+# formula with keys s <= tau).
+# ---------------------------------------------------------------------------
+
+def _prompt(rng, b, hq, h, ts, d, scale=1.0):
+    Q = (rng.standard_normal((b, hq, ts, d)) * scale).astype(np.float16)
+    K = (rng.standard_normal((b, h, ts, d)) * scale).astype(np.float16)
+    V = rng.standard_normal((b, h, ts, d)).astype(np.float16)
+    return Q, K, V
+
+
+def test_prefill_attention_first_row_and_equal_keys():
+    """Row 0 sees one key: it is v_0.  With every key equal the weights are
+    uniform: row tau is the mean of v_0 .. v_tau."""
+    rng = np.random.default_rng(21)
+    Q, K, V = _prompt(rng, 2, 4, 2, 40, 64)
+    t = [40, 17]
+    out = oracle.prefill_attention(Q, K, V, t)
+    for i in range(2):
+        for qh in range(4):
+            assert np.array_equal(out[i, qh, 0], V[i, qh // 2, 0].astype(np.float64))
+    Ke = np.broadcast_to(K[:, :, :1], K.shape).copy()
+    out = oracle.prefill_attention(Q, Ke, V, t)
+    for i in range(2):
+        for qh in range(4):
+            v = V[i, qh // 2].astype(np.float64)
+            mean = np.cumsum(v, axis=0) / np.arange(1, 41)[:, None]
+            np.testing.assert_allclose(out[i, qh, :t[i]], mean[:t[i]], rtol=1e-12, atol=1e-12)
+            assert not out[i, qh, t[i]:].any()   # rows past t untouched
+
+
+def test_prefill_attention_is_causal():
+    """Row tau depends on keys and values s <= tau only."""
+    rng = np.random.default_rng(22)
+    Q, K, V = _prompt(rng, 1, 2, 1, 50, 64)
+    a = oracle.prefill_attention(Q, K, V, [50])
+    K2, V2 = K.copy(), V.copy()
+    K2[:, :, 30:] = rng.standard_normal(K2[:, :, 30:].shape).astype(np.float16)
+    V2[:, :, 30:] = rng.standard_normal(V2[:, :, 30:].shape).astype(np.float16)
+    b = oracle.prefill_attention(Q, K2, V2, [50])
+    assert np.array_equal(a[:, :, :30], b[:, :, :30])
+    assert np.abs(a[:, :, 30:] - b[:, :, 30:]).max() > 1e-2
+
+
+def test_prefill_attention_last_row_equals_decode():
+    """The last prompt row attends to every key: it is the decode attention
+    of that query over an unquantized cache holding the prompt (the decode
+    routine, fp32, with its own scores and softmax)."""
+    rng = np.random.default_rng(23)
+    b, hq, h, t, d = 2, 8, 2, 100, 128
+    Q, K, V = _prompt(rng, b, hq, h, t, d, scale=2.0)
+    out = oracle.prefill_attention(Q, K, V, [t, t])
+    c = oracle.Cache(b, h, d, 2, 2, 32, 128, 256)   # t < R: nothing quantized
+    c.prefill(K, V, np.array([t, t], np.int32))
+    dec = c.decode(np.ascontiguousarray(Q[:, :, t - 1]))
+    np.testing.assert_allclose(dec, out[:, :, t - 1], rtol=2e-5, atol=2e-5)
+    c.close()
+
+
+def test_prefill_attention_gqa_and_rows():
+    """Query heads of one kv head equal an MHA problem with the kv head
+    repeated; a listed subset of rows equals the same rows of the full
+    computation."""
+    rng = np.random.default_rng(24)
+    Q, K, V = _prompt(rng, 2, 6, 2, 33, 64)
+    t = [33, 20]
+    g = oracle.prefill_attention(Q, K, V, t)
+    m = oracle.prefill_attention(Q, np.repeat(K, 3, axis=1), np.repeat(V, 3, axis=1), t)
+    assert np.array_equal(g, m)
+    rows = np.array([[0, 0, 0], [0, 5, 32], [1, 3, 19], [1, 2, 7]], np.int32)
+    s = oracle.prefill_attention(Q, K, V, t, rows=rows)
+    for k, (i, qh, tau) in enumerate(rows):
+        assert np.array_equal(s[k], g[i, qh, tau])
