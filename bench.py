@@ -1,10 +1,15 @@
 #!/usr/bin/env python3
 """Benchmark: KIVI quantized-KV decode step on one GB300.
 
-A step is one decode step of the whole cache: kivi_append (the lazy key-block
-flush / value-queue pop of the KIVI residual window, then the new token) and
-kivi_decode_attn (split-K attention over quantized + fp16 segments, merge).
-Prefill packing runs once before timing and is reported separately.
+A step is one decode step of the whole cache: one kivi_append_decode call --
+the append (the lazy key-block flush / value-queue pop of the KIVI residual
+window, then the new token) and the split-K attention over the quantized and
+fp16 segments with its merge.  Where it pays (see kivi.h) that is one launch
+of the decode kernel, which appends the token itself; otherwise the append
+kernel and the decode kernel.  --two times kivi_append + kivi_decode_attn,
+--probs the step with per-token attention weights.  Prefill packing runs
+once before timing and is reported separately; --prefill-attn times the
+prefill with its causal attention (kivi_prefill_attn) instead.
 
 Prints ONE JSON line.  Default workload: Llama-3-8B GQA layer shape at 32k
 context (batch 8, 32 query / 8 kv heads, d 128, 2-bit K/V, G 32, R 128).
@@ -288,7 +293,7 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 6),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "impl": "reference",
-        "config": workload_config(w),
+        "config": workload_config(w, step_mode(args)),
         "cpu_baseline": {"value": round(us, 3), "unit": "us/step", "cores": cores,
                          "kind": "oracle", "sample": sample, "cpu_model": cpu_model(),
                          "prefill_us": round(prefill_s * 1e6, 1)},
@@ -300,15 +305,16 @@ def run_reference(args, w):
     return 0
 
 
+EXTRA_LAUNCHES = {"two": 1, "fused": 0, "probs": 2}
 STEP_NAMES = {"two": "kivi_append + kivi_decode_attn", "fused": "kivi_append_decode",
               "probs": "kivi_append + kivi_decode_attn_probs (weights, accumulated mass)"}
 
 
 def step_mode(args) -> str:
-    return "probs" if getattr(args, "probs", False) else ("fused" if getattr(args, "fused", False) else "two")
+    return "probs" if getattr(args, "probs", False) else ("two" if getattr(args, "two", False) else "fused")
 
 
-def workload_config(w, mode="two"):
+def workload_config(w, mode="fused"):
     T = int(w.lengths().max()) + 1
     return {"workload": w.name,
             "step": STEP_NAMES[mode], "b": w.b, "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d,
@@ -338,15 +344,19 @@ def run_ours(args, w):
     Vd = torch.from_numpy(Vh).to(dev)
     del Kh, Vh
     stream = torch.cuda.current_stream(dev)
-    # prefill pack, timed once (after one untimed run)
+    # prefill pack: median of five timed runs after one untimed run (K and V
+    # are each larger than L2 at the long workloads)
     cache.prefill(Kd, Vd, lens)
     torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    cache.prefill(Kd, Vd, lens)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    prefill_ms = e0.elapsed_time(e1)
+    pre = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        cache.prefill(Kd, Vd, lens)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        pre.append(e0.elapsed_time(e1))
+    prefill_ms = statistics.median(pre)
     del Kd, Vd
     torch.cuda.empty_cache()
 
@@ -395,7 +405,7 @@ def run_ours(args, w):
     def timed(n0, profile):
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        nbytes = []
+        nbytes, nlaunch = [], []
         cache.profile(profile)
         cache.profile_read()
         barrier(dist, dev)
@@ -407,20 +417,23 @@ def run_ours(args, w):
             ends[n].record(stream)
             T, Tqk, Tqv = cache.lengths()
             nbytes.append(algorithmic_bytes(w, T, Tqk, Tqv, scores=mode == "probs"))
+            # the library's launches of the step's last call, plus the
+            # separate append call and the weights' finalizing kernel
+            nlaunch.append(cache.plan()[1] + EXTRA_LAUNCHES[mode])
         torch.cuda.synchronize(dev)
         barrier(dist, dev)
         prof = cache.profile_read()
         cache.profile(False)
-        return [a.elapsed_time(b) for a, b in zip(starts, ends)], nbytes, prof
+        return [a.elapsed_time(b) for a, b in zip(starts, ends)], nbytes, prof, nlaunch
 
     with ClockSampler(local) as clk:
-        step_ms, _, _ = timed(args.warmup, False)
-        inst_ms, bytes_steps, (attn_ms_total, attn_launches) = timed(args.warmup + args.steps, True)
+        step_ms, _, _, step_launches = timed(args.warmup, False)
+        inst_ms, bytes_steps, (attn_ms_total, attn_launches), _ = timed(args.warmup + args.steps, True)
     ms_per_step = reduce_max(sum(step_ms) / args.steps, dist, dev)
     ms_instrumented = reduce_max(sum(inst_ms) / args.steps, dist, dev)
     attn_ms = reduce_max(attn_ms_total / max(1, attn_launches), dist, dev)
     assert cache.check() == 0, "device status word set during the benchmark"
-    splits, launches = cache.plan()
+    splits = cache.plan()[0]
 
     # ---- end to end through the C ABI with host buffers ------------------
     pin_k = [torch.from_numpy(x).pin_memory() for x in host_k]
@@ -479,7 +492,7 @@ def run_ours(args, w):
                      "traffic": NCU_TRAFFIC.get(source_hash()) if mode != "probs" else None},
         "e2e": {"value": round(e2e_per * 1e3, 3), "unit": "us/step",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * (launches + {"two": 1, "fused": 1, "probs": 2}[mode]),
+        "gpu_launches": int(sum(step_launches)),
         "splits": splits,
         "clocks": clk.summary(),
         "source_hash": source_hash(),
@@ -497,11 +510,12 @@ def run_ours(args, w):
 
 def run_ncu_case(args, w):
     """Minimal launch sequence for profiler captures: prefill the workload,
-    append one token, then --steps decode calls (no flush buffer, no oracle)."""
+    append one token, then --steps decode calls (no flush buffer, no oracle);
+    with --fused, --steps kivi_append_decode calls instead."""
     import torch
     from bit_quantized_kv_quantize_gb300 import kivi as K
     dev = torch.device("cuda", 0)
-    cap = int(w.lengths().max()) + 8
+    cap = int(w.lengths().max()) + args.steps + 8
     cache = K.KiviCache(w.b, w.h_kv, w.d, w.kbits, w.vbits, w.G, w.R, cap)
     Kh, Vh, lens = W.prefill_kv(w)
     Kd, Vd = torch.from_numpy(Kh).to(dev), torch.from_numpy(Vh).to(dev)
@@ -514,13 +528,88 @@ def run_ncu_case(args, w):
     cache.append(torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev))
     q = torch.from_numpy(W.step_q(w, 0)).to(dev)
     out = torch.empty_like(q)
-    for _ in range(args.steps):
-        cache.decode(q, out)
+    for s in range(args.steps):
+        if args.fused:
+            k, v = W.step_kv(w, s + 1)
+            cache.append_decode(torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev), q, out)
+        else:
+            cache.decode(q, out)
     torch.cuda.synchronize(dev)
     assert cache.check() == 0
     T, Tqk, Tqv = cache.lengths()
     print(json.dumps({"ncu_case": w.name, "decode_calls": args.steps, "plan": cache.plan(),
                       "bytes_per_decode": algorithmic_bytes(w, T, Tqk, Tqv)}), flush=True)
+    cache.close()
+    return 0
+
+
+def prefill_attn_flops(w, lens) -> float:
+    """2 x the multiply-adds of the prompt's causal attention: q.k and p v,
+    d each, per query head and (row tau, key s <= tau) pair."""
+    pairs = sum(int(n) * (int(n) + 1) // 2 for n in lens)
+    return 4.0 * w.h_q * w.d * pairs
+
+
+def run_prefill_attn(args, w):
+    """kivi_prefill_attn (causal attention + the cache's quantize / pack in
+    its epilogue, one launch) on the workload's prompt, against kivi_prefill
+    (the pack kernels alone).  Inputs (K, V, Q: about 4 GB at 32k) exceed L2;
+    median of the timed calls."""
+    import torch
+    from bit_quantized_kv_quantize_gb300 import kivi as K
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    Kh, Vh, lens = W.prefill_kv(w)
+    Qh = W.prefill_q(w)
+    Kd, Vd, Qd = (torch.from_numpy(x).to(dev) for x in (Kh, Vh, Qh))
+    del Kh, Vh, Qh
+    out = torch.empty_like(Qd)
+    cache = K.KiviCache(w.b, w.h_kv, w.d, w.kbits, w.vbits, w.G, w.R, int(lens.max()) + 8)
+    stream = torch.cuda.current_stream(dev)
+    n = max(1, min(args.steps, 10))
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        ts = []
+        for _ in range(n):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts)
+
+    with ClockSampler(dev.index) as clk:
+        us = timed(lambda: cache.prefill_attn(Qd, Kd, Vd, lens, out=out))
+        pack_us = timed(lambda: cache.prefill(Kd, Vd, lens))
+    assert cache.check() == 0
+    flops = prefill_attn_flops(w, lens)
+    tf = flops / (us * 1e-6) / 1e12
+    peak = None
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        with open(pk) as f:
+            peak = json.load(f).get("bf16_tflops")
+    line = {
+        "metric": "causal prefill attention with the KIVI quantize/pack epilogue, us per call (1xGB300)",
+        "value": round(us, 1), "unit": "us/call", "n_gpus": 1, "steps": n, "warmup": args.warmup,
+        "higher_is_better": False, "vs_baseline": None, "dtype": "f16 in, f32 accumulate",
+        "data": "synthetic", "impl": "ours",
+        "config": {"workload": w.name, "call": "kivi_prefill_attn", "b": w.b, "h_q": w.h_q, "h_kv": w.h_kv,
+                   "d": w.d, "k_bits": w.kbits, "v_bits": w.vbits, "G": w.G, "R": w.R,
+                   "tokens": int(lens.max()), "l2": "inputs larger than L2"},
+        "pack_only_us": round(pack_us, 1),
+        "roofline": {"bound": "tensor", "achieved": round(tf, 1),
+                     "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tf / peak, 3) if peak else None,
+                     "peak_source": "measured bf16_tflops (the fp16 MMA rate is the same)" if peak else None,
+                     "flops_per_call": flops},
+        "gpu_launches": n,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
     cache.close()
     return 0
 
@@ -537,14 +626,17 @@ def main(argv=None):
     ap.add_argument("--group", type=int, choices=(16, 32, 64, 128), help="override the group size G")
     ap.add_argument("--residual", type=int, help="override the residual length R (a multiple of G)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--fused", action="store_true",
-                    help="time a step as one kivi_append_decode call instead of kivi_append + "
-                         "kivi_decode_attn")
+    ap.add_argument("--two", action="store_true",
+                    help="time a step as kivi_append + kivi_decode_attn instead of one "
+                         "kivi_append_decode call")
+    ap.add_argument("--fused", action="store_true", help="the default step (one kivi_append_decode call)")
     ap.add_argument("--probs", action="store_true",
                     help="time a step as kivi_append + kivi_decode_attn_probs (per-token weights "
                          "and their accumulated mass)")
     ap.add_argument("--ncu", action="store_true",
                     help="run only prefill, one append and --steps decode calls (profiler captures)")
+    ap.add_argument("--prefill-attn", action="store_true",
+                    help="time kivi_prefill_attn (causal attention + pack epilogue) against kivi_prefill")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -559,6 +651,8 @@ def main(argv=None):
         return run_reference(args, w)
     if args.ncu:
         return run_ncu_case(args, w)
+    if args.prefill_attn:
+        return run_prefill_attn(args, w)
     return run_ours(args, w)
 
 

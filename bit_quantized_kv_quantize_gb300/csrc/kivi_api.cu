@@ -7,6 +7,7 @@
 // caller's stream.
 #include <atomic>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -216,7 +217,7 @@ kivi_status launch_append(kivi_cache *c, const void *k, const void *v, kivi_stre
 // Plan and launch the decode kernel; units come from (T, Tqk, Tqv).
 kivi_status launch_decode(kivi_cache *c, const void *q, int h_q, void *out, kivi_stream_t stream,
                           const int *T, const int *Tqk, const int *Tqv, const char *what,
-                          const ProbsOut *po = nullptr) {
+                          const ProbsOut *po = nullptr, const FusedStep *fs = nullptr) {
     DecodeUnits units;
     DecodePlan plan = kivi_plan_decode(c->g, h_q, T, Tqk, Tqv, c->num_sms, &units);
     cudaEvent_t e0 = nullptr, e1 = nullptr;
@@ -237,9 +238,65 @@ kivi_status launch_decode(kivi_cache *c, const void *q, int h_q, void *out, kivi
     int maxT = 0;
     for (int i = 0; i < c->g.b; ++i) maxT = T[i] > maxT ? T[i] : maxT;
     cudaError_t e = kivi_launch_decode(c->g, c->dv, (const __half *)q, h_q, (__half *)out, plan, units,
-                                       (cudaStream_t)stream, e0, e1, po, maxT);
+                                       (cudaStream_t)stream, e0, e1, po, maxT, fs);
     if (e != cudaSuccess) return fail_cuda(c, e, what);
     c->last_plan = plan;
+    return KIVI_OK;
+}
+
+// Whether kivi_append_decode appends inside the decode launch.  The fused
+// kernel relies on one head group per kv head (h_q / h_kv <= 4: every
+// window block has a single reader CTA), and it pays only while the
+// (sequence, kv head) pairs do not outnumber the persistent CTAs: each
+// pair's append is a short serial task on one CTA, where the append kernel
+// runs them all at once (measured on GB300: one launch saves 2-5 us per
+// step with 8-64 pairs, and costs 5-10 us with 512).  KIVI_FUSED_STEP=0
+// keeps the two launches, =1 forces the fused one where it is possible.
+bool fused_step(const kivi_cache *c, int h_q) {
+    if (h_q / c->g.h > 4) return false;
+    const char *e = getenv("KIVI_FUSED_STEP");
+    if (e && e[0] == '0' && e[1] == 0) return false;
+    if (e && e[0] == '1' && e[1] == 0) return true;
+    return (long)c->g.b * c->g.h <= 2L * c->num_sms;
+}
+
+// One step as one launch: the decode kernel appends every sequence whose
+// key window is not full (item 4: the new token and at most one popped
+// value token); sequences that flush their key window now are appended
+// first by the append kernel, restricted to them (a second launch on those
+// steps only).  The units count an appended sequence's value queue before
+// its pop.  Both kernels write the counters after the append into the
+// other set, which then becomes current.
+kivi_status launch_fused_step(kivi_cache *c, const void *k, const void *v, const void *q, int h_q, void *out,
+                              kivi_stream_t stream) {
+    const int b = c->g.b, R = c->g.R;
+    std::vector<int> Tp(b), Tqkp(b), Tqvp(b);
+    bool any_flush = false;
+    for (int i = 0; i < b; ++i) {
+        const bool flush = c->T[i] - c->Tqk[i] == R, pop = c->T[i] - c->Tqv[i] == R + 1;
+        Tp[i] = c->T[i] + 1;
+        Tqkp[i] = c->Tqk[i] + (flush ? R : 0);
+        Tqvp[i] = c->Tqv[i] + (flush && pop ? 1 : 0);
+        any_flush |= flush;
+    }
+    int *nxt = c->cnt + (size_t)(1 - c->parity) * 3 * b;
+    if (any_flush) {
+        AppendCounters ac;   // entries past b are never read
+        memcpy(ac.T, c->T.data(), (size_t)b * sizeof(int));
+        memcpy(ac.Tqk, c->Tqk.data(), (size_t)b * sizeof(int));
+        memcpy(ac.Tqv, c->Tqv.data(), (size_t)b * sizeof(int));
+        cudaError_t e = kivi_launch_append(c->g, c->dv, (const __half *)k, (const __half *)v, ac, nxt,
+                                           (cudaStream_t)stream, true);
+        if (e != cudaSuccess) return fail_cuda(c, e, "append_decode");
+    }
+    const FusedStep fs{(const __half *)k, (const __half *)v, nxt};
+    kivi_status s = launch_decode(c, q, h_q, out, stream, Tp.data(), Tqkp.data(), Tqvp.data(), "append_decode",
+                                  nullptr, &fs);
+    if (s != KIVI_OK) return s;
+    c->last_plan.launches += any_flush ? 1 : 0;
+    c->parity ^= 1;
+    point_counters(c);
+    advance_mirror(c);
     return KIVI_OK;
 }
 
@@ -408,6 +465,56 @@ kivi_status kivi_prefill(kivi_cache_t c, const void *K, const void *V, const int
     return KIVI_OK;
 }
 
+kivi_status kivi_prefill_attn(kivi_cache_t c, const void *q, const void *K, const void *V, const int32_t *t,
+                              int t_stride, int h_q, void *out, kivi_stream_t stream) {
+    g_err[0] = 0;
+    kivi_status s = check_handle(c);
+    if (s != KIVI_OK) return s;
+    if (c->g.G > 64 || (c->g.d != 64 && c->g.d != 128)) {
+        set_err("prefill attention supports d 64 or 128 and G <= 64");
+        return KIVI_ERR_UNSUPPORTED;
+    }
+    if (h_q < c->g.h || h_q % c->g.h != 0 || h_q / c->g.h > KIVI_MAX_QPERKV) {
+        set_err("h_q must be a multiple of h_kv, at most %s%ld times it", "", KIVI_MAX_QPERKV);
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (!t || t_stride < 0) {
+        set_err("t is null or t_stride negative");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    SeqLens lens;
+    int maxt = 0;
+    for (int i = 0; i < c->g.b; ++i) {
+        if (t[i] < 0 || t[i] > t_stride) {
+            set_err("t[i] outside [0, t_stride] for i = %s%ld", "", i);
+            return KIVI_ERR_INVALID_ARG;
+        }
+        if (t[i] > c->max_tokens) {
+            set_err("t[i] above max_tokens for i = %s%ld", "", i);
+            return KIVI_ERR_CAPACITY;
+        }
+        lens.t[i] = t[i];
+        maxt = t[i] > maxt ? t[i] : maxt;
+    }
+    if (maxt > 0 && (!q || !K || !V || !out)) {
+        set_err("q, K, V or out is null");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    if (maxt > 0 && (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out))) {
+        set_err("q, K, V and out must be 16-byte aligned");
+        return KIVI_ERR_INVALID_ARG;
+    }
+    cudaError_t e = kivi_launch_prefill_attn(c->g, c->dv, (const __half *)q, (const __half *)K, (const __half *)V,
+                                             (__half *)out, lens, t_stride, h_q, (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail_cuda(c, e, "prefill_attn");
+    for (int i = 0; i < c->g.b; ++i) {
+        c->T[i] = t[i];
+        c->Tqk[i] = t[i] - t[i] % c->g.R;
+        c->Tqv[i] = t[i] > c->g.R ? t[i] - c->g.R : 0;
+    }
+    return KIVI_OK;
+}
+
 kivi_status kivi_append(kivi_cache_t c, const void *k, const void *v, kivi_stream_t stream) {
     g_err[0] = 0;
     kivi_status s = check_handle(c);
@@ -462,9 +569,12 @@ kivi_status kivi_append_decode(kivi_cache_t c, const void *k, const void *v, con
     if (s != KIVI_OK) return s;
     s = check_decode_args(c, q, h_q, out);
     if (s != KIVI_OK) return s;
+    if (fused_step(c, h_q)) return launch_fused_step(c, k, v, q, h_q, out, stream);
     s = launch_append(c, k, v, stream, "append_decode");
     if (s != KIVI_OK) return s;
-    return launch_decode(c, q, h_q, out, stream, c->T.data(), c->Tqk.data(), c->Tqv.data(), "append_decode");
+    s = launch_decode(c, q, h_q, out, stream, c->T.data(), c->Tqk.data(), c->Tqv.data(), "append_decode");
+    if (s == KIVI_OK) c->last_plan.launches += 1;
+    return s;
 }
 
 kivi_status kivi_cache_lengths(kivi_cache_t c, int32_t *T, int32_t *Tqk, int32_t *Tqv) {

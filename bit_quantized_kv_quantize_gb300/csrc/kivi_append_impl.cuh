@@ -11,13 +11,6 @@
 #pragma once
 #include "kivi_internal.cuh"
 
-// Counters of one sequence before an append are in range.
-__device__ __forceinline__ bool append_counters_ok(const KiviGeom &g, int T, int Tqk, int Tqv) {
-    const int R = g.R;
-    return T >= 0 && T < g.fcap && Tqk >= 0 && Tqk % R == 0 && T - Tqk >= 0 && T - Tqk <= R && Tqv >= 0 &&
-           T - Tqv >= 0 && T - Tqv <= R + 1;
-}
-
 // Append the token (knew, vnew: fp16 [b][h][d]) to slice (i, j) whose
 // counters are T, Tqk, Tqv (in range).  Called by every thread of a CTA (any
 // block size); the counters themselves are left to the caller.

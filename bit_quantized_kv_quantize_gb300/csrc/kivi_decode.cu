@@ -20,6 +20,12 @@ cudaError_t kivi_launch_decode_d128(const KiviGeom &, const KiviDev &, const __h
                                     const DecodePlan &, const DecodeUnits &, cudaStream_t);
 cudaError_t kivi_launch_decode_d256(const KiviGeom &, const KiviDev &, const __half *, int, __half *,
                                     const DecodePlan &, const DecodeUnits &, cudaStream_t);
+cudaError_t kivi_launch_decode_fused_d64(const KiviGeom &, const KiviDev &, const __half *, int, __half *,
+                                         const DecodePlan &, const DecodeUnits &, const FusedStep &, cudaStream_t);
+cudaError_t kivi_launch_decode_fused_d128(const KiviGeom &, const KiviDev &, const __half *, int, __half *,
+                                          const DecodePlan &, const DecodeUnits &, const FusedStep &, cudaStream_t);
+cudaError_t kivi_launch_decode_fused_d256(const KiviGeom &, const KiviDev &, const __half *, int, __half *,
+                                          const DecodePlan &, const DecodeUnits &, const FusedStep &, cudaStream_t);
 cudaError_t kivi_launch_decode_probs_d64(const KiviGeom &, const KiviDev &, const __half *, int, __half *,
                                          const DecodePlan &, const DecodeUnits &, const ProbsOut &,
                                          cudaStream_t);
@@ -110,10 +116,17 @@ DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *T, const int *
 cudaError_t kivi_launch_decode(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq,
                                __half *out, const DecodePlan &plan, const DecodeUnits &units,
                                cudaStream_t st, cudaEvent_t ev0, cudaEvent_t ev1, const ProbsOut *po,
-                               int maxT) {
+                               int maxT, const FusedStep *fs) {
+    if (po && fs) return cudaErrorInvalidValue;
     if (ev0) cudaEventRecord(ev0, st);
     cudaError_t e;
-    if (po) {
+    if (fs) {
+        switch (g.d) {
+        case 64: e = kivi_launch_decode_fused_d64(g, dv, q, hq, out, plan, units, *fs, st); break;
+        case 128: e = kivi_launch_decode_fused_d128(g, dv, q, hq, out, plan, units, *fs, st); break;
+        default: e = kivi_launch_decode_fused_d256(g, dv, q, hq, out, plan, units, *fs, st); break;
+        }
+    } else if (po) {
         switch (g.d) {
         case 64: e = kivi_launch_decode_probs_d64(g, dv, q, hq, out, plan, units, *po, st); break;
         case 128: e = kivi_launch_decode_probs_d128(g, dv, q, hq, out, plan, units, *po, st); break;

@@ -30,6 +30,7 @@
 // with log-sum-exp weights and writes the fp16 output.
 #pragma once
 #include "kivi_internal.cuh"
+#include "kivi_mma.cuh"
 
 namespace {
 
@@ -39,10 +40,6 @@ constexpr int kMaxWaitIters = 1 << 24;   // bounded mbarrier waits
 // ---------------------------------------------------------------------------
 // PTX helpers
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ unsigned smem_u32(const void *p) {
-    return (unsigned)__cvta_generic_to_shared(p);
-}
-
 __device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
@@ -109,28 +106,12 @@ __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, unsign
         : "memory");
 }
 
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
     return r;
 }
 
-__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
-__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
 __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) { return h2u(__hmul2(u2h(a), u2h(b))); }
 __device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
@@ -287,9 +268,10 @@ __host__ __device__ __forceinline__ size_t warp_region(const KiviGeom &g, int st
     size_t m = ring > res ? ring : res;
     return (m + 127) / 128 * 128;
 }
-// the warps' ring barriers and the CTA's mixed-block barrier
+// the warps' ring barriers, the CTA's mixed-block barrier and the fused
+// append's
 __host__ __device__ __forceinline__ size_t bar_region(int warps, int stages) {
-    return ((size_t)(warps * stages + 1) * 8 + 127) / 128 * 128;
+    return ((size_t)(warps * stages + 2) * 8 + 127) / 128 * 128;
 }
 // bytes a mixed block stages in the ring: its record, up to 64 key and 64
 // value rows of 2 d bytes, and a zero row
@@ -311,6 +293,109 @@ __device__ __forceinline__ void copy_rows(unsigned char *dst, const __half *win,
     const int n1 = min(n, ring - r0);
     bulk_g2s(dst, win + (size_t)r0 * D, (unsigned)n1 * D * 2, bar);
     if (n > n1) bulk_g2s(dst + (size_t)n1 * D * 2, win, (unsigned)(n - n1) * D * 2, bar);
+}
+
+// ---------------------------------------------------------------------------
+// The append of one (sequence, kv head) pair inside a decode launch (item
+// 4's one-token maintenance), by one warp of the CTA that owns the pair's
+// append.  rows: [3][D] fp16 in shared memory, filled by bulk copies the
+// warp issued at the start of the segment on fbar: the value token leaving
+// the queue (row 0, when pop), the new key and the new value.  When the
+// value queue is full its oldest token Tqv0 is quantized per token (item 3:
+// groups of G channels) into the record of its block with the append
+// kernel's arithmetic (qparams, qcode), a token opening a 16-token value
+// block first clearing that block; the new rows go to their window slots
+// (T0 mod R, T0 mod (R + 1): the latter the popped token's slot), and the
+// sequence's counters after the append to nxt (kv head 0).  Out of line:
+// it runs once per pair and stays off the streaming loop's registers.
+// The global writes are ordered before the launch's later bulk copies of
+// the record by a proxy fence here and the barrier before those copies.
+// ---------------------------------------------------------------------------
+template <int D, int KB, int VB, int SH>
+__device__ __noinline__ void fused_append_pair(const KiviGeom &g, const KiviDev &dv, const FusedStep &fs, int i,
+                                               int j, int T0, int Tqk, int Tqv0, bool pop, __half *rows,
+                                               uint64_t *fbar, unsigned phase) {
+    using RG = Rec<D, KB, VB, SH>;
+    constexpr int G = 16 << SH, NGI = D / G, M = D / 32;
+    constexpr int CPH = 16 / VB, NWV = D * VB / 128, WL = D * VB / 64, CS = WL < 4 ? WL : 4;
+    const int lane = threadIdx.x & 31;
+    if (!__all_sync(0xffffffffu, mbar_wait(fbar, phase))) {
+        if (lane == 0) atomicOr(dv.status, KIVI_FLAG_WAIT);
+        mbar_wait(fbar, phase);   // bounded: let the copies land before the rows are reused
+        return;
+    }
+    __half *vwin = dv.Vf + vf_slice(g, i, j);
+    if (pop) {
+        const __half *x = rows;
+        unsigned char *sc = reinterpret_cast<unsigned char *>(rows);   // the popped row, once read
+        const int tt = Tqv0 % KIVI_KBLK, vbl = tt >> 4, t16 = tt & 15;
+        unsigned char *grec = dv.blk + rec_off(g, i, j, Tqv0 / KIVI_KBLK);
+        uint32_t *vc = reinterpret_cast<uint32_t *>(grec + RG::OFF_VC) + (size_t)vbl * RG::VC_BLK;
+        __half *vsz = reinterpret_cast<__half *>(grec + RG::OFF_VSZ) + (size_t)vbl * RG::VSZ_BLK;
+        float v[M], mn[M], mx[M];
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            v[m] = __half2float(x[lane + 32 * m]);
+            mn[m] = mx[m] = v[m];
+        }
+        // group minima and maxima (exact in any order): over the lanes of
+        // a group, then over the 32-channel chunks a group spans
+#pragma unroll
+        for (int m = 0; m < M; ++m)
+#pragma unroll
+            for (int o = 1; o < (G < 32 ? G : 32); o <<= 1) {
+                mn[m] = fminf(mn[m], __shfl_xor_sync(0xffffffffu, mn[m], o));
+                mx[m] = fmaxf(mx[m], __shfl_xor_sync(0xffffffffu, mx[m], o));
+            }
+        if (t16 == 0) {   // a fresh value block
+            for (int e = lane; e < RG::VC_BLK; e += 32) vc[e] = 0u;
+            for (int e = lane; e < RG::VSZ_BLK / 2; e += 32) reinterpret_cast<uint32_t *>(vsz)[e] = 0u;
+        }
+        __syncwarp();   // the block is cleared and every lane has read its channels
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            float gmn = mn[m], gmx = mx[m];
+#pragma unroll
+            for (int m2 = 0; m2 < M; ++m2)
+                if (G > 32 && m2 != m && (32 * m2) / G == (32 * m) / G) {
+                    gmn = fminf(gmn, mn[m2]);
+                    gmx = fmaxf(gmx, mx[m2]);
+                }
+            const QParams p = qparams(gmn, gmx, VB);
+            sc[lane + 32 * m] = (unsigned char)qcode(v[m], p.sf, p.zf, VB);
+            const int c = lane + 32 * m;
+            if (c % G == 0) {   // the group's first channel writes its scale and zero
+                const int gi = c / G, ps = vsz_pos(t16);
+                vsz[gi * 16 + ps] = p.s16;
+                vsz[(NGI + gi) * 16 + ps] = p.z16;
+            }
+        }
+        __syncwarp();
+        // the token's 16-bit halves: channel class gg (8) x channel word w
+        const int p8 = t16 >> 3, tq = (t16 & 7) >> 1, half = t16 & 1;
+        for (int e = lane; e < 8 * NWV; e += 32) {
+            const int gg = e / NWV, w = e - gg * NWV;
+            uint32_t bits = 0;
+#pragma unroll
+            for (int r = 0; r < CPH; ++r) bits |= (uint32_t)sc[8 * (w * CPH + r) + gg] << (r * VB);
+            const int L = 4 * gg + tq, u = p8 * NWV + w;
+            reinterpret_cast<uint16_t *>(vc + (size_t)(u / CS) * 32 * CS + (size_t)L * CS + (u % CS))[half] =
+                (uint16_t)bits;
+        }
+    }
+    for (int e = lane; e < D / 4; e += 32) {
+        const bool isv = e >= D / 8;
+        const int c8 = isv ? e - D / 8 : e;
+        __half *dst = isv ? vwin + (size_t)(T0 % (g.R + 1)) * D : dv.Kf + kf_slice(g, i, j) + (size_t)(T0 % g.R) * D;
+        reinterpret_cast<uint4 *>(dst)[c8] = reinterpret_cast<const uint4 *>(rows + (isv ? 2 : 1) * D)[c8];
+    }
+    if (j == 0 && lane == 0) {
+        fs.nxt[i] = T0 + 1;
+        fs.nxt[g.b + i] = Tqk;
+        fs.nxt[2 * g.b + i] = Tqv0 + (pop ? 1 : 0);
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
 }
 
 // Stage block kb: one bulk copy of its record (packed keys, key scale/zero
@@ -341,16 +426,6 @@ __device__ __forceinline__ void prefetch_rows(const __half *win, int ring, int a
     if (n > n1) prefetch_l2(win, (unsigned)(n - n1) * D * 2, policy);
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(smem_u32(p)));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *p) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(smem_u32(p)));
-}
 
 // ---------------------------------------------------------------------------
 // Per-warp running state of one (sequence, kv head, head group) segment.
@@ -771,10 +846,10 @@ __host__ __device__ __forceinline__ long long cta_of_unit(long long u, long long
     return ((u + 1) * C - 1) / U;
 }
 
-template <int D, int KB, int VB, int SH, bool PROBS>
+template <int D, int KB, int VB, int SH, bool PROBS, bool FUSED>
 __global__ void __launch_bounds__(256, 2)
     decode_kernel(KiviGeom g, KiviDev dv, const __half *__restrict__ q, int hq,
-                  __half *__restrict__ out, DecodePlan plan, DecodeUnits units, ProbsOut po) {
+                  __half *__restrict__ out, DecodePlan plan, DecodeUnits units, ProbsOut po, FusedStep fs) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int NJ = D / 16;
     const int nw = blockDim.x >> 5;
@@ -793,14 +868,17 @@ __global__ void __launch_bounds__(256, 2)
     const int C = gridDim.x, c = blockIdx.x;
     long long u = (long long)c * U / C;
     const long long u_end = (long long)(c + 1) * U / C;
-    __shared__ int s_seg[5];
+    __shared__ int s_seg[9];   // i, jq, o0, o1, Wi; T, Tqk, Tqv (after the append); fused flags
     __shared__ int s_last;
     __shared__ float sML[8];    // per head: max over the warps (or partials), then the weighted sum of l
     __shared__ float sWt[32];   // [warp][head]: the warp's weight
+    __shared__ __align__(16) __half s_frows[FUSED ? 3 * D : 8];   // the fused append's rows
+    __shared__ unsigned s_fphase;                                 // ... and the phase of their barrier
     // The barriers live for the whole kernel: a warp's n-th block (counted
     // across all its segments) goes to slot n % stages and completes phase
     // n / stages of that slot's barrier.
-    if (threadIdx.x <= nw * plan.stages) mbar_init(bars + threadIdx.x, 1);
+    if (threadIdx.x <= nw * plan.stages + 1) mbar_init(bars + threadIdx.x, 1);
+    if (threadIdx.x == 0) s_fphase = 0u;
     fence_mbar_init();
     __syncthreads();
     // The kernel is launched as a programmatic dependent of the one before
@@ -815,6 +893,7 @@ __global__ void __launch_bounds__(256, 2)
     bool dead = false;     // a wait of this warp timed out: it streams no more blocks
     bool cdead = false;   // a wait of the CTA's mixed-block barrier timed out
     uint64_t *cbar = bars + nw * plan.stages;   // the CTA's mixed-block barrier
+    uint64_t *fbar = cbar + 1;                   // the fused append's rows
     unsigned cphase = 0;
     const uint64_t pol_stream = policy_evict_first();
     // mixed blocks staged per round: as many regions as the ring holds (<= 2)
@@ -835,6 +914,28 @@ __global__ void __launch_bounds__(256, 2)
             s_seg[2] = (int)(rem % Wi);
             s_seg[3] = (int)min((long long)Wi, rem % Wi + (u_end - u));
             s_seg[4] = Wi;
+            // Counters.  FUSED: the device holds them before this step's
+            // append; a sequence whose key window is not full is appended by
+            // this launch (flag 1; flag 2: its value queue's oldest token
+            // pops), the others were appended by the launch before (the
+            // counters after the append follow from item 4's schedule
+            // either way).
+            int T = dv.T[lo], Tqk = dv.Tqk[lo], Tqv = dv.Tqv[lo], fl = 0;
+            if constexpr (FUSED) {
+                if (append_counters_ok(g, T, Tqk, Tqv)) {
+                    const bool pop = T - Tqv == g.R + 1, app = T - Tqk != g.R;
+                    fl = (app ? 1 : 0) | (pop ? 2 : 0);
+                    if (!app) Tqk += g.R;
+                    Tqv += pop ? 1 : 0;
+                    T += 1;
+                } else {
+                    atomicOr(dv.status, KIVI_FLAG_COUNTER);
+                }
+            }
+            s_seg[5] = T;
+            s_seg[6] = Tqk;
+            s_seg[7] = Tqv;
+            s_seg[8] = fl;
         }
         // the rings were last written and read by generic stores and loads
         // (the previous segment's merge): order them before the async copies
@@ -843,8 +944,12 @@ __global__ void __launch_bounds__(256, 2)
         const int i = s_seg[0], jq = s_seg[1], o0 = s_seg[2], o1 = s_seg[3], Wi = s_seg[4];
         const int j = jq / QG, qg = jq % QG;
         const int e0 = qg * 4, nh = min(4, hg - e0);
-        const int T = dv.T[i], Tqk = dv.Tqk[i], Tqv = dv.Tqv[i];
-        const int nfull = min(Tqk, Tqv) / KIVI_KBLK;
+        const int T = s_seg[5], Tqk = s_seg[6], Tqv = s_seg[7];
+        const bool app = FUSED && (s_seg[8] & 1), pop = FUSED && (s_seg[8] & 2);
+        const int Tqv0 = pop ? Tqv - 1 : Tqv;   // the value queue before this launch's pop
+        // an appending sequence stages the popped token's block as a window
+        // block: it counts its value queue before the pop
+        const int nfull = min(Tqk, app ? Tqv0 : Tqv) / KIVI_KBLK;
         const int nblk = (T + KIVI_KBLK - 1) / KIVI_KBLK;
         const int nfh = units.full[i];
         const int MW = units.mixed_weight;
@@ -920,6 +1025,32 @@ __global__ void __launch_bounds__(256, 2)
             ++issued;
         };
         while (more && issued < plan.stages) take_and_issue();
+        // FUSED: the pair's append is done by the CTA holding, in this
+        // segment, the block its maintenance touches (the popped value
+        // token's, else the new token's), with its last warp, while that
+        // warp's first ring copies are in flight: the rows it needs are
+        // bulk-copied, then fused_append_pair.  No other CTA of the launch
+        // reads what it writes (the popped token's record fields, which this
+        // CTA stages afterwards; the window slots the new token takes, which
+        // every CTA skips).
+        if constexpr (FUSED) {
+            if (app && qg == 0 && warp == nw - 1) {
+                const int ob = (pop ? Tqv0 : T - 1) / KIVI_KBLK;
+                const int xo = first_at_least(ob);
+                if (xo >= xm && xo < nD && blk(xo) == ob) {
+                    if (lane == 0) {
+                        const size_t kv_off = ((size_t)i * g.h + j) * D;
+                        mbar_expect_tx(fbar, (pop ? 3u : 2u) * 2 * D);
+                        if (pop) bulk_g2s(s_frows, vwin + (size_t)(Tqv0 % (g.R + 1)) * D, 2 * D, fbar);
+                        bulk_g2s(s_frows + D, fs.k + kv_off, 2 * D, fbar);
+                        bulk_g2s(s_frows + 2 * D, fs.v + kv_off, 2 * D, fbar);
+                    }
+                    fused_append_pair<D, KB, VB, SH>(g, dv, fs, i, j, T - 1, Tqk, Tqv0, pop, s_frows, fbar, s_fphase);
+                    if (lane == 0) s_fphase ^= 1u;
+                    __syncwarp();
+                }
+            }
+        }
         __syncwarp();
         MixCtx mc;   // unused by the packed path
         bool timed_out = false;
@@ -960,7 +1091,13 @@ __global__ void __launch_bounds__(256, 2)
         // of the round's block k goes to warp (4 k + t) mod nw).  The rows
         // are not padded: the tiles' ldmatrix reads conflict on banks, a
         // small cost next to more copies.
+        // Row r of a block's key (value) rows is token tb + r.  An appending
+        // sequence's new token T0 is not read from the windows (its slots
+        // are being written by the pair's owner): its key and value rows
+        // are copied from the step's inputs with the round's other copies.
         const int RS = 2 * D;
+        // the new token T0 = T - 1 if appended here (else none: T)
+        const int tnew = (FUSED && (s_seg[8] & 1)) ? T - 1 : T;
         for (int x0 = xm; x0 < nD && !cdead; x0 += mper) {
             const int nrb = min(mper, nD - x0);
             fence_proxy_async();   // earlier generic reads and writes of the ring
@@ -968,17 +1105,26 @@ __global__ void __launch_bounds__(256, 2)
             if (warp == 0) {
                 unsigned bytes = 0;
                 for (int k = 0; k < nrb; ++k) {
-                    const int kb = blk(x0 + k), tb = kb * KIVI_KBLK, te = min(tb + KIVI_KBLK, T);
+                    const int kb = blk(x0 + k), tb = kb * KIVI_KBLK, te = min(tb + KIVI_KBLK, tnew);
                     bytes += RG::BYTES + (rows_to_stage(max(tb, Tqk), te, g.R) +
                                          rows_to_stage(max(tb, Tqv), te, g.R + 1)) * 2 * D;
+                    if (tnew < T && tnew >= tb && tnew < tb + KIVI_KBLK) bytes += 4 * D;
                 }
                 if (lane == 0) mbar_expect_tx(cbar, bytes);
                 for (int k = 0; k < nrb && lane == 0; ++k) {
-                    const int kb = blk(x0 + k), tb = kb * KIVI_KBLK, te = min(tb + KIVI_KBLK, T);
+                    const int kb = blk(x0 + k), tb = kb * KIVI_KBLK, te = min(tb + KIVI_KBLK, tnew);
                     unsigned char *reg = ring + (size_t)k * mreg;
+                    const int ka = max(tb, Tqk), va = max(tb, Tqv);
                     bulk_g2s(reg, recs + (size_t)kb * RG::BYTES, (unsigned)RG::BYTES, cbar);
-                    copy_rows<D>(reg + RG::BYTES, kwin, g.R, max(tb, Tqk), te, cbar);
-                    copy_rows<D>(reg + RG::BYTES + (size_t)KIVI_KBLK * RS, vwin, g.R + 1, max(tb, Tqv), te, cbar);
+                    copy_rows<D>(reg + RG::BYTES + (size_t)(ka - tb) * RS, kwin, g.R, ka, te, cbar);
+                    copy_rows<D>(reg + RG::BYTES + (size_t)(KIVI_KBLK + va - tb) * RS, vwin, g.R + 1, va, te,
+                                 cbar);
+                    if (tnew < T && tnew >= tb && tnew < tb + KIVI_KBLK) {
+                        const size_t kv_off = ((size_t)i * g.h + j) * D;
+                        bulk_g2s(reg + RG::BYTES + (size_t)(tnew - tb) * RS, fs.k + kv_off, 2 * D, cbar);
+                        bulk_g2s(reg + RG::BYTES + (size_t)(KIVI_KBLK + tnew - tb) * RS, fs.v + kv_off, 2 * D,
+                                 cbar);
+                    }
                 }
             }
             for (int k = 0; k < nrb; ++k) {
@@ -1007,8 +1153,8 @@ __global__ void __launch_bounds__(256, 2)
                 mc.Tqv = Tqv;
                 mc.krows = reg + RG::BYTES;
                 mc.vrows = reg + RG::BYTES + (size_t)KIVI_KBLK * RS;
-                mc.ka = max(tb, Tqk);
-                mc.va = max(tb, Tqv);
+                mc.ka = tb;
+                mc.va = tb;
                 mc.zrow = reg + RG::BYTES + (size_t)2 * KIVI_KBLK * RS;
                 mc.RS = RS;
                 do_block<D, KB, VB, SH, true, PROBS>(A, qB, reg, alpha, mc, PROBS && prow ? prow + tb : nullptr);
@@ -1174,9 +1320,10 @@ __global__ void __launch_bounds__(256, 2)
     }
 }
 
-template <int D, int KB, int VB, int SH, bool PROBS>
+template <int D, int KB, int VB, int SH, bool PROBS, bool FUSED>
 cudaError_t launch_t(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, __half *out,
-                     const DecodePlan &plan, const DecodeUnits &units, const ProbsOut &po, cudaStream_t st) {
+                     const DecodePlan &plan, const DecodeUnits &units, const ProbsOut &po, const FusedStep &fs,
+                     cudaStream_t st) {
     using RG = Rec<D, KB, VB, SH>;
     if (g.rec_bytes != RG::BYTES || g.off_ksz != RG::OFF_KSZ || g.off_vc != RG::OFF_VC ||
         g.off_vsz != RG::OFF_VSZ || g.vc_blk != RG::VC_BLK || g.vsz_blk != RG::VSZ_BLK)
@@ -1184,7 +1331,7 @@ cudaError_t launch_t(const KiviGeom &g, const KiviDev &dv, const __half *q, int 
     size_t rings = (size_t)plan.warps * warp_region(g, plan.stages);
     if (rings < mixed_region(g)) rings = mixed_region(g);
     const size_t smem = bar_region(plan.warps, plan.stages) + rings;
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, KB, VB, SH, PROBS>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, KB, VB, SH, PROBS, FUSED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // programmatic dependent launch: the CTAs may be placed while the
@@ -1199,29 +1346,34 @@ cudaError_t launch_t(const KiviGeom &g, const KiviDev &dv, const __half *q, int 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<D, KB, VB, SH, PROBS>, g, dv, q, hq, out, plan, units, po);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<D, KB, VB, SH, PROBS, FUSED>, g, dv, q, hq, out, plan, units, po,
+                              fs);
 }
 
-template <int D, int KB, int VB, bool PROBS>
+template <int D, int KB, int VB, bool PROBS, bool FUSED>
 cudaError_t launch_g(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, __half *out,
-                     const DecodePlan &plan, const DecodeUnits &units, const ProbsOut &po, cudaStream_t st) {
+                     const DecodePlan &plan, const DecodeUnits &units, const ProbsOut &po, const FusedStep &fs,
+                     cudaStream_t st) {
     switch (g.G) {
-    case 16: return launch_t<D, KB, VB, 0, PROBS>(g, dv, q, hq, out, plan, units, po, st);
-    case 32: return launch_t<D, KB, VB, 1, PROBS>(g, dv, q, hq, out, plan, units, po, st);
-    case 64: return launch_t<D, KB, VB, 2, PROBS>(g, dv, q, hq, out, plan, units, po, st);
+    case 16: return launch_t<D, KB, VB, 0, PROBS, FUSED>(g, dv, q, hq, out, plan, units, po, fs, st);
+    case 32: return launch_t<D, KB, VB, 1, PROBS, FUSED>(g, dv, q, hq, out, plan, units, po, fs, st);
+    case 64: return launch_t<D, KB, VB, 2, PROBS, FUSED>(g, dv, q, hq, out, plan, units, po, fs, st);
     default:
-        if constexpr (D >= 128) return launch_t<D, KB, VB, 3, PROBS>(g, dv, q, hq, out, plan, units, po, st);
+        if constexpr (D >= 128) return launch_t<D, KB, VB, 3, PROBS, FUSED>(g, dv, q, hq, out, plan, units, po, fs, st);
         return cudaErrorInvalidValue;
     }
 }
 
-template <int D, bool PROBS>
+// PROBS: the weights variant; FUSED: the variant that appends (fs).
+template <int D, bool PROBS, bool FUSED = false>
 cudaError_t launch_d(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq, __half *out,
-                     const DecodePlan &plan, const DecodeUnits &units, const ProbsOut &po, cudaStream_t st) {
-    if (g.kbits == 2 && g.vbits == 2) return launch_g<D, 2, 2, PROBS>(g, dv, q, hq, out, plan, units, po, st);
-    if (g.kbits == 2 && g.vbits == 4) return launch_g<D, 2, 4, PROBS>(g, dv, q, hq, out, plan, units, po, st);
-    if (g.kbits == 4 && g.vbits == 2) return launch_g<D, 4, 2, PROBS>(g, dv, q, hq, out, plan, units, po, st);
-    return launch_g<D, 4, 4, PROBS>(g, dv, q, hq, out, plan, units, po, st);
+                     const DecodePlan &plan, const DecodeUnits &units, const ProbsOut &po, cudaStream_t st,
+                     const FusedStep &fs = FusedStep{nullptr, nullptr, nullptr}) {
+    static_assert(!(PROBS && FUSED), "the weights variant does not append");
+    if (g.kbits == 2 && g.vbits == 2) return launch_g<D, 2, 2, PROBS, FUSED>(g, dv, q, hq, out, plan, units, po, fs, st);
+    if (g.kbits == 2 && g.vbits == 4) return launch_g<D, 2, 4, PROBS, FUSED>(g, dv, q, hq, out, plan, units, po, fs, st);
+    if (g.kbits == 4 && g.vbits == 2) return launch_g<D, 4, 2, PROBS, FUSED>(g, dv, q, hq, out, plan, units, po, fs, st);
+    return launch_g<D, 4, 4, PROBS, FUSED>(g, dv, q, hq, out, plan, units, po, fs, st);
 }
 
 }  // namespace

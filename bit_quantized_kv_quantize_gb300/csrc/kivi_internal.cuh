@@ -93,6 +93,17 @@ struct ProbsOut {
     long long ld;
 };
 
+// A decode launch that also appends this step's token (kivi_append_decode
+// on one-token steps): k, v are the new rows (fp16 [b][h][d]); the kernel
+// appends every sequence whose key window is not full (the others were
+// appended by a preceding append launch restricted to them) and writes
+// those sequences' counters after the append into nxt ([3][b], the other
+// counter set).  The decode kernel reads the counters before the append.
+struct FusedStep {
+    const __half *k, *v;
+    int *nxt;
+};
+
 struct SeqLens {
     int t[KIVI_MAX_BATCH];
 };
@@ -119,6 +130,13 @@ __host__ __device__ __forceinline__ size_t flush_smem_bytes(const KiviGeom &g) {
 struct AppendCounters {
     int T[KIVI_MAX_BATCH], Tqk[KIVI_MAX_BATCH], Tqv[KIVI_MAX_BATCH];
 };
+
+// Counters of one sequence before an append are in range.
+__device__ __forceinline__ bool append_counters_ok(const KiviGeom &g, int T, int Tqk, int Tqv) {
+    const int R = g.R;
+    return T >= 0 && T < g.fcap && Tqk >= 0 && Tqk % R == 0 && T - Tqk >= 0 && T - Tqk <= R && Tqv >= 0 &&
+           T - Tqv >= 0 && T - Tqv <= R + 1;
+}
 
 // ---- records and slice bases ----------------------------------------------------
 __host__ __device__ __forceinline__ size_t rec_off(const KiviGeom &g, int i, int j, int kb) {
@@ -306,10 +324,20 @@ int kivi_check_shape(int b, int h_kv, int d, int k_bits, int v_bits, int G, int 
 cudaError_t kivi_launch_prefill(const KiviGeom &g, const KiviDev &dv, const __half *K,
                                 const __half *V, const SeqLens &lens, int t_stride,
                                 cudaStream_t st);
+// The prefill with its causal attention (kivi_prefill_attn.cu): O = the
+// attention of Q over K, V (fp16 [b][hq][t_stride][d] and [b][h][t_stride][d])
+// and the cache filled as kivi_launch_prefill fills it.  d in {64, 128},
+// G <= 64 (cudaErrorInvalidValue otherwise).
+cudaError_t kivi_launch_prefill_attn(const KiviGeom &g, const KiviDev &dv, const __half *Q, const __half *K,
+                                     const __half *V, __half *O, const SeqLens &lens, int t_stride, int hq,
+                                     cudaStream_t st);
 // nxt: the other counter set ([3][b]: T, Tqk, Tqv), which receives the
 // counters after the append (dv's set is left as it was).
+// only_flush: append only the sequences whose key window is full now (the
+// others' CTAs return at once; a fused decode launch appends them).
 cudaError_t kivi_launch_append(const KiviGeom &g, const KiviDev &dv, const __half *k,
-                               const __half *v, const AppendCounters &ac, int *nxt, cudaStream_t st);
+                               const __half *v, const AppendCounters &ac, int *nxt, cudaStream_t st,
+                               bool only_flush = false);
 DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *T, const int *Tqk, const int *Tqv,
                             int num_sms, DecodeUnits *units);
 // partial slots per (sequence, query head) a cache of this shape allocates
@@ -320,7 +348,11 @@ cudaError_t kivi_launch_probs_finalize(const KiviGeom &g, const KiviDev &dv, int
                                        int maxT, cudaStream_t st);
 // po (may be null): also write the per-token weights (launches the
 // finalizing kernel after the decode kernel; maxT = max_i T_i).
+// fs (may be null; not with po): the launch also appends the step's token
+// (FusedStep).  Its units come from the counters after the append, except
+// that a sequence the launch appends counts its value queue before the pop
+// (the popped token's block is staged as a window block).
 cudaError_t kivi_launch_decode(const KiviGeom &g, const KiviDev &dv, const __half *q, int hq,
                                __half *out, const DecodePlan &plan, const DecodeUnits &units,
                                cudaStream_t st, cudaEvent_t ev0, cudaEvent_t ev1,
-                               const ProbsOut *po = nullptr, int maxT = 0);
+                               const ProbsOut *po = nullptr, int maxT = 0, const FusedStep *fs = nullptr);

@@ -23,7 +23,7 @@ EXPORTS = ["kivi_cache_create", "kivi_cache_destroy", "kivi_prefill", "kivi_appe
            "kivi_cache_export", "kivi_cache_check", "kivi_profile_enable", "kivi_profile_read",
            "kivi_decode_plan", "kivi_status_str", "kivi_last_error", "kivi_abi_version",
            "kivi_decode_attn_noalloc", "kivi_cache_export_records", "kivi_append_decode",
-           "kivi_decode_attn_probs", "kivi_plan_preview"]
+           "kivi_decode_attn_probs", "kivi_plan_preview", "kivi_prefill_attn"]
 
 
 class KiviError(RuntimeError):
@@ -45,6 +45,7 @@ def _load():
     L.kivi_cache_create.argtypes = [i32] * 8 + [ctypes.POINTER(vp)]
     L.kivi_cache_destroy.argtypes = [vp]
     L.kivi_prefill.argtypes = [vp, vp, vp, vp, i32, vp]
+    L.kivi_prefill_attn.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, vp]
     L.kivi_append.argtypes = [vp, vp, vp, vp]
     L.kivi_decode_attn.argtypes = [vp, vp, i32, vp, vp]
     L.kivi_decode_attn_probs.argtypes = [vp, vp, i32, vp, vp, vp, ctypes.c_int64, vp]
@@ -136,6 +137,22 @@ class KiviCache:
         vp = _dev_fp16(V, (self.b, self.h_kv, ts, self.d), "V")
         _check(lib.kivi_prefill(self._h, kp, vp, t.ctypes.data, ts, _stream(stream)))
 
+    def prefill_attn(self, Q, K, V, t, out=None, stream=None):
+        """prefill(K, V, t) and the prompt's causal attention: Q CUDA fp16
+        [b, h_q, t_stride, d] -> out (same shape; rows past each sequence's
+        length untouched).  One launch."""
+        import torch
+        t = np.ascontiguousarray(np.broadcast_to(np.asarray(t, np.int32), (self.b,)))
+        ts, hq = K.shape[2], Q.shape[1]
+        qp = _dev_fp16(Q, (self.b, hq, ts, self.d), "Q")
+        kp = _dev_fp16(K, (self.b, self.h_kv, ts, self.d), "K")
+        vp = _dev_fp16(V, (self.b, self.h_kv, ts, self.d), "V")
+        if out is None:
+            out = torch.zeros_like(Q)
+        op = _dev_fp16(out, (self.b, hq, ts, self.d), "out")
+        _check(lib.kivi_prefill_attn(self._h, qp, kp, vp, t.ctypes.data, ts, hq, op, _stream(stream)))
+        return out
+
     def append(self, k, v, stream=None):
         """k, v: CUDA fp16 [b, h_kv, d]."""
         kp = _dev_fp16(k, (self.b, self.h_kv, self.d), "k")
@@ -177,8 +194,9 @@ class KiviCache:
     def append_decode(self, k, v, q, out=None, stream=None):
         """append(k, v) then decode(q) in one call; returns out.
 
-        Two launches on the stream: the append kernel, then the decode
-        kernel as its programmatic dependent."""
+        One launch where the decode kernel appends the token itself (see
+        kivi_append_decode in kivi.h for when), else the append kernel and
+        the decode kernel as its programmatic dependent."""
         import torch
         hq = q.shape[1]
         kp = _dev_fp16(k, (self.b, self.h_kv, self.d), "k")

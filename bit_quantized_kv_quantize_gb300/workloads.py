@@ -76,7 +76,7 @@ WORKLOADS = {
                           prefill=131071, steps=1, n_outlier=_outliers(128), outlier_scale=10.0),
 }
 
-_KIND = {"K": 1, "V": 2, "q": 3, "k_new": 4, "v_new": 5, "outlier": 6}
+_KIND = {"K": 1, "V": 2, "q": 3, "k_new": 4, "v_new": 5, "outlier": 6, "Q": 7}
 
 
 def _gen(seed: int, kind: str, a: int, b: int = 0) -> np.random.Generator:
@@ -129,6 +129,29 @@ def prefill_kv(w: Workload, t_stride: int | None = None, threads: int | None = N
         for ij in todo:
             fill(ij)
     return K, V, lens
+
+
+def prefill_q(w: Workload, t_stride: int | None = None, threads: int | None = None):
+    """The prompt's queries: fp16 [b, h_q, t_stride, d], N(0, 1) per element,
+    tokens past a sequence's length zero (inputs of the prefill attention)."""
+    lens = w.lengths()
+    t_stride = int(t_stride or lens.max() or 1)
+    Q = np.zeros((w.b, w.h_q, t_stride, w.d), np.float16)
+
+    def fill(ih):
+        i, h = ih
+        n = int(lens[i])
+        Q[i, h, :n] = _gen(w.seed, "Q", i, h).standard_normal((n, w.d), dtype=np.float32).astype(np.float16)
+
+    todo = [(i, h) for i in range(w.b) for h in range(w.h_q)]
+    nthreads = threads or min(16, os.cpu_count() or 1)
+    if nthreads > 1 and len(todo) > 1:
+        with ThreadPoolExecutor(nthreads) as ex:
+            list(ex.map(fill, todo))
+    else:
+        for ih in todo:
+            fill(ih)
+    return Q
 
 
 def step_kv(w: Workload, step: int):

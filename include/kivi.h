@@ -82,6 +82,23 @@ kivi_status kivi_cache_destroy(kivi_cache_t c);
 kivi_status kivi_prefill(kivi_cache_t c, const void *K, const void *V, const int32_t *t,
                          int t_stride, kivi_stream_t stream);
 
+/* Prefill with its attention: kivi_prefill(K, V, t, t_stride) and, from
+ * the same pass over K and V, the prompt's causal attention in full
+ * precision ("Literature audit -- Group 2", section 1 KIVI: its backends
+ * list runs the prefill's attention on the unquantized K/V and quantizes
+ * the cache after it; its limitations paragraph lists that unfused
+ * quantization as open).  For sequence i, query head h (kv head
+ * h / (h_q / h_kv)) and token tau < t[i]:
+ *   out[i][h][tau] = sum_{s <= tau} softmax_s(q[i][h][tau] . K[i][j][s] / sqrt(d)) V[i][j][s]
+ * q and out: fp16 [b][h_q][t_stride][d] (device, 16-byte aligned); rows
+ * tau >= t[i] of out are not written.  The cache afterwards is bitwise the
+ * one kivi_prefill leaves.  Scores accumulate in fp32; the softmax weights
+ * enter the weighted sum of values rounded to fp16.  One launch.  Supports
+ * d 64 or 128 and G <= 64 (KIVI_ERR_UNSUPPORTED otherwise); h_q a multiple
+ * of h_kv, at most 8 times it. */
+kivi_status kivi_prefill_attn(kivi_cache_t c, const void *q, const void *K, const void *V, const int32_t *t,
+                              int t_stride, int h_q, void *out, kivi_stream_t stream);
+
 /* Append one token to every sequence: k and v fp16 [b][h_kv][d] (device).
  * First, per sequence, the maintenance of item 4 left over from the previous
  * step: the fp16 key block is quantized if it holds R keys, and the oldest
@@ -126,9 +143,25 @@ kivi_status kivi_decode_attn_probs(kivi_cache_t c, const void *q, int h_q, void 
                                    float *mass, int64_t ld, kivi_stream_t stream);
 
 /* One decode step in one call: kivi_append(k, v) then kivi_decode_attn(q,
- * h_q, out), launched back to back on `stream` once both sets of arguments
- * have been validated (a failed call changes nothing; KIVI_ERR_CAPACITY if a
- * sequence is full).  Results are those of the two calls. */
+ * h_q, out), once both sets of arguments have been validated (a failed call
+ * changes nothing; KIVI_ERR_CAPACITY if a sequence is full).  The cache
+ * afterwards is bitwise the one the two calls leave; out agrees with theirs
+ * within the decode tolerance (the work may be split differently).
+ *
+ * With h_q / h_kv <= 4 and no more (sequence, kv head) pairs than twice
+ * the GPU's SM count, the step is one kernel launch: the decode kernel
+ * appends the token itself (item 4's one-token maintenance: the new key
+ * and value, and the value token leaving the queue, quantized per token as
+ * in kivi_append) for every sequence whose key window is not full.  On a
+ * step where some sequence's key window is full (every R steps per
+ * sequence) the append kernel first handles just those sequences (two
+ * launches).  Otherwise the call launches the append kernel and then the
+ * decode kernel (with many pairs the append kernel's parallel appends are
+ * faster than appends spread over the persistent decode CTAs).  The
+ * environment variable KIVI_FUSED_STEP=0 forces two launches, =1 the fused
+ * kernel wherever h_q / h_kv <= 4.  kivi_decode_plan reports the call's
+ * launches.  k and v must stay unchanged until the call's work on `stream`
+ * completes (the fused kernel reads them). */
 kivi_status kivi_append_decode(kivi_cache_t c, const void *k, const void *v, const void *q, int h_q,
                                void *out, kivi_stream_t stream);
 
@@ -199,8 +232,11 @@ kivi_status kivi_cache_check(kivi_cache_t c, uint32_t *flags, kivi_stream_t stre
 kivi_status kivi_profile_enable(kivi_cache_t c, int on);
 kivi_status kivi_profile_read(kivi_cache_t c, double *total_ms, int *launches);
 
-/* How the last kivi_decode_attn call was launched (HOST outputs, any may be
- * NULL): persistent CTAs of the decode kernel and kernel launches per call. */
+/* How the last decode call (kivi_decode_attn, kivi_decode_attn_probs or
+ * kivi_append_decode) was launched (HOST outputs, any may be NULL):
+ * persistent CTAs of the decode kernel, and the call's launches of the
+ * decode kernel (1) plus kivi_append_decode's append kernel when it
+ * launched one (the weights' finalizing kernel is not counted). */
 kivi_status kivi_decode_plan(kivi_cache_t c, int *splits, int *launches);
 
 /* A packed cache held in caller-owned device memory: the block records

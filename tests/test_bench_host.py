@@ -55,11 +55,12 @@ def test_step_modes_and_config():
     class A:
         pass
     a = A()
+    assert bench.step_mode(a) == "fused"   # the default: one kivi_append_decode call
+    a.two = True
     assert bench.step_mode(a) == "two"
-    a.fused = True
-    assert bench.step_mode(a) == "fused"
     a.probs = True
     assert bench.step_mode(a) == "probs"
+    assert bench.prefill_attn_flops(W.WORKLOADS["tiny_kivi2"], [3]) == 4.0 * 2 * 64 * 6
     w = W.WORKLOADS["llama3_8b_gqa_32k"]
     for mode, name in bench.STEP_NAMES.items():
         cfg = bench.workload_config(w, mode)

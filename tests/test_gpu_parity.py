@@ -117,6 +117,10 @@ FUSED = [
     (3, 2, 2, 64, 2, 2, 32, 32, [0, 1, 31], 70),
     (2, 1, 3, 256, 2, 2, 64, 128, [300, 64], 135),
     (2, 2, 4, 128, 2, 2, 128, 128, [511, 128], 130),
+    # G = 16 and 4-bit keys at d = 64 (pops open fresh value blocks)
+    (4, 2, 2, 64, 4, 2, 16, 64, [0, 63, 64, 130], 140),
+    # two head groups per kv head: the two-launch path
+    (2, 1, 8, 128, 2, 4, 16, 64, [100, 0], 80),
 ]
 
 
@@ -136,6 +140,39 @@ def test_fused_step_ragged(case):
         p.step_fused(k, v, q, f"fused step {s}")
         if s % 9 == 0 or s == steps - 1:
             p.check_state(f"fused step {s}")
+
+
+def test_fused_step_launch_count(monkeypatch):
+    """kivi_append_decode is one launch on steps without a key-window
+    flush, two on flush steps, and two with KIVI_FUSED_STEP=0, with more
+    than one head group per kv head, or with more (sequence, kv head) pairs
+    than twice the SM count (unless KIVI_FUSED_STEP=1)."""
+    h, d, R = 2, 64, 32
+    rng = np.random.default_rng(5)
+    many = torch.cuda.get_device_properties(0).multi_processor_count + 1   # b h > 2 SMs
+    for b, hq, env in ((2, 4, None), (2, 4, "0"), (2, 16, None), (many, 2, None), (many, 2, "1")):
+        if env is None:
+            monkeypatch.delenv("KIVI_FUSED_STEP", raising=False)
+        else:
+            monkeypatch.setenv("KIVI_FUSED_STEP", env)
+        Kh, Vh = _rand_kv(rng, b, h, 40, d)
+        c = K.KiviCache(b, h, d, 2, 2, 32, R, 128)
+        c.prefill(_dev(Kh), _dev(Vh), np.array([40, 9] * (b // 2) + [40] * (b % 2), np.int32))
+        one = env != "0" and hq // h <= 4 and (env == "1" or b * h <= 2 * (many - 1))
+        nflush = 0
+        for s in range(30):
+            T, Tqk, _ = c.lengths()
+            flush = bool(np.any(T - Tqk == R))
+            k = _dev(rng.standard_normal((b, h, d)).astype(np.float16))
+            v = _dev(rng.standard_normal((b, h, d)).astype(np.float16))
+            q = _dev(rng.standard_normal((b, hq, d)).astype(np.float16))
+            c.append_decode(k, v, q)
+            launches = c.plan()[1]
+            assert launches == (1 + flush if one else 2), (hq, env, s, launches)
+            nflush += flush
+        assert 0 < nflush < 30
+        assert c.check() == 0
+        c.close()
 
 
 def test_fused_step_matches_two_calls():

@@ -1,0 +1,127 @@
+"""GPU parity of kivi_prefill_attn: the prompt's causal attention (fp16
+inputs, fp32 scores, fp16 softmax weights in the value product) against the
+oracle's double-precision causal attention, within 2e-3 max-abs and 1e-3
+relative L2 over the valid rows; and the cache it leaves, bitwise against
+kivi_prefill's and the oracle's."""
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+from bit_quantized_kv_quantize_gb300 import workloads as W
+from tests import kivi_testutil as U
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from bit_quantized_kv_quantize_gb300 import kivi as K
+    import os
+    oracle.set_threads(os.cpu_count() or 1)
+
+
+def _dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def _compare_rows(got, ref, lens, what):
+    """got, ref: [b, hq, ts, d]; compare the rows tau < lens[i] as one output."""
+    g = np.concatenate([got[i, :, :n].reshape(-1, got.shape[-1]) for i, n in enumerate(lens) if n])
+    r = np.concatenate([ref[i, :, :n].reshape(-1, ref.shape[-1]) for i, n in enumerate(lens) if n])
+    return U.compare_output(g, r, what)
+
+
+CASES = [
+    # b, h_kv, h_q, d, k_bits, v_bits, G, R, lens
+    (2, 2, 4, 64, 2, 2, 32, 32, [100, 1]),
+    (1, 2, 2, 128, 4, 4, 16, 64, [257]),
+    (3, 1, 8, 128, 2, 4, 64, 128, [0, 64, 600]),
+    (2, 4, 8, 128, 2, 2, 32, 128, [1000, 777]),
+    (2, 2, 6, 64, 4, 2, 16, 32, [63, 65]),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"pa{i}" for i in range(len(CASES))])
+def test_prefill_attn_parity(case):
+    b, h, hq, d, kb, vb, G, R, lens = case
+    rng = np.random.default_rng(zlib.crc32(str(case).encode()))
+    ts = max(max(lens), 1) + 5
+    Q = (rng.standard_normal((b, hq, ts, d)) * 1.5).astype(np.float16)
+    Kh = (rng.standard_normal((b, h, ts, d)) * 1.5).astype(np.float16)
+    Vh = rng.standard_normal((b, h, ts, d)).astype(np.float16)
+    Kh[:, :, :, 3] *= 8   # an outlier channel
+    t = np.array(lens, np.int32)
+    cap = max(max(lens), 1) + 8
+    a = K.KiviCache(b, h, d, kb, vb, G, R, cap)
+    out = torch.full((b, hq, ts, d), 7.0, dtype=torch.float16, device="cuda")   # sentinel past each length
+    a.prefill_attn(_dev(Q), _dev(Kh), _dev(Vh), t, out=out)
+    got = out.float().cpu().numpy()
+    ref = oracle.prefill_attention(Q, Kh, Vh, t)
+    _compare_rows(got, ref, lens, f"prefill attention {case}")
+    for i, n in enumerate(lens):
+        assert np.all(got[i, :, n:] == 7.0), "rows past the length were written"
+    # the cache: bitwise kivi_prefill's, and the oracle's
+    p = K.KiviCache(b, h, d, kb, vb, G, R, cap)
+    p.prefill(_dev(Kh), _dev(Vh), t)
+    ea, ep = a.export(), p.export()
+    for key in ea:
+        assert np.array_equal(ea[key], ep[key]), key
+    assert all(np.array_equal(x, y) for x, y in zip(a.lengths(), p.lengths()))
+    o = oracle.Cache(b, h, d, kb, vb, G, R, cap)
+    o.prefill(Kh, Vh, t)
+    g = U.geometry(b, h, d, kb, vb, G, R, cap)
+    oex = o.export()
+    T, Tqk, Tqv = o.lengths()
+    for i in range(b):
+        for j in range(h):
+            U.compare_slice(ea, g, i, j, oex, g, i, j, int(T[i]), int(Tqk[i]), int(Tqv[i]), what=f"{case} {i} {j}")
+    # the cache decodes as the oracle does
+    q = rng.standard_normal((b, hq, d)).astype(np.float16)
+    U.compare_output(a.decode(_dev(q)).float().cpu().numpy(), o.decode(q), f"decode after {case}")
+    assert a.check() == 0
+    for c in (a, p):
+        c.close()
+    o.close()
+
+
+def test_prefill_attn_unsupported_shapes():
+    for d, G in ((256, 32), (128, 128)):
+        c = K.KiviCache(1, 1, d, 2, 2, G, 128, 256)
+        x = torch.zeros((1, 1, 64, d), dtype=torch.float16, device="cuda")
+        with pytest.raises(K.KiviError):
+            c.prefill_attn(x, x, x, [64])
+        c.close()
+
+
+def test_prefill_attn_full_llama3_8b_gqa_32k():
+    """The 32k GQA workload at full size: sampled rows (the first, the tile
+    edges, the last, random ones) of every (sequence, query head) against
+    the oracle; the cache bitwise against kivi_prefill's."""
+    w = W.WORKLOADS["llama3_8b_gqa_32k"]
+    Kh, Vh, lens = W.prefill_kv(w)
+    Q = W.prefill_q(w)
+    cap = int(lens.max()) + 8
+    a = K.KiviCache(w.b, w.h_kv, w.d, w.kbits, w.vbits, w.G, w.R, cap)
+    out = a.prefill_attn(_dev(Q), _dev(Kh), _dev(Vh), lens)
+    rng = np.random.default_rng(7)
+    rows = []
+    for i in range(w.b):
+        n = int(lens[i])
+        for qh in range(w.h_q):
+            taus = {0, 63, 64, 65, n // 2, n - 65, n - 1} | set(rng.integers(0, n, 3).tolist())
+            rows += [(i, qh, tau) for tau in sorted(taus)]
+    rows = np.array(rows, np.int32)
+    ref = oracle.prefill_attention(Q, Kh, Vh, lens, rows=rows)
+    ix = torch.from_numpy(rows.astype(np.int64)).cuda()
+    g = out[ix[:, 0], ix[:, 1], ix[:, 2]].float().cpu().numpy()
+    del out
+    U.compare_output(g, ref, "prefill attention 32k sampled rows")
+    p = K.KiviCache(w.b, w.h_kv, w.d, w.kbits, w.vbits, w.G, w.R, cap)
+    p.prefill(_dev(Kh), _dev(Vh), lens)
+    ea, ep = a.export(), p.export()
+    for key in ea:
+        assert np.array_equal(ea[key], ep[key]), key
+    assert a.check() == 0
+    a.close()
+    p.close()
