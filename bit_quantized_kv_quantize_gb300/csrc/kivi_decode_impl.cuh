@@ -36,6 +36,8 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxWaitIters = 1 << 24;   // bounded mbarrier waits
+constexpr int kFastMerge = 16;   // partials a pair's final merge reads in one round trip ...
+constexpr int kFastMergeV = 4;   // ... with at most this many accumulators a thread
 
 // ---------------------------------------------------------------------------
 // PTX helpers
@@ -1224,7 +1226,84 @@ __global__ void __launch_bounds__(256, 2)
             if (s_last) *tk = 0u;
         }
         __syncthreads();
-        if (s_last) {
+        if (s_last && np <= kFastMerge &&
+            np <= kFastMergeV * max(1, min(8, (int)blockDim.x / (nh * NC4)))) {
+            // Merge the pair's partials (up to kFastMerge of them) with one
+            // round trip: each thread loads every partial's (m, l) of its
+            // head, and m and the column's accumulator of its own partials
+            // sub, sub + S, ... (at most kFastMergeV), all together, forms
+            // the weights itself, and the S subsets of a column are summed
+            // in shared memory (the ring is free: the warps' results were
+            // merged above).
+            __threadfence();
+            const int ncol = nh * NC4;
+            const int S = max(1, min(8, (int)blockDim.x / ncol));
+            float4 *sm_a = reinterpret_cast<float4 *>(ring);   // [S][ncol]
+            for (int it = threadIdx.x; it < ncol * S; it += blockDim.x) {
+                const int col = it % ncol, sub = it / ncol;
+                const int e = col / NC4, c4 = col % NC4;
+                const float *hp = prow0 + (size_t)e * g.smax * PS;
+                float2 ml[kFastMerge];
+                float mv[kFastMergeV];
+                float4 v[kFastMergeV];
+#pragma unroll
+                for (int y = 0; y < kFastMerge; ++y)
+                    ml[y] = y < np ? __ldcg(reinterpret_cast<const float2 *>(hp + (size_t)y * PS))
+                                   : make_float2(-INFINITY, 0.f);
+#pragma unroll
+                for (int y = 0; y < kFastMergeV; ++y) {
+                    const int ys = sub + y * S;
+                    mv[y] = ys < np ? __ldcg(hp + (size_t)ys * PS) : -INFINITY;
+                    v[y] = ys < np ? __ldcg(reinterpret_cast<const float4 *>(hp + (size_t)ys * PS + 4 + 4 * c4))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                float M = -INFINITY;
+#pragma unroll
+                for (int y = 0; y < kFastMerge; ++y) M = fmaxf(M, ml[y].x);
+                float L = 0.f;
+                if (M != -INFINITY)
+#pragma unroll
+                    for (int y = 0; y < kFastMerge; ++y)
+                        if (y < np) L = fmaf(ex2(ml[y].x - M), ml[y].y, L);
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (M != -INFINITY)
+#pragma unroll
+                    for (int y = 0; y < kFastMergeV; ++y) {
+                        if (sub + y * S >= np) continue;
+                        const float w = ex2(mv[y] - M) * inv;
+                        a4.x = fmaf(w, v[y].x, a4.x);
+                        a4.y = fmaf(w, v[y].y, a4.y);
+                        a4.z = fmaf(w, v[y].z, a4.z);
+                        a4.w = fmaf(w, v[y].w, a4.w);
+                    }
+                sm_a[it] = a4;
+                if constexpr (PROBS) {
+                    if (c4 == 0 && sub == 0) {
+                        float *mlo = dv.ml + ((size_t)i * hq + j * hg + e0 + e) * 2;
+                        mlo[0] = M;
+                        mlo[1] = inv;
+                    }
+                }
+            }
+            __syncthreads();
+            for (int col = threadIdx.x; col < ncol; col += blockDim.x) {
+                const int e = col / NC4, c4 = col % NC4;
+                float4 a4 = sm_a[col];
+                for (int k = 1; k < S; ++k) {
+                    const float4 b4 = sm_a[k * ncol + col];
+                    a4.x += b4.x;
+                    a4.y += b4.y;
+                    a4.z += b4.z;
+                    a4.w += b4.w;
+                }
+                const __half2 lo = __floats2half2_rn(a4.x, a4.y), hi = __floats2half2_rn(a4.z, a4.w);
+                uint2 o2;
+                o2.x = h2u(lo);
+                o2.y = h2u(hi);
+                *reinterpret_cast<uint2 *>(out + ((size_t)i * hq + j * hg + e0 + e) * D + 4 * c4) = o2;
+            }
+        } else if (s_last) {
             // Merge the pair's partials: their (m, l) come into shared memory
             // with one round trip, each head's weights are formed there by
             // one warp, then the accumulators are read as float4 columns,

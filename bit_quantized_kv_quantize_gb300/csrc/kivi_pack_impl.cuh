@@ -203,6 +203,7 @@ __device__ __forceinline__ void pack_key_tile(const __half *xs, float *sfz, int 
     // odd tokens of one group and channel pair (the min / max of fp16
     // values is exact in fp16), then lane th takes channel c + th.
     int slow = 0;
+#pragma unroll 2
     for (int e = threadIdx.x; e < NG * D; e += blockDim.x) {
         const int th = (e >> 4) & 1;
         const int cp = (e & 15) | ((e >> 5) << 4);
@@ -250,6 +251,8 @@ __device__ __forceinline__ void pack_key_tile(const __half *xs, float *sfz, int 
     constexpr int GW = cph / RPG;
     constexpr int kc_blk = 2 * D * KBITS;
     const int nblk = (ntok + KIVI_KBLK - 1) / KIVI_KBLK;
+    // words are independent: unrolled so that a thread keeps several in flight
+#pragma unroll 4
     for (int e = threadIdx.x; e < nblk * kc_blk; e += blockDim.x) {
         const int kbl = e / kc_blk, wb = e - kbl * kc_blk;
         const KWord kw = kword_decode(wb, KBITS);
@@ -304,6 +307,7 @@ __device__ __forceinline__ void pack_value_tile(const uint32_t *xs2, float2 *sfz
     // scale and zero per (token, channel group), both tokens of a pair at once
     const int nvblk = (ntok + KIVI_VBLK - 1) / KIVI_VBLK;   // value blocks touched
     int slow = 0;
+#pragma unroll 2
     for (int e = threadIdx.x; e < nvblk * 8 * ngi; e += blockDim.x) {
         const int k = e / ngi, gi = e - k * ngi;
         const int tau = tok0 + 2 * k;   // even: the pair's halves are adjacent in a scale row
@@ -341,6 +345,8 @@ __device__ __forceinline__ void pack_value_tile(const uint32_t *xs2, float2 *sfz
     constexpr int cs = D * VBITS / 64 < 4 ? D * VBITS / 64 : 4;
     constexpr int cph = 16 / VBITS;
     constexpr int vc_blk = D * VBITS / 2;
+    // words are independent: unrolled so that a thread keeps several in flight
+#pragma unroll 4
     for (int e = threadIdx.x; e < nvblk * vc_blk; e += blockDim.x) {
         const int vbl = e / vc_blk, wb = e - vbl * vc_blk;
         const VWord vw = vword_decode(wb, D, VBITS, cs);
