@@ -21,7 +21,7 @@ SOURCES = ["kivi_api.cu", "kivi_pack.cu", "kivi_decode.cu", "kivi_decode_d64.cu"
            "kivi_decode_fused_d128.cu", "kivi_decode_fused_d256.cu", "kivi_probs.cu", "kivi_noalloc.cu",
            "kivi_prefill_attn.cu"]
 HEADERS = ["kivi_internal.cuh", "kivi_decode_impl.cuh", "kivi_pack_impl.cuh", "kivi_append_impl.cuh",
-           "kivi_mma.cuh"]
+           "kivi_mma.cuh", "kivi_tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # IEEE division and rounding stay exact: no --use_fast_math anywhere.
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

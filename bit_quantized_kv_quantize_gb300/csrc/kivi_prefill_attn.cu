@@ -1,5 +1,6 @@
 // kivi_prefill_attn.cu -- causal prefill attention over the prompt's fp16
-// keys and values, with the cache's quantize-and-pack in its epilogue.
+// keys and values on the 5th-generation tensor cores, with the cache's
+// quantize-and-pack in its epilogue.
 //
 // Method: "Literature audit -- Group 2", section 1 KIVI.  Its list of
 // supported backends runs the prefill's attention in full precision (flash
@@ -7,24 +8,16 @@
 // afterwards; its limitations paragraph lists that unfused quantization as
 // open.  This kernel does both in one pass over K and V: the attention of
 // core-algorithm item 5's formula with a causal mask over the raw fp16 keys
-// and values, and, in the epilogue of the CTA that holds a 64-token tile of
-// K and V for its own query rows (its diagonal tile), the prefill split and
-// packing of items 2-4 for that tile.
-//
-// Layout.  A CTA computes 64 query rows of one query head (4 warps, 16 rows
-// each) and walks the key tiles 0..(its own) with an online softmax
-// (flash-attention style): scores and P V on m16n8k16 fp16 MMAs with fp32
-// accumulation, P rounded to fp16 for the second product.  K and V tiles
-// are double-buffered in shared memory by asynchronous 16-byte copies, in a
-// swizzled layout (16-byte chunk c of row r at chunk c ^ (r mod 8)) that
-// keeps the ldmatrix reads free of bank conflicts.  Grid: (query tiles,
-// query heads, sequences), the longest tiles first.
+// and values, and, in the epilogue of the CTA that holds the 64-token K and
+// V tiles of its own query rows (its diagonal tiles), the prefill split and
+// packing of items 2-4 for those tiles.
 #include "kivi_mma.cuh"
 #include "kivi_pack_impl.cuh"
+#include "kivi_tcgen05.cuh"
 
 namespace {
 
-constexpr int kTileRows = 64;   // query rows and keys per tile
+constexpr int kTileRows = 64;   // tokens of a packed tile
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -32,34 +25,26 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// halves offset of 16-byte chunk c of row r in a swizzled [64][D] tile
-template <int D>
-__device__ __forceinline__ int swz(int r, int c) {
-    return r * D + ((c ^ (r & 7)) << 3);
-}
-
-// rows [0, valid) of a [64][D] tile from src (rows D apart), the rest zero
-template <int D>
-__device__ __forceinline__ void load_tile(__half *dst, const __half *src, int valid) {
-    constexpr int CPR = D / 8;
-    const int last = valid > 0 ? valid - 1 : 0;
-    for (int e = threadIdx.x; e < kTileRows * CPR; e += blockDim.x) {
-        const int r = e / CPR, c = e - r * CPR;
-        cp_async16(dst + swz<D>(r, c), src + (size_t)min(r, last) * D + 8 * c, r < valid);
-    }
-}
-
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// byte offset of 16-byte chunk c of row r in a [rows][D] fp16 tile in the
+// tensor cores' no-swizzle core-matrix layout (8 rows x 16 bytes, 128
+// contiguous bytes; 8-row groups 16 D bytes apart)
+template <int D>
+__device__ __forceinline__ int chunk_at(int r, int c) {
+    return (r >> 3) * 16 * D + c * 128 + (r & 7) * 16;
+}
+
 // The cache's share of the diagonal tile [tb, tb + 64) of (sequence i, kv
 // head j): keys [tb, nqk) and values [tb, nqv) packed by the prefill pack
 // kernels' tile routines, window tokens copied to their fp16 slots.  kt, vt:
-// the swizzled K and V tiles; work: free shared memory for the staging.
+// the K and V tiles (core-matrix layout); work: free shared memory for the
+// staging.
 template <int D, int KB, int VB, int G>
-__device__ void pack_diagonal(const KiviGeom &g, const KiviDev &dv, const __half *kt, const __half *vt,
+__device__ void pack_diagonal(const KiviGeom &g, const KiviDev &dv, const unsigned char *kt, const unsigned char *vt,
                               unsigned char *work, int i, int j, int tb, int t) {
     constexpr int CPR = D / 8;
     const int nqk = t - t % g.R, nqv = t > g.R ? t - g.R : 0;
@@ -73,7 +58,7 @@ __device__ void pack_diagonal(const KiviGeom &g, const KiviDev &dv, const __half
         for (int e = threadIdx.x; e < kTileRows * CPR; e += blockDim.x) {
             const int r = e / CPR, c = e - r * CPR;
             *reinterpret_cast<uint4 *>(xs + (size_t)r * key_xsd(D) + 8 * c) =
-                r < ntk ? *reinterpret_cast<const uint4 *>(kt + swz<D>(r, c)) : zero;
+                r < ntk ? *reinterpret_cast<const uint4 *>(kt + chunk_at<D>(r, c)) : zero;
         }
         __syncthreads();
         pack_key_tile<KB, G, D>(xs, sfz, ntk, dv.blk + rec_off(g, i, j, tb / KIVI_KBLK), g.rec_bytes, g.off_ksz);
@@ -85,8 +70,9 @@ __device__ void pack_diagonal(const KiviGeom &g, const KiviDev &dv, const __half
         float2 *sfz = reinterpret_cast<float2 *>(work + (size_t)32 * value_ps(D) * 4);
         for (int e = threadIdx.x; e < 32 * CPR; e += blockDim.x) {
             const int k = e / CPR, c = e - k * CPR;
-            const uint4 a = 2 * k < ntv ? *reinterpret_cast<const uint4 *>(vt + swz<D>(2 * k, c)) : zero;
-            const uint4 b = 2 * k + 1 < ntv ? *reinterpret_cast<const uint4 *>(vt + swz<D>(2 * k + 1, c)) : zero;
+            const uint4 a = 2 * k < ntv ? *reinterpret_cast<const uint4 *>(vt + chunk_at<D>(2 * k, c)) : zero;
+            const uint4 b =
+                2 * k + 1 < ntv ? *reinterpret_cast<const uint4 *>(vt + chunk_at<D>(2 * k + 1, c)) : zero;
             uint4 lo, hi;
             lo.x = __byte_perm(a.x, b.x, 0x5410);
             lo.y = __byte_perm(a.x, b.x, 0x7632);
@@ -111,41 +97,93 @@ __device__ void pack_diagonal(const KiviGeom &g, const KiviDev &dv, const __half
     for (int e = threadIdx.x; e < (te - tb) * CPR; e += blockDim.x) {
         const int tau = tb + e / CPR, c = e % CPR;
         if (tau >= nqk)
-            kf[(size_t)(tau % g.R) * CPR + c] = *reinterpret_cast<const uint4 *>(kt + swz<D>(tau - tb, c));
+            kf[(size_t)(tau % g.R) * CPR + c] = *reinterpret_cast<const uint4 *>(kt + chunk_at<D>(tau - tb, c));
         if (tau >= nqv)
-            vf[(size_t)(tau % (g.R + 1)) * CPR + c] = *reinterpret_cast<const uint4 *>(vt + swz<D>(tau - tb, c));
+            vf[(size_t)(tau % (g.R + 1)) * CPR + c] =
+                *reinterpret_cast<const uint4 *>(vt + chunk_at<D>(tau - tb, c));
     }
 }
 
 template <int D, int KB, int VB>
-__device__ void pack_diagonal_g(const KiviGeom &g, const KiviDev &dv, const __half *kt, const __half *vt,
-                                unsigned char *work, int i, int j, int tb, int t) {
+__device__ void pack_diagonal_g(const KiviGeom &g, const KiviDev &dv, const unsigned char *kt,
+                                const unsigned char *vt, unsigned char *work, int i, int j, int tb, int t) {
     switch (g.G) {
     case 16: pack_diagonal<D, KB, VB, 16>(g, dv, kt, vt, work, i, j, tb, t); break;
     case 32: pack_diagonal<D, KB, VB, 32>(g, dv, kt, vt, work, i, j, tb, t); break;
     default: pack_diagonal<D, KB, VB, 64>(g, dv, kt, vt, work, i, j, tb, t); break;
     }
 }
-
-// Q, O: fp16 [b][hq][t_stride][D]; K, V: fp16 [b][h_kv][t_stride][D].
 template <int D>
-__global__ void __launch_bounds__(128, 2)
-    prefill_attn_kernel(KiviGeom g, KiviDev dv, const __half *__restrict__ Q, const __half *__restrict__ K,
-                        const __half *__restrict__ V, __half *__restrict__ O, SeqLens lens, int t_stride,
-                        int hq) {
+__device__ void pack_diagonal_bits(const KiviGeom &g, const KiviDev &dv, const unsigned char *kt,
+                                   const unsigned char *vt, unsigned char *work, int i, int j, int tb, int t) {
+    if (g.kbits == 2 && g.vbits == 2) pack_diagonal_g<D, 2, 2>(g, dv, kt, vt, work, i, j, tb, t);
+    else if (g.kbits == 2) pack_diagonal_g<D, 2, 4>(g, dv, kt, vt, work, i, j, tb, t);
+    else if (g.vbits == 2) pack_diagonal_g<D, 4, 2>(g, dv, kt, vt, work, i, j, tb, t);
+    else pack_diagonal_g<D, 4, 4>(g, dv, kt, vt, work, i, j, tb, t);
+}
+
+// ---------------------------------------------------------------------------
+// The attention on the 5th-generation tensor cores (tcgen05): a CTA
+// is 128 query rows of one query head, 4 warps, and thread r owns row r
+// (tensor-memory lane r).  Per 64-key tile: S = Q K^T (M 128, N 64, K d)
+// into tensor memory; each thread reads its row of S, applies the causal
+// mask and the online softmax (base 2, its whole row in registers), and
+// writes its fp16 weights P into shared memory; O += P V (M 128, N d, K 64)
+// accumulates in tensor memory.  One thread issues the MMAs; their
+// completion arrives on an mbarrier (bounded waits).  K and V tiles are
+// double-buffered by 16-byte cp.async copies.  The running maximum is
+// raised lazily: O and the row sum are rescaled only when a row's maximum
+// grows by more than 8 (log2 units), so P stays below 2^8.
+// Shared memory (no-swizzle core-matrix layouts, 8 rows x 16 bytes each):
+//   Q [128][D], K and V [2][64][D], P [128][64]: 112 KB at d = 128.
+// Tensor memory: S in columns 0-63, O in 64-(64 + D): 256 columns.
+// ---------------------------------------------------------------------------
+constexpr int kTcRows = 128, kTcKeys = 64;
+
+// rows [0, valid) of a [rows][D] fp16 tile from src (rows D apart) into
+// core-matrix layout (8-row groups 16 D bytes apart), the rest zero
+template <int D>
+__device__ __forceinline__ void load_core(unsigned char *dst, const __half *src, int rows, int valid) {
+    constexpr int CPR = D / 8;
+    const int last = valid > 0 ? valid - 1 : 0;
+    for (int e = threadIdx.x; e < rows * CPR; e += blockDim.x) {
+        const int r = e / CPR, c = e - r * CPR;
+        cp_async16(dst + (r >> 3) * 16 * D + c * 128 + (r & 7) * 16, src + (size_t)min(r, last) * D + 8 * c,
+                   r < valid);
+    }
+}
+
+__device__ __forceinline__ bool tc_wait_bar(uint64_t *bar, unsigned phase) {
+    for (int it = 0; it < (1 << 24); ++it) {
+        unsigned ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(tc_smem_u32(bar)), "r"(phase)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
+template <int D>
+__global__ void __launch_bounds__(128, 1)
+    prefill_attn_tc_kernel(KiviGeom g, KiviDev dv, const __half *__restrict__ Q, const __half *__restrict__ K,
+                           const __half *__restrict__ V, __half *__restrict__ O, SeqLens lens, int t_stride,
+                           int hq) {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int TILE = kTileRows * D;   // halves
-    constexpr int NK = D / 16, NO = D / 8;
-    // [stage 0: K, V][Q][stage 1: K, V]: once the loop is over, the stage
-    // not holding the diagonal tile and Q's are one free stretch of 3 tiles
-    __half *st0 = reinterpret_cast<__half *>(smem);
-    __half *sq = st0 + 2 * TILE;
-    __half *st1 = sq + TILE;
+    constexpr int QB = kTcRows * D * 2, KVB = kTcKeys * D * 2, SBO = 16 * D;
+    unsigned char *sQ = smem;
+    unsigned char *sKV = smem + QB;   // stage s: K at sKV + 2 s KVB, V after it
+    unsigned char *sP = sKV + 4 * KVB;
+    __shared__ __align__(8) uint64_t bars[2];   // S done, O done
+    __shared__ uint32_t s_taddr;
     const int qt = gridDim.x - 1 - blockIdx.x;   // the longest tiles first
     const int h = blockIdx.y, i = blockIdx.z;
     const int hg = hq / g.h, j = h / hg;
     const int t = lens.t[i];
-    const int tb = qt * kTileRows;
+    const int tb = qt * kTcRows;
     if (tb >= t) {
         if (tb == 0 && h == 0 && threadIdx.x == 0) {   // an empty sequence
             dv.T[i] = 0;
@@ -154,139 +192,162 @@ __global__ void __launch_bounds__(128, 2)
         }
         return;
     }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const __half *kbase = K + ((size_t)i * g.h + j) * t_stride * D;
     const __half *vbase = V + ((size_t)i * g.h + j) * t_stride * D;
-    load_tile<D>(sq, Q + (((size_t)i * hq + h) * t_stride + tb) * D, min(kTileRows, t - tb));
-    load_tile<D>(st0, kbase, min(kTileRows, t));
-    load_tile<D>(st0 + TILE, vbase, min(kTileRows, t));
+    const int nt = min((t + kTcKeys - 1) / kTcKeys, (tb + kTcRows) / kTcKeys);   // key tiles
+    load_core<D>(sQ, Q + (((size_t)i * hq + h) * t_stride + tb) * D, kTcRows, min(kTcRows, t - tb));
+    load_core<D>(sKV, kbase, kTcKeys, min(kTcKeys, t));
+    load_core<D>(sKV + KVB, vbase, kTcKeys, min(kTcKeys, t));
     cp_async_commit();
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_u32(&bars[0])) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_u32(&bars[1])) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) tc_alloc(&s_taddr, 256);
     cp_async_wait<0>();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
     __syncthreads();
-
-    // the warp's 16 query rows as A fragments
-    uint32_t qa[NK][4];
-#pragma unroll
-    for (int kk = 0; kk < NK; ++kk)
-        ldsm_x4(qa[kk], sq + swz<D>(warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1), 2 * kk + (lane >> 4)));
-
+    tc_fence_after();
+    const uint32_t taddr = s_taddr;
+    const uint32_t tS = taddr, tO = taddr + 64;
+    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;   // this warp's tensor-memory lanes
+    constexpr uint32_t ID_S = tc_idesc_f16(kTcRows, kTcKeys, 0), ID_O = tc_idesc_f16(kTcRows, D, 1);
     const float sl2 = 1.4426950408889634f / sqrtf((float)D);   // log2(e) / sqrt(d)
-    float o[NO][4];
+    const int row = tb + tid;
+    float mref = -INFINITY, lsum = 0.f;   // the row's reference maximum (raw score units) and sum
+    unsigned ph = 0;
+    int nS = 0, nO = 0;   // commits issued on each barrier (the same count in every thread)
+    bool ok = true;
+    for (int kt = 0; kt < nt && ok; ++kt) {
+        const int st = kt & 1;
+        unsigned char *sK = sKV + 2 * st * KVB, *sV = sK + KVB;
+        if (tid == 0) {
 #pragma unroll
-    for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-    const int row0 = tb + warp * 16 + gq;   // rows row0 and row0 + 8
-
-    for (int kt = 0; kt <= qt; ++kt) {
-        const __half *ks = (kt & 1) ? st1 : st0;
-        const __half *vs = ks + TILE;
-        if (kt < qt) {   // the next tile streams in while this one is used
-            __half *kn = (kt & 1) ? st0 : st1;
-            const int nb = (kt + 1) * kTileRows;
-            load_tile<D>(kn, kbase + (size_t)nb * D, min(kTileRows, t - nb));
-            load_tile<D>(kn + TILE, vbase + (size_t)nb * D, min(kTileRows, t - nb));
+            for (int k = 0; k < D / 16; ++k)
+                tc_mma_f16(tS, tc_desc(sQ + 256 * k, 128, SBO), tc_desc(sK + 256 * k, 128, SBO), ID_S, k > 0);
+            tc_commit(&bars[0]);
+        }
+        ++nS;
+        if (kt + 1 < nt) {   // the next tile streams into the other stage (its last MMAs are done)
+            unsigned char *nK = sKV + 2 * (st ^ 1) * KVB;
+            const int nb = (kt + 1) * kTcKeys;
+            load_core<D>(nK, kbase + (size_t)nb * D, kTcKeys, min(kTcKeys, t - nb));
+            load_core<D>(nK + KVB, vbase + (size_t)nb * D, kTcKeys, min(kTcKeys, t - nb));
             cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
         }
+        ok = __syncthreads_and(tc_wait_bar(&bars[0], ph));
+        if (!ok) break;
+        tc_fence_after();
+        // this row's 64 scores
+        uint32_t sr[2][32];
+        tc_ld32(tS + lane_off, sr[0]);
+        tc_ld32(tS + lane_off + 32, sr[1]);
+        tc_wait_ld();
+        float sc[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+            const int key = kt * kTcKeys + c;
+            sc[c] = key > row ? -INFINITY : __uint_as_float(sr[c >> 5][c & 31]);
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) mx = fmaxf(mx, sc[c]);
+        // lazy rescale: only when the maximum grew by more than 2^8 in weight
+        const bool grow = mx != -INFINITY && (mref == -INFINITY || (mx - mref) * sl2 > 8.f);
+        const float alpha = grow && mref != -INFINITY ? ex2((mref - mx) * sl2) : 1.f;
+        if (grow) mref = mx;
+        if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t o[32];
+                tc_ld32(tO + lane_off + c0, o);
+                tc_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                tc_st32(tO + lane_off + c0, o);
+            }
+            tc_wait_st();
+        }
+        lsum *= alpha;
+        const float ms = mref * sl2;
+        uint32_t pw[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            const float p0 = ex2(fmaf(sc[2 * c], sl2, -ms)), p1 = ex2(fmaf(sc[2 * c + 1], sl2, -ms));
+            lsum += p0 + p1;
+            pw[c] = pack_h2(p0, p1);
+        }
+        // P row: 8 chunks of 8 keys, core (row / 8, chunk) at (row / 8) 1024 + chunk 128
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4 *>(sP + (tid >> 3) * 1024 + c * 128 + (tid & 7) * 16) =
+                make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
         __syncthreads();
-
-        // scores of the warp's 16 rows against the tile's 64 keys
-        float sc[8][4];
+        tc_fence_after();
+        if (tid == 0) {
 #pragma unroll
-        for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < NK; ++kk)
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                uint32_t b[4];
-                ldsm_x4(b, ks + swz<D>(16 * p + (lane & 7) + 8 * (lane >> 4), 2 * kk + ((lane >> 3) & 1)));
-                mma16816(sc[2 * p], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b[0], b[1]);
-                mma16816(sc[2 * p + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b[2], b[3]);
-            }
-        if (kt == qt) {   // causal mask: key > row
-#pragma unroll
-            for (int n = 0; n < 8; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (tb + 8 * n + 2 * tq + (e & 1) > row0 + 8 * (e >> 1)) sc[n][e] = -INFINITY;
+            for (int k = 0; k < kTcKeys / 16; ++k)
+                tc_mma_f16(tO, tc_desc(sP + 256 * k, 128, 1024), tc_desc(sV + 2 * k * SBO, SBO, 128), ID_O,
+                           kt > 0 || k > 0);
+            tc_commit(&bars[1]);
         }
-        // online softmax (base 2): new row maxima over the quad's 16 keys each
-        float mx0 = mrow[0], mx1 = mrow[1];
-#pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
-            mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
-        }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float al0 = ex2((mrow[0] - mx0) * sl2), al1 = ex2((mrow[1] - mx1) * sl2);
-        mrow[0] = mx0;
-        mrow[1] = mx1;
-        const float ms0 = mx0 * sl2, ms1 = mx1 * sl2;
-        float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            sc[n][0] = ex2(fmaf(sc[n][0], sl2, -ms0));
-            sc[n][1] = ex2(fmaf(sc[n][1], sl2, -ms0));
-            sc[n][2] = ex2(fmaf(sc[n][2], sl2, -ms1));
-            sc[n][3] = ex2(fmaf(sc[n][3], sl2, -ms1));
-            ls0 += sc[n][0] + sc[n][1];
-            ls1 += sc[n][2] + sc[n][3];
-        }
-        lrow[0] = fmaf(lrow[0], al0, ls0);
-        lrow[1] = fmaf(lrow[1], al1, ls1);
-#pragma unroll
-        for (int n = 0; n < NO; ++n) {
-            o[n][0] *= al0;
-            o[n][1] *= al0;
-            o[n][2] *= al1;
-            o[n][3] *= al1;
-        }
-        // P V: P (fp16) as the A operand, 16 keys per step
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t a0 = pack_h2(sc[2 * kk][0], sc[2 * kk][1]);
-            const uint32_t a1 = pack_h2(sc[2 * kk][2], sc[2 * kk][3]);
-            const uint32_t a2 = pack_h2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-            const uint32_t a3 = pack_h2(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-#pragma unroll
-            for (int nn = 0; nn < NO / 2; ++nn) {
-                uint32_t b[4];
-                ldsm_x4_t(b, vs + swz<D>(16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1), 2 * nn + (lane >> 4)));
-                mma16816(o[2 * nn], a0, a1, a2, a3, b[0], b[1]);
-                mma16816(o[2 * nn + 1], a0, a1, a2, a3, b[2], b[3]);
-            }
-        }
-        __syncthreads();   // the stage is refilled two tiles on
+        ++nO;
+        ok = __syncthreads_and(tc_wait_bar(&bars[1], ph));
+        ph ^= 1u;
+        if (kt + 1 < nt) cp_async_wait<0>();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
     }
-
-    // rows' sums over the quad, then the output rows inside the sequence
-    float l0 = lrow[0], l1 = lrow[1];
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const float r0 = 1.f / l0, r1 = 1.f / l1;
-    __half *orow = O + (((size_t)i * hq + h) * t_stride + row0) * D + 2 * tq;
+    if (!ok) {
+        // a wait ran out: flag it, let every issued MMA finish (bounded:
+        // each barrier's last commit completes phase (commits - 1) mod 2)
+        // before the tensor memory is released, write nothing
+        if (tid == 0) atomicOr(dv.status, KIVI_FLAG_WAIT);
+        if (nS > 0) tc_wait_bar(&bars[0], (unsigned)(nS - 1) & 1u);
+        if (nO > 0) tc_wait_bar(&bars[1], (unsigned)(nO - 1) & 1u);
+    } else {
+        // the output rows (tcgen05.ld is warp-wide: every lane loads, the
+        // rows inside the sequence are stored)
+        const float r = 1.f / lsum;
+        __half *orow = O + (((size_t)i * hq + h) * t_stride + min(row, t - 1)) * D;
 #pragma unroll
-    for (int n = 0; n < NO; ++n) {
-        if (row0 < t) *reinterpret_cast<uint32_t *>(orow + 8 * n) = pack_h2(o[n][0] * r0, o[n][1] * r0);
-        if (row0 + 8 < t)
-            *reinterpret_cast<uint32_t *>(orow + (size_t)8 * D + 8 * n) = pack_h2(o[n][2] * r1, o[n][3] * r1);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tc_ld32(tO + lane_off + c0, o);
+            tc_wait_ld();
+            if (row < t)
+#pragma unroll
+                for (int c = 0; c < 32; c += 8)
+                    *reinterpret_cast<uint4 *>(orow + c0 + c) =
+                        make_uint4(pack_h2(__uint_as_float(o[c]) * r, __uint_as_float(o[c + 1]) * r),
+                                   pack_h2(__uint_as_float(o[c + 2]) * r, __uint_as_float(o[c + 3]) * r),
+                                   pack_h2(__uint_as_float(o[c + 4]) * r, __uint_as_float(o[c + 5]) * r),
+                                   pack_h2(__uint_as_float(o[c + 6]) * r, __uint_as_float(o[c + 7]) * r));
+        }
     }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc_dealloc(taddr, 256);
+    if (!ok) return;
 
-    // epilogue: the first query head of each kv head packs its diagonal tile
+    // epilogue: the first query head of each kv head packs the tile's two
+    // 64-token key / value tiles, still in the two stages; Q's region holds
+    // the staging
     if (h % hg == 0) {
-        const __half *kd = (qt & 1) ? st1 : st0;
-        unsigned char *work = reinterpret_cast<unsigned char *>((qt & 1) ? st0 : sq);
-        if (g.kbits == 2 && g.vbits == 2) pack_diagonal_g<D, 2, 2>(g, dv, kd, kd + TILE, work, i, j, tb, t);
-        else if (g.kbits == 2) pack_diagonal_g<D, 2, 4>(g, dv, kd, kd + TILE, work, i, j, tb, t);
-        else if (g.vbits == 2) pack_diagonal_g<D, 4, 2>(g, dv, kd, kd + TILE, work, i, j, tb, t);
-        else pack_diagonal_g<D, 4, 4>(g, dv, kd, kd + TILE, work, i, j, tb, t);
+        for (int k = 0; k < 2; ++k) {
+            const int kb = tb + k * kTcKeys, kt = kb / kTcKeys;
+            if (kb >= t) break;
+            const unsigned char *sK = sKV + 2 * (kt & 1) * KVB;
+            pack_diagonal_bits<D>(g, dv, sK, sK + KVB, sQ, i, j, kb, t);
+            __syncthreads();   // the staging is reused
+        }
         if (tb == 0 && j == 0 && threadIdx.x == 0) {
             dv.T[i] = t;
             dv.Tqk[i] = t - t % g.R;
@@ -296,14 +357,14 @@ __global__ void __launch_bounds__(128, 2)
 }
 
 template <int D>
-cudaError_t launch_d(const KiviGeom &g, const KiviDev &dv, const __half *Q, const __half *K, const __half *V,
-                     __half *O, const SeqLens &lens, int t_stride, int hq, int maxt, cudaStream_t st) {
-    const size_t smem = (size_t)5 * kTileRows * D * 2;
-    cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+cudaError_t launch_tc(const KiviGeom &g, const KiviDev &dv, const __half *Q, const __half *K, const __half *V,
+                      __half *O, const SeqLens &lens, int t_stride, int hq, int maxt, cudaStream_t st) {
+    const size_t smem = (size_t)kTcRows * D * 2 + (size_t)4 * kTcKeys * D * 2 + (size_t)kTcRows * kTcKeys * 2;
+    cudaError_t e = cudaFuncSetAttribute(prefill_attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    const int nqt = maxt > 0 ? (maxt + kTileRows - 1) / kTileRows : 1;
-    prefill_attn_kernel<D><<<dim3(nqt, hq, g.b), 128, smem, st>>>(g, dv, Q, K, V, O, lens, t_stride, hq);
+    const int nqt = maxt > 0 ? (maxt + kTcRows - 1) / kTcRows : 1;
+    prefill_attn_tc_kernel<D><<<dim3(nqt, hq, g.b), 128, smem, st>>>(g, dv, Q, K, V, O, lens, t_stride, hq);
     return cudaGetLastError();
 }
 
@@ -315,6 +376,6 @@ cudaError_t kivi_launch_prefill_attn(const KiviGeom &g, const KiviDev &dv, const
     if (g.G > 64 || (g.d != 64 && g.d != 128)) return cudaErrorInvalidValue;
     int maxt = 0;
     for (int i = 0; i < g.b; ++i) maxt = lens.t[i] > maxt ? lens.t[i] : maxt;
-    return g.d == 64 ? launch_d<64>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st)
-                     : launch_d<128>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st);
+    return g.d == 64 ? launch_tc<64>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st)
+                     : launch_tc<128>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st);
 }
