@@ -123,20 +123,27 @@ __device__ void pack_diagonal_bits(const KiviGeom &g, const KiviDev &dv, const u
 }
 
 // ---------------------------------------------------------------------------
-// The attention on the 5th-generation tensor cores (tcgen05): a CTA
-// is 128 query rows of one query head, 4 warps, and thread r owns row r
-// (tensor-memory lane r).  Per 64-key tile: S = Q K^T (M 128, N 64, K d)
-// into tensor memory; each thread reads its row of S, applies the causal
-// mask and the online softmax (base 2, its whole row in registers), and
-// writes its fp16 weights P into shared memory; O += P V (M 128, N d, K 64)
-// accumulates in tensor memory.  One thread issues the MMAs; their
-// completion arrives on an mbarrier (bounded waits).  K and V tiles are
-// double-buffered by 16-byte cp.async copies.  The running maximum is
-// raised lazily: O and the row sum are rescaled only when a row's maximum
-// grows by more than 8 (log2 units), so P stays below 2^8.
+// The attention on the 5th-generation tensor cores (tcgen05): a CTA is 128
+// query rows of one query head, 4 warps, and thread r owns row r (tensor-
+// memory lane r).  Per 64-key tile kt: S = Q K^T (M 128, N 64, K d) into one
+// of two S buffers in tensor memory; each thread reads its row of S, applies
+// the causal mask and the online softmax (base 2, its whole row in
+// registers) and writes its fp16 weights P back over the S buffer (two
+// weights a column), where O += P V (M 128, N d, K 64) takes them as its A
+// operand; O accumulates in tensor memory.  One thread issues the MMAs;
+// their completion arrives on mbarriers (bounded waits).
+//
+// Pipeline: S of tile kt + 1 is issued before the softmax of tile kt (its
+// buffer is free once P V of tile kt - 1, which read P from it, is done), so
+// the tensor core computes it while the threads work.  K is loaded two
+// tiles ahead and V one tile ahead (16-byte cp.async copies, two stages
+// each).  The running maximum is raised lazily: O and the row sum are
+// rescaled only when a row's maximum grows by more than 8 (log2 units), so
+// P stays below 2^8.
 // Shared memory (no-swizzle core-matrix layouts, 8 rows x 16 bytes each):
-//   Q [128][D], K and V [2][64][D], P [128][64]: 112 KB at d = 128.
-// Tensor memory: S in columns 0-63, O in 64-(64 + D): 256 columns.
+//   Q [128][D], K [2][64][D], V [2][64][D]: 96 KB at d = 128.
+// Tensor memory: S / P buffers in columns 0-63 and 64-127, O in
+// 128-(128 + D): 256 columns.
 // ---------------------------------------------------------------------------
 constexpr int kTcRows = 128, kTcKeys = 64;
 
@@ -167,6 +174,15 @@ __device__ __forceinline__ bool tc_wait_bar(uint64_t *bar, unsigned phase) {
     return false;
 }
 
+// shared-memory writes (cp.async landed, generic stores) and tensor-memory
+// stores of every thread ordered before what the issuing thread does next
+__device__ __forceinline__ void tc_sync() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
 template <int D>
 __global__ void __launch_bounds__(128, 1)
     prefill_attn_tc_kernel(KiviGeom g, KiviDev dv, const __half *__restrict__ Q, const __half *__restrict__ K,
@@ -175,9 +191,9 @@ __global__ void __launch_bounds__(128, 1)
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int QB = kTcRows * D * 2, KVB = kTcKeys * D * 2, SBO = 16 * D;
     unsigned char *sQ = smem;
-    unsigned char *sKV = smem + QB;   // stage s: K at sKV + 2 s KVB, V after it
-    unsigned char *sP = sKV + 4 * KVB;
-    __shared__ __align__(8) uint64_t bars[2];   // S done, O done
+    unsigned char *sK = smem + QB;        // stage s at sK + s KVB
+    unsigned char *sV = sK + 2 * KVB;     // stage s at sV + s KVB
+    __shared__ __align__(8) uint64_t bars[3];   // S buffer 0 done, S buffer 1 done, P V done
     __shared__ uint32_t s_taddr;
     const int qt = gridDim.x - 1 - blockIdx.x;   // the longest tiles first
     const int h = blockIdx.y, i = blockIdx.z;
@@ -196,52 +212,64 @@ __global__ void __launch_bounds__(128, 1)
     const __half *kbase = K + ((size_t)i * g.h + j) * t_stride * D;
     const __half *vbase = V + ((size_t)i * g.h + j) * t_stride * D;
     const int nt = min((t + kTcKeys - 1) / kTcKeys, (tb + kTcRows) / kTcKeys);   // key tiles
+    auto tile_rows = [&](int kt) { return min(kTcKeys, t - kt * kTcKeys); };
     load_core<D>(sQ, Q + (((size_t)i * hq + h) * t_stride + tb) * D, kTcRows, min(kTcRows, t - tb));
-    load_core<D>(sKV, kbase, kTcKeys, min(kTcKeys, t));
-    load_core<D>(sKV + KVB, vbase, kTcKeys, min(kTcKeys, t));
+    load_core<D>(sK, kbase, kTcKeys, tile_rows(0));
+    load_core<D>(sV, vbase, kTcKeys, tile_rows(0));
+    if (nt > 1) load_core<D>(sK + KVB, kbase + (size_t)kTcKeys * D, kTcKeys, tile_rows(1));
     cp_async_commit();
     if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_u32(&bars[0])) : "memory");
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_u32(&bars[1])) : "memory");
+        for (int k = 0; k < 3; ++k)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_u32(&bars[k])) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) tc_alloc(&s_taddr, 256);
     cp_async_wait<0>();
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t taddr = s_taddr;
-    const uint32_t tS = taddr, tO = taddr + 64;
+    tc_sync();
+    const uint32_t taddr = s_taddr, tO = taddr + 128;
     const uint32_t lane_off = (uint32_t)(32 * warp) << 16;   // this warp's tensor-memory lanes
     constexpr uint32_t ID_S = tc_idesc_f16(kTcRows, kTcKeys, 0), ID_O = tc_idesc_f16(kTcRows, D, 1);
     const float sl2 = 1.4426950408889634f / sqrtf((float)D);   // log2(e) / sqrt(d)
     const int row = tb + tid;
-    float mref = -INFINITY, lsum = 0.f;   // the row's reference maximum (raw score units) and sum
-    unsigned ph = 0;
-    int nS = 0, nO = 0;   // commits issued on each barrier (the same count in every thread)
-    bool ok = true;
-    for (int kt = 0; kt < nt && ok; ++kt) {
-        const int st = kt & 1;
-        unsigned char *sK = sKV + 2 * st * KVB, *sV = sK + KVB;
-        if (tid == 0) {
+    auto issue_s = [&](int kt) {   // S of tile kt into buffer kt mod 2 (one thread)
+        const uint32_t tS = taddr + 64 * (kt & 1);
+        const unsigned char *k = sK + (kt & 1) * KVB;
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k)
-                tc_mma_f16(tS, tc_desc(sQ + 256 * k, 128, SBO), tc_desc(sK + 256 * k, 128, SBO), ID_S, k > 0);
-            tc_commit(&bars[0]);
-        }
-        ++nS;
-        if (kt + 1 < nt) {   // the next tile streams into the other stage (its last MMAs are done)
-            unsigned char *nK = sKV + 2 * (st ^ 1) * KVB;
-            const int nb = (kt + 1) * kTcKeys;
-            load_core<D>(nK, kbase + (size_t)nb * D, kTcKeys, min(kTcKeys, t - nb));
-            load_core<D>(nK + KVB, vbase + (size_t)nb * D, kTcKeys, min(kTcKeys, t - nb));
-            cp_async_commit();
-        }
-        ok = __syncthreads_and(tc_wait_bar(&bars[0], ph));
+        for (int c = 0; c < D / 16; ++c)
+            tc_mma_f16(tS, tc_desc(sQ + 256 * c, 128, SBO), tc_desc(k + 256 * c, 128, SBO), ID_S, c > 0);
+        tc_commit(&bars[kt & 1]);
+    };
+    float mref = -INFINITY, lsum = 0.f;   // the row's reference maximum (raw score units) and sum
+    int nS0 = 0, nS1 = 0, nO = 0;   // commits issued on each barrier (the same in every thread)
+    bool ok = true;
+    if (tid == 0) issue_s(0);
+    nS0 = 1;
+    for (int kt = 0; kt < nt; ++kt) {
+        const int b = kt & 1;
+        // S of this tile is done (K of this tile is free)
+        ok = __syncthreads_and(tc_wait_bar(&bars[b], (unsigned)(kt >> 1) & 1u));
         if (!ok) break;
         tc_fence_after();
+        // P V of the previous tile is done (its P buffer, V stage and O are free)
+        if (kt > 0) {
+            ok = __syncthreads_and(tc_wait_bar(&bars[2], (unsigned)(kt - 1) & 1u));
+            if (!ok) break;
+        }
+        // the copies of K of the next tile and V of this one (issued one
+        // iteration ago) have landed
+        cp_async_wait<0>();
+        tc_sync();
+        if (kt + 1 < nt) {
+            if (tid == 0) issue_s(kt + 1);
+            if (b) ++nS0; else ++nS1;
+        }
+        // K two tiles on into this tile's K stage, V of the next tile into
+        // the other V stage
+        if (kt + 2 < nt) load_core<D>(sK + b * KVB, kbase + (size_t)(kt + 2) * kTcKeys * D, kTcKeys, tile_rows(kt + 2));
+        if (kt + 1 < nt) load_core<D>(sV + (b ^ 1) * KVB, vbase + (size_t)(kt + 1) * kTcKeys * D, kTcKeys, tile_rows(kt + 1));
+        cp_async_commit();
         // this row's 64 scores
+        const uint32_t tS = taddr + 64 * b;
         uint32_t sr[2][32];
         tc_ld32(tS + lane_off, sr[0]);
         tc_ld32(tS + lane_off + 32, sr[1]);
@@ -269,7 +297,6 @@ __global__ void __launch_bounds__(128, 1)
                 for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
                 tc_st32(tO + lane_off + c0, o);
             }
-            tc_wait_st();
         }
         lsum *= alpha;
         const float ms = mref * sl2;
@@ -280,39 +307,31 @@ __global__ void __launch_bounds__(128, 1)
             lsum += p0 + p1;
             pw[c] = pack_h2(p0, p1);
         }
-        // P row: 8 chunks of 8 keys, core (row / 8, chunk) at (row / 8) 1024 + chunk 128
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4 *>(sP + (tid >> 3) * 1024 + c * 128 + (tid & 7) * 16) =
-                make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
+        // P over the S buffer: column c = weights of keys 2c, 2c + 1
+        tc_st32(tS + lane_off, pw);
+        tc_wait_st();
+        tc_sync();
         if (tid == 0) {
+            const unsigned char *v = sV + b * KVB;
 #pragma unroll
-            for (int k = 0; k < kTcKeys / 16; ++k)
-                tc_mma_f16(tO, tc_desc(sP + 256 * k, 128, 1024), tc_desc(sV + 2 * k * SBO, SBO, 128), ID_O,
-                           kt > 0 || k > 0);
-            tc_commit(&bars[1]);
+            for (int c = 0; c < kTcKeys / 16; ++c)
+                tc_mma_f16_ta(tO, tS + 8 * c, tc_desc(v + 2 * c * SBO, SBO, 128), ID_O, kt > 0 || c > 0);
+            tc_commit(&bars[2]);
         }
         ++nO;
-        ok = __syncthreads_and(tc_wait_bar(&bars[1], ph));
-        ph ^= 1u;
-        if (kt + 1 < nt) cp_async_wait<0>();
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
     }
+    if (ok && nO > 0) ok = __syncthreads_and(tc_wait_bar(&bars[2], (unsigned)(nO - 1) & 1u));
     if (!ok) {
         // a wait ran out: flag it, let every issued MMA finish (bounded:
         // each barrier's last commit completes phase (commits - 1) mod 2)
         // before the tensor memory is released, write nothing
         if (tid == 0) atomicOr(dv.status, KIVI_FLAG_WAIT);
-        if (nS > 0) tc_wait_bar(&bars[0], (unsigned)(nS - 1) & 1u);
-        if (nO > 0) tc_wait_bar(&bars[1], (unsigned)(nO - 1) & 1u);
+        if (nS0 > 0) tc_wait_bar(&bars[0], (unsigned)(nS0 - 1) & 1u);
+        if (nS1 > 0) tc_wait_bar(&bars[1], (unsigned)(nS1 - 1) & 1u);
+        if (nO > 0) tc_wait_bar(&bars[2], (unsigned)(nO - 1) & 1u);
+        cp_async_wait<0>();
     } else {
+        tc_fence_after();
         // the output rows (tcgen05.ld is warp-wide: every lane loads, the
         // rows inside the sequence are stored)
         const float r = 1.f / lsum;
@@ -338,14 +357,13 @@ __global__ void __launch_bounds__(128, 1)
     if (!ok) return;
 
     // epilogue: the first query head of each kv head packs the tile's two
-    // 64-token key / value tiles, still in the two stages; Q's region holds
+    // 64-token key / value tiles, still in their stages; Q's region holds
     // the staging
     if (h % hg == 0) {
         for (int k = 0; k < 2; ++k) {
             const int kb = tb + k * kTcKeys, kt = kb / kTcKeys;
             if (kb >= t) break;
-            const unsigned char *sK = sKV + 2 * (kt & 1) * KVB;
-            pack_diagonal_bits<D>(g, dv, sK, sK + KVB, sQ, i, j, kb, t);
+            pack_diagonal_bits<D>(g, dv, sK + (kt & 1) * KVB, sV + (kt & 1) * KVB, sQ, i, j, kb, t);
             __syncthreads();   // the staging is reused
         }
         if (tb == 0 && j == 0 && threadIdx.x == 0) {
@@ -359,7 +377,7 @@ __global__ void __launch_bounds__(128, 1)
 template <int D>
 cudaError_t launch_tc(const KiviGeom &g, const KiviDev &dv, const __half *Q, const __half *K, const __half *V,
                       __half *O, const SeqLens &lens, int t_stride, int hq, int maxt, cudaStream_t st) {
-    const size_t smem = (size_t)kTcRows * D * 2 + (size_t)4 * kTcKeys * D * 2 + (size_t)kTcRows * kTcKeys * 2;
+    const size_t smem = (size_t)kTcRows * D * 2 + (size_t)4 * kTcKeys * D * 2;
     cudaError_t e = cudaFuncSetAttribute(prefill_attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;

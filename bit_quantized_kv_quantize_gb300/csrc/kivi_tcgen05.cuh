@@ -53,6 +53,15 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d, uint64_t a, uint64_t b, u
         "l"(a), "l"(b), "r"(idesc), "r"(acc ? 1 : 0)
         : "memory");
 }
+// the same with A in tensor memory (a: its address; lane = row, column c =
+// fp16 pair (2c, 2c + 1) of K)
+__device__ __forceinline__ void tc_mma_f16_ta(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, bool acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(acc ? 1 : 0)
+        : "memory");
+}
 // the barrier completes one arrival when the MMAs issued so far are done
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
