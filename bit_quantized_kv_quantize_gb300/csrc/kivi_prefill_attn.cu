@@ -11,6 +11,11 @@
 // and values, and, in the epilogue of the CTA that holds the 64-token K and
 // V tiles of its own query rows (its diagonal tiles), the prefill split and
 // packing of items 2-4 for those tiles.
+#include <cstring>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "kivi_mma.cuh"
 #include "kivi_pack_impl.cuh"
 #include "kivi_tcgen05.cuh"
@@ -19,23 +24,17 @@ namespace {
 
 constexpr int kTileRows = 64;   // tokens of a packed tile
 
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// byte offset of 16-byte chunk c of row r in a [rows][D] fp16 tile in the
-// tensor cores' no-swizzle core-matrix layout (8 rows x 16 bytes, 128
-// contiguous bytes; 8-row groups 16 D bytes apart)
+// byte offset of 16-byte chunk c of row r in a 64-row fp16 tile in the
+// tensor cores' no-swizzle core-matrix layout, chunk-major (the attention
+// kernel's layout below)
 template <int D>
 __device__ __forceinline__ int chunk_at(int r, int c) {
-    return (r >> 3) * 16 * D + c * 128 + (r & 7) * 16;
+    return c * kTileRows * 16 + r * 16;
 }
 
 // The cache's share of the diagonal tile [tb, tb + 64) of (sequence i, kv
@@ -130,34 +129,33 @@ __device__ void pack_diagonal_bits(const KiviGeom &g, const KiviDev &dv, const u
 // the causal mask and the online softmax (base 2, its whole row in
 // registers) and writes its fp16 weights P back over the S buffer (two
 // weights a column), where O += P V (M 128, N d, K 64) takes them as its A
-// operand; O accumulates in tensor memory.  One thread issues the MMAs;
-// their completion arrives on mbarriers (bounded waits).
+// operand; O accumulates in tensor memory.  One thread issues the MMAs and
+// the tile copies; completions arrive on mbarriers (bounded waits).
 //
 // Pipeline: S of tile kt + 1 is issued before the softmax of tile kt (its
-// buffer is free once P V of tile kt - 1, which read P from it, is done), so
-// the tensor core computes it while the threads work.  K is loaded two
-// tiles ahead and V one tile ahead (16-byte cp.async copies, two stages
-// each).  The running maximum is raised lazily: O and the row sum are
-// rescaled only when a row's maximum grows by more than 8 (log2 units), so
-// P stays below 2^8.
-// Shared memory (no-swizzle core-matrix layouts, 8 rows x 16 bytes each):
+// buffer is free once P V of tile kt - 1, which read P from it, is done).
+// Q, K and V tiles come by TMA, one tensor copy each, K two tiles ahead and
+// V one tile ahead (two stages each).  The running maximum is raised
+// lazily: O and the row sum are rescaled only when a row's maximum grows by
+// more than 8 (log2 units), so P stays below 2^8.
+//
+// Tiles in shared memory use the no-swizzle core-matrix layout, chunk-major:
+// row r, 16-byte chunk c of a tile of ROWS rows at byte c ROWS 16 + r 16
+// (core matrices of 8 rows x 16 bytes contiguous).  A tensor map over the
+// fp16 [rows][D] array with dimensions (8 elements, rows, D / 8 chunks) and
+// strides (2 D bytes, 16 bytes) writes exactly this with one copy per tile
+// (rows past the array read as zero); value rows past the sequence are
+// zeroed after the copy, as the weights they meet are zero.
 //   Q [128][D], K [2][64][D], V [2][64][D]: 96 KB at d = 128.
 // Tensor memory: S / P buffers in columns 0-63 and 64-127, O in
 // 128-(128 + D): 256 columns.
 // ---------------------------------------------------------------------------
 constexpr int kTcRows = 128, kTcKeys = 64;
 
-// rows [0, valid) of a [rows][D] fp16 tile from src (rows D apart) into
-// core-matrix layout (8-row groups 16 D bytes apart), the rest zero
-template <int D>
-__device__ __forceinline__ void load_core(unsigned char *dst, const __half *src, int rows, int valid) {
-    constexpr int CPR = D / 8;
-    const int last = valid > 0 ? valid - 1 : 0;
-    for (int e = threadIdx.x; e < rows * CPR; e += blockDim.x) {
-        const int r = e / CPR, c = e - r * CPR;
-        cp_async16(dst + (r >> 3) * 16 * D + c * 128 + (r & 7) * 16, src + (size_t)min(r, last) * D + 8 * c,
-                   r < valid);
-    }
+// byte offset of 16-byte chunk c of row r in a chunk-major tile of ROWS rows
+template <int ROWS>
+__device__ __forceinline__ int cm_at(int r, int c) {
+    return c * ROWS * 16 + r * 16;
 }
 
 __device__ __forceinline__ bool tc_wait_bar(uint64_t *bar, unsigned phase) {
@@ -174,8 +172,21 @@ __device__ __forceinline__ bool tc_wait_bar(uint64_t *bar, unsigned phase) {
     return false;
 }
 
-// shared-memory writes (cp.async landed, generic stores) and tensor-memory
-// stores of every thread ordered before what the issuing thread does next
+// one TMA tile copy (rows row0.. of the tensor map's array, all D columns)
+// into dst, completing `bytes` on bar (one thread)
+__device__ __forceinline__ void tma_tile(void *dst, const CUtensorMap *tm, int row0, uint64_t *bar,
+                                         unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc_smem_u32(bar)), "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+        "%4}], [%5];" ::"r"(tc_smem_u32(dst)),
+        "l"(tm), "r"(0), "r"(row0), "r"(0), "r"(tc_smem_u32(bar))
+        : "memory");
+}
+
+// shared-memory writes (generic stores) and tensor-memory stores of every
+// thread ordered before what the issuing thread does next
 __device__ __forceinline__ void tc_sync() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
@@ -185,15 +196,18 @@ __device__ __forceinline__ void tc_sync() {
 
 template <int D>
 __global__ void __launch_bounds__(128, 1)
-    prefill_attn_tc_kernel(KiviGeom g, KiviDev dv, const __half *__restrict__ Q, const __half *__restrict__ K,
-                           const __half *__restrict__ V, __half *__restrict__ O, SeqLens lens, int t_stride,
-                           int hq) {
+    prefill_attn_tc_kernel(KiviGeom g, KiviDev dv, const __grid_constant__ CUtensorMap tmQ,
+                           const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                           __half *__restrict__ O, SeqLens lens, int t_stride, int hq) {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int QB = kTcRows * D * 2, KVB = kTcKeys * D * 2, SBO = 16 * D;
+    constexpr int QB = kTcRows * D * 2, KVB = kTcKeys * D * 2;
+    constexpr unsigned QLBO = kTcRows * 16, KLBO = kTcKeys * 16;   // chunk strides
     unsigned char *sQ = smem;
-    unsigned char *sK = smem + QB;        // stage s at sK + s KVB
-    unsigned char *sV = sK + 2 * KVB;     // stage s at sV + s KVB
-    __shared__ __align__(8) uint64_t bars[3];   // S buffer 0 done, S buffer 1 done, P V done
+    unsigned char *sK = smem + QB;      // stage s at sK + s KVB
+    unsigned char *sV = sK + 2 * KVB;   // stage s at sV + s KVB
+    // S buffer 0 and 1 done, P V done, Q landed, K stage 0 / 1 landed, V stage 0 / 1 landed
+    __shared__ __align__(8) uint64_t bars[8];
+    uint64_t *const bS = bars, *const bO = bars + 2, *const bQ = bars + 3, *const bK = bars + 4, *const bV = bars + 6;
     __shared__ uint32_t s_taddr;
     const int qt = gridDim.x - 1 - blockIdx.x;   // the longest tiles first
     const int h = blockIdx.y, i = blockIdx.z;
@@ -209,23 +223,29 @@ __global__ void __launch_bounds__(128, 1)
         return;
     }
     const int tid = threadIdx.x, warp = tid >> 5;
-    const __half *kbase = K + ((size_t)i * g.h + j) * t_stride * D;
-    const __half *vbase = V + ((size_t)i * g.h + j) * t_stride * D;
+    const int krow0 = (i * g.h + j) * t_stride;   // this kv head's first row in K and V
     const int nt = min((t + kTcKeys - 1) / kTcKeys, (tb + kTcRows) / kTcKeys);   // key tiles
-    auto tile_rows = [&](int kt) { return min(kTcKeys, t - kt * kTcKeys); };
-    load_core<D>(sQ, Q + (((size_t)i * hq + h) * t_stride + tb) * D, kTcRows, min(kTcRows, t - tb));
-    load_core<D>(sK, kbase, kTcKeys, tile_rows(0));
-    load_core<D>(sV, vbase, kTcKeys, tile_rows(0));
-    if (nt > 1) load_core<D>(sK + KVB, kbase + (size_t)kTcKeys * D, kTcKeys, tile_rows(1));
-    cp_async_commit();
+    // copies issued per barrier (the same count in every thread)
+    int nQ = 0, nK0 = 0, nK1 = 0, nV0 = 0, nV1 = 0, nS0 = 0, nS1 = 0, nO = 0;
     if (tid == 0) {
-        for (int k = 0; k < 3; ++k)
+        for (int k = 0; k < 8; ++k)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_u32(&bars[k])) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    __syncthreads();
+    if (tid == 0) {
+        tma_tile(sQ, &tmQ, (i * hq + h) * t_stride + tb, bQ, QB);
+        tma_tile(sK, &tmK, krow0, &bK[0], KVB);
+        tma_tile(sV, &tmV, krow0, &bV[0], KVB);
+        if (nt > 1) tma_tile(sK + KVB, &tmK, krow0 + kTcKeys, &bK[1], KVB);
+    }
+    nQ = nK0 = nV0 = 1;
+    nK1 = nt > 1 ? 1 : 0;
     if (warp == 0) tc_alloc(&s_taddr, 256);
-    cp_async_wait<0>();
-    tc_sync();
+    bool ok = tc_wait_bar(bQ, 0) && tc_wait_bar(&bK[0], 0);
+    tc_fence_before();
+    ok = __syncthreads_and(ok);
+    tc_fence_after();
     const uint32_t taddr = s_taddr, tO = taddr + 128;
     const uint32_t lane_off = (uint32_t)(32 * warp) << 16;   // this warp's tensor-memory lanes
     constexpr uint32_t ID_S = tc_idesc_f16(kTcRows, kTcKeys, 0), ID_O = tc_idesc_f16(kTcRows, D, 1);
@@ -236,38 +256,37 @@ __global__ void __launch_bounds__(128, 1)
         const unsigned char *k = sK + (kt & 1) * KVB;
 #pragma unroll
         for (int c = 0; c < D / 16; ++c)
-            tc_mma_f16(tS, tc_desc(sQ + 256 * c, 128, SBO), tc_desc(k + 256 * c, 128, SBO), ID_S, c > 0);
-        tc_commit(&bars[kt & 1]);
+            tc_mma_f16(tS, tc_desc(sQ + 2 * c * QLBO, QLBO, 128), tc_desc(k + 2 * c * KLBO, KLBO, 128), ID_S, c > 0);
+        tc_commit(&bS[kt & 1]);
     };
     float mref = -INFINITY, lsum = 0.f;   // the row's reference maximum (raw score units) and sum
-    int nS0 = 0, nS1 = 0, nO = 0;   // commits issued on each barrier (the same in every thread)
-    bool ok = true;
-    if (tid == 0) issue_s(0);
-    nS0 = 1;
-    for (int kt = 0; kt < nt; ++kt) {
+    if (ok) {
+        if (tid == 0) issue_s(0);
+        nS0 = 1;
+    }
+    for (int kt = 0; kt < nt && ok; ++kt) {
         const int b = kt & 1;
-        // S of this tile is done (K of this tile is free)
-        ok = __syncthreads_and(tc_wait_bar(&bars[b], (unsigned)(kt >> 1) & 1u));
+        // S of this tile done (its K stage is free), P V of the previous
+        // tile done (its S / P buffer, V stage and O are free), K of the
+        // next tile landed
+        bool w = tc_wait_bar(&bS[b], (unsigned)(kt >> 1) & 1u);
+        if (kt > 0) w = w && tc_wait_bar(bO, (unsigned)(kt - 1) & 1u);
+        if (kt + 1 < nt) w = w && tc_wait_bar(&bK[b ^ 1], (unsigned)((kt + 1) >> 1) & 1u);
+        ok = __syncthreads_and(w);
         if (!ok) break;
         tc_fence_after();
-        // P V of the previous tile is done (its P buffer, V stage and O are free)
-        if (kt > 0) {
-            ok = __syncthreads_and(tc_wait_bar(&bars[2], (unsigned)(kt - 1) & 1u));
-            if (!ok) break;
+        if (tid == 0) {
+            if (kt + 1 < nt) issue_s(kt + 1);
+            if (kt + 2 < nt) tma_tile(sK + b * KVB, &tmK, krow0 + (kt + 2) * kTcKeys, &bK[b], KVB);
+            if (kt + 1 < nt) tma_tile(sV + (b ^ 1) * KVB, &tmV, krow0 + (kt + 1) * kTcKeys, &bV[b ^ 1], KVB);
         }
-        // the copies of K of the next tile and V of this one (issued one
-        // iteration ago) have landed
-        cp_async_wait<0>();
-        tc_sync();
         if (kt + 1 < nt) {
-            if (tid == 0) issue_s(kt + 1);
             if (b) ++nS0; else ++nS1;
+            if (b) ++nV0; else ++nV1;
         }
-        // K two tiles on into this tile's K stage, V of the next tile into
-        // the other V stage
-        if (kt + 2 < nt) load_core<D>(sK + b * KVB, kbase + (size_t)(kt + 2) * kTcKeys * D, kTcKeys, tile_rows(kt + 2));
-        if (kt + 1 < nt) load_core<D>(sV + (b ^ 1) * KVB, vbase + (size_t)(kt + 1) * kTcKeys * D, kTcKeys, tile_rows(kt + 1));
-        cp_async_commit();
+        if (kt + 2 < nt) {
+            if (b) ++nK1; else ++nK0;
+        }
         // this row's 64 scores
         const uint32_t tS = taddr + 64 * b;
         uint32_t sr[2][32];
@@ -310,26 +329,40 @@ __global__ void __launch_bounds__(128, 1)
         // P over the S buffer: column c = weights of keys 2c, 2c + 1
         tc_st32(tS + lane_off, pw);
         tc_wait_st();
+        // V of this tile landed; its rows past the sequence zeroed (they
+        // meet zero weights, and the array there holds whatever it holds)
+        if (!tc_wait_bar(&bV[b], (unsigned)(kt >> 1) & 1u)) {
+            ok = false;
+        } else if (kt * kTcKeys + kTcKeys > t) {
+            const int r0 = t - kt * kTcKeys;
+            unsigned char *v = sV + b * KVB;
+            for (int e = tid; e < (kTcKeys - r0) * (D / 8); e += blockDim.x) {
+                const int r = r0 + e / (D / 8), c = e % (D / 8);
+                *reinterpret_cast<uint4 *>(v + cm_at<kTcKeys>(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
         tc_sync();
         if (tid == 0) {
             const unsigned char *v = sV + b * KVB;
 #pragma unroll
             for (int c = 0; c < kTcKeys / 16; ++c)
-                tc_mma_f16_ta(tO, tS + 8 * c, tc_desc(v + 2 * c * SBO, SBO, 128), ID_O, kt > 0 || c > 0);
-            tc_commit(&bars[2]);
+                tc_mma_f16_ta(tO, tS + 8 * c, tc_desc(v + 256 * c, 128, KLBO), ID_O, kt > 0 || c > 0);
+            tc_commit(bO);
         }
         ++nO;
     }
-    if (ok && nO > 0) ok = __syncthreads_and(tc_wait_bar(&bars[2], (unsigned)(nO - 1) & 1u));
+    if (ok && nO > 0) ok = __syncthreads_and(tc_wait_bar(bO, (unsigned)(nO - 1) & 1u));
     if (!ok) {
-        // a wait ran out: flag it, let every issued MMA finish (bounded:
-        // each barrier's last commit completes phase (commits - 1) mod 2)
-        // before the tensor memory is released, write nothing
+        // a wait ran out: flag it, let every issued copy and MMA finish
+        // (bounded: each barrier's last arrival completes phase (count - 1)
+        // mod 2) before shared and tensor memory are released, write nothing
         if (tid == 0) atomicOr(dv.status, KIVI_FLAG_WAIT);
-        if (nS0 > 0) tc_wait_bar(&bars[0], (unsigned)(nS0 - 1) & 1u);
-        if (nS1 > 0) tc_wait_bar(&bars[1], (unsigned)(nS1 - 1) & 1u);
-        if (nO > 0) tc_wait_bar(&bars[2], (unsigned)(nO - 1) & 1u);
-        cp_async_wait<0>();
+        const int cnt[8] = {nS0, nS1, nO, nQ, nK0, nK1, nV0, nV1};
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (cnt[k] > 0) tc_wait_bar(&bars[k], (unsigned)(cnt[k] - 1) & 1u);
     } else {
         tc_fence_after();
         // the output rows (tcgen05.ld is warp-wide: every lane loads, the
@@ -358,8 +391,9 @@ __global__ void __launch_bounds__(128, 1)
 
     // epilogue: the first query head of each kv head packs the tile's two
     // 64-token key / value tiles, still in their stages; Q's region holds
-    // the staging
+    // the staging (generic stores after the copies' and MMAs' accesses)
     if (h % hg == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         for (int k = 0; k < 2; ++k) {
             const int kb = tb + k * kTcKeys, kt = kb / kTcKeys;
             if (kb >= t) break;
@@ -374,15 +408,57 @@ __global__ void __launch_bounds__(128, 1)
     }
 }
 
+// The encoder of TMA tensor maps, from the driver (through the runtime, no
+// link to the driver library); null if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// Tensor map over an fp16 [rows][D] array giving chunk-major core-matrix
+// tiles of box_rows rows (see above): dimensions (8, rows, D / 8), strides
+// (2 D bytes, 16 bytes), box (8, box_rows, D / 8).
+cudaError_t make_tile_map(CUtensorMap *tm, const __half *base, long long rows, int D, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dim[3] = {8, (cuuint64_t)rows, (cuuint64_t)(D / 8)};
+    const cuuint64_t str[2] = {(cuuint64_t)D * 2, 16};
+    const cuuint32_t box[3] = {8, (cuuint32_t)box_rows, (cuuint32_t)(D / 8)};
+    const cuuint32_t es[3] = {1, 1, 1};
+    const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half *>(base), dim, str, box, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int D>
 cudaError_t launch_tc(const KiviGeom &g, const KiviDev &dv, const __half *Q, const __half *K, const __half *V,
                       __half *O, const SeqLens &lens, int t_stride, int hq, int maxt, cudaStream_t st) {
     const size_t smem = (size_t)kTcRows * D * 2 + (size_t)4 * kTcKeys * D * 2;
-    cudaError_t e = cudaFuncSetAttribute(prefill_attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    const long long ts = t_stride > 0 ? t_stride : 1;
+    CUtensorMap tq, tk, tv;   // unused when every sequence is empty (the CTAs only write counters)
+    memset(&tq, 0, sizeof tq);
+    memset(&tk, 0, sizeof tk);
+    memset(&tv, 0, sizeof tv);
+    cudaError_t e = cudaSuccess;
+    if (maxt > 0) {
+        e = make_tile_map(&tq, Q, (long long)g.b * hq * ts, D, kTcRows);
+        if (e == cudaSuccess) e = make_tile_map(&tk, K, (long long)g.b * g.h * ts, D, kTcKeys);
+        if (e == cudaSuccess) e = make_tile_map(&tv, V, (long long)g.b * g.h * ts, D, kTcKeys);
+        if (e != cudaSuccess) return e;
+    }
+    e = cudaFuncSetAttribute(prefill_attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int nqt = maxt > 0 ? (maxt + kTcRows - 1) / kTcRows : 1;
-    prefill_attn_tc_kernel<D><<<dim3(nqt, hq, g.b), 128, smem, st>>>(g, dv, Q, K, V, O, lens, t_stride, hq);
+    prefill_attn_tc_kernel<D><<<dim3(nqt, hq, g.b), 128, smem, st>>>(g, dv, tq, tk, tv, O, lens, t_stride, hq);
     return cudaGetLastError();
 }
 
@@ -394,6 +470,7 @@ cudaError_t kivi_launch_prefill_attn(const KiviGeom &g, const KiviDev &dv, const
     if (g.G > 64 || (g.d != 64 && g.d != 128)) return cudaErrorInvalidValue;
     int maxt = 0;
     for (int i = 0; i < g.b; ++i) maxt = lens.t[i] > maxt ? lens.t[i] : maxt;
+    if (maxt > 0 && ((long long)g.b * hq * t_stride >= (1LL << 31))) return cudaErrorInvalidValue;   // TMA row coordinates
     return g.d == 64 ? launch_tc<64>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st)
                      : launch_tc<128>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st);
 }

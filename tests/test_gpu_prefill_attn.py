@@ -125,3 +125,16 @@ def test_prefill_attn_full_llama3_8b_gqa_32k():
     assert a.check() == 0
     a.close()
     p.close()
+
+
+def test_prefill_attn_all_empty():
+    """Every sequence empty: nothing attended, the counters reset, and a
+    decode afterwards writes zero outputs (as after kivi_prefill)."""
+    c = K.KiviCache(2, 2, 64, 2, 2, 32, 32, 128)
+    x = torch.zeros((2, 2, 4, 64), dtype=torch.float16, device="cuda")
+    c.prefill_attn(x, x, x, [0, 0])
+    assert all(not np.any(a) for a in c.lengths())
+    out = c.decode(torch.ones((2, 2, 64), dtype=torch.float16, device="cuda"))
+    assert not out.float().abs().sum().item()
+    assert c.check() == 0
+    c.close()
