@@ -49,7 +49,7 @@ FALLBACK_HBM_GBS = 6800.0
 # mode (the one-launch step's kernel, and the plain one); reported only
 # while the kernel source is unchanged (llama3_8b_gqa_32k, the default
 # workload).
-NCU_TRAFFIC = {"177e5be2affb6ab7": {"fused": 204156672 + 6489088, "two": 205777408 + 3242752}}
+NCU_TRAFFIC = {"615a5d7bf756c11f": {"fused": 204156160 + 6497280, "two": 205765376 + 2815488}}
 
 
 def algorithmic_bytes(w: W.Workload, T, Tqk, Tqv, scores: bool = False) -> int:
@@ -80,7 +80,7 @@ def load_peaks():
 def source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("kivi_decode.cu", "kivi_decode_impl.cuh", "kivi_internal.cuh"):
+    for f in ("kivi_decode.cu", "kivi_decode_impl.cuh", "kivi_internal.cuh", "kivi_mma.cuh"):
         with open(os.path.join(ROOT, "bit_quantized_kv_quantize_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

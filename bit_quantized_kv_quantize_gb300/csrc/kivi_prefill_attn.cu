@@ -269,9 +269,21 @@ __global__ void __launch_bounds__(128, 1)
         // S of this tile done (its K stage is free), P V of the previous
         // tile done (its S / P buffer, V stage and O are free), K of the
         // next tile landed
+        // (and V of this tile landed, its rows past the sequence zeroed:
+        // they meet zero weights, and the array there holds whatever it
+        // holds; the zeros are ordered before P V by the sync below)
         bool w = tc_wait_bar(&bS[b], (unsigned)(kt >> 1) & 1u);
         if (kt > 0) w = w && tc_wait_bar(bO, (unsigned)(kt - 1) & 1u);
         if (kt + 1 < nt) w = w && tc_wait_bar(&bK[b ^ 1], (unsigned)((kt + 1) >> 1) & 1u);
+        w = w && tc_wait_bar(&bV[b], (unsigned)(kt >> 1) & 1u);
+        if (w && kt * kTcKeys + kTcKeys > t) {
+            const int r0 = t - kt * kTcKeys;
+            unsigned char *v = sV + b * KVB;
+            for (int e = tid; e < (kTcKeys - r0) * (D / 8); e += blockDim.x) {
+                const int r = r0 + e / (D / 8), c = e % (D / 8);
+                *reinterpret_cast<uint4 *>(v + cm_at<kTcKeys>(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
         ok = __syncthreads_and(w);
         if (!ok) break;
         tc_fence_after();
@@ -294,10 +306,15 @@ __global__ void __launch_bounds__(128, 1)
         tc_ld32(tS + lane_off + 32, sr[1]);
         tc_wait_ld();
         float sc[64];
+        if (kt * kTcKeys + kTcKeys - 1 > tb) {   // a tile the causal mask cuts (the CTA's last two)
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-            const int key = kt * kTcKeys + c;
-            sc[c] = key > row ? -INFINITY : __uint_as_float(sr[c >> 5][c & 31]);
+            for (int c = 0; c < 64; ++c) {
+                const int key = kt * kTcKeys + c;
+                sc[c] = key > row ? -INFINITY : __uint_as_float(sr[c >> 5][c & 31]);
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) sc[c] = __uint_as_float(sr[c >> 5][c & 31]);
         }
         float mx = -INFINITY;
 #pragma unroll
@@ -329,20 +346,6 @@ __global__ void __launch_bounds__(128, 1)
         // P over the S buffer: column c = weights of keys 2c, 2c + 1
         tc_st32(tS + lane_off, pw);
         tc_wait_st();
-        // V of this tile landed; its rows past the sequence zeroed (they
-        // meet zero weights, and the array there holds whatever it holds)
-        if (!tc_wait_bar(&bV[b], (unsigned)(kt >> 1) & 1u)) {
-            ok = false;
-        } else if (kt * kTcKeys + kTcKeys > t) {
-            const int r0 = t - kt * kTcKeys;
-            unsigned char *v = sV + b * KVB;
-            for (int e = tid; e < (kTcKeys - r0) * (D / 8); e += blockDim.x) {
-                const int r = r0 + e / (D / 8), c = e % (D / 8);
-                *reinterpret_cast<uint4 *>(v + cm_at<kTcKeys>(r, c)) = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
         tc_sync();
         if (tid == 0) {
             const unsigned char *v = sV + b * KVB;
