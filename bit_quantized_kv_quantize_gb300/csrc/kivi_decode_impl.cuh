@@ -1304,24 +1304,64 @@ __global__ void __launch_bounds__(256, 2)
                 *reinterpret_cast<uint2 *>(out + ((size_t)i * hq + j * hg + e0 + e) * D + 4 * c4) = o2;
             }
         } else if (s_last) {
-            // Merge the pair's partials: their (m, l) come into shared memory
-            // with one round trip, each head's weights are formed there by
-            // one warp, then the accumulators are read as float4 columns,
-            // S partials in flight per column (S threads a column, summed in
-            // shared memory).  The ring is free: the warps' results were
-            // merged above.
+            // Merge the pair's partials.  When they fit in the ring (free:
+            // the warps' results were merged above) beside the scratch
+            // below, they are bulk-copied there, one copy per head, with one
+            // round trip; otherwise they are read from global memory.  Their
+            // (m, l) go to shared memory, each head's weights are formed
+            // there by one warp, then the accumulators are read as float4
+            // columns, S partials per column in flight (S threads a column,
+            // summed in shared memory).
             __threadfence();
-            float *sm_m = reinterpret_cast<float *>(ring);   // [nh][np]
+            const int ncol = nh * NC4;
+            const int S = max(1, min(8, (int)blockDim.x / ncol));
+            const size_t hbytes = (size_t)np * PS * 4;   // one head's partials
+            const bool staged = !cdead && (size_t)nh * hbytes + (size_t)8 * np * 4 + (size_t)S * ncol * 16 <=
+                                              max((size_t)nw * wstride, mreg);
+            float *stage = reinterpret_cast<float *>(ring);   // [nh][np][PS] when staged
+            float *sm_m = reinterpret_cast<float *>(ring + (staged ? (size_t)nh * hbytes : 0));   // [nh][np]
             float *sm_w = sm_m + 4 * np;                      // [nh][np]: l, then the weights
             float4 *sm_a = reinterpret_cast<float4 *>(sm_w + 4 * np);   // [S][nh NC4] (16-byte aligned)
-            for (int x = threadIdx.x; x < nh * np; x += blockDim.x) {
+            // head e's partial y: stage + (e np + y) PS, else prow0 + (e smax + y) PS
+            const size_t hst = staged ? (size_t)np * PS : (size_t)g.smax * PS;
+            bool mok = true;
+            if (staged) {
+                fence_proxy_async();   // the ring's earlier generic reads and writes
+                __syncthreads();
+                if (threadIdx.x == 0) {
+                    // the partials were written by generic stores (of this and
+                    // the other CTAs, ordered by the ticket): order them
+                    // before the asynchronous copies that read them
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    mbar_expect_tx(cbar, (unsigned)(nh * hbytes));
+                    for (int e = 0; e < nh; ++e)
+                        bulk_g2s(stage + (size_t)e * np * PS, prow0 + (size_t)e * g.smax * PS, (unsigned)hbytes,
+                                 cbar);
+                }
+                const bool ok = mbar_wait(cbar, cphase);
+                cphase ^= 1u;
+                if (!__syncthreads_and(ok)) {
+                    if (threadIdx.x == 0) atomicOr(dv.status, KIVI_FLAG_WAIT);
+                    mbar_wait(cbar, cphase ^ 1u);   // bounded: let the copies land before the ring is reused
+                    cdead = true;
+                    mok = false;
+                }
+            }
+            const float *pbase = staged ? stage : prow0;
+            auto ld2 = [&](const float *p) {
+                return staged ? *reinterpret_cast<const float2 *>(p) : __ldcg(reinterpret_cast<const float2 *>(p));
+            };
+            auto ld4 = [&](const float *p) {
+                return staged ? *reinterpret_cast<const float4 *>(p) : __ldcg(reinterpret_cast<const float4 *>(p));
+            };
+            for (int x = threadIdx.x; mok && x < nh * np; x += blockDim.x) {
                 const int e = x / np, y = x % np;
-                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(prow0 + ((size_t)e * g.smax + y) * PS));
+                const float2 ml = ld2(pbase + (size_t)e * hst + (size_t)y * PS);
                 sm_m[x] = ml.x;
                 sm_w[x] = ml.y;
             }
             __syncthreads();
-            if (warp < nh) {
+            if (mok && warp < nh) {
                 const int e = warp;
                 float M = -INFINITY;
                 for (int y = lane; y < np; y += 32) M = fmaxf(M, sm_m[e * np + y]);
@@ -1346,20 +1386,18 @@ __global__ void __launch_bounds__(256, 2)
             // (column, subset) items: S subsets of the partials per float4
             // column when the CTA has threads for them, else one; each
             // thread takes items in turn
-            const int ncol = nh * NC4;
-            const int S = max(1, min(8, (int)blockDim.x / ncol));
-            for (int it = threadIdx.x; it < ncol * S; it += blockDim.x) {
+            for (int it = threadIdx.x; mok && it < ncol * S; it += blockDim.x) {
                 const int col = it % ncol, sub = it / ncol;
                 const int e = col / NC4, c4 = col % NC4;
-                const float *src = prow0 + (size_t)e * g.smax * PS + 4 + 4 * c4;
+                const float *src = pbase + (size_t)e * hst + 4 + 4 * c4;
                 const float *wr = sm_w + e * np;
                 float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
                 int y = sub;
                 for (; y + 3 * S < np; y += 4 * S) {   // four partials in flight
-                    const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(src + (size_t)y * PS));
-                    const float4 v1 = __ldcg(reinterpret_cast<const float4 *>(src + (size_t)(y + S) * PS));
-                    const float4 v2 = __ldcg(reinterpret_cast<const float4 *>(src + (size_t)(y + 2 * S) * PS));
-                    const float4 v3 = __ldcg(reinterpret_cast<const float4 *>(src + (size_t)(y + 3 * S) * PS));
+                    const float4 v0 = ld4(src + (size_t)y * PS);
+                    const float4 v1 = ld4(src + (size_t)(y + S) * PS);
+                    const float4 v2 = ld4(src + (size_t)(y + 2 * S) * PS);
+                    const float4 v3 = ld4(src + (size_t)(y + 3 * S) * PS);
                     const float w0 = wr[y], w1 = wr[y + S], w2 = wr[y + 2 * S], w3 = wr[y + 3 * S];
                     a4.x = fmaf(w0, v0.x, fmaf(w1, v1.x, fmaf(w2, v2.x, fmaf(w3, v3.x, a4.x))));
                     a4.y = fmaf(w0, v0.y, fmaf(w1, v1.y, fmaf(w2, v2.y, fmaf(w3, v3.y, a4.y))));
@@ -1367,7 +1405,7 @@ __global__ void __launch_bounds__(256, 2)
                     a4.w = fmaf(w0, v0.w, fmaf(w1, v1.w, fmaf(w2, v2.w, fmaf(w3, v3.w, a4.w))));
                 }
                 for (; y < np; y += S) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + (size_t)y * PS));
+                    const float4 v = ld4(src + (size_t)y * PS);
                     const float w0 = wr[y];
                     a4.x = fmaf(w0, v.x, a4.x);
                     a4.y = fmaf(w0, v.y, a4.y);
