@@ -127,17 +127,19 @@ __device__ void pack_diagonal_bits(const KiviGeom &g, const KiviDev &dv, const u
 // memory lane r).  Per 64-key tile kt: S = Q K^T (M 128, N 64, K d) into one
 // of two S buffers in tensor memory; each thread reads its row of S, applies
 // the causal mask and the online softmax (base 2, its whole row in
-// registers) and writes its fp16 weights P back over the S buffer (two
-// weights a column), where O += P V (M 128, N d, K 64) takes them as its A
+// registers) and writes its fp16 weights P into a shared-memory tile laid
+// out like Q, from which O += P V (M 128, N d, K 64) takes them as its A
 // operand; O accumulates in tensor memory.  One thread issues the MMAs and
 // the tile copies; completions arrive on mbarriers (bounded waits).
 //
-// Pipeline: S of tile kt + 1 is issued before the softmax of tile kt (its
-// buffer is free once P V of tile kt - 1, which read P from it, is done).
-// Q, K and V tiles come by TMA, one tensor copy each, K two tiles ahead and
-// V one tile ahead (two stages each).  The running maximum is raised
-// lazily: O and the row sum are rescaled only when a row's maximum grows by
-// more than 8 (log2 units), so P stays below 2^8.
+// Pipeline: S of tile kt + 1 is issued as tile kt starts (its buffer held
+// S of tile kt - 1, already read), so it runs under the softmax of tile kt;
+// P V of tile kt - 1 runs under that softmax too, which waits for it only
+// before writing P over the P tile (and before a rescale of O).  Q, K and V
+// tiles come by TMA, one tensor copy each, K two tiles ahead and V one tile
+// ahead (two stages each).  The running maximum is raised lazily: O and the
+// row sum are rescaled only when a row's maximum grows by more than 8 (log2
+// units), so P stays below 2^8.
 //
 // Tiles in shared memory use the no-swizzle core-matrix layout, chunk-major:
 // row r, 16-byte chunk c of a tile of ROWS rows at byte c ROWS 16 + r 16
@@ -146,9 +148,9 @@ __device__ void pack_diagonal_bits(const KiviGeom &g, const KiviDev &dv, const u
 // strides (2 D bytes, 16 bytes) writes exactly this with one copy per tile
 // (rows past the array read as zero); value rows past the sequence are
 // zeroed after the copy, as the weights they meet are zero.
-//   Q [128][D], K [2][64][D], V [2][64][D]: 96 KB at d = 128.
-// Tensor memory: S / P buffers in columns 0-63 and 64-127, O in
-// 128-(128 + D): 256 columns.
+//   Q [128][D], K [2][64][D], V [2][64][D], P [128][64]: 112 KB at d = 128.
+// Tensor memory: S buffers in columns 0-63 and 64-127, O in 128-(128 + D):
+// 256 columns.
 // ---------------------------------------------------------------------------
 constexpr int kTcRows = 128, kTcKeys = 64;
 
@@ -205,6 +207,7 @@ __global__ void __launch_bounds__(128, 1)
     unsigned char *sQ = smem;
     unsigned char *sK = smem + QB;      // stage s at sK + s KVB
     unsigned char *sV = sK + 2 * KVB;   // stage s at sV + s KVB
+    unsigned char *sP = sV + 2 * KVB;   // [128][64] weights, laid out like Q
     // S buffer 0 and 1 done, P V done, Q landed, K stage 0 / 1 landed, V stage 0 / 1 landed
     __shared__ __align__(8) uint64_t bars[8];
     uint64_t *const bS = bars, *const bO = bars + 2, *const bQ = bars + 3, *const bK = bars + 4, *const bV = bars + 6;
@@ -264,40 +267,29 @@ __global__ void __launch_bounds__(128, 1)
         if (tid == 0) issue_s(0);
         nS0 = 1;
     }
+    // what thread 0 issued at tile kt (slot kt mod 2): 1 S of the next tile,
+    // 2 K of the tile after it, 4 V of the next tile
+    __shared__ int s_issued[2];
     for (int kt = 0; kt < nt && ok; ++kt) {
         const int b = kt & 1;
-        // S of this tile done (its K stage is free), P V of the previous
-        // tile done (its S / P buffer, V stage and O are free), K of the
-        // next tile landed
-        // (and V of this tile landed, its rows past the sequence zeroed:
-        // they meet zero weights, and the array there holds whatever it
-        // holds; the zeros are ordered before P V by the sync below)
+        // S of this tile done: its K stage is free
         bool w = tc_wait_bar(&bS[b], (unsigned)(kt >> 1) & 1u);
-        if (kt > 0) w = w && tc_wait_bar(bO, (unsigned)(kt - 1) & 1u);
-        if (kt + 1 < nt) w = w && tc_wait_bar(&bK[b ^ 1], (unsigned)((kt + 1) >> 1) & 1u);
-        w = w && tc_wait_bar(&bV[b], (unsigned)(kt >> 1) & 1u);
-        if (w && kt * kTcKeys + kTcKeys > t) {
-            const int r0 = t - kt * kTcKeys;
-            unsigned char *v = sV + b * KVB;
-            for (int e = tid; e < (kTcKeys - r0) * (D / 8); e += blockDim.x) {
-                const int r = r0 + e / (D / 8), c = e % (D / 8);
-                *reinterpret_cast<uint4 *>(v + cm_at<kTcKeys>(r, c)) = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        ok = __syncthreads_and(w);
-        if (!ok) break;
         tc_fence_after();
-        if (tid == 0) {
-            if (kt + 1 < nt) issue_s(kt + 1);
-            if (kt + 2 < nt) tma_tile(sK + b * KVB, &tmK, krow0 + (kt + 2) * kTcKeys, &bK[b], KVB);
-            if (kt + 1 < nt) tma_tile(sV + (b ^ 1) * KVB, &tmV, krow0 + (kt + 1) * kTcKeys, &bV[b ^ 1], KVB);
-        }
-        if (kt + 1 < nt) {
-            if (b) ++nS0; else ++nS1;
-            if (b) ++nV0; else ++nV1;
-        }
-        if (kt + 2 < nt) {
-            if (b) ++nK1; else ++nK0;
+        int is = 0;
+        if (tid == 0 && w && kt + 1 < nt) {
+            // S of the next tile into the other buffer (S of tile kt - 1,
+            // read by every thread before the last tile's barrier)
+            if (tc_wait_bar(&bK[b ^ 1], (unsigned)((kt + 1) >> 1) & 1u)) {
+                tc_fence_after();
+                issue_s(kt + 1);
+                is = 1;
+                if (kt + 2 < nt) {
+                    tma_tile(sK + b * KVB, &tmK, krow0 + (kt + 2) * kTcKeys, &bK[b], KVB);
+                    is |= 2;
+                }
+            } else {
+                w = false;
+            }
         }
         // this row's 64 scores
         const uint32_t tS = taddr + 64 * b;
@@ -316,13 +308,32 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
             for (int c = 0; c < 64; ++c) sc[c] = __uint_as_float(sr[c >> 5][c & 31]);
         }
-        float mx = -INFINITY;
+        // the row maximum over eight independent chains
+        float m8[8];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) mx = fmaxf(mx, sc[c]);
+        for (int k = 0; k < 8; ++k) m8[k] = sc[k];
+#pragma unroll
+        for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], sc[c]);
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         // lazy rescale: only when the maximum grew by more than 2^8 in weight
         const bool grow = mx != -INFINITY && (mref == -INFINITY || (mx - mref) * sl2 > 8.f);
         const float alpha = grow && mref != -INFINITY ? ex2((mref - mx) * sl2) : 1.f;
         if (grow) mref = mx;
+        const float ms = mref * sl2;
+        uint32_t pw[32];
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            const float p0 = ex2(fmaf(sc[2 * c], sl2, -ms)), p1 = ex2(fmaf(sc[2 * c + 1], sl2, -ms));
+            l4[c & 3] += p0 + p1;
+            pw[c] = pack_h2(p0, p1);
+        }
+        lsum = lsum * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+        // P V of the previous tile done: O holds its sum, the P tile and
+        // that tile's V stage are free
+        if (kt > 0) w = tc_wait_bar(bO, (unsigned)(kt - 1) & 1u) && w;
+        tc_fence_after();
         if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -334,24 +345,50 @@ __global__ void __launch_bounds__(128, 1)
                 tc_st32(tO + lane_off + c0, o);
             }
         }
-        lsum *= alpha;
-        const float ms = mref * sl2;
-        uint32_t pw[32];
+        // P: row tid, chunk c (keys 8c .. 8c + 7) at c 128 16 + 16 tid
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            const float p0 = ex2(fmaf(sc[2 * c], sl2, -ms)), p1 = ex2(fmaf(sc[2 * c + 1], sl2, -ms));
-            lsum += p0 + p1;
-            pw[c] = pack_h2(p0, p1);
+        for (int c = 0; c < kTcKeys / 8; ++c)
+            *reinterpret_cast<uint4 *>(sP + cm_at<kTcRows>(tid, c)) =
+                make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+        if (tid == 0 && w && kt + 1 < nt) {
+            tma_tile(sV + (b ^ 1) * KVB, &tmV, krow0 + (kt + 1) * kTcKeys, &bV[b ^ 1], KVB);
+            is |= 4;
         }
-        // P over the S buffer: column c = weights of keys 2c, 2c + 1
-        tc_st32(tS + lane_off, pw);
+        if (tid == 0) s_issued[b] = is;
+        // V of this tile landed; its rows past the sequence zeroed (they
+        // meet zero weights, and the array there holds whatever it holds)
+        w = tc_wait_bar(&bV[b], (unsigned)(kt >> 1) & 1u) && w;
+        if (w && kt * kTcKeys + kTcKeys > t) {
+            const int r0 = t - kt * kTcKeys;
+            unsigned char *v = sV + b * KVB;
+            for (int e = tid; e < (kTcKeys - r0) * (D / 8); e += blockDim.x) {
+                const int r = r0 + e / (D / 8), c = e % (D / 8);
+                *reinterpret_cast<uint4 *>(v + cm_at<kTcKeys>(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
         tc_wait_st();
-        tc_sync();
+        // the P tile, the zeroed rows and O's rescale before P V
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        ok = __syncthreads_and(w);
+        tc_fence_after();
+        const int isb = s_issued[b];
+        if (isb & 1) {
+            if (b) ++nS0; else ++nS1;
+        }
+        if (isb & 2) {
+            if (b) ++nK1; else ++nK0;
+        }
+        if (isb & 4) {
+            if (b) ++nV0; else ++nV1;
+        }
+        if (!ok) break;
         if (tid == 0) {
             const unsigned char *v = sV + b * KVB;
 #pragma unroll
             for (int c = 0; c < kTcKeys / 16; ++c)
-                tc_mma_f16_ta(tO, tS + 8 * c, tc_desc(v + 256 * c, 128, KLBO), ID_O, kt > 0 || c > 0);
+                tc_mma_f16(tO, tc_desc(sP + 2 * c * QLBO, QLBO, 128), tc_desc(v + 256 * c, 128, KLBO), ID_O,
+                           kt > 0 || c > 0);
             tc_commit(bO);
         }
         ++nO;
@@ -445,7 +482,7 @@ cudaError_t make_tile_map(CUtensorMap *tm, const __half *base, long long rows, i
 template <int D>
 cudaError_t launch_tc(const KiviGeom &g, const KiviDev &dv, const __half *Q, const __half *K, const __half *V,
                       __half *O, const SeqLens &lens, int t_stride, int hq, int maxt, cudaStream_t st) {
-    const size_t smem = (size_t)kTcRows * D * 2 + (size_t)4 * kTcKeys * D * 2;
+    const size_t smem = (size_t)kTcRows * D * 2 + (size_t)4 * kTcKeys * D * 2 + (size_t)kTcRows * kTcKeys * 2;
     const long long ts = t_stride > 0 ? t_stride : 1;
     CUtensorMap tq, tk, tv;   // unused when every sequence is empty (the CTAs only write counters)
     memset(&tq, 0, sizeof tq);
