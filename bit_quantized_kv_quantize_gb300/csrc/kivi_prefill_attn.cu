@@ -196,70 +196,81 @@ __device__ __forceinline__ void tc_sync() {
     tc_fence_after();
 }
 
-template <int D>
-__global__ void __launch_bounds__(128, 1)
+// NH query heads of one kv head per CTA (1, or 2 when a kv head serves an
+// even number of query heads): each K and V tile then feeds NH heads' MMAs.
+// Thread tid owns row tid mod 128 of head slot tid / 128; head slot e has
+// its own Q and P tiles and tensor-memory columns [256 e, 256 e + 256).
+template <int D, int NH>
+__global__ void __launch_bounds__(128 * NH, 1)
     prefill_attn_tc_kernel(KiviGeom g, KiviDev dv, const __grid_constant__ CUtensorMap tmQ,
                            const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                            __half *__restrict__ O, SeqLens lens, int t_stride, int hq) {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int QB = kTcRows * D * 2, KVB = kTcKeys * D * 2;
+    constexpr int QB = kTcRows * D * 2, KVB = kTcKeys * D * 2, PB = kTcRows * kTcKeys * 2;
     constexpr unsigned QLBO = kTcRows * 16, KLBO = kTcKeys * 16;   // chunk strides
-    unsigned char *sQ = smem;
-    unsigned char *sK = smem + QB;      // stage s at sK + s KVB
-    unsigned char *sV = sK + 2 * KVB;   // stage s at sV + s KVB
-    unsigned char *sP = sV + 2 * KVB;   // [128][64] weights, laid out like Q
+    unsigned char *sQ = smem;                // head slot e at sQ + e QB
+    unsigned char *sK = smem + NH * QB;      // stage s at sK + s KVB
+    unsigned char *sV = sK + 2 * KVB;        // stage s at sV + s KVB
+    unsigned char *sP = sV + 2 * KVB;        // [128][64] weights of head slot e at sP + e PB, laid out like Q
     // S buffer 0 and 1 done, P V done, Q landed, K stage 0 / 1 landed, V stage 0 / 1 landed
     __shared__ __align__(8) uint64_t bars[8];
     uint64_t *const bS = bars, *const bO = bars + 2, *const bQ = bars + 3, *const bK = bars + 4, *const bV = bars + 6;
     __shared__ uint32_t s_taddr;
     const int qt = gridDim.x - 1 - blockIdx.x;   // the longest tiles first
-    const int h = blockIdx.y, i = blockIdx.z;
-    const int hg = hq / g.h, j = h / hg;
+    const int tid = threadIdx.x, warp = tid >> 5, hs = tid >> 7, rr = tid & 127;
+    const int h0 = blockIdx.y * NH, h = h0 + hs, i = blockIdx.z;   // the CTA's first head, this thread's
+    const int hg = hq / g.h, j = h0 / hg;
     const int t = lens.t[i];
     const int tb = qt * kTcRows;
     if (tb >= t) {
-        if (tb == 0 && h == 0 && threadIdx.x == 0) {   // an empty sequence
+        if (tb == 0 && h0 == 0 && threadIdx.x == 0) {   // an empty sequence
             dv.T[i] = 0;
             dv.Tqk[i] = 0;
             dv.Tqv[i] = 0;
         }
         return;
     }
-    const int tid = threadIdx.x, warp = tid >> 5;
     const int krow0 = (i * g.h + j) * t_stride;   // this kv head's first row in K and V
     const int nt = min((t + kTcKeys - 1) / kTcKeys, (tb + kTcRows) / kTcKeys);   // key tiles
     // copies issued per barrier (the same count in every thread)
     int nQ = 0, nK0 = 0, nK1 = 0, nV0 = 0, nV1 = 0, nS0 = 0, nS1 = 0, nO = 0;
     if (tid == 0) {
-        for (int k = 0; k < 8; ++k)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_u32(&bars[k])) : "memory");
+        for (int k = 0; k < 8; ++k)   // Q's: one arrival per head slot's copy
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(tc_smem_u32(&bars[k])),
+                         "r"(k == 3 ? NH : 1)
+                         : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     if (tid == 0) {
-        tma_tile(sQ, &tmQ, (i * hq + h) * t_stride + tb, bQ, QB);
+#pragma unroll
+        for (int e = 0; e < NH; ++e) tma_tile(sQ + e * QB, &tmQ, (i * hq + h0 + e) * t_stride + tb, bQ, QB);
         tma_tile(sK, &tmK, krow0, &bK[0], KVB);
         tma_tile(sV, &tmV, krow0, &bV[0], KVB);
         if (nt > 1) tma_tile(sK + KVB, &tmK, krow0 + kTcKeys, &bK[1], KVB);
     }
     nQ = nK0 = nV0 = 1;
     nK1 = nt > 1 ? 1 : 0;
-    if (warp == 0) tc_alloc(&s_taddr, 256);
+    if (warp == 0) tc_alloc(&s_taddr, 256 * NH);
     bool ok = tc_wait_bar(bQ, 0) && tc_wait_bar(&bK[0], 0);
     tc_fence_before();
     ok = __syncthreads_and(ok);
     tc_fence_after();
-    const uint32_t taddr = s_taddr, tO = taddr + 128;
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;   // this warp's tensor-memory lanes
+    const uint32_t taddr = s_taddr, tH = taddr + 256 * hs, tO = tH + 128;   // this head slot's columns
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;            // this warp's tensor-memory lanes
     constexpr uint32_t ID_S = tc_idesc_f16(kTcRows, kTcKeys, 0), ID_O = tc_idesc_f16(kTcRows, D, 1);
     const float sl2 = 1.4426950408889634f / sqrtf((float)D);   // log2(e) / sqrt(d)
-    const int row = tb + tid;
-    auto issue_s = [&](int kt) {   // S of tile kt into buffer kt mod 2 (one thread)
-        const uint32_t tS = taddr + 64 * (kt & 1);
+    const int row = tb + rr;
+    auto issue_s = [&](int kt) {   // S of tile kt into buffer kt mod 2 of every head slot (one thread)
         const unsigned char *k = sK + (kt & 1) * KVB;
 #pragma unroll
-        for (int c = 0; c < D / 16; ++c)
-            tc_mma_f16(tS, tc_desc(sQ + 2 * c * QLBO, QLBO, 128), tc_desc(k + 2 * c * KLBO, KLBO, 128), ID_S, c > 0);
+        for (int e = 0; e < NH; ++e) {
+            const uint32_t tS = taddr + 256 * e + 64 * (kt & 1);
+#pragma unroll
+            for (int c = 0; c < D / 16; ++c)
+                tc_mma_f16(tS, tc_desc(sQ + e * QB + 2 * c * QLBO, QLBO, 128), tc_desc(k + 2 * c * KLBO, KLBO, 128),
+                           ID_S, c > 0);
+        }
         tc_commit(&bS[kt & 1]);
     };
     float mref = -INFINITY, lsum = 0.f;   // the row's reference maximum (raw score units) and sum
@@ -292,7 +303,7 @@ __global__ void __launch_bounds__(128, 1)
             }
         }
         // this row's 64 scores
-        const uint32_t tS = taddr + 64 * b;
+        const uint32_t tS = tH + 64 * b;
         uint32_t sr[2][32];
         tc_ld32(tS + lane_off, sr[0]);
         tc_ld32(tS + lane_off + 32, sr[1]);
@@ -345,10 +356,10 @@ __global__ void __launch_bounds__(128, 1)
                 tc_st32(tO + lane_off + c0, o);
             }
         }
-        // P: row tid, chunk c (keys 8c .. 8c + 7) at c 128 16 + 16 tid
+        // P: row rr, chunk c (keys 8c .. 8c + 7) at c 128 16 + 16 rr
 #pragma unroll
         for (int c = 0; c < kTcKeys / 8; ++c)
-            *reinterpret_cast<uint4 *>(sP + cm_at<kTcRows>(tid, c)) =
+            *reinterpret_cast<uint4 *>(sP + hs * PB + cm_at<kTcRows>(rr, c)) =
                 make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
         if (tid == 0 && w && kt + 1 < nt) {
             tma_tile(sV + (b ^ 1) * KVB, &tmV, krow0 + (kt + 1) * kTcKeys, &bV[b ^ 1], KVB);
@@ -386,9 +397,11 @@ __global__ void __launch_bounds__(128, 1)
         if (tid == 0) {
             const unsigned char *v = sV + b * KVB;
 #pragma unroll
-            for (int c = 0; c < kTcKeys / 16; ++c)
-                tc_mma_f16(tO, tc_desc(sP + 2 * c * QLBO, QLBO, 128), tc_desc(v + 256 * c, 128, KLBO), ID_O,
-                           kt > 0 || c > 0);
+            for (int e = 0; e < NH; ++e)
+#pragma unroll
+                for (int c = 0; c < kTcKeys / 16; ++c)
+                    tc_mma_f16(taddr + 256 * e + 128, tc_desc(sP + e * PB + 2 * c * QLBO, QLBO, 128),
+                               tc_desc(v + 256 * c, 128, KLBO), ID_O, kt > 0 || c > 0);
             tc_commit(bO);
         }
         ++nO;
@@ -426,13 +439,13 @@ __global__ void __launch_bounds__(128, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tc_dealloc(taddr, 256);
+    if (warp == 0) tc_dealloc(taddr, 256 * NH);
     if (!ok) return;
 
     // epilogue: the first query head of each kv head packs the tile's two
     // 64-token key / value tiles, still in their stages; Q's region holds
     // the staging (generic stores after the copies' and MMAs' accesses)
-    if (h % hg == 0) {
+    if (h0 % hg == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         for (int k = 0; k < 2; ++k) {
             const int kb = tb + k * kTcKeys, kt = kb / kTcKeys;
@@ -479,10 +492,11 @@ cudaError_t make_tile_map(CUtensorMap *tm, const __half *base, long long rows, i
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D>
+template <int D, int NH>
 cudaError_t launch_tc(const KiviGeom &g, const KiviDev &dv, const __half *Q, const __half *K, const __half *V,
                       __half *O, const SeqLens &lens, int t_stride, int hq, int maxt, cudaStream_t st) {
-    const size_t smem = (size_t)kTcRows * D * 2 + (size_t)4 * kTcKeys * D * 2 + (size_t)kTcRows * kTcKeys * 2;
+    const size_t smem =
+        (size_t)NH * kTcRows * D * 2 + (size_t)4 * kTcKeys * D * 2 + (size_t)NH * kTcRows * kTcKeys * 2;
     const long long ts = t_stride > 0 ? t_stride : 1;
     CUtensorMap tq, tk, tv;   // unused when every sequence is empty (the CTAs only write counters)
     memset(&tq, 0, sizeof tq);
@@ -495,10 +509,12 @@ cudaError_t launch_tc(const KiviGeom &g, const KiviDev &dv, const __half *Q, con
         if (e == cudaSuccess) e = make_tile_map(&tv, V, (long long)g.b * g.h * ts, D, kTcKeys);
         if (e != cudaSuccess) return e;
     }
-    e = cudaFuncSetAttribute(prefill_attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(prefill_attn_tc_kernel<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
     if (e != cudaSuccess) return e;
     const int nqt = maxt > 0 ? (maxt + kTcRows - 1) / kTcRows : 1;
-    prefill_attn_tc_kernel<D><<<dim3(nqt, hq, g.b), 128, smem, st>>>(g, dv, tq, tk, tv, O, lens, t_stride, hq);
+    prefill_attn_tc_kernel<D, NH>
+        <<<dim3(nqt, hq / NH, g.b), 128 * NH, smem, st>>>(g, dv, tq, tk, tv, O, lens, t_stride, hq);
     return cudaGetLastError();
 }
 
@@ -511,6 +527,10 @@ cudaError_t kivi_launch_prefill_attn(const KiviGeom &g, const KiviDev &dv, const
     int maxt = 0;
     for (int i = 0; i < g.b; ++i) maxt = lens.t[i] > maxt ? lens.t[i] : maxt;
     if (maxt > 0 && ((long long)g.b * hq * t_stride >= (1LL << 31))) return cudaErrorInvalidValue;   // TMA row coordinates
-    return g.d == 64 ? launch_tc<64>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st)
-                     : launch_tc<128>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st);
+    // two query heads a CTA when a kv head serves an even number of them
+    // (d = 128: the 160 KB of shared memory keep one CTA, which holds all
+    // 512 tensor-memory columns, per SM)
+    if (g.d == 64) return launch_tc<64, 1>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st);
+    return (hq / g.h) % 2 == 0 ? launch_tc<128, 2>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st)
+                               : launch_tc<128, 1>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st);
 }
