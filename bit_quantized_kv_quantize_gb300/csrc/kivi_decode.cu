@@ -74,14 +74,19 @@ DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *T, const int *
     p.stages = env_int("KIVI_DECODE_STAGES", stages);
     while (p.stages > 2 && (size_t)p.warps * p.stages * sb > 220 * 1024) --p.stages;
 
-    // units per pair of each sequence
+    // units per pair of each sequence: a lead of units standing for the
+    // fixed cost of a segment (its set-up and its merge: a CTA whose range
+    // takes in a pair's start gets that many fewer blocks), one per fully
+    // quantized block, MW per block holding window tokens
     const int MW = env_int("KIVI_DECODE_MIXED_WEIGHT", 12);
+    const char *le = getenv("KIVI_DECODE_LEAD");
     units->mixed_weight = MW;
+    units->lead = le && *le ? (atoi(le) > 0 ? atoi(le) : 0) : 3;
     units->start[0] = 0;
     for (int i = 0; i < g.b; ++i) {
         const int nf = (Tqk[i] < Tqv[i] ? Tqk[i] : Tqv[i]) / KIVI_KBLK;
         const int nb = (T[i] + KIVI_KBLK - 1) / KIVI_KBLK;
-        int w = nf + MW * (nb - nf);
+        int w = units->lead + nf + MW * (nb - nf);
         if (w < 1) w = 1;   // an empty sequence still gets its (zero) output written
         units->full[i] = nf;
         units->start[i + 1] = units->start[i] + w;

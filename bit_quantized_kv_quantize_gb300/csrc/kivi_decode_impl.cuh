@@ -972,15 +972,18 @@ __global__ void __launch_bounds__(256, 2)
         if constexpr (PROBS)
             if (tq < nh) prow = po.p + ((size_t)i * hq + j * hg + e0 + tq) * (size_t)po.ld;
 
-        // Blocks of the segment: units [o0, min(o1, nfh)) are blocks of the
-        // same index, units nfh + MW m in [o0, o1) are block nfh + m; blocks
-        // past the data (>= nblk) are skipped.
+        // Blocks of the segment: past the pair's lead of units.lead units
+        // (no blocks), with b0, b1 the segment's range counted from the
+        // lead's end, units [b0, min(b1, nfh)) are blocks of the same index,
+        // units nfh + MW m in [b0, b1) are block nfh + m; blocks past the
+        // data (>= nblk) are skipped.
         const unsigned char *recs = dv.blk + rec_off(g, i, j, 0);
-        const int nA = max(0, min(o1, nfh) - o0);
-        const int m0 = o0 > nfh ? (o0 - nfh + MW - 1) / MW : 0;
-        const int m1 = o1 > nfh ? (o1 - nfh + MW - 1) / MW : 0;
+        const int b0 = max(o0 - units.lead, 0), b1 = max(o1 - units.lead, 0);
+        const int nA = max(0, min(b1, nfh) - b0);
+        const int m0 = b0 > nfh ? (b0 - nfh + MW - 1) / MW : 0;
+        const int m1 = b1 > nfh ? (b1 - nfh + MW - 1) / MW : 0;
         const int nL = nA + max(0, m1 - m0);
-        auto blk = [&](int x) { return x < nA ? o0 + x : nfh + m0 + (x - nA); };
+        auto blk = [&](int x) { return x < nA ? b0 + x : nfh + m0 + (x - nA); };
         auto first_at_least = [&](int kb) {   // first x with blk(x) >= kb (blk increases)
             int lo = 0, hi = nL;
             while (lo < hi) {
@@ -1219,9 +1222,14 @@ __global__ void __launch_bounds__(256, 2)
         }
         __syncthreads();
         if (threadIdx.x == 0) {
-            __threadfence();
+            // one acquire-release add: it releases the partial the CTA's
+            // threads wrote before the barrier above (a release is cumulative)
+            // and, in the last CTA, acquires every earlier CTA's partial (the
+            // adds on the ticket form one release sequence); the barrier below
+            // passes the acquire on to the merging threads
             unsigned *tk = dv.merge_ticket + ((size_t)i * g.h + j) * 4 + qg;
-            const unsigned prev = atomicAdd(tk, 1u);
+            unsigned prev;
+            asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(tk) : "memory");
             s_last = prev == (unsigned)np - 1u;
             if (s_last) *tk = 0u;
         }
@@ -1235,7 +1243,6 @@ __global__ void __launch_bounds__(256, 2)
             // the weights itself, and the S subsets of a column are summed
             // in shared memory (the ring is free: the warps' results were
             // merged above).
-            __threadfence();
             const int ncol = nh * NC4;
             const int S = max(1, min(8, (int)blockDim.x / ncol));
             float4 *sm_a = reinterpret_cast<float4 *>(ring);   // [S][ncol]
@@ -1312,7 +1319,6 @@ __global__ void __launch_bounds__(256, 2)
             // there by one warp, then the accumulators are read as float4
             // columns, S partials per column in flight (S threads a column,
             // summed in shared memory).
-            __threadfence();
             const int ncol = nh * NC4;
             const int S = max(1, min(8, (int)blockDim.x / ncol));
             const size_t hbytes = (size_t)np * PS * 4;   // one head's partials

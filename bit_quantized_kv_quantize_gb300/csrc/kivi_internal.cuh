@@ -311,6 +311,7 @@ struct DecodePlan {
 struct DecodeUnits {
     long long total;
     int mixed_weight;
+    int lead;   // units of a pair ahead of its blocks (no work: they stand for a segment's fixed cost)
     int start[KIVI_MAX_BATCH + 1];
     int full[KIVI_MAX_BATCH];
 };

@@ -45,13 +45,14 @@ def state_after(t, steps, R):
 def test_default_workload_plan(lib):
     """b = 8, 32 query / 8 kv heads, d = 128, 2-bit, G = 32, R = 128, 32767
     tokens + 1 appended, 152 SMs: two CTAs per SM, eight warps, each pair's
-    units = full blocks + 12 per block holding fp16 tokens."""
+    units = a lead of 3 (a segment's fixed cost) + full blocks + 12 per
+    block holding fp16 tokens."""
     T, Tqk, Tqv = state_after(32767, 1, 128)
     rc, p = preview(lib, (8, 8, 128, 2, 2, 32, 128, 40000), 32, [T] * 8, [Tqk] * 8, [Tqv] * 8, 152)
     assert rc == 0
     assert p["ctas"] == 304 and p["warps"] == 8 and p["stages"] >= 2
     nf, nb = min(Tqk, Tqv) // 64, -(-T // 64)
-    assert p["units"] == 8 * 8 * (nf + 12 * (nb - nf))
+    assert p["units"] == 8 * 8 * (3 + nf + 12 * (nb - nf))
     assert p["max_parts"] <= p["slots"]
 
 
