@@ -870,7 +870,8 @@ __global__ void __launch_bounds__(256, 2)
     const int C = gridDim.x, c = blockIdx.x;
     long long u = (long long)c * U / C;
     const long long u_end = (long long)(c + 1) * U / C;
-    __shared__ int s_seg[9];   // i, jq, o0, o1, Wi; T, Tqk, Tqv (after the append); fused flags
+    __shared__ int s_seg[11];   // i, jq, o0, o1, Wi; T, Tqk, Tqv (after the append); fused flags;
+                                // the pair's first CTA and its number of CTAs (partials)
     __shared__ int s_last;
     __shared__ float sML[8];    // per head: max over the warps (or partials), then the weighted sum of l
     __shared__ float sWt[32];   // [warp][head]: the warp's weight
@@ -916,6 +917,12 @@ __global__ void __launch_bounds__(256, 2)
             s_seg[2] = (int)(rem % Wi);
             s_seg[3] = (int)min((long long)Wi, rem % Wi + (u_end - u));
             s_seg[4] = Wi;
+            {   // the CTAs that share this pair (64-bit divisions: one thread, here)
+                const long long Pp = u - rem % Wi;
+                const int cf = (int)cta_of_unit(Pp, U, C);
+                s_seg[9] = cf;
+                s_seg[10] = (int)cta_of_unit(Pp + Wi - 1, U, C) - cf + 1;
+            }
             // Counters.  FUSED: the device holds them before this step's
             // append; a sequence whose key window is not full is appended by
             // this launch (flag 1; flag 2: its value queue's oldest token
@@ -1196,9 +1203,7 @@ __global__ void __launch_bounds__(256, 2)
             }
         }
         __syncthreads();
-        const long long Pp = (long long)HQG * units.start[i] + (long long)jq * Wi;
-        const int cfirst = (int)cta_of_unit(Pp, U, C);
-        const int np = (int)cta_of_unit(Pp + Wi - 1, U, C) - cfirst + 1;
+        const int cfirst = s_seg[9], np = s_seg[10];
         const int slot = c - cfirst;
         float *const prow0 = dv.part + ((size_t)i * hq + j * hg + e0) * g.smax * PS;   // head e: + e smax PS
         for (int x = threadIdx.x; x < nh * (NC4 + 1); x += blockDim.x) {
