@@ -628,6 +628,8 @@ def main(argv=None):
     ap.add_argument("--v-bits", type=int, choices=(2, 4), help="override the workload's value bits")
     ap.add_argument("--group", type=int, choices=(16, 32, 64, 128), help="override the group size G")
     ap.add_argument("--residual", type=int, help="override the residual length R (a multiple of G)")
+    ap.add_argument("--tokens", type=int,
+                    help="override the prompt length (a smaller case of the workload, for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--two", action="store_true",
                     help="time a step as kivi_append + kivi_decode_attn instead of one "
@@ -645,8 +647,10 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     w = W.WORKLOADS[args.workload]
     over = {k: v for k, v in (("kbits", args.k_bits), ("vbits", args.v_bits), ("G", args.group),
-                              ("R", args.residual)) if v is not None}
-    if over:   # a variant of the workload (bits / group / residual sweep)
+                              ("R", args.residual), ("prefill", args.tokens)) if v is not None}
+    if over:   # a variant of the workload (bits / group / residual sweep, a shorter prompt)
+        if args.tokens is not None and (args.tokens < 1 or w.ragged):
+            ap.error("--tokens needs a positive count and a workload of equal lengths")
         w = W.small(w, **over)
         if w.R % w.G or w.d % w.G:
             ap.error("need R % G == 0 and d % G == 0")
