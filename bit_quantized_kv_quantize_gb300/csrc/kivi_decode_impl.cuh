@@ -844,8 +844,10 @@ __device__ __forceinline__ void warp_result(WarpAcc<D> &A, float *wres) {
 // segment; the last CTA to finish a segment of that (i, j, qg) merges all
 // of its partials.
 // ---------------------------------------------------------------------------
-__host__ __device__ __forceinline__ long long cta_of_unit(long long u, long long U, int C) {
-    return ((u + 1) * C - 1) / U;
+__host__ __device__ __forceinline__ int cta_of_unit(long long u, long long U, int C) {
+    if ((unsigned long long)U * (unsigned)C < (1ull << 32))   // 32-bit arithmetic suffices (u < U)
+        return (int)(((unsigned)(u + 1) * (unsigned)C - 1u) / (unsigned)U);
+    return (int)(((u + 1) * C - 1) / U);
 }
 
 template <int D, int KB, int VB, int SH, bool PROBS, bool FUSED>
@@ -910,26 +912,27 @@ __global__ void __launch_bounds__(256, 2)
                 const int mid = (lo + hi) >> 1;
                 if ((long long)HQG * units.start[mid] <= u) lo = mid; else hi = mid;
             }
+            // Counters (read first: their loads are in flight during the
+            // arithmetic below).  FUSED: the device holds them before this
+            // step's append; a sequence whose key window is not full is
+            // appended by this launch (flag 1; flag 2: its value queue's
+            // oldest token pops), the others were appended by the launch
+            // before (the counters after the append follow from item 4's
+            // schedule either way).
+            int T = dv.T[lo], Tqk = dv.Tqk[lo], Tqv = dv.Tqv[lo], fl = 0;
             const int Wi = units.start[lo + 1] - units.start[lo];
             const long long rem = u - (long long)HQG * units.start[lo];
+            const int o0 = (int)(rem % Wi);
             s_seg[0] = lo;
             s_seg[1] = (int)(rem / Wi);
-            s_seg[2] = (int)(rem % Wi);
-            s_seg[3] = (int)min((long long)Wi, rem % Wi + (u_end - u));
+            s_seg[2] = o0;
+            s_seg[3] = (int)min((long long)Wi, o0 + (u_end - u));
             s_seg[4] = Wi;
-            {   // the CTAs that share this pair (64-bit divisions: one thread, here)
-                const long long Pp = u - rem % Wi;
-                const int cf = (int)cta_of_unit(Pp, U, C);
-                s_seg[9] = cf;
-                s_seg[10] = (int)cta_of_unit(Pp + Wi - 1, U, C) - cf + 1;
-            }
-            // Counters.  FUSED: the device holds them before this step's
-            // append; a sequence whose key window is not full is appended by
-            // this launch (flag 1; flag 2: its value queue's oldest token
-            // pops), the others were appended by the launch before (the
-            // counters after the append follow from item 4's schedule
-            // either way).
-            int T = dv.T[lo], Tqk = dv.Tqk[lo], Tqv = dv.Tqv[lo], fl = 0;
+            // the CTAs that share this pair
+            const long long Pp = u - o0;
+            const int cf = cta_of_unit(Pp, U, C);
+            s_seg[9] = cf;
+            s_seg[10] = cta_of_unit(Pp + Wi - 1, U, C) - cf + 1;
             if constexpr (FUSED) {
                 if (append_counters_ok(g, T, Tqk, Tqv)) {
                     const bool pop = T - Tqv == g.R + 1, app = T - Tqk != g.R;
