@@ -219,7 +219,7 @@ kivi_status launch_decode(kivi_cache *c, const void *q, int h_q, void *out, kivi
                           const int *T, const int *Tqk, const int *Tqv, const char *what,
                           const ProbsOut *po = nullptr, const FusedStep *fs = nullptr) {
     DecodeUnits units;
-    DecodePlan plan = kivi_plan_decode(c->g, h_q, T, Tqk, Tqv, c->num_sms, &units);
+    DecodePlan plan = kivi_plan_decode(c->g, h_q, T, Tqk, Tqv, c->num_sms, &units, fs != nullptr);
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (c->profiling && c->nprof < kMaxProfile) {
         if ((int)c->ev.size() < 2 * (c->nprof + 1)) {

@@ -57,7 +57,7 @@ int kivi_partial_slots(int b, int h, int num_sms) {
 }
 
 DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *T, const int *Tqk, const int *Tqv,
-                            int num_sms, DecodeUnits *units) {
+                            int num_sms, DecodeUnits *units, bool fused) {
     DecodePlan p;
     const int hg = hq / g.h;
     p.qgroups = (hg + 3) / 4;
@@ -82,11 +82,28 @@ DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *T, const int *
     const char *le = getenv("KIVI_DECODE_LEAD");
     units->mixed_weight = MW;
     units->lead = le && *le ? (atoi(le) > 0 ? atoi(le) : 0) : 3;
+    // A launch that also appends: the pair's append falls to the CTA
+    // holding the pair's last blocks, which the partition charges with a
+    // tail of units after them (no blocks), scaled to the blocks a CTA
+    // takes (about 1 unit per 25, at most 4: ~2 us of a 32k CTA's ~60).
+    int tail = 0;
+    if (fused) {
+        long long base = 0;
+        for (int i = 0; i < g.b; ++i) {
+            const int nf = (Tqk[i] < Tqv[i] ? Tqk[i] : Tqv[i]) / KIVI_KBLK;
+            const int nb = (T[i] + KIVI_KBLK - 1) / KIVI_KBLK;
+            base += (long long)g.h * p.qgroups * (units->lead + nf + MW * (nb - nf));
+        }
+        const long long per_cta = base / ((long long)num_sms * kCtasPerSm);
+        tail = (int)(per_cta / 25 > 4 ? 4 : per_cta / 25);
+        const char *ta = getenv("KIVI_DECODE_FUSED_TAIL");
+        if (ta && *ta) tail = atoi(ta) > 0 ? atoi(ta) : 0;
+    }
     units->start[0] = 0;
     for (int i = 0; i < g.b; ++i) {
         const int nf = (Tqk[i] < Tqv[i] ? Tqk[i] : Tqv[i]) / KIVI_KBLK;
         const int nb = (T[i] + KIVI_KBLK - 1) / KIVI_KBLK;
-        int w = units->lead + nf + MW * (nb - nf);
+        int w = units->lead + nf + MW * (nb - nf) + tail;
         if (w < 1) w = 1;   // an empty sequence still gets its (zero) output written
         units->full[i] = nf;
         units->start[i + 1] = units->start[i] + w;

@@ -339,8 +339,10 @@ cudaError_t kivi_launch_prefill_attn(const KiviGeom &g, const KiviDev &dv, const
 cudaError_t kivi_launch_append(const KiviGeom &g, const KiviDev &dv, const __half *k,
                                const __half *v, const AppendCounters &ac, int *nxt, cudaStream_t st,
                                bool only_flush = false);
+// The decode plan and its work units (kivi_decode.cu); fused: the launch
+// also appends the step's token (its plan charges the owners' appends).
 DecodePlan kivi_plan_decode(const KiviGeom &g, int hq, const int *T, const int *Tqk, const int *Tqv,
-                            int num_sms, DecodeUnits *units);
+                            int num_sms, DecodeUnits *units, bool fused = false);
 // partial slots per (sequence, query head) a cache of this shape allocates
 int kivi_partial_slots(int b, int h, int num_sms);
 // Scores left in po.p by the decode kernel's weights variant -> weights

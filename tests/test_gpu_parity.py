@@ -142,6 +142,16 @@ def test_fused_step_ragged(case):
             p.check_state(f"fused step {s}")
 
 
+@pytest.mark.parametrize("tail,case", [(3, 0), (9, 1)])
+def test_fused_step_with_tail_units(monkeypatch, tail, case):
+    """The one-launch plan's trailing units (they hold no blocks) and the
+    pairs' lead units forced larger than these small shapes get: the same
+    results, step by step."""
+    monkeypatch.setenv("KIVI_DECODE_FUSED_TAIL", str(tail))
+    monkeypatch.setenv("KIVI_DECODE_LEAD", str(tail + 2))
+    test_fused_step_ragged(FUSED[case])
+
+
 def test_fused_step_launch_count(monkeypatch):
     """kivi_append_decode is one launch on steps without a key-window
     flush, two on flush steps, and two with KIVI_FUSED_STEP=0, with more
