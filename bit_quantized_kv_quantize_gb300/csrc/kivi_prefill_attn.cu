@@ -187,37 +187,59 @@ __device__ __forceinline__ void tma_tile(void *dst, const CUtensorMap *tm, int r
         : "memory");
 }
 
-// shared-memory writes (generic stores) and tensor-memory stores of every
-// thread ordered before what the issuing thread does next
-__device__ __forceinline__ void tc_sync() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+
+// A wait that also gives up when another warp of the CTA has given up
+// (*abort set): false then, or after the iteration limit.
+__device__ __forceinline__ bool tc_wait_bar_ab(uint64_t *bar, unsigned phase, const volatile int *abort) {
+    for (int it = 0; it < (1 << 24); ++it) {
+        unsigned ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(tc_smem_u32(bar)), "r"(phase)
+            : "memory");
+        if (ok) return true;
+        if ((it & 255) == 255 && *abort) return false;
+    }
+    return false;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc_smem_u32(bar)) : "memory");
 }
 
 // NH query heads of one kv head per CTA (1, or 2 when a kv head serves an
 // even number of query heads): each K and V tile then feeds NH heads' MMAs.
-// Thread tid owns row tid mod 128 of head slot tid / 128; head slot e has
-// its own Q and P tiles and tensor-memory columns [256 e, 256 e + 256).
+// Warps 0 .. 4 NH - 1 run the softmax: thread tid owns row tid mod 128 of
+// head slot tid / 128 (head slot e has its own Q and P tiles and tensor-
+// memory columns [256 e, 256 e + 256)).  Warp 4 NH is the producer: its
+// lane 0 issues every copy and MMA.  The two sides meet on mbarriers only:
+// S done (MMA commit), S read (every softmax warp), P written (every softmax
+// warp), P V done (MMA commit), and the copies' landings.
+// At most 168 registers a thread: a scheduler partition's 16 K registers
+// then hold three warps, so two one-head CTAs (five warps each) share an SM.
 template <int D, int NH>
-__global__ void __launch_bounds__(128 * NH, 1)
+__global__ void __maxnreg__(168)
     prefill_attn_tc_kernel(KiviGeom g, KiviDev dv, const __grid_constant__ CUtensorMap tmQ,
                            const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                            __half *__restrict__ O, SeqLens lens, int t_stride, int hq) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int QB = kTcRows * D * 2, KVB = kTcKeys * D * 2, PB = kTcRows * kTcKeys * 2;
     constexpr unsigned QLBO = kTcRows * 16, KLBO = kTcKeys * 16;   // chunk strides
+    constexpr int NSW = 4 * NH;   // softmax warps
     unsigned char *sQ = smem;                // head slot e at sQ + e QB
     unsigned char *sK = smem + NH * QB;      // stage s at sK + s KVB
     unsigned char *sV = sK + 2 * KVB;        // stage s at sV + s KVB
     unsigned char *sP = sV + 2 * KVB;        // [128][64] weights of head slot e at sP + e PB, laid out like Q
-    // S buffer 0 and 1 done, P V done, Q landed, K stage 0 / 1 landed, V stage 0 / 1 landed
-    __shared__ __align__(8) uint64_t bars[8];
-    uint64_t *const bS = bars, *const bO = bars + 2, *const bQ = bars + 3, *const bK = bars + 4, *const bV = bars + 6;
+    // S buffer 0 / 1 done, P V done, Q landed, K stage 0 / 1 landed, V stage
+    // 0 / 1 landed, S buffer 0 / 1 read, P written
+    __shared__ __align__(8) uint64_t bars[11];
+    uint64_t *const bS = bars, *const bO = bars + 2, *const bQ = bars + 3, *const bK = bars + 4, *const bV = bars + 6,
+                    *const bSr = bars + 8, *const bP = bars + 10;
     __shared__ uint32_t s_taddr;
+    __shared__ int s_abort;   // a wait ran out: every warp stops
     const int qt = gridDim.x - 1 - blockIdx.x;   // the longest tiles first
-    const int tid = threadIdx.x, warp = tid >> 5, hs = tid >> 7, rr = tid & 127;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, hs = min(tid >> 7, NH - 1), rr = tid & 127;
     const int h0 = blockIdx.y * NH, h = h0 + hs, i = blockIdx.z;   // the CTA's first head, this thread's
     const int hg = hq / g.h, j = h0 / hg;
     const int t = lens.t[i];
@@ -232,213 +254,232 @@ __global__ void __launch_bounds__(128 * NH, 1)
     }
     const int krow0 = (i * g.h + j) * t_stride;   // this kv head's first row in K and V
     const int nt = min((t + kTcKeys - 1) / kTcKeys, (tb + kTcRows) / kTcKeys);   // key tiles
-    // copies issued per barrier (the same count in every thread)
-    int nQ = 0, nK0 = 0, nK1 = 0, nV0 = 0, nV1 = 0, nS0 = 0, nS1 = 0, nO = 0;
     if (tid == 0) {
-        for (int k = 0; k < 8; ++k)   // Q's: one arrival per head slot's copy
+        for (int k = 0; k < 11; ++k)   // Q's: one arrival per head slot's copy; S read, P written: per softmax warp
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(tc_smem_u32(&bars[k])),
-                         "r"(k == 3 ? NH : 1)
+                         "r"(k == 3 ? NH : k >= 8 ? NSW : 1)
                          : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        s_abort = 0;
     }
     __syncthreads();
-    if (tid == 0) {
-#pragma unroll
-        for (int e = 0; e < NH; ++e) tma_tile(sQ + e * QB, &tmQ, (i * hq + h0 + e) * t_stride + tb, bQ, QB);
-        tma_tile(sK, &tmK, krow0, &bK[0], KVB);
-        tma_tile(sV, &tmV, krow0, &bV[0], KVB);
-        if (nt > 1) tma_tile(sK + KVB, &tmK, krow0 + kTcKeys, &bK[1], KVB);
-    }
-    nQ = nK0 = nV0 = 1;
-    nK1 = nt > 1 ? 1 : 0;
     if (warp == 0) tc_alloc(&s_taddr, 256 * NH);
-    bool ok = tc_wait_bar(bQ, 0) && tc_wait_bar(&bK[0], 0);
     tc_fence_before();
-    ok = __syncthreads_and(ok);
+    __syncthreads();
     tc_fence_after();
-    const uint32_t taddr = s_taddr, tH = taddr + 256 * hs, tO = tH + 128;   // this head slot's columns
-    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;            // this warp's tensor-memory lanes
-    constexpr uint32_t ID_S = tc_idesc_f16(kTcRows, kTcKeys, 0), ID_O = tc_idesc_f16(kTcRows, D, 1);
-    const float sl2 = 1.4426950408889634f / sqrtf((float)D);   // log2(e) / sqrt(d)
-    const int row = tb + rr;
-    auto issue_s = [&](int kt) {   // S of tile kt into buffer kt mod 2 of every head slot (one thread)
-        const unsigned char *k = sK + (kt & 1) * KVB;
+    const uint32_t taddr = s_taddr;
+    const volatile int *abort = &s_abort;
+    bool ok = true;
+    float lsum = 0.f;
+    if (warp == NSW) {
+        // ---- the producer: copies and MMAs (lane 0) ----
+        if (lane == 0) {
+            constexpr uint32_t ID_S = tc_idesc_f16(kTcRows, kTcKeys, 0), ID_O = tc_idesc_f16(kTcRows, D, 1);
+            auto issue_s = [&](int kt) {   // S of tile kt into buffer kt mod 2 of every head slot
+                const unsigned char *k = sK + (kt & 1) * KVB;
 #pragma unroll
-        for (int e = 0; e < NH; ++e) {
-            const uint32_t tS = taddr + 256 * e + 64 * (kt & 1);
+                for (int e = 0; e < NH; ++e) {
+                    const uint32_t tS = taddr + 256 * e + 64 * (kt & 1);
 #pragma unroll
-            for (int c = 0; c < D / 16; ++c)
-                tc_mma_f16(tS, tc_desc(sQ + e * QB + 2 * c * QLBO, QLBO, 128), tc_desc(k + 2 * c * KLBO, KLBO, 128),
-                           ID_S, c > 0);
-        }
-        tc_commit(&bS[kt & 1]);
-    };
-    float mref = -INFINITY, lsum = 0.f;   // the row's reference maximum (raw score units) and sum
-    if (ok) {
-        if (tid == 0) issue_s(0);
-        nS0 = 1;
-    }
-    // what thread 0 issued at tile kt (slot kt mod 2): 1 S of the next tile,
-    // 2 K of the tile after it, 4 V of the next tile
-    __shared__ int s_issued[2];
-    for (int kt = 0; kt < nt && ok; ++kt) {
-        const int b = kt & 1;
-        // S of this tile done: its K stage is free
-        bool w = tc_wait_bar(&bS[b], (unsigned)(kt >> 1) & 1u);
-        tc_fence_after();
-        int is = 0;
-        if (tid == 0 && w && kt + 1 < nt) {
-            // S of the next tile into the other buffer (S of tile kt - 1,
-            // read by every thread before the last tile's barrier)
-            if (tc_wait_bar(&bK[b ^ 1], (unsigned)((kt + 1) >> 1) & 1u)) {
+                    for (int c = 0; c < D / 16; ++c)
+                        tc_mma_f16(tS, tc_desc(sQ + e * QB + 2 * c * QLBO, QLBO, 128),
+                                   tc_desc(k + 2 * c * KLBO, KLBO, 128), ID_S, c > 0);
+                }
+                tc_commit(&bS[kt & 1]);
+            };
+            // completions issued per barrier (for the drain after a time-out)
+            int nK[2] = {1, nt > 1 ? 1 : 0}, nV[2] = {1, 0}, nS[2] = {0, 0}, nO = 0;
+#pragma unroll
+            for (int e = 0; e < NH; ++e) tma_tile(sQ + e * QB, &tmQ, (i * hq + h0 + e) * t_stride + tb, bQ, QB);
+            tma_tile(sK, &tmK, krow0, &bK[0], KVB);
+            tma_tile(sV, &tmV, krow0, &bV[0], KVB);
+            if (nt > 1) tma_tile(sK + KVB, &tmK, krow0 + kTcKeys, &bK[1], KVB);
+            ok = tc_wait_bar_ab(bQ, 0, abort) && tc_wait_bar_ab(&bK[0], 0, abort);
+            if (ok) {
                 tc_fence_after();
-                issue_s(kt + 1);
-                is = 1;
-                if (kt + 2 < nt) {
+                issue_s(0);
+                nS[0] = 1;
+            }
+            for (int kt = 0; kt < nt && ok; ++kt) {
+                const int b = kt & 1;
+                if (kt + 1 < nt) {
+                    // S of the next tile: its K landed, its buffer (S of tile
+                    // kt - 1) read by every softmax warp
+                    ok = tc_wait_bar_ab(&bK[b ^ 1], (unsigned)((kt + 1) >> 1) & 1u, abort) &&
+                         (kt == 0 || tc_wait_bar_ab(&bSr[b ^ 1], (unsigned)((kt - 1) >> 1) & 1u, abort));
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(kt + 1);
+                    ++nS[b ^ 1];
+                }
+                if (kt + 2 < nt) {   // K two tiles on, into the stage S of this tile read
+                    ok = tc_wait_bar_ab(&bS[b], (unsigned)(kt >> 1) & 1u, abort);
+                    if (!ok) break;
                     tma_tile(sK + b * KVB, &tmK, krow0 + (kt + 2) * kTcKeys, &bK[b], KVB);
-                    is |= 2;
+                    ++nK[b];
+                }
+                if (kt + 1 < nt) {   // V of the next tile, into the stage P V of the previous tile read
+                    ok = kt == 0 || tc_wait_bar_ab(bO, (unsigned)(kt - 1) & 1u, abort);
+                    if (!ok) break;
+                    tma_tile(sV + (b ^ 1) * KVB, &tmV, krow0 + (kt + 1) * kTcKeys, &bV[b ^ 1], KVB);
+                    ++nV[b ^ 1];
+                }
+                // P V of this tile: its weights written and, on the tile the
+                // sequence cuts, V's rows past it zeroed (every softmax warp)
+                ok = tc_wait_bar_ab(bP, (unsigned)kt & 1u, abort) &&
+                     tc_wait_bar_ab(&bV[b], (unsigned)(kt >> 1) & 1u, abort);
+                if (!ok) break;
+                tc_fence_after();
+                const unsigned char *v = sV + b * KVB;
+#pragma unroll
+                for (int e = 0; e < NH; ++e)
+#pragma unroll
+                    for (int c = 0; c < kTcKeys / 16; ++c)
+                        tc_mma_f16(taddr + 256 * e + 128, tc_desc(sP + e * PB + 2 * c * QLBO, QLBO, 128),
+                                   tc_desc(v + 256 * c, 128, KLBO), ID_O, kt > 0 || c > 0);
+                tc_commit(bO);
+                ++nO;
+            }
+            if (!ok) {
+                // flag it, and let every issued copy and MMA finish (bounded:
+                // each barrier's last completion is phase (count - 1) mod 2)
+                // before shared and tensor memory are released
+                s_abort = 1;
+                atomicOr(dv.status, KIVI_FLAG_WAIT);
+                const int cnt[8] = {nS[0], nS[1], nO, 1, nK[0], nK[1], nV[0], nV[1]};
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (cnt[k] > 0) tc_wait_bar(&bars[k], (unsigned)(cnt[k] - 1) & 1u);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---- the softmax warps ----
+        const uint32_t tH = taddr + 256 * hs, tO = tH + 128;          // this head slot's columns
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;   // this warp's tensor-memory lanes
+        const float sl2 = 1.4426950408889634f / sqrtf((float)D);      // log2(e) / sqrt(d)
+        const int row = tb + rr;
+        float mref = -INFINITY;   // the row's reference maximum (raw score units)
+        for (int kt = 0; kt < nt; ++kt) {
+            const int b = kt & 1;
+            ok = __all_sync(0xffffffffu, tc_wait_bar_ab(&bS[b], (unsigned)(kt >> 1) & 1u, abort));
+            if (!ok) break;
+            tc_fence_after();
+            // this row's 64 scores; then the S buffer is free for the producer
+            const uint32_t tS = tH + 64 * b;
+            uint32_t sr[2][32];
+            tc_ld32(tS + lane_off, sr[0]);
+            tc_ld32(tS + lane_off + 32, sr[1]);
+            tc_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bSr[b]);
+            float sc[64];
+            if (kt * kTcKeys + kTcKeys - 1 > tb) {   // a tile the causal mask cuts (the CTA's last two)
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const int key = kt * kTcKeys + c;
+                    sc[c] = key > row ? -INFINITY : __uint_as_float(sr[c >> 5][c & 31]);
                 }
             } else {
-                w = false;
-            }
-        }
-        // this row's 64 scores
-        const uint32_t tS = tH + 64 * b;
-        uint32_t sr[2][32];
-        tc_ld32(tS + lane_off, sr[0]);
-        tc_ld32(tS + lane_off + 32, sr[1]);
-        tc_wait_ld();
-        float sc[64];
-        if (kt * kTcKeys + kTcKeys - 1 > tb) {   // a tile the causal mask cuts (the CTA's last two)
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const int key = kt * kTcKeys + c;
-                sc[c] = key > row ? -INFINITY : __uint_as_float(sr[c >> 5][c & 31]);
+                for (int c = 0; c < 64; ++c) sc[c] = __uint_as_float(sr[c >> 5][c & 31]);
+            }
+            // the row maximum over eight independent chains
+            float m8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m8[k] = sc[k];
+#pragma unroll
+            for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], sc[c]);
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            // lazy rescale: only when the maximum grew by more than 2^8 in weight
+            const bool grow = mx != -INFINITY && (mref == -INFINITY || (mx - mref) * sl2 > 8.f);
+            const float alpha = grow && mref != -INFINITY ? ex2((mref - mx) * sl2) : 1.f;
+            if (grow) mref = mx;
+            const float ms = mref * sl2;
+            uint32_t pw[32];
+            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float p0 = ex2(fmaf(sc[2 * c], sl2, -ms)), p1 = ex2(fmaf(sc[2 * c + 1], sl2, -ms));
+                l4[c & 3] += p0 + p1;
+                pw[c] = pack_h2(p0, p1);
+            }
+            lsum = lsum * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+            // P V of the previous tile done: O holds its sum, the P tile is free
+            if (kt > 0) {
+                ok = __all_sync(0xffffffffu, tc_wait_bar_ab(bO, (unsigned)(kt - 1) & 1u, abort));
+                if (!ok) break;
+                tc_fence_after();
+            }
+            if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tc_ld32(tO + lane_off + c0, o);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                    tc_st32(tO + lane_off + c0, o);
+                }
+                tc_wait_st();
+            }
+            // P: row rr, chunk c (keys 8c .. 8c + 7) at c 128 16 + 16 rr
+#pragma unroll
+            for (int c = 0; c < kTcKeys / 8; ++c)
+                *reinterpret_cast<uint4 *>(sP + hs * PB + cm_at<kTcRows>(rr, c)) =
+                    make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+            // V's rows past the sequence on the tile it cuts: zeroed once
+            // the tile landed (they meet zero weights, and the array there
+            // holds whatever it holds), a share per softmax warp
+            if (kt * kTcKeys + kTcKeys > t) {
+                ok = __all_sync(0xffffffffu, tc_wait_bar_ab(&bV[b], (unsigned)(kt >> 1) & 1u, abort));
+                if (!ok) break;
+                const int r0 = t - kt * kTcKeys;
+                unsigned char *v = sV + b * KVB;
+                for (int e = tid; e < (kTcKeys - r0) * (D / 8); e += 32 * NSW) {
+                    const int r = r0 + e / (D / 8), c = e % (D / 8);
+                    *reinterpret_cast<uint4 *>(v + cm_at<kTcKeys>(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            // the P tile, the zeroed rows and O's rescale before P V
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bP);
+        }
+        // the last P V done
+        if (ok) ok = __all_sync(0xffffffffu, tc_wait_bar_ab(bO, (unsigned)(nt - 1) & 1u, abort));
+        if (!ok) {   // stop the others' waits too
+            if (lane == 0) {
+                s_abort = 1;
+                atomicOr(dv.status, KIVI_FLAG_WAIT);
             }
         } else {
-#pragma unroll
-            for (int c = 0; c < 64; ++c) sc[c] = __uint_as_float(sr[c >> 5][c & 31]);
-        }
-        // the row maximum over eight independent chains
-        float m8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = sc[k];
-#pragma unroll
-        for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], sc[c]);
-        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-        // lazy rescale: only when the maximum grew by more than 2^8 in weight
-        const bool grow = mx != -INFINITY && (mref == -INFINITY || (mx - mref) * sl2 > 8.f);
-        const float alpha = grow && mref != -INFINITY ? ex2((mref - mx) * sl2) : 1.f;
-        if (grow) mref = mx;
-        const float ms = mref * sl2;
-        uint32_t pw[32];
-        float l4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            const float p0 = ex2(fmaf(sc[2 * c], sl2, -ms)), p1 = ex2(fmaf(sc[2 * c + 1], sl2, -ms));
-            l4[c & 3] += p0 + p1;
-            pw[c] = pack_h2(p0, p1);
-        }
-        lsum = lsum * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
-        // P V of the previous tile done: O holds its sum, the P tile and
-        // that tile's V stage are free
-        if (kt > 0) w = tc_wait_bar(bO, (unsigned)(kt - 1) & 1u) && w;
-        tc_fence_after();
-        if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            tc_fence_after();
+            // the output rows (tcgen05.ld is warp-wide: every lane loads, the
+            // rows inside the sequence are stored)
+            const float r = 1.f / lsum;
+            __half *orow = O + (((size_t)i * hq + h) * t_stride + min(row, t - 1)) * D;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];
                 tc_ld32(tO + lane_off + c0, o);
                 tc_wait_ld();
+                if (row < t)
 #pragma unroll
-                for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                tc_st32(tO + lane_off + c0, o);
+                    for (int c = 0; c < 32; c += 8)
+                        *reinterpret_cast<uint4 *>(orow + c0 + c) =
+                            make_uint4(pack_h2(__uint_as_float(o[c]) * r, __uint_as_float(o[c + 1]) * r),
+                                       pack_h2(__uint_as_float(o[c + 2]) * r, __uint_as_float(o[c + 3]) * r),
+                                       pack_h2(__uint_as_float(o[c + 4]) * r, __uint_as_float(o[c + 5]) * r),
+                                       pack_h2(__uint_as_float(o[c + 6]) * r, __uint_as_float(o[c + 7]) * r));
             }
-        }
-        // P: row rr, chunk c (keys 8c .. 8c + 7) at c 128 16 + 16 rr
-#pragma unroll
-        for (int c = 0; c < kTcKeys / 8; ++c)
-            *reinterpret_cast<uint4 *>(sP + hs * PB + cm_at<kTcRows>(rr, c)) =
-                make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-        if (tid == 0 && w && kt + 1 < nt) {
-            tma_tile(sV + (b ^ 1) * KVB, &tmV, krow0 + (kt + 1) * kTcKeys, &bV[b ^ 1], KVB);
-            is |= 4;
-        }
-        if (tid == 0) s_issued[b] = is;
-        // V of this tile landed; its rows past the sequence zeroed (they
-        // meet zero weights, and the array there holds whatever it holds)
-        w = tc_wait_bar(&bV[b], (unsigned)(kt >> 1) & 1u) && w;
-        if (w && kt * kTcKeys + kTcKeys > t) {
-            const int r0 = t - kt * kTcKeys;
-            unsigned char *v = sV + b * KVB;
-            for (int e = tid; e < (kTcKeys - r0) * (D / 8); e += blockDim.x) {
-                const int r = r0 + e / (D / 8), c = e % (D / 8);
-                *reinterpret_cast<uint4 *>(v + cm_at<kTcKeys>(r, c)) = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        tc_wait_st();
-        // the P tile, the zeroed rows and O's rescale before P V
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc_fence_before();
-        ok = __syncthreads_and(w);
-        tc_fence_after();
-        const int isb = s_issued[b];
-        if (isb & 1) {
-            if (b) ++nS0; else ++nS1;
-        }
-        if (isb & 2) {
-            if (b) ++nK1; else ++nK0;
-        }
-        if (isb & 4) {
-            if (b) ++nV0; else ++nV1;
-        }
-        if (!ok) break;
-        if (tid == 0) {
-            const unsigned char *v = sV + b * KVB;
-#pragma unroll
-            for (int e = 0; e < NH; ++e)
-#pragma unroll
-                for (int c = 0; c < kTcKeys / 16; ++c)
-                    tc_mma_f16(taddr + 256 * e + 128, tc_desc(sP + e * PB + 2 * c * QLBO, QLBO, 128),
-                               tc_desc(v + 256 * c, 128, KLBO), ID_O, kt > 0 || c > 0);
-            tc_commit(bO);
-        }
-        ++nO;
-    }
-    if (ok && nO > 0) ok = __syncthreads_and(tc_wait_bar(bO, (unsigned)(nO - 1) & 1u));
-    if (!ok) {
-        // a wait ran out: flag it, let every issued copy and MMA finish
-        // (bounded: each barrier's last arrival completes phase (count - 1)
-        // mod 2) before shared and tensor memory are released, write nothing
-        if (tid == 0) atomicOr(dv.status, KIVI_FLAG_WAIT);
-        const int cnt[8] = {nS0, nS1, nO, nQ, nK0, nK1, nV0, nV1};
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            if (cnt[k] > 0) tc_wait_bar(&bars[k], (unsigned)(cnt[k] - 1) & 1u);
-    } else {
-        tc_fence_after();
-        // the output rows (tcgen05.ld is warp-wide: every lane loads, the
-        // rows inside the sequence are stored)
-        const float r = 1.f / lsum;
-        __half *orow = O + (((size_t)i * hq + h) * t_stride + min(row, t - 1)) * D;
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tc_ld32(tO + lane_off + c0, o);
-            tc_wait_ld();
-            if (row < t)
-#pragma unroll
-                for (int c = 0; c < 32; c += 8)
-                    *reinterpret_cast<uint4 *>(orow + c0 + c) =
-                        make_uint4(pack_h2(__uint_as_float(o[c]) * r, __uint_as_float(o[c + 1]) * r),
-                                   pack_h2(__uint_as_float(o[c + 2]) * r, __uint_as_float(o[c + 3]) * r),
-                                   pack_h2(__uint_as_float(o[c + 4]) * r, __uint_as_float(o[c + 5]) * r),
-                                   pack_h2(__uint_as_float(o[c + 6]) * r, __uint_as_float(o[c + 7]) * r));
         }
     }
     tc_fence_before();
-    __syncthreads();
+    ok = __syncthreads_and(ok) && !s_abort;
     if (warp == 0) tc_dealloc(taddr, 256 * NH);
     if (!ok) return;
 
@@ -514,7 +555,7 @@ cudaError_t launch_tc(const KiviGeom &g, const KiviDev &dv, const __half *Q, con
     if (e != cudaSuccess) return e;
     const int nqt = maxt > 0 ? (maxt + kTcRows - 1) / kTcRows : 1;
     prefill_attn_tc_kernel<D, NH>
-        <<<dim3(nqt, hq / NH, g.b), 128 * NH, smem, st>>>(g, dv, tq, tk, tv, O, lens, t_stride, hq);
+        <<<dim3(nqt, hq / NH, g.b), 128 * NH + 32, smem, st>>>(g, dv, tq, tk, tv, O, lens, t_stride, hq);
     return cudaGetLastError();
 }
 
