@@ -49,7 +49,7 @@ FALLBACK_HBM_GBS = 6800.0
 # mode (the one-launch step's kernel, and the plain one); reported only
 # while the kernel source is unchanged (llama3_8b_gqa_32k, the default
 # workload).
-NCU_TRAFFIC = {"615a5d7bf756c11f": {"fused": 204156160 + 6497280, "two": 205765376 + 2815488}}
+NCU_TRAFFIC = {"bb3f0f9965f09fa2": {"fused": 204187136 + 6169344, "two": 205768960 + 2484736}}
 
 
 def algorithmic_bytes(w: W.Workload, T, Tqk, Tqv, scores: bool = False) -> int:
