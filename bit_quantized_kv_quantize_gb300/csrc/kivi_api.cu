@@ -204,6 +204,7 @@ kivi_status launch_append(kivi_cache *c, const void *k, const void *v, kivi_stre
     memcpy(ac.T, c->T.data(), (size_t)b * sizeof(int));
     memcpy(ac.Tqk, c->Tqk.data(), (size_t)b * sizeof(int));
     memcpy(ac.Tqv, c->Tqv.data(), (size_t)b * sizeof(int));
+    append_order(ac, b, c->g.R);
     int *nxt = c->cnt + (size_t)(1 - c->parity) * 3 * b;
     cudaError_t e = kivi_launch_append(c->g, c->dv, (const __half *)k, (const __half *)v, ac, nxt,
                                        (cudaStream_t)stream);
@@ -285,6 +286,7 @@ kivi_status launch_fused_step(kivi_cache *c, const void *k, const void *v, const
         memcpy(ac.T, c->T.data(), (size_t)b * sizeof(int));
         memcpy(ac.Tqk, c->Tqk.data(), (size_t)b * sizeof(int));
         memcpy(ac.Tqv, c->Tqv.data(), (size_t)b * sizeof(int));
+        append_order(ac, b, c->g.R);
         cudaError_t e = kivi_launch_append(c->g, c->dv, (const __half *)k, (const __half *)v, ac, nxt,
                                            (cudaStream_t)stream, true);
         if (e != cudaSuccess) return fail_cuda(c, e, "append_decode");

@@ -129,7 +129,18 @@ __host__ __device__ __forceinline__ size_t flush_smem_bytes(const KiviGeom &g) {
 // parameters: the append needs no device read before its row loads).
 struct AppendCounters {
     int T[KIVI_MAX_BATCH], Tqk[KIVI_MAX_BATCH], Tqv[KIVI_MAX_BATCH];
+    // the sequence of each grid row: sequences that flush their key window
+    // first, so that their long CTAs start in the launch's first wave
+    int order[KIVI_MAX_BATCH];
 };
+// Fills ac.order (b sequences, residual length R) from ac's counters.
+inline void append_order(AppendCounters &ac, int b, int R) {
+    int n = 0;
+    for (int i = 0; i < b; ++i)
+        if (ac.T[i] - ac.Tqk[i] == R) ac.order[n++] = i;
+    for (int i = 0; i < b; ++i)
+        if (ac.T[i] - ac.Tqk[i] != R) ac.order[n++] = i;
+}
 
 // Counters of one sequence before an append are in range.
 __device__ __forceinline__ bool append_counters_ok(const KiviGeom &g, int T, int Tqk, int Tqv) {

@@ -174,7 +174,8 @@ __global__ void prefill_residual_kernel(KiviGeom g, KiviDev dv, const __half *__
 }
 
 // ---------------------------------------------------------------------------
-// Append: one CTA per (kv head, sequence): append_pair (kivi_append_impl.cuh),
+// Append: one CTA per (kv head, sequence; grid row y is sequence
+// ac.order[y], the flushing ones first): append_pair (kivi_append_impl.cuh),
 // then the last CTA of a sequence to finish advances that sequence's
 // counters (all CTAs read them first).
 // ---------------------------------------------------------------------------
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__(1024) append_kernel(KiviGeom g, KiviDev dv,
     // the decode launch that usually follows may start its set-up now: it
     // waits for this whole grid before it reads anything
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int j = blockIdx.x, i = blockIdx.y;
+    const int j = blockIdx.x, i = ac.order[blockIdx.y];
     const int R = g.R;
     const int T = ac.T[i], Tqk = ac.Tqk[i], Tqv = ac.Tqv[i];
     if (only_flush && T - Tqk != R) return;
