@@ -188,6 +188,11 @@ __device__ __forceinline__ void tma_tile(void *dst, const CUtensorMap *tm, int r
 }
 
 
+// K and V stages of the attention CTA: three with two heads (192 KB at
+// d = 128, one CTA per SM: each copy then has two tiles of lead), two with
+// one head (two CTAs per SM).
+__host__ __device__ constexpr int kv_stages(int NH) { return NH == 2 ? 3 : 2; }
+
 // A wait that also gives up when another warp of the CTA has given up
 // (*abort set): false then, or after the iteration limit.
 __device__ __forceinline__ bool tc_wait_bar_ab(uint64_t *bar, unsigned phase, const volatile int *abort) {
@@ -227,15 +232,20 @@ __global__ void __maxnreg__(168)
     constexpr int QB = kTcRows * D * 2, KVB = kTcKeys * D * 2, PB = kTcRows * kTcKeys * 2;
     constexpr unsigned QLBO = kTcRows * 16, KLBO = kTcKeys * 16;   // chunk strides
     constexpr int NSW = 4 * NH;   // softmax warps
+    constexpr int KS = kv_stages(NH);   // K and V stages: tile m in stage m mod KS
     unsigned char *sQ = smem;                // head slot e at sQ + e QB
     unsigned char *sK = smem + NH * QB;      // stage s at sK + s KVB
-    unsigned char *sV = sK + 2 * KVB;        // stage s at sV + s KVB
-    unsigned char *sP = sV + 2 * KVB;        // [128][64] weights of head slot e at sP + e PB, laid out like Q
-    // S buffer 0 / 1 done, P V done, Q landed, K stage 0 / 1 landed, V stage
-    // 0 / 1 landed, S buffer 0 / 1 read, P written
-    __shared__ __align__(8) uint64_t bars[11];
-    uint64_t *const bS = bars, *const bO = bars + 2, *const bQ = bars + 3, *const bK = bars + 4, *const bV = bars + 6,
-                    *const bSr = bars + 8, *const bP = bars + 10;
+    unsigned char *sV = sK + KS * KVB;       // stage s at sV + s KVB
+    unsigned char *sP = sV + KS * KVB;       // [128][64] weights of head slot e at sP + e PB, laid out like Q
+    // S buffer 0 / 1 done, P V done, Q landed, K stages landed, V stages
+    // landed, S buffer 0 / 1 read, P written
+    constexpr int NB = 7 + 2 * KS;
+    __shared__ __align__(8) uint64_t bars[NB];
+    uint64_t *const bS = bars, *const bO = bars + 2, *const bQ = bars + 3, *const bK = bars + 4,
+                    *const bV = bars + 4 + KS, *const bSr = bars + 4 + 2 * KS, *const bP = bars + 6 + 2 * KS;
+    // K / V tile m: its stage and the phase its landing completes
+    auto stg = [](int m) { return m % KS; };
+    auto sph = [](int m) { return (unsigned)(m / KS) & 1u; };
     __shared__ uint32_t s_taddr;
     __shared__ int s_abort;   // a wait ran out: every warp stops
     const int qt = gridDim.x - 1 - blockIdx.x;   // the longest tiles first
@@ -255,9 +265,9 @@ __global__ void __maxnreg__(168)
     const int krow0 = (i * g.h + j) * t_stride;   // this kv head's first row in K and V
     const int nt = min((t + kTcKeys - 1) / kTcKeys, (tb + kTcRows) / kTcKeys);   // key tiles
     if (tid == 0) {
-        for (int k = 0; k < 11; ++k)   // Q's: one arrival per head slot's copy; S read, P written: per softmax warp
+        for (int k = 0; k < NB; ++k)   // Q's: one arrival per head slot's copy; S read, P written: per softmax warp
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(tc_smem_u32(&bars[k])),
-                         "r"(k == 3 ? NH : k >= 8 ? NSW : 1)
+                         "r"(k == 3 ? NH : k >= 4 + 2 * KS ? NSW : 1)
                          : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_abort = 0;
@@ -276,7 +286,7 @@ __global__ void __maxnreg__(168)
         if (lane == 0) {
             constexpr uint32_t ID_S = tc_idesc_f16(kTcRows, kTcKeys, 0), ID_O = tc_idesc_f16(kTcRows, D, 1);
             auto issue_s = [&](int kt) {   // S of tile kt into buffer kt mod 2 of every head slot
-                const unsigned char *k = sK + (kt & 1) * KVB;
+                const unsigned char *k = sK + stg(kt) * KVB;
 #pragma unroll
                 for (int e = 0; e < NH; ++e) {
                     const uint32_t tS = taddr + 256 * e + 64 * (kt & 1);
@@ -288,12 +298,17 @@ __global__ void __maxnreg__(168)
                 tc_commit(&bS[kt & 1]);
             };
             // completions issued per barrier (for the drain after a time-out)
-            int nK[2] = {1, nt > 1 ? 1 : 0}, nV[2] = {1, 0}, nS[2] = {0, 0}, nO = 0;
+            int nK[KS], nV[KS], nS[2] = {0, 0}, nO = 0;
 #pragma unroll
             for (int e = 0; e < NH; ++e) tma_tile(sQ + e * QB, &tmQ, (i * hq + h0 + e) * t_stride + tb, bQ, QB);
-            tma_tile(sK, &tmK, krow0, &bK[0], KVB);
-            tma_tile(sV, &tmV, krow0, &bV[0], KVB);
-            if (nt > 1) tma_tile(sK + KVB, &tmK, krow0 + kTcKeys, &bK[1], KVB);
+            // K of the first KS tiles, V of the first KS - 1 (their stages are free)
+#pragma unroll
+            for (int m = 0; m < KS; ++m) {
+                nK[m] = m < nt ? 1 : 0;
+                nV[m] = m < nt && m < KS - 1 ? 1 : 0;
+                if (nK[m]) tma_tile(sK + m * KVB, &tmK, krow0 + m * kTcKeys, &bK[m], KVB);
+                if (nV[m]) tma_tile(sV + m * KVB, &tmV, krow0 + m * kTcKeys, &bV[m], KVB);
+            }
             ok = tc_wait_bar_ab(bQ, 0, abort) && tc_wait_bar_ab(&bK[0], 0, abort);
             if (ok) {
                 tc_fence_after();
@@ -305,32 +320,33 @@ __global__ void __maxnreg__(168)
                 if (kt + 1 < nt) {
                     // S of the next tile: its K landed, its buffer (S of tile
                     // kt - 1) read by every softmax warp
-                    ok = tc_wait_bar_ab(&bK[b ^ 1], (unsigned)((kt + 1) >> 1) & 1u, abort) &&
+                    ok = tc_wait_bar_ab(&bK[stg(kt + 1)], sph(kt + 1), abort) &&
                          (kt == 0 || tc_wait_bar_ab(&bSr[b ^ 1], (unsigned)((kt - 1) >> 1) & 1u, abort));
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(kt + 1);
                     ++nS[b ^ 1];
                 }
-                if (kt + 2 < nt) {   // K two tiles on, into the stage S of this tile read
+                if (kt + KS < nt) {   // K KS tiles on, into the stage S of this tile read
                     ok = tc_wait_bar_ab(&bS[b], (unsigned)(kt >> 1) & 1u, abort);
                     if (!ok) break;
-                    tma_tile(sK + b * KVB, &tmK, krow0 + (kt + 2) * kTcKeys, &bK[b], KVB);
-                    ++nK[b];
+                    tma_tile(sK + stg(kt) * KVB, &tmK, krow0 + (kt + KS) * kTcKeys, &bK[stg(kt)], KVB);
+                    ++nK[stg(kt)];
                 }
-                if (kt + 1 < nt) {   // V of the next tile, into the stage P V of the previous tile read
+                if (kt + KS - 1 < nt) {   // V KS - 1 tiles on, into the stage P V of tile kt - 1 read
                     ok = kt == 0 || tc_wait_bar_ab(bO, (unsigned)(kt - 1) & 1u, abort);
                     if (!ok) break;
-                    tma_tile(sV + (b ^ 1) * KVB, &tmV, krow0 + (kt + 1) * kTcKeys, &bV[b ^ 1], KVB);
-                    ++nV[b ^ 1];
+                    const int vs = stg(kt + KS - 1);   // tile kt - 1's stage (at kt = 0: the last, unused)
+                    tma_tile(sV + vs * KVB, &tmV, krow0 + (kt + KS - 1) * kTcKeys, &bV[vs], KVB);
+                    ++nV[vs];
                 }
                 // P V of this tile: its weights written and, on the tile the
                 // sequence cuts, V's rows past it zeroed (every softmax warp)
                 ok = tc_wait_bar_ab(bP, (unsigned)kt & 1u, abort) &&
-                     tc_wait_bar_ab(&bV[b], (unsigned)(kt >> 1) & 1u, abort);
+                     tc_wait_bar_ab(&bV[stg(kt)], sph(kt), abort);
                 if (!ok) break;
                 tc_fence_after();
-                const unsigned char *v = sV + b * KVB;
+                const unsigned char *v = sV + stg(kt) * KVB;
 #pragma unroll
                 for (int e = 0; e < NH; ++e)
 #pragma unroll
@@ -346,10 +362,15 @@ __global__ void __maxnreg__(168)
                 // before shared and tensor memory are released
                 s_abort = 1;
                 atomicOr(dv.status, KIVI_FLAG_WAIT);
-                const int cnt[8] = {nS[0], nS[1], nO, 1, nK[0], nK[1], nV[0], nV[1]};
+                const int cnt[4] = {nS[0], nS[1], nO, 1};
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
+                for (int k = 0; k < 4; ++k)
                     if (cnt[k] > 0) tc_wait_bar(&bars[k], (unsigned)(cnt[k] - 1) & 1u);
+#pragma unroll
+                for (int m = 0; m < KS; ++m) {
+                    if (nK[m] > 0) tc_wait_bar(&bK[m], (unsigned)(nK[m] - 1) & 1u);
+                    if (nV[m] > 0) tc_wait_bar(&bV[m], (unsigned)(nV[m] - 1) & 1u);
+                }
             }
         }
         __syncwarp();
@@ -434,10 +455,10 @@ __global__ void __maxnreg__(168)
             // the tile landed (they meet zero weights, and the array there
             // holds whatever it holds), a share per softmax warp
             if (kt * kTcKeys + kTcKeys > t) {
-                ok = __all_sync(0xffffffffu, tc_wait_bar_ab(&bV[b], (unsigned)(kt >> 1) & 1u, abort));
+                ok = __all_sync(0xffffffffu, tc_wait_bar_ab(&bV[stg(kt)], sph(kt), abort));
                 if (!ok) break;
                 const int r0 = t - kt * kTcKeys;
-                unsigned char *v = sV + b * KVB;
+                unsigned char *v = sV + stg(kt) * KVB;
                 for (int e = tid; e < (kTcKeys - r0) * (D / 8); e += 32 * NSW) {
                     const int r = r0 + e / (D / 8), c = e % (D / 8);
                     *reinterpret_cast<uint4 *>(v + cm_at<kTcKeys>(r, c)) = make_uint4(0u, 0u, 0u, 0u);
@@ -491,7 +512,7 @@ __global__ void __maxnreg__(168)
         for (int k = 0; k < 2; ++k) {
             const int kb = tb + k * kTcKeys, kt = kb / kTcKeys;
             if (kb >= t) break;
-            pack_diagonal_bits<D>(g, dv, sK + (kt & 1) * KVB, sV + (kt & 1) * KVB, sQ, i, j, kb, t);
+            pack_diagonal_bits<D>(g, dv, sK + stg(kt) * KVB, sV + stg(kt) * KVB, sQ, i, j, kb, t);
             __syncthreads();   // the staging is reused
         }
         if (tb == 0 && j == 0 && threadIdx.x == 0) {
@@ -536,8 +557,8 @@ cudaError_t make_tile_map(CUtensorMap *tm, const __half *base, long long rows, i
 template <int D, int NH>
 cudaError_t launch_tc(const KiviGeom &g, const KiviDev &dv, const __half *Q, const __half *K, const __half *V,
                       __half *O, const SeqLens &lens, int t_stride, int hq, int maxt, cudaStream_t st) {
-    const size_t smem =
-        (size_t)NH * kTcRows * D * 2 + (size_t)4 * kTcKeys * D * 2 + (size_t)NH * kTcRows * kTcKeys * 2;
+    const size_t smem = (size_t)NH * kTcRows * D * 2 + (size_t)2 * kv_stages(NH) * kTcKeys * D * 2 +
+                        (size_t)NH * kTcRows * kTcKeys * 2;
     const long long ts = t_stride > 0 ? t_stride : 1;
     CUtensorMap tq, tk, tv;   // unused when every sequence is empty (the CTAs only write counters)
     memset(&tq, 0, sizeof tq);
