@@ -192,6 +192,9 @@ __device__ __forceinline__ void tma_tile(void *dst, const CUtensorMap *tm, int r
 // d = 128, one CTA per SM: each copy then has two tiles of lead), two with
 // one head (two CTAs per SM).
 __host__ __device__ constexpr int kv_stages(int NH) { return NH == 2 ? 3 : 2; }
+// Producer warps: two with two heads; one with one head (a sixth warp would
+// leave one CTA per SM at 168 registers: the 4k MHA call went 410 -> 444 us).
+__host__ __device__ constexpr int producer_warps(int NH) { return NH == 2 ? 2 : 1; }
 
 // A wait that also gives up when another warp of the CTA has given up
 // (*abort set): false then, or after the iteration limit.
@@ -217,8 +220,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 // even number of query heads): each K and V tile then feeds NH heads' MMAs.
 // Warps 0 .. 4 NH - 1 run the softmax: thread tid owns row tid mod 128 of
 // head slot tid / 128 (head slot e has its own Q and P tiles and tensor-
-// memory columns [256 e, 256 e + 256)).  Warp 4 NH is the producer: its
-// lane 0 issues every copy and MMA.  The two sides meet on mbarriers only:
+// memory columns [256 e, 256 e + 256)).  With two heads, two producer
+// warps, each issuing from its lane 0, so that one's waits do not hold the
+// other's MMAs back (a tcgen05.mma issue waits while the tensor pipe is
+// busy): warp 8 the Q and K copies and S = Q K^T, warp 9 the V copies and
+// O += P V (a commit tracks its own thread's MMAs); with one head, warp 4
+// issues everything.  The warps meet on mbarriers only:
 // S done (MMA commit), S read (every softmax warp), P written (every softmax
 // warp), P V done (MMA commit), and the copies' landings.
 // At most 168 registers a thread: a scheduler partition's 16 K registers
@@ -232,6 +239,7 @@ __global__ void __maxnreg__(168)
     constexpr int QB = kTcRows * D * 2, KVB = kTcKeys * D * 2, PB = kTcRows * kTcKeys * 2;
     constexpr unsigned QLBO = kTcRows * 16, KLBO = kTcKeys * 16;   // chunk strides
     constexpr int NSW = 4 * NH;   // softmax warps
+    constexpr int NPROD = producer_warps(NH);
     constexpr int KS = kv_stages(NH);   // K and V stages: tile m in stage m mod KS
     unsigned char *sQ = smem;                // head slot e at sQ + e QB
     unsigned char *sK = smem + NH * QB;      // stage s at sK + s KVB
@@ -281,10 +289,10 @@ __global__ void __maxnreg__(168)
     const volatile int *abort = &s_abort;
     bool ok = true;
     float lsum = 0.f;
-    if (warp == NSW) {
-        // ---- the producer: copies and MMAs (lane 0) ----
+    constexpr uint32_t ID_S = tc_idesc_f16(kTcRows, kTcKeys, 0), ID_O = tc_idesc_f16(kTcRows, D, 1);
+    if (NPROD == 1 && warp == NSW) {
+        // ---- one producer (lane 0): every copy and MMA ----
         if (lane == 0) {
-            constexpr uint32_t ID_S = tc_idesc_f16(kTcRows, kTcKeys, 0), ID_O = tc_idesc_f16(kTcRows, D, 1);
             auto issue_s = [&](int kt) {   // S of tile kt into buffer kt mod 2 of every head slot
                 const unsigned char *k = sK + stg(kt) * KVB;
 #pragma unroll
@@ -371,6 +379,114 @@ __global__ void __maxnreg__(168)
                     if (nK[m] > 0) tc_wait_bar(&bK[m], (unsigned)(nK[m] - 1) & 1u);
                     if (nV[m] > 0) tc_wait_bar(&bV[m], (unsigned)(nV[m] - 1) & 1u);
                 }
+            }
+        }
+        __syncwarp();
+    } else if (NPROD == 2 && warp == NSW) {
+        // ---- the S producer (lane 0): Q and K copies, S = Q K^T ----
+        if (lane == 0) {
+            auto issue_s = [&](int kt) {   // S of tile kt into buffer kt mod 2 of every head slot
+                const unsigned char *k = sK + stg(kt) * KVB;
+#pragma unroll
+                for (int e = 0; e < NH; ++e) {
+                    const uint32_t tS = taddr + 256 * e + 64 * (kt & 1);
+#pragma unroll
+                    for (int c = 0; c < D / 16; ++c)
+                        tc_mma_f16(tS, tc_desc(sQ + e * QB + 2 * c * QLBO, QLBO, 128),
+                                   tc_desc(k + 2 * c * KLBO, KLBO, 128), ID_S, c > 0);
+                }
+                tc_commit(&bS[kt & 1]);
+            };
+            // completions issued per barrier (for the drain after a time-out)
+            int nK[KS], nS[2] = {0, 0};
+#pragma unroll
+            for (int e = 0; e < NH; ++e) tma_tile(sQ + e * QB, &tmQ, (i * hq + h0 + e) * t_stride + tb, bQ, QB);
+#pragma unroll
+            for (int m = 0; m < KS; ++m) {   // K of the first KS tiles
+                nK[m] = m < nt ? 1 : 0;
+                if (nK[m]) tma_tile(sK + m * KVB, &tmK, krow0 + m * kTcKeys, &bK[m], KVB);
+            }
+            ok = tc_wait_bar_ab(bQ, 0, abort) && tc_wait_bar_ab(&bK[0], 0, abort);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                nS[0] = 1;
+            }
+            for (int kt = 0; kt < nt && ok; ++kt) {
+                const int b = kt & 1;
+                if (kt + 1 < nt) {
+                    // S of the next tile: its K landed, its buffer (S of tile
+                    // kt - 1) read by every softmax warp
+                    ok = tc_wait_bar_ab(&bK[stg(kt + 1)], sph(kt + 1), abort) &&
+                         (kt == 0 || tc_wait_bar_ab(&bSr[b ^ 1], (unsigned)((kt - 1) >> 1) & 1u, abort));
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(kt + 1);
+                    ++nS[b ^ 1];
+                }
+                if (kt + KS < nt) {   // K KS tiles on, into the stage S of this tile read
+                    ok = tc_wait_bar_ab(&bS[b], (unsigned)(kt >> 1) & 1u, abort);
+                    if (!ok) break;
+                    tma_tile(sK + stg(kt) * KVB, &tmK, krow0 + (kt + KS) * kTcKeys, &bK[stg(kt)], KVB);
+                    ++nK[stg(kt)];
+                }
+            }
+            if (!ok) {
+                // flag it, and let every copy and MMA this thread issued finish
+                // (bounded: each barrier's last completion is phase
+                // (count - 1) mod 2) before shared and tensor memory are released
+                s_abort = 1;
+                atomicOr(dv.status, KIVI_FLAG_WAIT);
+                tc_wait_bar(bQ, 0u);
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    if (nS[k] > 0) tc_wait_bar(&bS[k], (unsigned)(nS[k] - 1) & 1u);
+#pragma unroll
+                for (int m = 0; m < KS; ++m)
+                    if (nK[m] > 0) tc_wait_bar(&bK[m], (unsigned)(nK[m] - 1) & 1u);
+            }
+        }
+        __syncwarp();
+    } else if (NPROD == 2 && warp == NSW + 1) {
+        // ---- the P V producer (lane 0): V copies, O += P V ----
+        if (lane == 0) {
+            int nV[KS], nO = 0;
+#pragma unroll
+            for (int m = 0; m < KS; ++m) {   // V of the first KS - 1 tiles
+                nV[m] = m < nt && m < KS - 1 ? 1 : 0;
+                if (nV[m]) tma_tile(sV + m * KVB, &tmV, krow0 + m * kTcKeys, &bV[m], KVB);
+            }
+            for (int kt = 0; kt < nt && ok; ++kt) {
+                if (kt + KS - 1 < nt) {   // V KS - 1 tiles on, into the stage P V of tile kt - 1 read
+                    ok = kt == 0 || tc_wait_bar_ab(bO, (unsigned)(kt - 1) & 1u, abort);
+                    if (!ok) break;
+                    const int vs = stg(kt + KS - 1);   // tile kt - 1's stage (at kt = 0: the last, unused)
+                    tma_tile(sV + vs * KVB, &tmV, krow0 + (kt + KS - 1) * kTcKeys, &bV[vs], KVB);
+                    ++nV[vs];
+                }
+                // P V of this tile: its weights written and, on the tile the
+                // sequence cuts, V's rows past it zeroed (every softmax warp)
+                ok = tc_wait_bar_ab(bP, (unsigned)kt & 1u, abort) &&
+                     tc_wait_bar_ab(&bV[stg(kt)], sph(kt), abort);
+                if (!ok) break;
+                tc_fence_after();
+                const unsigned char *v = sV + stg(kt) * KVB;
+#pragma unroll
+                for (int e = 0; e < NH; ++e)
+#pragma unroll
+                    for (int c = 0; c < kTcKeys / 16; ++c)
+                        tc_mma_f16(taddr + 256 * e + 128, tc_desc(sP + e * PB + 2 * c * QLBO, QLBO, 128),
+                                   tc_desc(v + 256 * c, 128, KLBO), ID_O, kt > 0 || c > 0);
+                tc_commit(bO);
+                ++nO;
+            }
+            if (!ok) {   // as above
+                s_abort = 1;
+                atomicOr(dv.status, KIVI_FLAG_WAIT);
+                if (nO > 0) tc_wait_bar(bO, (unsigned)(nO - 1) & 1u);
+#pragma unroll
+                for (int m = 0; m < KS; ++m)
+                    if (nV[m] > 0) tc_wait_bar(&bV[m], (unsigned)(nV[m] - 1) & 1u);
             }
         }
         __syncwarp();
@@ -576,7 +692,8 @@ cudaError_t launch_tc(const KiviGeom &g, const KiviDev &dv, const __half *Q, con
     if (e != cudaSuccess) return e;
     const int nqt = maxt > 0 ? (maxt + kTcRows - 1) / kTcRows : 1;
     prefill_attn_tc_kernel<D, NH>
-        <<<dim3(nqt, hq / NH, g.b), 128 * NH + 32, smem, st>>>(g, dv, tq, tk, tv, O, lens, t_stride, hq);
+        <<<dim3(nqt, hq / NH, g.b), 128 * NH + 32 * producer_warps(NH), smem, st>>>(g, dv, tq, tk, tv, O, lens,
+                                                                                 t_stride, hq);
     return cudaGetLastError();
 }
 
