@@ -49,7 +49,7 @@ FALLBACK_HBM_GBS = 6800.0
 # mode (the one-launch step's kernel, and the plain one); reported only
 # while the kernel source is unchanged (llama3_8b_gqa_32k, the default
 # workload).
-NCU_TRAFFIC = {"bb3f0f9965f09fa2": {"fused": 204187136 + 6169344, "two": 205768960 + 2484736}}
+NCU_TRAFFIC = {"3b1e4c20734282ed": {"fused": 204195072 + 6233600, "two": 205795584 + 2664448}}
 
 
 def algorithmic_bytes(w: W.Workload, T, Tqk, Tqv, scores: bool = False) -> int:
