@@ -189,11 +189,14 @@ __device__ __forceinline__ void tma_tile(void *dst, const CUtensorMap *tm, int r
 
 
 // K and V stages of the attention CTA: three with two heads (192 KB at
-// d = 128, one CTA per SM: each copy then has two tiles of lead), two with
-// one head (two CTAs per SM).
-__host__ __device__ constexpr int kv_stages(int NH) { return NH == 2 ? 3 : 2; }
-// Producer warps: two with two heads; one with one head (a sixth warp would
-// leave one CTA per SM at 168 registers: the 4k MHA call went 410 -> 444 us).
+// d = 128, one CTA per SM: each copy then has two tiles of lead), four with
+// two query tiles of one head (224 KB: the CTA's four diagonal tiles are
+// still in their stages for the pack epilogue), two with one head (two CTAs
+// per SM).
+__host__ __device__ constexpr int kv_stages(int NH, bool QT) { return QT ? 4 : NH == 2 ? 3 : 2; }
+// Producer warps: two with two slots; one with one (a sixth warp would
+// leave one CTA per SM at 168 registers: a one-slot 4k MHA call went 410 ->
+// 444 us).
 __host__ __device__ constexpr int producer_warps(int NH) { return NH == 2 ? 2 : 1; }
 
 // A wait that also gives up when another warp of the CTA has given up
@@ -216,11 +219,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc_smem_u32(bar)) : "memory");
 }
 
-// NH query heads of one kv head per CTA (1, or 2 when a kv head serves an
-// even number of query heads): each K and V tile then feeds NH heads' MMAs.
-// Warps 0 .. 4 NH - 1 run the softmax: thread tid owns row tid mod 128 of
-// head slot tid / 128 (head slot e has its own Q and P tiles and tensor-
-// memory columns [256 e, 256 e + 256)).  With two heads, two producer
+// NH slots of 128 query rows per CTA: NH query heads of one kv head (QT
+// false: 1, or 2 when a kv head serves an even number of query heads), or
+// (QT) NH consecutive query tiles of one head; each K and V tile then feeds
+// every slot's MMAs.  Warps 0 .. 4 NH - 1 run the softmax: thread tid owns
+// row tid mod 128 of slot tid / 128 (slot e has its own Q and P tiles and
+// tensor-memory columns [256 e, 256 e + 256)).  With two heads, two producer
 // warps, each issuing from its lane 0, so that one's waits do not hold the
 // other's MMAs back (a tcgen05.mma issue waits while the tensor pipe is
 // busy): warp 8 the Q and K copies and S = Q K^T, warp 9 the V copies and
@@ -230,7 +234,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 // warp), P V done (MMA commit), and the copies' landings.
 // At most 168 registers a thread: a scheduler partition's 16 K registers
 // then hold three warps, so two one-head CTAs (five warps each) share an SM.
-template <int D, int NH>
+template <int D, int NH, bool QT>
 __global__ void __maxnreg__(168)
     prefill_attn_tc_kernel(KiviGeom g, KiviDev dv, const __grid_constant__ CUtensorMap tmQ,
                            const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -240,7 +244,8 @@ __global__ void __maxnreg__(168)
     constexpr unsigned QLBO = kTcRows * 16, KLBO = kTcKeys * 16;   // chunk strides
     constexpr int NSW = 4 * NH;   // softmax warps
     constexpr int NPROD = producer_warps(NH);
-    constexpr int KS = kv_stages(NH);   // K and V stages: tile m in stage m mod KS
+    constexpr int KS = kv_stages(NH, QT);   // K and V stages: tile m in stage m mod KS
+    constexpr int CR = QT ? NH * kTcRows : kTcRows;   // the CTA's query rows
     unsigned char *sQ = smem;                // head slot e at sQ + e QB
     unsigned char *sK = smem + NH * QB;      // stage s at sK + s KVB
     unsigned char *sV = sK + KS * KVB;       // stage s at sV + s KVB
@@ -258,10 +263,12 @@ __global__ void __maxnreg__(168)
     __shared__ int s_abort;   // a wait ran out: every warp stops
     const int qt = gridDim.x - 1 - blockIdx.x;   // the longest tiles first
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, hs = min(tid >> 7, NH - 1), rr = tid & 127;
-    const int h0 = blockIdx.y * NH, h = h0 + hs, i = blockIdx.z;   // the CTA's first head, this thread's
+    // the CTA's first head, this thread's (QT: one head, slot e = query tile e)
+    const int h0 = QT ? blockIdx.y : blockIdx.y * NH, h = QT ? h0 : h0 + hs, i = blockIdx.z;
     const int hg = hq / g.h, j = h0 / hg;
     const int t = lens.t[i];
-    const int tb = qt * kTcRows;
+    const int tb = qt * CR;                                 // the CTA's first query row
+    const int tbs = tb + (QT ? hs * kTcRows : 0);           // this thread's slot's first row
     if (tb >= t) {
         if (tb == 0 && h0 == 0 && threadIdx.x == 0) {   // an empty sequence
             dv.T[i] = 0;
@@ -271,7 +278,7 @@ __global__ void __maxnreg__(168)
         return;
     }
     const int krow0 = (i * g.h + j) * t_stride;   // this kv head's first row in K and V
-    const int nt = min((t + kTcKeys - 1) / kTcKeys, (tb + kTcRows) / kTcKeys);   // key tiles
+    const int nt = min((t + kTcKeys - 1) / kTcKeys, (tb + CR) / kTcKeys);   // key tiles
     if (tid == 0) {
         for (int k = 0; k < NB; ++k)   // Q's: one arrival per head slot's copy; S read, P written: per softmax warp
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(tc_smem_u32(&bars[k])),
@@ -308,7 +315,9 @@ __global__ void __maxnreg__(168)
             // completions issued per barrier (for the drain after a time-out)
             int nK[KS], nV[KS], nS[2] = {0, 0}, nO = 0;
 #pragma unroll
-            for (int e = 0; e < NH; ++e) tma_tile(sQ + e * QB, &tmQ, (i * hq + h0 + e) * t_stride + tb, bQ, QB);
+            for (int e = 0; e < NH; ++e)
+                tma_tile(sQ + e * QB, &tmQ, (i * hq + h0 + (QT ? 0 : e)) * t_stride + tb + (QT ? e * kTcRows : 0), bQ,
+                         QB);
             // K of the first KS tiles, V of the first KS - 1 (their stages are free)
 #pragma unroll
             for (int m = 0; m < KS; ++m) {
@@ -400,7 +409,9 @@ __global__ void __maxnreg__(168)
             // completions issued per barrier (for the drain after a time-out)
             int nK[KS], nS[2] = {0, 0};
 #pragma unroll
-            for (int e = 0; e < NH; ++e) tma_tile(sQ + e * QB, &tmQ, (i * hq + h0 + e) * t_stride + tb, bQ, QB);
+            for (int e = 0; e < NH; ++e)
+                tma_tile(sQ + e * QB, &tmQ, (i * hq + h0 + (QT ? 0 : e)) * t_stride + tb + (QT ? e * kTcRows : 0), bQ,
+                         QB);
 #pragma unroll
             for (int m = 0; m < KS; ++m) {   // K of the first KS tiles
                 nK[m] = m < nt ? 1 : 0;
@@ -495,7 +506,7 @@ __global__ void __maxnreg__(168)
         const uint32_t tH = taddr + 256 * hs, tO = tH + 128;          // this head slot's columns
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;   // this warp's tensor-memory lanes
         const float sl2 = 1.4426950408889634f / sqrtf((float)D);      // log2(e) / sqrt(d)
-        const int row = tb + rr;
+        const int row = tbs + rr;
         float mref = -INFINITY;   // the row's reference maximum (raw score units)
         for (int kt = 0; kt < nt; ++kt) {
             const int b = kt & 1;
@@ -512,7 +523,7 @@ __global__ void __maxnreg__(168)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bSr[b]);
             float sc[64];
-            if (kt * kTcKeys + kTcKeys - 1 > tb) {   // a tile the causal mask cuts (the CTA's last two)
+            if (kt * kTcKeys + kTcKeys - 1 > tbs) {   // a tile the causal mask cuts (the slot's last two)
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const int key = kt * kTcKeys + c;
@@ -625,7 +636,7 @@ __global__ void __maxnreg__(168)
     // the staging (generic stores after the copies' and MMAs' accesses)
     if (h0 % hg == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < CR / kTcKeys; ++k) {
             const int kb = tb + k * kTcKeys, kt = kb / kTcKeys;
             if (kb >= t) break;
             pack_diagonal_bits<D>(g, dv, sK + stg(kt) * KVB, sV + stg(kt) * KVB, sQ, i, j, kb, t);
@@ -670,10 +681,10 @@ cudaError_t make_tile_map(CUtensorMap *tm, const __half *base, long long rows, i
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, int NH>
+template <int D, int NH, bool QT>
 cudaError_t launch_tc(const KiviGeom &g, const KiviDev &dv, const __half *Q, const __half *K, const __half *V,
                       __half *O, const SeqLens &lens, int t_stride, int hq, int maxt, cudaStream_t st) {
-    const size_t smem = (size_t)NH * kTcRows * D * 2 + (size_t)2 * kv_stages(NH) * kTcKeys * D * 2 +
+    const size_t smem = (size_t)NH * kTcRows * D * 2 + (size_t)2 * kv_stages(NH, QT) * kTcKeys * D * 2 +
                         (size_t)NH * kTcRows * kTcKeys * 2;
     const long long ts = t_stride > 0 ? t_stride : 1;
     CUtensorMap tq, tk, tv;   // unused when every sequence is empty (the CTAs only write counters)
@@ -687,13 +698,14 @@ cudaError_t launch_tc(const KiviGeom &g, const KiviDev &dv, const __half *Q, con
         if (e == cudaSuccess) e = make_tile_map(&tv, V, (long long)g.b * g.h * ts, D, kTcKeys);
         if (e != cudaSuccess) return e;
     }
-    e = cudaFuncSetAttribute(prefill_attn_tc_kernel<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(prefill_attn_tc_kernel<D, NH, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    const int nqt = maxt > 0 ? (maxt + kTcRows - 1) / kTcRows : 1;
-    prefill_attn_tc_kernel<D, NH>
-        <<<dim3(nqt, hq / NH, g.b), 128 * NH + 32 * producer_warps(NH), smem, st>>>(g, dv, tq, tk, tv, O, lens,
-                                                                                 t_stride, hq);
+    constexpr int CR = QT ? NH * kTcRows : kTcRows;
+    const int nqt = maxt > 0 ? (maxt + CR - 1) / CR : 1;
+    prefill_attn_tc_kernel<D, NH, QT>
+        <<<dim3(nqt, QT ? hq : hq / NH, g.b), 128 * NH + 32 * producer_warps(NH), smem, st>>>(g, dv, tq, tk, tv, O,
+                                                                                            lens, t_stride, hq);
     return cudaGetLastError();
 }
 
@@ -709,7 +721,9 @@ cudaError_t kivi_launch_prefill_attn(const KiviGeom &g, const KiviDev &dv, const
     // two query heads a CTA when a kv head serves an even number of them
     // (d = 128: the 160 KB of shared memory keep one CTA, which holds all
     // 512 tensor-memory columns, per SM)
-    if (g.d == 64) return launch_tc<64, 1>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st);
-    return (hq / g.h) % 2 == 0 ? launch_tc<128, 2>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st)
-                               : launch_tc<128, 1>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st);
+    if (g.d == 64) return launch_tc<64, 1, false>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st);
+    // d = 128: two query heads of a kv head a CTA when a kv head serves an
+    // even number of them, else two query tiles of one head
+    return (hq / g.h) % 2 == 0 ? launch_tc<128, 2, false>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st)
+                               : launch_tc<128, 2, true>(g, dv, Q, K, V, O, lens, t_stride, hq, maxt, st);
 }

@@ -40,7 +40,8 @@ CASES = [
     (2, 4, 8, 128, 2, 2, 32, 128, [1000, 777]),
     (2, 2, 6, 64, 4, 2, 16, 32, [63, 65]),
     (1, 1, 6, 128, 2, 2, 32, 128, [300]),      # d 128, even group: two query heads a CTA
-    (2, 2, 6, 128, 4, 2, 32, 64, [200, 129]),  # d 128, odd group: one query head a CTA
+    (2, 2, 6, 128, 4, 2, 32, 64, [200, 129]),  # d 128, odd group: two query tiles of one head a CTA
+    (2, 2, 2, 128, 2, 4, 32, 64, [1000, 517]),  # MHA, longer: two query tiles a CTA, its four diagonal tiles packed
 ]
 
 
