@@ -127,19 +127,21 @@ __device__ void pack_diagonal_bits(const KiviGeom &g, const KiviDev &dv, const u
 // memory lane r).  Per 64-key tile kt: S = Q K^T (M 128, N 64, K d) into one
 // of two S buffers in tensor memory; each thread reads its row of S, applies
 // the causal mask and the online softmax (base 2, its whole row in
-// registers) and writes its fp16 weights P into a shared-memory tile laid
-// out like Q, from which O += P V (M 128, N d, K 64) takes them as its A
-// operand; O accumulates in tensor memory.  One thread issues the MMAs and
-// the tile copies; completions arrive on mbarriers (bounded waits).
+// registers) and writes its fp16 weights P back over the first 32 columns
+// of the same S buffer (fp16 pairs, its own lane), from which O += P V
+// (M 128, N d, K 64) takes them as its A operand: P never passes through
+// shared memory, whose bandwidth the S MMAs' operands already fill (an
+// M 128 x N 64 x K 16 MMA reads 6 KB of them in its 48 cycles).  O
+// accumulates in tensor memory.  Completions arrive on mbarriers (bounded
+// waits).
 //
 // Pipeline: S of tile kt + 1 is issued as tile kt starts (its buffer held
-// S of tile kt - 1, already read), so it runs under the softmax of tile kt;
-// P V of tile kt - 1 runs under that softmax too, which waits for it only
-// before writing P over the P tile (and before a rescale of O).  Q, K and V
-// tiles come by TMA, one tensor copy each, K two tiles ahead and V one tile
-// ahead (two stages each).  The running maximum is raised lazily: O and the
-// row sum are rescaled only when a row's maximum grows by more than 8 (log2
-// units), so P stays below 2^8.
+// S and P of tile kt - 1: free once P V of tile kt - 1 is done), so it runs
+// under the softmax of tile kt; P V of tile kt - 1 runs under that softmax
+// too, which waits for it only before a rescale of O.  Q, K and V tiles
+// come by TMA, one tensor copy each, a few stages deep.  The running
+// maximum is raised lazily: O and the row sum are rescaled only when a
+// row's maximum grows by more than 8 (log2 units), so P stays below 2^8.
 //
 // Tiles in shared memory use the no-swizzle core-matrix layout, chunk-major:
 // row r, 16-byte chunk c of a tile of ROWS rows at byte c ROWS 16 + r 16
@@ -148,9 +150,9 @@ __device__ void pack_diagonal_bits(const KiviGeom &g, const KiviDev &dv, const u
 // strides (2 D bytes, 16 bytes) writes exactly this with one copy per tile
 // (rows past the array read as zero); value rows past the sequence are
 // zeroed after the copy, as the weights they meet are zero.
-//   Q [128][D], K [2][64][D], V [2][64][D], P [128][64]: 112 KB at d = 128.
-// Tensor memory: S buffers in columns 0-63 and 64-127, O in 128-(128 + D):
-// 256 columns.
+// Per 128-row slot: Q [128][D] and its tensor-memory columns, S / P buffers
+// in 0-63 and 64-127, O in 128-(128 + D): 256 columns; K and V stages
+// [64][D] each, shared by the slots.
 // ---------------------------------------------------------------------------
 constexpr int kTcRows = 128, kTcKeys = 64;
 
@@ -188,11 +190,11 @@ __device__ __forceinline__ void tma_tile(void *dst, const CUtensorMap *tm, int r
 }
 
 
-// K and V stages of the attention CTA: three with two heads (192 KB at
-// d = 128, one CTA per SM: each copy then has two tiles of lead), four with
-// two query tiles of one head (224 KB: the CTA's four diagonal tiles are
-// still in their stages for the pack epilogue), two with one head (two CTAs
-// per SM).
+// K and V stages of the attention CTA: three with two heads (160 KB at
+// d = 128; the CTA holds all 512 tensor-memory columns, one CTA per SM),
+// four with two query tiles of one head (192 KB: the CTA's four diagonal
+// tiles are still in their stages for the pack epilogue), two with one head
+// (two CTAs per SM).
 __host__ __device__ constexpr int kv_stages(int NH, bool QT) { return QT ? 4 : NH == 2 ? 3 : 2; }
 // Producer warps: two with two slots; one with one (a sixth warp would
 // leave one CTA per SM at 168 registers: a one-slot 4k MHA call went 410 ->
@@ -223,15 +225,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 // false: 1, or 2 when a kv head serves an even number of query heads), or
 // (QT) NH consecutive query tiles of one head; each K and V tile then feeds
 // every slot's MMAs.  Warps 0 .. 4 NH - 1 run the softmax: thread tid owns
-// row tid mod 128 of slot tid / 128 (slot e has its own Q and P tiles and
+// row tid mod 128 of slot tid / 128 (slot e has its own Q tile and
 // tensor-memory columns [256 e, 256 e + 256)).  With two heads, two producer
 // warps, each issuing from its lane 0, so that one's waits do not hold the
 // other's MMAs back (a tcgen05.mma issue waits while the tensor pipe is
 // busy): warp 8 the Q and K copies and S = Q K^T, warp 9 the V copies and
 // O += P V (a commit tracks its own thread's MMAs); with one head, warp 4
-// issues everything.  The warps meet on mbarriers only:
-// S done (MMA commit), S read (every softmax warp), P written (every softmax
-// warp), P V done (MMA commit), and the copies' landings.
+// issues everything.  The warps meet on mbarriers only, one per S / P
+// buffer: S done (MMA commit), P written (every softmax warp), P V done
+// (MMA commit: the buffer is free again); and the copies' landings.
 // At most 168 registers a thread: a scheduler partition's 16 K registers
 // then hold three warps, so two one-head CTAs (five warps each) share an SM.
 template <int D, int NH, bool QT>
@@ -240,7 +242,7 @@ __global__ void __maxnreg__(168)
                            const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                            __half *__restrict__ O, SeqLens lens, int t_stride, int hq) {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int QB = kTcRows * D * 2, KVB = kTcKeys * D * 2, PB = kTcRows * kTcKeys * 2;
+    constexpr int QB = kTcRows * D * 2, KVB = kTcKeys * D * 2;
     constexpr unsigned QLBO = kTcRows * 16, KLBO = kTcKeys * 16;   // chunk strides
     constexpr int NSW = 4 * NH;   // softmax warps
     constexpr int NPROD = producer_warps(NH);
@@ -249,13 +251,13 @@ __global__ void __maxnreg__(168)
     unsigned char *sQ = smem;                // head slot e at sQ + e QB
     unsigned char *sK = smem + NH * QB;      // stage s at sK + s KVB
     unsigned char *sV = sK + KS * KVB;       // stage s at sV + s KVB
-    unsigned char *sP = sV + KS * KVB;       // [128][64] weights of head slot e at sP + e PB, laid out like Q
-    // S buffer 0 / 1 done, P V done, Q landed, K stages landed, V stages
-    // landed, S buffer 0 / 1 read, P written
+    // S buffer 0 / 1 done, P V of buffer 0 / 1's tile done (the buffer is
+    // free), Q landed, K stages landed, V stages landed, P of buffer 0 / 1
+    // written
     constexpr int NB = 7 + 2 * KS;
     __shared__ __align__(8) uint64_t bars[NB];
-    uint64_t *const bS = bars, *const bO = bars + 2, *const bQ = bars + 3, *const bK = bars + 4,
-                    *const bV = bars + 4 + KS, *const bSr = bars + 4 + 2 * KS, *const bP = bars + 6 + 2 * KS;
+    uint64_t *const bS = bars, *const bF = bars + 2, *const bQ = bars + 4, *const bK = bars + 5,
+                    *const bV = bK + KS, *const bP = bV + KS;
     // K / V tile m: its stage and the phase its landing completes
     auto stg = [](int m) { return m % KS; };
     auto sph = [](int m) { return (unsigned)(m / KS) & 1u; };
@@ -280,9 +282,9 @@ __global__ void __maxnreg__(168)
     const int krow0 = (i * g.h + j) * t_stride;   // this kv head's first row in K and V
     const int nt = min((t + kTcKeys - 1) / kTcKeys, (tb + CR) / kTcKeys);   // key tiles
     if (tid == 0) {
-        for (int k = 0; k < NB; ++k)   // Q's: one arrival per head slot's copy; S read, P written: per softmax warp
+        for (int k = 0; k < NB; ++k)   // Q's: one arrival per head slot's copy; P written: per softmax warp
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(tc_smem_u32(&bars[k])),
-                         "r"(k == 3 ? NH : k >= 4 + 2 * KS ? NSW : 1)
+                         "r"(k == 4 ? NH : k >= 5 + 2 * KS ? NSW : 1)
                          : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_abort = 0;
@@ -297,6 +299,20 @@ __global__ void __maxnreg__(168)
     bool ok = true;
     float lsum = 0.f;
     constexpr uint32_t ID_S = tc_idesc_f16(kTcRows, kTcKeys, 0), ID_O = tc_idesc_f16(kTcRows, D, 1);
+    // O += P V of tile kt for every head slot: P (fp16 pairs) in the first 32
+    // columns of the slot's S buffer kt mod 2, V from its stage; the commit
+    // frees the S buffer and V's stage
+    auto issue_pv = [&](int kt) {
+        const int b = kt & 1;
+        const unsigned char *v = sV + stg(kt) * KVB;
+#pragma unroll
+        for (int e = 0; e < NH; ++e)
+#pragma unroll
+            for (int c = 0; c < kTcKeys / 16; ++c)
+                tc_mma_f16_ta(taddr + 256 * e + 128, taddr + 256 * e + 64 * b + 8 * c,
+                              tc_desc(v + 256 * c, 128, KLBO), ID_O, kt > 0 || c > 0);
+        tc_commit(&bF[b]);
+    };
     if (NPROD == 1 && warp == NSW) {
         // ---- one producer (lane 0): every copy and MMA ----
         if (lane == 0) {
@@ -313,7 +329,7 @@ __global__ void __maxnreg__(168)
                 tc_commit(&bS[kt & 1]);
             };
             // completions issued per barrier (for the drain after a time-out)
-            int nK[KS], nV[KS], nS[2] = {0, 0}, nO = 0;
+            int nK[KS], nV[KS], nS[2] = {0, 0}, nF[2] = {0, 0};
 #pragma unroll
             for (int e = 0; e < NH; ++e)
                 tma_tile(sQ + e * QB, &tmQ, (i * hq + h0 + (QT ? 0 : e)) * t_stride + tb + (QT ? e * kTcRows : 0), bQ,
@@ -335,10 +351,10 @@ __global__ void __maxnreg__(168)
             for (int kt = 0; kt < nt && ok; ++kt) {
                 const int b = kt & 1;
                 if (kt + 1 < nt) {
-                    // S of the next tile: its K landed, its buffer (S of tile
-                    // kt - 1) read by every softmax warp
+                    // S of the next tile: its K landed, its buffer free (P V
+                    // of tile kt - 1 read its weights there)
                     ok = tc_wait_bar_ab(&bK[stg(kt + 1)], sph(kt + 1), abort) &&
-                         (kt == 0 || tc_wait_bar_ab(&bSr[b ^ 1], (unsigned)((kt - 1) >> 1) & 1u, abort));
+                         (kt == 0 || tc_wait_bar_ab(&bF[b ^ 1], (unsigned)((kt - 1) >> 1) & 1u, abort));
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(kt + 1);
@@ -351,7 +367,7 @@ __global__ void __maxnreg__(168)
                     ++nK[stg(kt)];
                 }
                 if (kt + KS - 1 < nt) {   // V KS - 1 tiles on, into the stage P V of tile kt - 1 read
-                    ok = kt == 0 || tc_wait_bar_ab(bO, (unsigned)(kt - 1) & 1u, abort);
+                    ok = kt == 0 || tc_wait_bar_ab(&bF[b ^ 1], (unsigned)((kt - 1) >> 1) & 1u, abort);
                     if (!ok) break;
                     const int vs = stg(kt + KS - 1);   // tile kt - 1's stage (at kt = 0: the last, unused)
                     tma_tile(sV + vs * KVB, &tmV, krow0 + (kt + KS - 1) * kTcKeys, &bV[vs], KVB);
@@ -359,19 +375,12 @@ __global__ void __maxnreg__(168)
                 }
                 // P V of this tile: its weights written and, on the tile the
                 // sequence cuts, V's rows past it zeroed (every softmax warp)
-                ok = tc_wait_bar_ab(bP, (unsigned)kt & 1u, abort) &&
+                ok = tc_wait_bar_ab(&bP[b], (unsigned)(kt >> 1) & 1u, abort) &&
                      tc_wait_bar_ab(&bV[stg(kt)], sph(kt), abort);
                 if (!ok) break;
                 tc_fence_after();
-                const unsigned char *v = sV + stg(kt) * KVB;
-#pragma unroll
-                for (int e = 0; e < NH; ++e)
-#pragma unroll
-                    for (int c = 0; c < kTcKeys / 16; ++c)
-                        tc_mma_f16(taddr + 256 * e + 128, tc_desc(sP + e * PB + 2 * c * QLBO, QLBO, 128),
-                                   tc_desc(v + 256 * c, 128, KLBO), ID_O, kt > 0 || c > 0);
-                tc_commit(bO);
-                ++nO;
+                issue_pv(kt);
+                ++nF[b];
             }
             if (!ok) {
                 // flag it, and let every issued copy and MMA finish (bounded:
@@ -379,10 +388,12 @@ __global__ void __maxnreg__(168)
                 // before shared and tensor memory are released
                 s_abort = 1;
                 atomicOr(dv.status, KIVI_FLAG_WAIT);
-                const int cnt[4] = {nS[0], nS[1], nO, 1};
+                tc_wait_bar(bQ, 0u);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    if (cnt[k] > 0) tc_wait_bar(&bars[k], (unsigned)(cnt[k] - 1) & 1u);
+                for (int k = 0; k < 2; ++k) {
+                    if (nS[k] > 0) tc_wait_bar(&bS[k], (unsigned)(nS[k] - 1) & 1u);
+                    if (nF[k] > 0) tc_wait_bar(&bF[k], (unsigned)(nF[k] - 1) & 1u);
+                }
 #pragma unroll
                 for (int m = 0; m < KS; ++m) {
                     if (nK[m] > 0) tc_wait_bar(&bK[m], (unsigned)(nK[m] - 1) & 1u);
@@ -426,10 +437,10 @@ __global__ void __maxnreg__(168)
             for (int kt = 0; kt < nt && ok; ++kt) {
                 const int b = kt & 1;
                 if (kt + 1 < nt) {
-                    // S of the next tile: its K landed, its buffer (S of tile
-                    // kt - 1) read by every softmax warp
+                    // S of the next tile: its K landed, its buffer free (P V
+                    // of tile kt - 1 read its weights there)
                     ok = tc_wait_bar_ab(&bK[stg(kt + 1)], sph(kt + 1), abort) &&
-                         (kt == 0 || tc_wait_bar_ab(&bSr[b ^ 1], (unsigned)((kt - 1) >> 1) & 1u, abort));
+                         (kt == 0 || tc_wait_bar_ab(&bF[b ^ 1], (unsigned)((kt - 1) >> 1) & 1u, abort));
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(kt + 1);
@@ -461,15 +472,16 @@ __global__ void __maxnreg__(168)
     } else if (NPROD == 2 && warp == NSW + 1) {
         // ---- the P V producer (lane 0): V copies, O += P V ----
         if (lane == 0) {
-            int nV[KS], nO = 0;
+            int nV[KS], nF[2] = {0, 0};
 #pragma unroll
             for (int m = 0; m < KS; ++m) {   // V of the first KS - 1 tiles
                 nV[m] = m < nt && m < KS - 1 ? 1 : 0;
                 if (nV[m]) tma_tile(sV + m * KVB, &tmV, krow0 + m * kTcKeys, &bV[m], KVB);
             }
             for (int kt = 0; kt < nt && ok; ++kt) {
+                const int b = kt & 1;
                 if (kt + KS - 1 < nt) {   // V KS - 1 tiles on, into the stage P V of tile kt - 1 read
-                    ok = kt == 0 || tc_wait_bar_ab(bO, (unsigned)(kt - 1) & 1u, abort);
+                    ok = kt == 0 || tc_wait_bar_ab(&bF[b ^ 1], (unsigned)((kt - 1) >> 1) & 1u, abort);
                     if (!ok) break;
                     const int vs = stg(kt + KS - 1);   // tile kt - 1's stage (at kt = 0: the last, unused)
                     tma_tile(sV + vs * KVB, &tmV, krow0 + (kt + KS - 1) * kTcKeys, &bV[vs], KVB);
@@ -477,24 +489,19 @@ __global__ void __maxnreg__(168)
                 }
                 // P V of this tile: its weights written and, on the tile the
                 // sequence cuts, V's rows past it zeroed (every softmax warp)
-                ok = tc_wait_bar_ab(bP, (unsigned)kt & 1u, abort) &&
+                ok = tc_wait_bar_ab(&bP[b], (unsigned)(kt >> 1) & 1u, abort) &&
                      tc_wait_bar_ab(&bV[stg(kt)], sph(kt), abort);
                 if (!ok) break;
                 tc_fence_after();
-                const unsigned char *v = sV + stg(kt) * KVB;
-#pragma unroll
-                for (int e = 0; e < NH; ++e)
-#pragma unroll
-                    for (int c = 0; c < kTcKeys / 16; ++c)
-                        tc_mma_f16(taddr + 256 * e + 128, tc_desc(sP + e * PB + 2 * c * QLBO, QLBO, 128),
-                                   tc_desc(v + 256 * c, 128, KLBO), ID_O, kt > 0 || c > 0);
-                tc_commit(bO);
-                ++nO;
+                issue_pv(kt);
+                ++nF[b];
             }
             if (!ok) {   // as above
                 s_abort = 1;
                 atomicOr(dv.status, KIVI_FLAG_WAIT);
-                if (nO > 0) tc_wait_bar(bO, (unsigned)(nO - 1) & 1u);
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    if (nF[k] > 0) tc_wait_bar(&bF[k], (unsigned)(nF[k] - 1) & 1u);
 #pragma unroll
                 for (int m = 0; m < KS; ++m)
                     if (nV[m] > 0) tc_wait_bar(&bV[m], (unsigned)(nV[m] - 1) & 1u);
@@ -513,15 +520,12 @@ __global__ void __maxnreg__(168)
             ok = __all_sync(0xffffffffu, tc_wait_bar_ab(&bS[b], (unsigned)(kt >> 1) & 1u, abort));
             if (!ok) break;
             tc_fence_after();
-            // this row's 64 scores; then the S buffer is free for the producer
+            // this row's 64 scores (P takes their place)
             const uint32_t tS = tH + 64 * b;
             uint32_t sr[2][32];
             tc_ld32(tS + lane_off, sr[0]);
             tc_ld32(tS + lane_off + 32, sr[1]);
             tc_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bSr[b]);
             float sc[64];
             if (kt * kTcKeys + kTcKeys - 1 > tbs) {   // a tile the causal mask cuts (the slot's last two)
 #pragma unroll
@@ -555,13 +559,12 @@ __global__ void __maxnreg__(168)
                 pw[c] = pack_h2(p0, p1);
             }
             lsum = lsum * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
-            // P V of the previous tile done: O holds its sum, the P tile is free
-            if (kt > 0) {
-                ok = __all_sync(0xffffffffu, tc_wait_bar_ab(bO, (unsigned)(kt - 1) & 1u, abort));
+            // a rescale of O, once P V of the previous tile added to it
+            if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                ok = __all_sync(0xffffffffu,
+                                tc_wait_bar_ab(&bF[b ^ 1], (unsigned)((kt - 1) >> 1) & 1u, abort));
                 if (!ok) break;
                 tc_fence_after();
-            }
-            if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t o[32];
@@ -571,13 +574,10 @@ __global__ void __maxnreg__(168)
                     for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
                     tc_st32(tO + lane_off + c0, o);
                 }
-                tc_wait_st();
             }
-            // P: row rr, chunk c (keys 8c .. 8c + 7) at c 128 16 + 16 rr
-#pragma unroll
-            for (int c = 0; c < kTcKeys / 8; ++c)
-                *reinterpret_cast<uint4 *>(sP + hs * PB + cm_at<kTcRows>(rr, c)) =
-                    make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+            // P: this row's 64 weights as fp16 pairs over the first 32
+            // columns of the S buffer (the A operand of P V)
+            tc_st32(tS + lane_off, pw);
             // V's rows past the sequence on the tile it cuts: zeroed once
             // the tile landed (they meet zero weights, and the array there
             // holds whatever it holds), a share per softmax warp
@@ -591,14 +591,17 @@ __global__ void __maxnreg__(168)
                     *reinterpret_cast<uint4 *>(v + cm_at<kTcKeys>(r, c)) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            // the P tile, the zeroed rows and O's rescale before P V
+            // P, O's rescale and the zeroed rows before P V
+            tc_wait_st();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bP);
+            if (lane == 0) mbar_arrive(&bP[b]);
         }
         // the last P V done
-        if (ok) ok = __all_sync(0xffffffffu, tc_wait_bar_ab(bO, (unsigned)(nt - 1) & 1u, abort));
+        if (ok)
+            ok = __all_sync(0xffffffffu,
+                            tc_wait_bar_ab(&bF[(nt - 1) & 1], (unsigned)((nt - 1) >> 1) & 1u, abort));
         if (!ok) {   // stop the others' waits too
             if (lane == 0) {
                 s_abort = 1;
@@ -684,8 +687,7 @@ cudaError_t make_tile_map(CUtensorMap *tm, const __half *base, long long rows, i
 template <int D, int NH, bool QT>
 cudaError_t launch_tc(const KiviGeom &g, const KiviDev &dv, const __half *Q, const __half *K, const __half *V,
                       __half *O, const SeqLens &lens, int t_stride, int hq, int maxt, cudaStream_t st) {
-    const size_t smem = (size_t)NH * kTcRows * D * 2 + (size_t)2 * kv_stages(NH, QT) * kTcKeys * D * 2 +
-                        (size_t)NH * kTcRows * kTcKeys * 2;
+    const size_t smem = (size_t)NH * kTcRows * D * 2 + (size_t)2 * kv_stages(NH, QT) * kTcKeys * D * 2;
     const long long ts = t_stride > 0 ? t_stride : 1;
     CUtensorMap tq, tk, tv;   // unused when every sequence is empty (the CTAs only write counters)
     memset(&tq, 0, sizeof tq);
