@@ -141,3 +141,55 @@ def test_prefill_attn_all_empty():
     assert not out.float().abs().sum().item()
     assert c.check() == 0
     c.close()
+
+
+RISING = [
+    # b, h_kv, h_q, d, lens: one variant of the kernel each
+    (1, 1, 2, 64, [700]),    # d 64: one slot a CTA
+    (1, 1, 2, 128, [700]),   # two query heads a CTA
+    (1, 1, 3, 128, [700]),   # two query tiles of one head a CTA
+]
+
+
+@pytest.mark.parametrize("case", RISING, ids=[f"rise{i}" for i in range(len(RISING))])
+def test_prefill_attn_rising_scores(case):
+    """Keys of the first 64-token tile are zero, so a row's maximum score
+    starts at 0 and jumps on a later tile: the kernel then rescales O and
+    the row sum (it does so only when the maximum grows by more than 8 in
+    log2 units), after the previous tile's P V and before the next.  The
+    case is checked to reach that branch on many rows before the GPU runs
+    it.  (Keys whose scale keeps rising along the prompt make late rows so
+    peaked that the fp16 weights' rounding alone comes to the tolerance: an
+    emulation of the kernel's arithmetic gives 2.2e-3 there.)"""
+    b, h, hq, d, lens = case
+    rng = np.random.default_rng(zlib.crc32(str(case).encode()))
+    ts = max(lens) + 5
+    Q = (rng.standard_normal((b, hq, ts, d)) * 1.5).astype(np.float16)
+    scale = np.where(np.arange(ts) < 64, 0.0, 1.0)[None, None, :, None]
+    Kh = (rng.standard_normal((b, h, ts, d)) * 1.5 * scale).astype(np.float16)
+    Vh = rng.standard_normal((b, h, ts, d)).astype(np.float16)
+    t = np.array(lens, np.int32)
+    # precondition: the running maximum of raw scores, taken over whole
+    # 64-key tiles, grows by more than 8 / (log2(e) / sqrt(d)) on many rows
+    lim = 8.0 * np.sqrt(d) / np.log2(np.e)
+    n, grows, rows = lens[0], 0, 0
+    for qh in range(hq):
+        s = Q[0, qh, :n].astype(np.float64) @ Kh[0, qh * h // hq, :n].astype(np.float64).T
+        for tau in range(128, n, 7):
+            m = s[tau, :64].max()
+            rows += 1
+            for k0 in range(64, tau + 1, 64):
+                mt = s[tau, k0:min(k0 + 64, tau + 1)].max()
+                if mt - m > lim:
+                    grows += 1
+                    break
+                m = max(m, mt)
+    assert grows > rows // 5, (grows, rows)
+    cap = max(lens) + 8
+    a = K.KiviCache(b, h, d, 2, 2, 32, 64, cap)
+    out = a.prefill_attn(_dev(Q), _dev(Kh), _dev(Vh), t)
+    got = out.float().cpu().numpy()
+    ref = oracle.prefill_attention(Q, Kh, Vh, t)
+    _compare_rows(got, ref, lens, f"prefill attention, rising scores {case}")
+    assert a.check() == 0
+    a.close()
